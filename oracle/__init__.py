@@ -1,0 +1,189 @@
+"""Plain CPU oracle for the MXFP4 speculative-verification hot path.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference legs may import this package.  The CUDA
+product path never imports, loads or calls it, and the two share no code: the
+oracle's arithmetic lives in ``mxs_oracle.c`` (plain C, double precision,
+written from the pages' definitions), and this module only marshals numpy
+arrays into it.
+
+What each entry point follows (page title, section):
+
+* ``e2m1_value`` / ``e8m0_value`` / ``dequant`` -- "Module 11. Speculative
+  Decoding and Quantization", §12 (E2M1 bit layout and magnitudes, E8M0 power
+  of two, 32-element MX blocks); "Next-Gen Speculative Decoding and FP4
+  Quantization ...", section "Microscaling FP4 (MX-FP4) Integration" (packed
+  [rows, K/2] nibbles and [rows, K/32] scales).
+* ``gemm`` -- the definition Y[m,n] = sum_k x[m,k] * w[n,k], summed in double.
+* ``pack`` -- Module 11 §12-§13 (one power-of-two scale per block, nearest grid
+  value, zero block gets scale 1).
+* ``spec_accept`` -- Module 11 §4 (left-to-right acceptance, residual
+  norm((p-q)+), bonus token) and §5 (strict "draw < acceptance", acceptance 0
+  where q = 0).
+
+Every function is pinned by ``tests/test_oracle_*.py`` against values the pages
+print, closed forms, invariants and brute force; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+_SRC = _HERE / "mxs_oracle.c"
+_LIB_PATH = _HERE / "libmxs_oracle.so"
+_lib = None
+
+ROW_BAD_DRAFT = 1
+ROW_ZERO_Q = 2
+ROW_ZERO_RESIDUAL = 4
+ROW_NONFINITE = 8
+
+
+def build(force: bool = False) -> Path:
+    """Compile ``mxs_oracle.c`` with the host C compiler (gcc)."""
+    if force or not _LIB_PATH.exists() or _LIB_PATH.stat().st_mtime < _SRC.stat().st_mtime:
+        tmp = _LIB_PATH.with_suffix(f".so.tmp{os.getpid()}")
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+               "-ffp-contract=off", "-fno-fast-math", "-o", str(tmp), str(_SRC), "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    p = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    lib.mxs_oracle_e2m1_value.argtypes = [ctypes.c_int]
+    lib.mxs_oracle_e2m1_value.restype = ctypes.c_double
+    lib.mxs_oracle_e8m0_value.argtypes = [ctypes.c_int]
+    lib.mxs_oracle_e8m0_value.restype = ctypes.c_double
+    lib.mxs_oracle_dequant.argtypes = [p, p, i64, i64, p]
+    lib.mxs_oracle_dequant.restype = ctypes.c_int
+    lib.mxs_oracle_gemm.argtypes = [p, p, p, i64, i64, i64, p, ctypes.c_int]
+    lib.mxs_oracle_gemm.restype = ctypes.c_int
+    lib.mxs_oracle_pack.argtypes = [p, i64, i64, p, p]
+    lib.mxs_oracle_pack.restype = ctypes.c_int
+    for name in ("mxs_oracle_spec_accept", "mxs_oracle_spec_accept_f64"):
+        fn = getattr(lib, name)
+        fn.argtypes = [p, p, p, p, i64, i64, i64, p, p, p, p, ctypes.c_int]
+        fn.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _c(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def e2m1_value(code: int) -> float:
+    return _load().mxs_oracle_e2m1_value(int(code))
+
+
+def e8m0_value(e: int) -> float:
+    return _load().mxs_oracle_e8m0_value(int(e))
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64, exactly (bf16 = top half of fp32)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def dequant(nibbles: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Packed MXFP4 [N, K/2] + [N, K/32] -> float64 [N, K]."""
+    nib = _c(nibbles, np.uint8)
+    sc = _c(scales, np.uint8)
+    N, half = nib.shape
+    K = 2 * half
+    assert sc.shape == (N, K // 32)
+    w = np.empty((N, K), dtype=np.float64)
+    rc = _load().mxs_oracle_dequant(_ptr(nib), _ptr(sc), N, K, _ptr(w))
+    if rc:
+        raise ValueError(f"oracle dequant failed ({rc})")
+    return w
+
+
+def gemm(x_bf16_bits: np.ndarray, nibbles: np.ndarray, scales: np.ndarray,
+         nthreads: int | None = None) -> np.ndarray:
+    """Y[M, N] (float64) = X (bf16 bit patterns [M, K]) . dequant(W)^T."""
+    x = _c(x_bf16_bits, np.uint16)
+    nib = _c(nibbles, np.uint8)
+    sc = _c(scales, np.uint8)
+    M, K = x.shape
+    N = nib.shape[0]
+    assert nib.shape == (N, K // 2) and sc.shape == (N, K // 32)
+    y = np.empty((M, N), dtype=np.float64)
+    rc = _load().mxs_oracle_gemm(_ptr(x), _ptr(nib), _ptr(sc), M, N, K, _ptr(y),
+                                 nthreads or default_threads())
+    if rc:
+        raise ValueError(f"oracle gemm failed ({rc})")
+    return y
+
+
+def pack(w: np.ndarray, *, dtype: str = "f32") -> tuple[np.ndarray, np.ndarray, bool]:
+    """Quantise [N, K] weights to (nibbles [N,K/2], scales [N,K/32], all_finite).
+
+    ``w`` is float32 values (dtype="f32") or bf16 bit patterns as uint16
+    (dtype="bf16"); both convert to float64 exactly before packing.
+    """
+    if dtype == "f32":
+        wd = np.ascontiguousarray(w, dtype=np.float32).astype(np.float64)
+    elif dtype == "bf16":
+        wd = bf16_bits_to_f64(w)
+    else:
+        raise ValueError(dtype)
+    wd = np.ascontiguousarray(wd)
+    N, K = wd.shape
+    nib = np.zeros((N, K // 2), dtype=np.uint8)
+    sc = np.zeros((N, K // 32), dtype=np.uint8)
+    rc = _load().mxs_oracle_pack(_ptr(wd), N, K, _ptr(nib), _ptr(sc))
+    if rc not in (0, 4):
+        raise ValueError(f"oracle pack failed ({rc})")
+    return nib, sc, rc == 0
+
+
+def spec_accept(p: np.ndarray, q: np.ndarray, draft: np.ndarray, u: np.ndarray,
+                nthreads: int | None = None, *, f64: bool = False):
+    """Acceptance + residual/bonus sampling for B rows.
+
+    p [B, K+1, V], q [B, K, V], draft [B, K] int32, u [B, K+1].
+    Returns (tokens [B, K+1] int32 padded with -1, n_emitted [B] int32,
+    row_flags [B] int32, edge_dist [B] float64) where edge_dist is the distance
+    of u[b, K] from the nearer edge of the chosen inverse-CDF bin.
+    """
+    dt = np.float64 if f64 else np.float32
+    p = _c(p, dt)
+    q = _c(q, dt)
+    u = _c(u, dt)
+    draft = _c(draft, np.int32)
+    B, K1, V = p.shape
+    K = K1 - 1
+    assert q.shape == (B, K, V) and draft.shape == (B, K) and u.shape == (B, K + 1)
+    tokens = np.empty((B, K + 1), dtype=np.int32)
+    n_emitted = np.empty(B, dtype=np.int32)
+    flags = np.empty(B, dtype=np.int32)
+    edge = np.empty(B, dtype=np.float64)
+    fn = _load().mxs_oracle_spec_accept_f64 if f64 else _load().mxs_oracle_spec_accept
+    rc = fn(_ptr(p), _ptr(q), _ptr(draft), _ptr(u), B, K, V, _ptr(tokens),
+            _ptr(n_emitted), _ptr(flags), _ptr(edge), nthreads or default_threads())
+    if rc:
+        raise ValueError(f"oracle spec_accept failed ({rc})")
+    return tokens, n_emitted, flags, edge
