@@ -1,0 +1,507 @@
+#!/usr/bin/env python
+"""Benchmark of the MXFP4 speculative-verification step on GB300.
+
+One step = the verification pass of a Llama-3-8B-shaped decoder over MX-FP4
+weights (32 layers x {QKV 4096->6144, O 4096->4096, gate+up 4096->28672,
+down 14336->4096} + lm_head 4096->128256 = 129 verify GEMMs at
+M = batch * (K_spec + 1) = 5) followed by spec_accept over the 128256-token
+vocabulary.  Weights are random MX-FP4 (exponents 118..132), X ~ N(0, 1)
+bf16, laws are softmaxed N(0, 2) logits; all synthetic and seeded.
+
+Reported value: algorithmic bytes of the step (W + scales + X + Y of every GEMM,
+plus the bytes spec_accept must read) / step time, in TB/s, with inputs
+resident in HBM (the 3.99 GB of weights per step exceed the 129 MB L2, so no
+flush is needed).  `e2e` repeats the step through the public API with the
+step's inputs copied from pinned host memory and the emitted tokens copied
+back inside the timed region.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mxs|reference]
+                       [--workload llama8b|llama8b_b4|llama8b_b16|llama8b_b64|llama70b]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "MXFP4 verify-GEMM achieved HBM TB/s (% of peak); spec_accept rows/sec"
+FALLBACK_HBM_GBS = 6800.0
+
+# Per-launch DRAM traffic of the verify GEMM (read + write bytes) divided by
+# its algorithmic bytes, from the ncu capture summarised in
+# profiles/mxfp4_gemm_kernel_llama8b.md, valid for the gemm.cu source whose
+# sha256 prefix is recorded beside it.  None until a capture exists.
+GEMM_TRAFFIC_RATIO = None
+GEMM_TRAFFIC_SRC_SHA = None
+
+WORKLOADS = {
+    # name: (model, B, K_spec)
+    "llama8b": ("llama8b", 1, 4),
+    "llama8b_b4": ("llama8b", 4, 4),
+    "llama8b_b16": ("llama8b", 16, 4),
+    "llama8b_b64": ("llama8b", 64, 4),
+    "llama70b": ("llama70b", 16, 4),
+}
+
+
+def gemm_bytes(M: int, N: int, K: int) -> int:
+    """Algorithmic bytes of one verify GEMM: W nibbles + E8M0 scales + bf16 X + fp32 Y."""
+    return N * K // 2 + N * K // 32 + 2 * M * K + 4 * M * N
+
+
+def accept_bytes(B: int, K: int, V: int, n_emitted: np.ndarray) -> int:
+    """Bytes spec_accept must read/write: gathers, uniforms, ids, the sampled law
+    (residual p_j, q_j when a draft was rejected, else p_K), outputs."""
+    total = 0
+    for b in range(B):
+        j = int(n_emitted[b]) - 1
+        law = 8 * V if j < K else 4 * V
+        total += 8 * K + 4 * (K + 1) + 4 * K + law + 4 * (K + 1) + 4
+    return total
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def src_sha() -> str:
+    with open(os.path.join(ROOT, "mxfp4_speculative_verification_gb300", "csrc", "gemm.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timings (the reference arm and the cpu_baseline leg)
+# ----------------------------------------------------------------------------
+def oracle_sample(model: str, M: int, B: int, K_spec: int, target_s: float):
+    """Time the oracle on whole layers of the stack (plus the lm_head and one
+    acceptance row per sequence) until about target_s seconds of work.
+    Returns (bytes, seconds, rows_per_s, description, threads)."""
+    import oracle
+
+    oracle.build()
+    threads = oracle.default_threads()
+    shapes = workloads.stack_shapes(model)
+    layer = shapes[:4]
+    head = shapes[-1]
+    total_b, total_t, n_layers = 0, 0.0, 0
+    x_cache = {}
+    while True:
+        for li, (_, K, N) in enumerate(layer):
+            nib, sc = workloads.mxfp4_weights(N, K, *workloads.LLAMA_EXP_RANGE, seed=n_layers, tensor_id=li)
+            if K not in x_cache:
+                x_cache[K] = workloads.bf16_normal(M, K, seed=0, tensor_id=K)
+            t0 = time.perf_counter()
+            oracle.gemm(x_cache[K], nib, sc, nthreads=threads)
+            total_t += time.perf_counter() - t0
+            total_b += gemm_bytes(M, N, K)
+        n_layers += 1
+        if total_t >= target_s or n_layers >= 2:
+            break
+    # a slice of the lm_head rows
+    _, K, N = head
+    rows = max(1024, int(N * min(1.0, 0.25 * target_s / max(total_t, 1e-3))))
+    rows = min(rows, N)
+    nib, sc = workloads.mxfp4_weights(rows, K, *workloads.LLAMA_EXP_RANGE, seed=99, tensor_id=9)
+    t0 = time.perf_counter()
+    oracle.gemm(x_cache.get(K, workloads.bf16_normal(M, K, seed=0, tensor_id=K)), nib, sc, nthreads=threads)
+    total_t += time.perf_counter() - t0
+    total_b += gemm_bytes(M, rows, K)
+    # acceptance rows
+    V = workloads.VOCAB_LLAMA
+    p, q, d, u = workloads.spec_inputs(B, K_spec, V, seed=0, logit_std=2.0)
+    t0 = time.perf_counter()
+    _, n, _, _ = oracle.spec_accept(p, q, d, u, nthreads=threads)
+    ta = time.perf_counter() - t0
+    total_t += ta
+    total_b += accept_bytes(B, K_spec, V, n)
+    desc = (f"{n_layers} full layer(s) of 4 GEMMs + {rows} of {N} lm_head rows at M={M}, "
+            f"plus spec_accept over {B} row(s), V={V}")
+    return total_b, total_t, B / ta, desc, threads
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    model, B, K_spec = WORKLOADS[args.workload]
+    M = B * (K_spec + 1)
+    times, bytes_ = [], 0
+    desc, threads, rows_s = "", 1, 0.0
+    for it in range(args.warmup + args.steps):
+        b, t, rs, desc, threads = oracle_sample(model, M, B, K_spec, target_s=1.0)
+        if it >= args.warmup:
+            times.append(t)
+            bytes_ = b
+            rows_s = rs
+    t_step = statistics.mean(times)
+    value = bytes_ / t_step / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(args.workload, model, B, K_spec),
+        "cpu_baseline": {"value": value, "unit": "TB/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "spec_accept_rows_per_s": rows_s,
+        "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(name, model, B, K_spec):
+    shapes = workloads.stack_shapes(model)
+    M = B * (K_spec + 1)
+    wbytes = sum(N * K // 2 + N * K // 32 for _, K, N in shapes)
+    return {"workload": f"{name}: {model}-shaped verification step, {len(shapes)} MXFP4 GEMMs at "
+                        f"M={M} (B={B}, K_spec={K_spec}) + spec_accept V={workloads.VOCAB_LLAMA}",
+            "gemms": len(shapes), "M": M, "B": B, "K_spec": K_spec, "V": workloads.VOCAB_LLAMA,
+            "weight_bytes_per_step": wbytes,
+            "l2": "weights per step exceed the 129 MB L2 (each GEMM's W is read once): no flush"}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def run_mxs(args, world, rank, local):
+    import torch
+
+    import mxfp4_speculative_verification_gb300 as mxs
+
+    mxs.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    model, B, K_spec = WORKLOADS[args.workload]
+    M = B * (K_spec + 1)
+    V = workloads.VOCAB_LLAMA
+    shapes = workloads.stack_shapes(model)
+    lo, hi = workloads.LLAMA_EXP_RANGE
+
+    # resident weights, one distinct MXFP4 matrix per GEMM
+    weights = []
+    for i, (_, K, N) in enumerate(shapes):
+        weights.append(workloads.device_mxfp4_weights(N, K, lo, hi, seed=1000 * rank + i, device=dev))
+    ks = sorted({K for _, K, _ in shapes})
+    x_host = {K: torch.from_numpy(workloads.bf16_normal(M, K, seed=rank, tensor_id=K).view(np.int16))
+              .view(torch.bfloat16).pin_memory() for K in ks}
+    x_dev = {K: x_host[K].to(dev) for K in ks}
+    ys = {}
+    for _, K, N in shapes:
+        ys.setdefault(N, torch.empty((M, N), dtype=torch.float32, device=dev))
+    ws_bytes = max(mxs.mxfp4_verify_gemm_workspace_size(M, N, K) for _, K, N in shapes)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    p, q, d, u = workloads.spec_inputs(B, K_spec, V, seed=rank, logit_std=2.0)
+    acc_host = [torch.from_numpy(a).pin_memory() for a in (p, q, d, u)]
+    acc_dev = [a.to(dev) for a in acc_host]
+    out_tok = torch.empty((B, K_spec + 1), dtype=torch.int32, device=dev)
+    n_emit = torch.empty((B,), dtype=torch.int32, device=dev)
+    tok_host = torch.empty_like(out_tok, device="cpu").pin_memory()
+    n_host = torch.empty_like(n_emit, device="cpu").pin_memory()
+
+    def gemms():
+        for (_, K, N), (nib, sc) in zip(shapes, weights):
+            mxs.mxfp4_verify_gemm(x_dev[K], nib, sc, out=ys[N], workspace=ws)
+
+    def accept(reps=1):
+        for _ in range(reps):
+            mxs.spec_accept(*acc_dev, out_tokens=out_tok, n_emitted=n_emit)
+
+    def step():
+        gemms()
+        accept()
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        step()  # eager warm-up: kernel attributes, first launches
+        torch.cuda.synchronize(dev)
+        n_emitted = n_emit.cpu().numpy()
+        g_step, g_gemm, g_acc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        ACC_REPS = 20
+        with torch.cuda.graph(g_step, stream=stream):
+            step()
+        with torch.cuda.graph(g_gemm, stream=stream):
+            gemms()
+        with torch.cuda.graph(g_acc, stream=stream):
+            accept(ACC_REPS)
+    torch.cuda.synchronize(dev)
+
+    gemm_b = sum(gemm_bytes(M, N, K) for _, K, N in shapes)
+    acc_b = accept_bytes(B, K_spec, V, n_emitted)
+    step_b = gemm_b + acc_b
+
+    def timed(graph, steps):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                graph.replay()
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                torch.distributed.barrier()
+            ev0.record(stream)
+            for _ in range(steps):
+                graph.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = ev0.elapsed_time(ev1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms / steps
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms_step = timed(g_step, args.steps)
+    ms_gemm = timed(g_gemm, args.steps)
+    ms_acc = timed(g_acc, args.steps) / ACC_REPS
+    clk = clocks.stop()
+
+    # end to end through the public API: pinned host inputs in, tokens out
+    def e2e_step():
+        for K in ks:
+            x_dev[K].copy_(x_host[K], non_blocking=True)
+        for a_d, a_h in zip(acc_dev, acc_host):
+            a_d.copy_(a_h, non_blocking=True)
+        step()
+        tok_host.copy_(out_tok, non_blocking=True)
+        n_host.copy_(n_emit, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e2e_s = (time.perf_counter() - t0) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = sum(x_host[K].numel() * 2 for K in ks) + sum(a.numel() * a.element_size() for a in acc_host)
+    d2h = tok_host.numel() * 4 + n_host.numel() * 4
+
+    peak, peak_kind = load_peaks()
+    achieved_gbs = gemm_b / (ms_gemm * 1e-3) / 1e9
+    launches = len(shapes)
+    traffic = None
+    if GEMM_TRAFFIC_RATIO is not None and GEMM_TRAFFIC_SRC_SHA == src_sha():
+        traffic = GEMM_TRAFFIC_RATIO * gemm_b / launches
+
+    if args.detail and rank == 0:
+        per_shape_detail(mxs, torch, stream, dev, shapes, weights, x_dev, ys, ws, M)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        b, t, rs, desc, threads = oracle_sample(model, M, B, K_spec, target_s=args.cpu_seconds)
+        cpu = {"value": b / t / 1e12, "unit": "TB/s", "cores": threads, "kind": "oracle",
+               "sample": desc, "spec_accept_rows_per_s": rs}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    value = world * step_b / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32",
+        "compute": "E2M1 weights decoded exactly to fp16, X rows power-of-two scaled to fp16, "
+                   "fp16 tensor-core products, fp32 accumulation; acceptance predicate exact (f64)",
+        "data": "synthetic",
+        "config": config_block(args.workload, model, B, K_spec),
+        "pct_of_peak": value * 1e3 / peak / world,
+        "roofline": {"bound": "hbm", "kernel": "mxfp4_verify_gemm (prep + mxfp4_gemm_kernel)",
+                     "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": achieved_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "bytes_per_launch": gemm_b / launches, "launches_per_step": launches,
+                     "avg_launch_us": ms_gemm * 1e3 / launches, "traffic": traffic},
+        "spec_accept": {"rows_per_s": B / (ms_acc * 1e-3), "us_per_call": ms_acc * 1e3,
+                        "bytes_per_call": acc_b, "mean_emitted": float(np.mean(n_emitted))},
+        "e2e": {"value": world * step_b / e2e_s / 1e12, "unit": "TB/s",
+                "ms_per_step": e2e_s * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "public Python API -> C ABI, eager launches, pinned host copies"},
+        "gpu_launches": args.steps * (2 * len(shapes) + 1),
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def per_shape_detail(mxs, torch, stream, dev, shapes, weights, x_dev, ys, ws, M):
+    """Per-shape GEMM bandwidth (stderr), each shape timed over all its layers."""
+    seen = {}
+    for i, (name, K, N) in enumerate(shapes):
+        seen.setdefault((K, N), []).append(i)
+    for (K, N), idx in seen.items():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in idx:
+                    mxs.mxfp4_verify_gemm(x_dev[K], *weights[i], out=ys[N], workspace=ws)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            reps = 10
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / (reps * len(idx))
+        gbs = gemm_bytes(M, N, K) / (us * 1e-6) / 1e9
+        print(f"detail K={K} N={N} M={M}: {us:.2f} us/launch, {gbs:.0f} GB/s", file=sys.stderr)
+
+
+def profile_target(args):
+    """A few launches of one kernel, for ncu (no timing, no JSON)."""
+    import torch
+
+    import mxfp4_speculative_verification_gb300 as mxs
+
+    mxs.build()
+    dev = torch.device("cuda:0")
+    model, B, K_spec = WORKLOADS[args.workload]
+    M = B * (K_spec + 1)
+    if args.profile_gemm:
+        K, N = (int(v) for v in args.profile_gemm.split(","))
+        nib, sc = workloads.device_mxfp4_weights(N, K, *workloads.LLAMA_EXP_RANGE, seed=0, device=dev)
+        x = workloads.device_bf16_normal(M, K, seed=1, device=dev)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        for _ in range(4):
+            mxs.mxfp4_verify_gemm(x, nib, sc, out=y)
+    else:
+        V = workloads.VOCAB_LLAMA
+        p, q, d, u = (torch.from_numpy(a).to(dev) for a in workloads.spec_inputs(B, K_spec, V, seed=0))
+        for _ in range(4):
+            mxs.spec_accept(p, q, d, u)
+    torch.cuda.synchronize()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mxs", choices=["mxs", "reference"])
+    ap.add_argument("--workload", default="llama8b", choices=sorted(WORKLOADS))
+    ap.add_argument("--detail", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-gemm", metavar="K,N",
+                    help="only run one verify GEMM of this shape (M from --workload) 4 times "
+                         "and exit; a small target for ncu captures")
+    ap.add_argument("--profile-accept", action="store_true",
+                    help="only run spec_accept of the workload 4 times and exit (ncu target)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup(args)
+    if args.profile_gemm or args.profile_accept:
+        profile_target(args)
+        return
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_mxs(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+/*
+ * mxs.h -- C ABI of the MXFP4 speculative-verification library (libmxs.so).
+ *
+ * The library runs the target model's verification step of speculative
+ * decoding over OCP MX-FP4 weights on one GB300 (sm_103a):
+ *
+ *   mxfp4_pack         real weights -> E2M1 nibbles + E8M0 block scales
+ *   mxfp4_verify_gemm  Y[M,N] = X[M,K] . dequant(W)^T, bf16 X, fp32 Y
+ *   spec_accept        left-to-right acceptance, residual / bonus sampling,
+ *                      emission of 1..K+1 tokens per sequence
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *   allocates nothing and never synchronises: work is enqueued on `stream`
+ *   (a cudaStream_t passed as void*; NULL = the legacy default stream) and
+ *   the call returns after the launch.
+ * - Host-side validation happens before any launch.  A non-zero mxs_status
+ *   means nothing was enqueued.  MXS_ERR_CUDA reports a launch failure.
+ * - Conditions only the device can see are OR-ed, stream-ordered, into
+ *   `dev_status` (an int32 in device memory, nullable) as MXS_DEV_* bits.
+ *   The library never clears it; the caller zeroes it when it wants a fresh
+ *   reading.
+ * - Layouts are row-major and dense (no strides).
+ */
+#ifndef MXS_H_
+#define MXS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t mxs_status;
+
+#define MXS_OK 0
+#define MXS_ERR_INVALID_ARG 1   /* bad size, NULL pointer, K % 32 != 0, ... */
+#define MXS_ERR_MISALIGNED 2    /* a pointer misses its alignment rule     */
+#define MXS_ERR_UNSUPPORTED 3   /* size beyond a documented limit           */
+#define MXS_ERR_CUDA 4          /* a CUDA call or launch failed             */
+#define MXS_ERR_WORKSPACE 5     /* workspace NULL or smaller than required  */
+
+/* Device-side condition bits written to *dev_status. */
+#define MXS_DEV_BAD_DRAFT 0x1       /* spec_accept: a draft id outside [0,V)          */
+#define MXS_DEV_ZERO_Q 0x2          /* spec_accept: a proposal with q(x) = 0 (reject) */
+#define MXS_DEV_ZERO_RESIDUAL 0x4   /* spec_accept: residual mass 0, sampled p_j      */
+#define MXS_DEV_NO_LAW 0x8          /* spec_accept: the law to sample has no mass     */
+#define MXS_DEV_NEAR_EDGE 0x10      /* spec_accept: u within 1e-5 of a CDF bin edge   */
+#define MXS_DEV_NONFINITE 0x20      /* mxfp4_pack: a block held Inf or NaN            */
+#define MXS_DEV_TIMEOUT 0x40        /* a bounded pipeline wait gave up                */
+
+/* Input element types for mxfp4_pack. */
+#define MXS_F32 0
+#define MXS_BF16 1
+
+/* ------------------------------------------------------------------------
+ * mxfp4_pack
+ *
+ * Quantises real weights W [N, K] into the MXFP4 format used by
+ * mxfp4_verify_gemm.  Format ("Module 11. Speculative Decoding and
+ * Quantization", §12; "Next-Gen Speculative Decoding and FP4 Quantization
+ * Shake Up LLM Inference Economics", section "Microscaling FP4 (MX-FP4)
+ * Integration"): each run of 32 consecutive elements along K shares one E8M0
+ * scale byte e (value 2^(e-127)); each element is a 4-bit E2M1 code
+ * (sign | 2 exponent bits, bias 1 | 1 fraction bit; magnitudes
+ * 0,0.5,1,1.5,2,3,4,6), two codes per byte, element k in byte k/2 with even
+ * k in the low nibble.
+ *
+ * Rule per block: amax = max |w|; e_unb = the smallest integer with
+ * amax <= 6 * 2^e_unb, clamped to [-127, 127] (no element is clipped);
+ * an all-zero block gets e_unb = 0 (scale 1).  Each element becomes the
+ * E2M1 value nearest to w / 2^e_unb, ties to the even fraction bit, with the
+ * sign bit of w kept (so -0.0 and small negatives give code 8).
+ *
+ *   w        device, [N, K] fp32 (w_dtype MXS_F32) or bf16 (MXS_BF16),
+ *            4- or 2-byte aligned
+ *   nibbles  device, [N, K/2] uint8, written
+ *   scales   device, [N, K/32] uint8, written
+ *   N >= 0, K >= 0, K % 32 == 0
+ * A block holding Inf or NaN gets scale byte 255 and zero nibbles and sets
+ * MXS_DEV_NONFINITE.
+ * ---------------------------------------------------------------------- */
+mxs_status mxfp4_pack(const void* w, int32_t w_dtype, int64_t N, int64_t K,
+                      uint8_t* nibbles, uint8_t* scales, int32_t* dev_status,
+                      void* stream);
+
+/* ------------------------------------------------------------------------
+ * mxfp4_verify_gemm
+ *
+ * The weight-streaming GEMM of the verification pass: Y = X . dequant(W)^T,
+ *   Y[m, n] = sum_k x[m, k] * e2m1(W[n, k]) * 2^(S[n, k/32] - 127),
+ * with M = batch * (K_spec + 1) candidate positions ("Module 11 ...", §10:
+ * verification as a short, wider decode; the fp32 accumulation and the
+ * [rows, K/2] / [rows, K/32] layouts follow the MX-FP4 GEMV of "Next-Gen
+ * Speculative Decoding and FP4 Quantization ...").
+ *
+ *   x          device, [M, K] bf16 (raw bits as uint16), 2-byte aligned
+ *   nibbles    device, [N, K/2] uint8, 16-byte aligned
+ *   scales     device, [N, K/32] uint8 (any alignment; copied to the
+ *              workspace first when K % 512 != 0 or not 16-byte aligned)
+ *   y          device, [M, N] fp32, 4-byte aligned, written
+ *   1 <= M <= 65536, 1 <= N <= 4194240, 32 <= K <= 1048576, K % 32 == 0;
+ *              rows are processed 64 at a time, each group one pass over W
+ *   workspace  device, >= mxfp4_verify_gemm_workspace_size(M, N, K) bytes,
+ *              16-byte aligned; scratch for the converted X (and the
+ *              realigned scales).  Two calls in flight at the same time must
+ *              not share a workspace.  The scales need no workspace copy when
+ *              K % 512 == 0 and `scales` is 16-byte aligned; with K % 512 == 0
+ *              a misaligned `scales` is rejected (MXS_ERR_MISALIGNED) because
+ *              the size query assumed the in-place layout.
+ *
+ * Accuracy: products are exact; sums are fp32.  Each x row is scaled by a
+ * power of two so that its largest |x| lies in [2^15, 2^16) before it is
+ * rounded to fp16 for the tensor cores: exact for every element within 2^29
+ * of that row's largest magnitude.
+ * ---------------------------------------------------------------------- */
+size_t mxfp4_verify_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles,
+                             const uint8_t* scales, float* y, int64_t M,
+                             int64_t N, int64_t K, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_status,
+                             void* stream);
+
+/* ------------------------------------------------------------------------
+ * spec_accept
+ *
+ * Exact speculative acceptance for B sequences with K draft tokens each
+ * ("Module 11. Speculative Decoding and Quantization", §4 and §5):
+ *   for i = 0..K-1: accept draft x_i while u[b,i] * q_i(x_i) < p_i(x_i)
+ *   (the real-number comparison, exact; q_i(x_i) = 0 is a rejection);
+ *   at the first rejection j sample the replacement from the residual
+ *   r = (p_j - q_j)+ / sum (p_j - q_j)+, or, when all K were accepted
+ *   (j = K), sample the bonus token from p_K.  The sample uses u[b,K] by
+ *   inverse CDF: the smallest t with r_t > 0 and prefix_t > u[b,K] * S.
+ *   Emits draft x_0..x_{j-1} and the sampled token; n_emitted = j + 1.
+ *
+ *   p           device, [B, K+1, V] fp32, target laws (p[b,K] = bonus law)
+ *   q           device, [B, K, V] fp32, draft laws
+ *   draft       device, [B, K] int32, draft token ids
+ *   u           device, [B, K+1] fp32, uniforms in [0, 1)
+ *   out_tokens  device, [B, K+1] int32, written, -1 after the last token
+ *   n_emitted   device, [B] int32, written (0 for an error row)
+ *   row_flags   device, [B] int32 or NULL: per-row MXS_DEV_* bits
+ *   1 <= B < 2^31, 0 <= K <= 32, 1 <= V <= 2^21
+ * Laws are used as given, never renormalised.  A row whose draft ids are not
+ * all in [0, V) is an error row (n_emitted 0, tokens -1, MXS_DEV_BAD_DRAFT).
+ * A residual with no mass falls back to p_j (MXS_DEV_ZERO_RESIDUAL); a law
+ * with no finite positive mass gives an error row (MXS_DEV_NO_LAW).
+ * MXS_DEV_NEAR_EDGE marks rows whose u[b,K] lay within 1e-5 (relative to S)
+ * of an edge of the chosen bin, where the fp32 inputs' rounding may decide
+ * the token.
+ * ---------------------------------------------------------------------- */
+mxs_status spec_accept(const float* p, const float* q, const int32_t* draft,
+                       const float* u, int64_t B, int64_t K, int64_t V,
+                       int32_t* out_tokens, int32_t* n_emitted,
+                       int32_t* row_flags, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * mxs_hbm_read_probe -- measurement helper (not part of the method):
+ * streams `bytes` (multiple of 16) from `src` and writes a checksum to
+ * *sink (device uint64).  Used to report a read-only HBM roofline.
+ * ---------------------------------------------------------------------- */
+mxs_status mxs_hbm_read_probe(const void* src, size_t bytes, uint64_t* sink,
+                              void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* mxs_status_string(mxs_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t mxs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXS_H_ */

@@ -1,0 +1,203 @@
+"""Python binding of libmxs: MXFP4 speculative verification on GB300 (sm_103a).
+
+The three calls of the C ABI (``include/mxs.h``) under the same names:
+
+* :func:`mxfp4_pack` -- real weights -> E2M1 nibbles + E8M0 scales;
+* :func:`mxfp4_verify_gemm` -- Y = X . dequant(W)^T, bf16 X, fp32 Y;
+* :func:`spec_accept` -- acceptance, residual / bonus sampling, emission.
+
+This module only marshals arguments: it checks dtypes, shapes and devices,
+allocates the output tensors with torch, and passes raw device pointers and
+the current CUDA stream to the library.  Every step of the computation runs in
+the library's CUDA kernels; there is no CPU fallback.  If ``libmxs.so`` is
+missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+import torch
+
+from . import _build
+
+__all__ = ["build", "lib", "mxfp4_pack", "mxfp4_verify_gemm", "mxfp4_verify_gemm_workspace_size",
+           "spec_accept", "hbm_read_probe", "MxsError", "DEV_FLAGS", "declared_symbols"]
+
+MXS_F32, MXS_BF16 = 0, 1
+DEV_FLAGS = {
+    "BAD_DRAFT": 0x1, "ZERO_Q": 0x2, "ZERO_RESIDUAL": 0x4, "NO_LAW": 0x8,
+    "NEAR_EDGE": 0x10, "NONFINITE": 0x20, "TIMEOUT": 0x40,
+}
+
+_lib = None
+
+
+class MxsError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> Path:
+    """Compile the CUDA library in-tree (nvcc, sm_103a)."""
+    return _build.build(force=force)
+
+
+def declared_symbols() -> list[str]:
+    """Function names declared in include/mxs.h."""
+    text = (_build.INCLUDE / "mxs.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                      text, flags=re.M)
+
+
+def lib():
+    """The loaded libmxs.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not _build.LIB.exists():
+        raise MxsError(f"{_build.LIB} is not built; run mxfp4_speculative_verification_gb300.build()")
+    L = ctypes.CDLL(str(_build.LIB))
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+    L.mxfp4_pack.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp]
+    L.mxfp4_pack.restype = i32
+    L.mxfp4_verify_gemm_workspace_size.argtypes = [i64, i64, i64]
+    L.mxfp4_verify_gemm_workspace_size.restype = sz
+    L.mxfp4_verify_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, sz, vp, vp]
+    L.mxfp4_verify_gemm.restype = i32
+    L.spec_accept.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, vp, vp, vp]
+    L.spec_accept.restype = i32
+    L.mxs_hbm_read_probe.argtypes = [vp, sz, vp, vp]
+    L.mxs_hbm_read_probe.restype = i32
+    L.mxs_status_string.argtypes = [i32]
+    L.mxs_status_string.restype = ctypes.c_char_p
+    L.mxs_version.argtypes = []
+    L.mxs_version.restype = i32
+    _lib = L
+    return L
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise MxsError(lib().mxs_status_string(status).decode())
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need_cuda(*ts: torch.Tensor) -> torch.device:
+    dev = ts[0].device
+    for t in ts:
+        if t is None:
+            continue
+        if t.device.type != "cuda" or t.device != dev:
+            raise MxsError("all tensors must live on the same CUDA device")
+        if not t.is_contiguous():
+            raise MxsError("tensors must be contiguous")
+    return dev
+
+
+# ---------------------------------------------------------------- pack
+def mxfp4_pack(w: torch.Tensor, *, nibbles: torch.Tensor | None = None,
+               scales: torch.Tensor | None = None, dev_status: torch.Tensor | None = None):
+    """Pack W [N, K] (fp32 or bf16, K % 32 == 0) into (nibbles [N, K/2], scales [N, K/32])."""
+    if w.dim() != 2:
+        raise MxsError("w must be 2-D [N, K]")
+    N, K = w.shape
+    if w.dtype == torch.float32:
+        dt = MXS_F32
+    elif w.dtype == torch.bfloat16:
+        dt = MXS_BF16
+    else:
+        raise MxsError("w must be float32 or bfloat16")
+    if nibbles is None:
+        nibbles = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((N, K // 32), dtype=torch.uint8, device=w.device)
+    dev = _need_cuda(w, nibbles, scales, dev_status)
+    _check(lib().mxfp4_pack(_ptr(w), dt, N, K, _ptr(nibbles), _ptr(scales), _ptr(dev_status),
+                            _stream(dev)))
+    return nibbles, scales
+
+
+# ---------------------------------------------------------------- GEMM
+_workspaces: dict = {}
+
+
+def mxfp4_verify_gemm_workspace_size(M: int, N: int, K: int) -> int:
+    return int(lib().mxfp4_verify_gemm_workspace_size(M, N, K))
+
+
+def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def mxfp4_verify_gemm(x: torch.Tensor, nibbles: torch.Tensor, scales: torch.Tensor, *,
+                      out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                      dev_status: torch.Tensor | None = None) -> torch.Tensor:
+    """Y[M, N] (fp32) = X[M, K] (bf16) . dequant(W)^T for MXFP4 W ([N, K/2] + [N, K/32])."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise MxsError("x must be a 2-D bfloat16 tensor [M, K]")
+    if nibbles.dtype != torch.uint8 or scales.dtype != torch.uint8:
+        raise MxsError("nibbles and scales must be uint8")
+    M, K = x.shape
+    N = nibbles.shape[0]
+    if nibbles.shape != (N, K // 2) or scales.shape != (N, K // 32):
+        raise MxsError("W shapes must be [N, K/2] and [N, K/32]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    dev = _need_cuda(x, nibbles, scales, out, workspace, dev_status)
+    need = mxfp4_verify_gemm_workspace_size(M, N, K)
+    if need == 0:
+        raise MxsError("unsupported GEMM shape")
+    if workspace is None:
+        workspace = _workspace(dev, need)
+    _check(lib().mxfp4_verify_gemm(_ptr(x), _ptr(nibbles), _ptr(scales), _ptr(out), M, N, K,
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _ptr(dev_status), _stream(dev)))
+    return out
+
+
+# ---------------------------------------------------------- acceptance
+def spec_accept(p: torch.Tensor, q: torch.Tensor, draft: torch.Tensor, u: torch.Tensor, *,
+                out_tokens: torch.Tensor | None = None, n_emitted: torch.Tensor | None = None,
+                row_flags: torch.Tensor | None = None, dev_status: torch.Tensor | None = None):
+    """Speculative acceptance for B rows.
+
+    p [B, K+1, V] fp32, q [B, K, V] fp32, draft [B, K] int32, u [B, K+1] fp32.
+    Returns (out_tokens [B, K+1] int32, n_emitted [B] int32).
+    """
+    if p.dtype != torch.float32 or q.dtype != torch.float32 or u.dtype != torch.float32:
+        raise MxsError("p, q and u must be float32")
+    if draft.dtype != torch.int32:
+        raise MxsError("draft must be int32")
+    B, K1, V = p.shape
+    K = K1 - 1
+    if q.shape != (B, K, V) or draft.shape != (B, K) or u.shape != (B, K + 1):
+        raise MxsError("shape mismatch: p [B,K+1,V], q [B,K,V], draft [B,K], u [B,K+1]")
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=p.device)
+    if n_emitted is None:
+        n_emitted = torch.empty((B,), dtype=torch.int32, device=p.device)
+    dev = _need_cuda(p, q, draft, u, out_tokens, n_emitted, row_flags, dev_status)
+    _check(lib().spec_accept(_ptr(p), _ptr(q), _ptr(draft), _ptr(u), B, K, V, _ptr(out_tokens),
+                             _ptr(n_emitted), _ptr(row_flags), _ptr(dev_status), _stream(dev)))
+    return out_tokens, n_emitted
+
+
+def hbm_read_probe(src: torch.Tensor, sink: torch.Tensor) -> None:
+    """Stream ``src`` once (read-only HBM roofline measurement)."""
+    dev = _need_cuda(src, sink)
+    _check(lib().mxs_hbm_read_probe(_ptr(src), src.numel() * src.element_size() // 16 * 16,
+                                    _ptr(sink), _stream(dev)))

@@ -1,0 +1,379 @@
+// spec_accept on sm_103a: exact left-to-right acceptance, residual or bonus
+// sampling and emission of 1..K+1 tokens per sequence.
+//
+// Operation: "Module 11. Speculative Decoding and Quantization", §4 (accept
+// x_i with probability min(1, p_i(x_i)/q_i(x_i)) from left to right; at the
+// first rejection draw the replacement from norm((p - q)+); when every
+// proposal survives draw the bonus token from the next position's law) and
+// §5 (block B18: the draw is accepted iff draw < acceptance, acceptance 0
+// where q = 0).  The page-3 diagram of "Next-Gen Speculative Decoding and FP4
+// Quantization ..." names this step the "Parallel Softmax & Acceptance
+// Evaluation Mask" of the batched verification kernel.
+//
+// One CTA (1024 threads) per sequence:
+//  * warp 0 gathers p_i(x_i), q_i(x_i), u_i for the K drafts, tests
+//    u*q < p exactly (an fp32 x fp32 product is exact in double) and finds the
+//    first rejection j with one ballot;
+//  * all 32 warps stream the one law that is sampled (residual row j, or p_K),
+//    128 elements per warp step with float4 loads, forming fp32 sums of each
+//    128-element sub-tile (warp shuffle tree) in shared memory;
+//  * a block-wide double scan over the sub-tile sums gives S and the sub-tile
+//    where the CDF crosses u_K * S; warp 0 rescans that sub-tile in double to
+//    find the token: the smallest t with r_t > 0 and C_t > u_K * S.
+#include <climits>
+
+#include "mxs_device.cuh"
+#include "mxs_internal.h"
+
+namespace mxs {
+
+constexpr int kAcceptThreads = 1024;
+constexpr int kAcceptWarps = kAcceptThreads / 32;
+constexpr int kSubTile = 128;  // elements per warp step (float4 per lane)
+constexpr double kNearEdge = 1e-5;
+
+struct AcceptParams {
+    const float* p;
+    const float* q;
+    const int32_t* draft;
+    const float* u;
+    int64_t V;
+    int K;
+    int nsub;  // ceil(V / kSubTile)
+    int32_t* out_tokens;
+    int32_t* n_emitted;
+    int32_t* row_flags;
+    int32_t* status;
+};
+
+// Residual (or bonus) mass of 4 consecutive elements starting at e.
+template <bool VEC>
+__device__ __forceinline__ void load_law4(const float* __restrict__ prow,
+                                          const float* __restrict__ qrow, bool use_res, int64_t e,
+                                          int64_t V, float (&r)[4]) {
+    if (VEC && e + 3 < V) {
+        const float4 pv = __ldcs(reinterpret_cast<const float4*>(prow + e));
+        float4 qv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (use_res) qv = __ldcs(reinterpret_cast<const float4*>(qrow + e));
+        if (use_res) {
+            r[0] = fmaxf(pv.x - qv.x, 0.f);
+            r[1] = fmaxf(pv.y - qv.y, 0.f);
+            r[2] = fmaxf(pv.z - qv.z, 0.f);
+            r[3] = fmaxf(pv.w - qv.w, 0.f);
+        } else {
+            r[0] = pv.x; r[1] = pv.y; r[2] = pv.z; r[3] = pv.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float v = 0.f;
+            if (e + i < V) {
+                const float pv = prow[e + i];
+                v = use_res ? fmaxf(pv - qrow[e + i], 0.f) : pv;
+            }
+            r[i] = v;
+        }
+    }
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Inclusive warp scan (double).
+__device__ __forceinline__ double warp_scan_d(double v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+// Stream the law once: per-sub-tile fp32 sums into subsum[], and the last
+// index with positive mass into *lastpos.
+template <bool VEC>
+__device__ void sum_pass(const float* __restrict__ prow, const float* __restrict__ qrow,
+                         bool use_res, int64_t V, int nsub, float* subsum, int* lastpos) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int lp = -1;
+    constexpr int U = 4;
+    for (int st0 = warp; st0 < nsub; st0 += U * kAcceptWarps) {
+        float r[U][4];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int st = st0 + k * kAcceptWarps;
+            if (st < nsub) {
+                load_law4<VEC>(prow, qrow, use_res, int64_t(st) * kSubTile + 4 * lane, V, r[k]);
+            } else {
+                r[k][0] = r[k][1] = r[k][2] = r[k][3] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int st = st0 + k * kAcceptWarps;
+            if (st >= nsub) break;
+            const float s = warp_sum_f((r[k][0] + r[k][1]) + (r[k][2] + r[k][3]));
+            if (lane == 0) subsum[st] = s;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (r[k][i] > 0.f) lp = max(lp, st * kSubTile + 4 * lane + i);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+    if (lane == 0 && lp >= 0) atomicMax(lastpos, lp);
+}
+
+// S = sum of the sub-tile sums, in a fixed order (thread-strided, then tree).
+__device__ double block_total(const float* subsum, int nsub, double* wtot) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    double s = 0.0;
+    for (int i = threadIdx.x; i < nsub; i += kAcceptThreads) s += double(subsum[i]);
+    s = warp_sum_d(s);
+    if (lane == 0) wtot[warp] = s;
+    __syncthreads();
+    double S = 0.0;
+    for (int w = 0; w < kAcceptWarps; ++w) S += wtot[w];
+    __syncthreads();
+    return S;
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kAcceptThreads) spec_accept_kernel(const AcceptParams P) {
+    extern __shared__ float subsum[];
+    __shared__ double wtot[kAcceptWarps];
+    __shared__ double sh_prefix;
+    __shared__ int sh_j, sh_flags, sh_err, sh_lastpos, sh_tstar;
+
+    const int64_t b = blockIdx.x;
+    const int K = P.K;
+    const int64_t V = P.V;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---------------------------------------------- acceptance (warp 0)
+    if (warp == 0) {
+        const bool active = lane < K;
+        const int x = active ? P.draft[b * K + lane] : 0;
+        const bool bad = active && (x < 0 || int64_t(x) >= V);
+        const unsigned badm = __ballot_sync(0xffffffffu, bad);
+        int j = K, flags = 0;
+        if (badm) {
+            flags = MXS_DEV_BAD_DRAFT;
+        } else {
+            bool rej = false, zq = false;
+            if (active) {
+                const float qx = P.q[(b * K + lane) * V + x];
+                const float px = P.p[(b * (K + 1) + lane) * V + x];
+                const float ui = P.u[b * (K + 1) + lane];
+                if (qx > 0.f) {
+                    rej = !(double(ui) * double(qx) < double(px));
+                } else {
+                    rej = true;
+                    zq = true;
+                }
+            }
+            const unsigned rm = __ballot_sync(0xffffffffu, rej);
+            const unsigned zm = __ballot_sync(0xffffffffu, zq);
+            if (rm) {
+                j = __ffs(int(rm)) - 1;
+                if ((zm >> j) & 1u) flags |= MXS_DEV_ZERO_Q;
+            }
+        }
+        if (lane == 0) {
+            sh_j = j;
+            sh_flags = flags;
+            sh_err = badm ? 1 : 0;
+            sh_lastpos = -1;
+            sh_tstar = INT_MAX;
+        }
+    }
+    __syncthreads();
+
+    const int j = sh_j;
+    int32_t* tok = P.out_tokens + b * (K + 1);
+    if (sh_err) {
+        if (threadIdx.x <= K) tok[threadIdx.x] = -1;
+        if (threadIdx.x == 0) {
+            P.n_emitted[b] = 0;
+            if (P.row_flags) P.row_flags[b] = sh_flags;
+            report(P.status, sh_flags);
+        }
+        return;
+    }
+
+    // --------------------------------------- the law: residual or bonus
+    bool use_res = j < K;
+    const float* prow = P.p + (b * (K + 1) + j) * V;
+    const float* qrow = use_res ? P.q + (b * K + j) * V : nullptr;
+    sum_pass<VEC>(prow, qrow, use_res, V, P.nsub, subsum, &sh_lastpos);
+    __syncthreads();
+    double S = block_total(subsum, P.nsub, wtot);
+    if (!(S > 0.0)) {
+        // A positive residual exists whenever rejection is possible; only the
+        // rounding of the inputs gets here.  Sample p_j instead.
+        if (threadIdx.x == 0) {
+            sh_flags |= MXS_DEV_ZERO_RESIDUAL;
+            sh_lastpos = -1;
+        }
+        __syncthreads();
+        use_res = false;
+        sum_pass<VEC>(prow, nullptr, false, V, P.nsub, subsum, &sh_lastpos);
+        __syncthreads();
+        S = block_total(subsum, P.nsub, wtot);
+    }
+    if (!(S > 0.0) || isinf(S) || isnan(S)) {
+        if (threadIdx.x <= K) tok[threadIdx.x] = -1;
+        if (threadIdx.x == 0) {
+            const int f = sh_flags | MXS_DEV_NO_LAW;
+            P.n_emitted[b] = 0;
+            if (P.row_flags) P.row_flags[b] = f;
+            report(P.status, f);
+        }
+        return;
+    }
+    const double uK = double(P.u[b * (K + 1) + K]);
+    const double thr = uK * S;
+
+    // --------------------------- locate the sub-tile where C crosses thr
+    {
+        const int per = (P.nsub + kAcceptThreads - 1) / kAcceptThreads;
+        const int s0 = min(P.nsub, int(threadIdx.x) * per);
+        const int s1 = min(P.nsub, s0 + per);
+        double local = 0.0;
+        for (int st = s0; st < s1; ++st) local += double(subsum[st]);
+        const double inc = warp_scan_d(local, lane);
+        if (lane == 31) wtot[warp] = inc;
+        __syncthreads();
+        if (warp == 0) {
+            const double wt = wtot[lane];
+            const double winc = warp_scan_d(wt, lane);
+            wtot[lane] = winc - wt;  // exclusive prefix of warp totals
+        }
+        __syncthreads();
+        double run = wtot[warp] + (inc - local);
+        for (int st = s0; st < s1; ++st) {
+            const float s = subsum[st];
+            const double end = run + double(s);
+            if (s > 0.f && end > thr) {
+                atomicMin(&sh_tstar, st);
+                break;
+            }
+            run = end;
+        }
+        __syncthreads();
+        // the owner of the first crossing publishes its starting prefix
+        run = wtot[warp] + (inc - local);
+        for (int st = s0; st < s1; ++st) {
+            if (st == sh_tstar) sh_prefix = run;
+            run += double(subsum[st]);
+        }
+        __syncthreads();
+    }
+
+    // ------------------------------ warp 0: exact position in the sub-tile
+    if (warp == 0) {
+        int pick = -1;
+        double before = 0.0, after = 0.0;
+        if (sh_tstar != INT_MAX) {
+            double run = sh_prefix;
+            for (int st = sh_tstar; st < P.nsub && pick < 0; ++st) {
+                float r[4];
+                load_law4<VEC>(prow, qrow, use_res, int64_t(st) * kSubTile + 4 * lane, V, r);
+                double c[4];
+                c[0] = double(r[0]);
+                c[1] = c[0] + double(r[1]);
+                c[2] = c[1] + double(r[2]);
+                c[3] = c[2] + double(r[3]);
+                const double lane_inc = warp_scan_d(c[3], lane);
+                const double base = run + (lane_inc - c[3]);
+                int first = 4;
+#pragma unroll
+                for (int i = 3; i >= 0; --i)
+                    if (r[i] > 0.f && base + c[i] > thr) first = i;
+                const unsigned hit = __ballot_sync(0xffffffffu, first < 4);
+                if (hit) {
+                    const int L = __ffs(int(hit)) - 1;
+                    const int fi = __shfl_sync(0xffffffffu, first, L);
+                    const double cb = __shfl_sync(0xffffffffu, base, L);
+                    double ci = 0.0, ri = 0.0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (i == fi) { ci = c[i]; ri = double(r[i]); }
+                    ci = __shfl_sync(0xffffffffu, ci, L);
+                    ri = __shfl_sync(0xffffffffu, ri, L);
+                    pick = st * kSubTile + 4 * L + fi;
+                    after = cb + ci;
+                    before = after - ri;
+                }
+                run += __shfl_sync(0xffffffffu, lane_inc, 31);
+            }
+        }
+        if (pick < 0) {
+            // rounding put u*S at or beyond the last positive mass
+            pick = sh_lastpos;
+            float rl[4];
+            const int64_t e = int64_t(pick) & ~int64_t(3);
+            load_law4<false>(prow, qrow, use_res, e, V, rl);
+            after = S;
+            before = S - double(rl[pick - e]);
+        }
+        if (lane == 0) {
+            int flags = sh_flags;
+            const double d0 = fabs(uK - before / S), d1 = fabs(uK - after / S);
+            if (fmin(d0, d1) < kNearEdge) flags |= MXS_DEV_NEAR_EDGE;
+            tok[j] = pick;
+            P.n_emitted[b] = j + 1;
+            if (P.row_flags) P.row_flags[b] = flags;
+            report(P.status, flags);
+        }
+    }
+    // emitted drafts, then padding
+    for (int i = threadIdx.x; i <= K; i += blockDim.x) {
+        if (i < j) tok[i] = P.draft[b * K + i];
+        else if (i > j) tok[i] = -1;
+    }
+}
+
+cudaError_t accept_run(const float* p, const float* q, const int32_t* draft, const float* u,
+                       int64_t B, int64_t K, int64_t V, int32_t* out_tokens, int32_t* n_emitted,
+                       int32_t* row_flags, int32_t* dev_status, cudaStream_t stream) {
+    AcceptParams P{};
+    P.p = p;
+    P.q = q;
+    P.draft = draft;
+    P.u = u;
+    P.V = V;
+    P.K = int(K);
+    P.nsub = int((V + kSubTile - 1) / kSubTile);
+    P.out_tokens = out_tokens;
+    P.n_emitted = n_emitted;
+    P.row_flags = row_flags;
+    P.status = dev_status;
+    const bool vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
+                     (K == 0 || reinterpret_cast<uintptr_t>(q) % 16 == 0);
+    const size_t smem = size_t(P.nsub) * sizeof(float);
+    cudaError_t err;
+    if (vec) {
+        err = cudaFuncSetAttribute(spec_accept_kernel<true>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (err != cudaSuccess) return err;
+        spec_accept_kernel<true><<<unsigned(B), kAcceptThreads, smem, stream>>>(P);
+    } else {
+        err = cudaFuncSetAttribute(spec_accept_kernel<false>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (err != cudaSuccess) return err;
+        spec_accept_kernel<false><<<unsigned(B), kAcceptThreads, smem, stream>>>(P);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace mxs

@@ -1,0 +1,95 @@
+// The C ABI of libmxs (declared in include/mxs.h): host-side validation,
+// then the launchers in gemm.cu, accept.cu and pack.cu.
+#include <cstdint>
+
+#include "mxs.h"
+#include "mxs_internal.h"
+
+namespace {
+
+constexpr int64_t kMaxM = 65536;
+constexpr int64_t kMaxN = 65535 * 64;
+constexpr int64_t kMaxK = 1 << 20;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+mxs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MXS_OK : MXS_ERR_CUDA; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+mxs_status mxfp4_pack(const void* w, int32_t w_dtype, int64_t N, int64_t K, uint8_t* nibbles,
+                      uint8_t* scales, int32_t* dev_status, void* stream) {
+    if (N < 0 || K < 0 || K % 32 != 0) return MXS_ERR_INVALID_ARG;
+    if (w_dtype != MXS_F32 && w_dtype != MXS_BF16) return MXS_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return MXS_OK;
+    if (!w || !nibbles || !scales) return MXS_ERR_INVALID_ARG;
+    if (N > (int64_t(1) << 40) / K) return MXS_ERR_UNSUPPORTED;
+    if (!aligned(w, w_dtype == MXS_F32 ? 4 : 2) || !aligned(dev_status, 4))
+        return MXS_ERR_MISALIGNED;
+    return cuda_status(
+        mxs::pack_run(w, w_dtype, N, K, nibbles, scales, dev_status, as_stream(stream)));
+}
+
+size_t mxfp4_verify_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (M < 1 || N < 1 || K < 32 || K % 32 != 0 || M > kMaxM || N > kMaxN || K > kMaxK) return 0;
+    // the in-place scale layout is assumed when K % 512 == 0
+    return mxs::gemm_workspace_layout(M, N, K, true).bytes;
+}
+
+mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles, const uint8_t* scales,
+                             float* y, int64_t M, int64_t N, int64_t K, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    if (!x || !nibbles || !scales || !y) return MXS_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return MXS_ERR_INVALID_ARG;
+    if (M > kMaxM || N > kMaxN || K > kMaxK) return MXS_ERR_UNSUPPORTED;
+    if (!aligned(x, 2) || !aligned(nibbles, 16) || !aligned(y, 4) || !aligned(dev_status, 4))
+        return MXS_ERR_MISALIGNED;
+    const bool sc_aligned = aligned(scales, 16);
+    if (K % 512 == 0 && !sc_aligned) return MXS_ERR_MISALIGNED;
+    const mxs::GemmWorkspace ws = mxs::gemm_workspace_layout(M, N, K, sc_aligned);
+    if (!workspace || workspace_bytes < ws.bytes) return MXS_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return MXS_ERR_MISALIGNED;
+    return cuda_status(mxs::gemm_run(static_cast<const uint16_t*>(x), nibbles, scales, y, M, N, K,
+                                     workspace, ws, dev_status, as_stream(stream)));
+}
+
+mxs_status spec_accept(const float* p, const float* q, const int32_t* draft, const float* u,
+                       int64_t B, int64_t K, int64_t V, int32_t* out_tokens, int32_t* n_emitted,
+                       int32_t* row_flags, int32_t* dev_status, void* stream) {
+    if (B < 1 || K < 0 || V < 1) return MXS_ERR_INVALID_ARG;
+    if (B > INT32_MAX || K > mxs::kAcceptMaxK || V > mxs::kAcceptMaxV) return MXS_ERR_UNSUPPORTED;
+    if (!p || !u || !out_tokens || !n_emitted) return MXS_ERR_INVALID_ARG;
+    if (K > 0 && (!q || !draft)) return MXS_ERR_INVALID_ARG;
+    if (!aligned(p, 4) || !aligned(q, 4) || !aligned(draft, 4) || !aligned(u, 4) ||
+        !aligned(out_tokens, 4) || !aligned(n_emitted, 4) || !aligned(row_flags, 4) ||
+        !aligned(dev_status, 4))
+        return MXS_ERR_MISALIGNED;
+    return cuda_status(mxs::accept_run(p, q, draft, u, B, K, V, out_tokens, n_emitted, row_flags,
+                                       dev_status, as_stream(stream)));
+}
+
+mxs_status mxs_hbm_read_probe(const void* src, size_t bytes, uint64_t* sink, void* stream) {
+    if (!src || !sink || bytes == 0 || bytes % 16 != 0) return MXS_ERR_INVALID_ARG;
+    if (!aligned(src, 16) || !aligned(sink, 8)) return MXS_ERR_MISALIGNED;
+    return cuda_status(mxs::hbm_read_probe_run(src, bytes, sink, as_stream(stream)));
+}
+
+const char* mxs_status_string(mxs_status status) {
+    switch (status) {
+        case MXS_OK: return "MXS_OK";
+        case MXS_ERR_INVALID_ARG: return "MXS_ERR_INVALID_ARG";
+        case MXS_ERR_MISALIGNED: return "MXS_ERR_MISALIGNED";
+        case MXS_ERR_UNSUPPORTED: return "MXS_ERR_UNSUPPORTED";
+        case MXS_ERR_CUDA: return "MXS_ERR_CUDA";
+        case MXS_ERR_WORKSPACE: return "MXS_ERR_WORKSPACE";
+        default: return "MXS_ERR_UNKNOWN";
+    }
+}
+
+int32_t mxs_version(void) { return 100; }
+
+}  // extern "C"

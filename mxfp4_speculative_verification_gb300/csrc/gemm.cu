@@ -1,0 +1,688 @@
+// mxfp4_verify_gemm on sm_103a: Y[M,N] = X[M,K] . dequant(W)^T.
+//
+// Operation: "Module 11. Speculative Decoding and Quantization", §10 (the
+// verification pass is a short, wider decode whose cost is the weight read,
+// §1) over MX-FP4 weights (§12; packed [rows, K/2] nibbles + [rows, K/32]
+// E8M0 scales with fp32 accumulation as in the MX-FP4 GEMV of "Next-Gen
+// Speculative Decoding and FP4 Quantization Shake Up LLM Inference
+// Economics").
+//
+// Design (HBM-bound for M <= 64: every weight byte is read exactly once):
+//  * a preparation kernel turns X [M, K] bf16 into fp16 tensor-core
+//    fragments (each row scaled by a power of two so that it fits fp16
+//    exactly), zeroes the split-K counters and, when needed, realigns the
+//    scale rows;
+//  * the main kernel is persistent: each CTA walks a list of work items
+//    (a tile of BN weight rows x one K range) and streams them through one
+//    continuous shared-memory ring, so the pipeline never drains between
+//    tiles.  One producer thread issues per 512-k stage two 2-D TMA tensor
+//    copies of nibbles (128-byte swizzle, evict-first), one of scales and
+//    one bulk copy of the stage's X fragments, all completing on one
+//    mbarrier.  Consumer warps each own 16 weight rows: ldmatrix fetches
+//    nibbles, the hardware E2M1->fp16 conversion decodes them, and
+//    mma.sync m16n8k16 multiplies (weights = MMA rows, candidate positions =
+//    MMA columns).  Each 16 x 32 block is accumulated separately and scaled
+//    in fp32 by its E8M0 scale, so the block scale is exact for every
+//    exponent;
+//  * when K is split, each work item writes its partial tile to the
+//    workspace and bumps a per-tile counter; the item that completes the
+//    count sums all partials in split order (deterministic) and writes Y.
+#include <cuda.h>  // CUtensorMap and the tensor-map enums (types only)
+
+#include <algorithm>
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+
+#include <cuda_fp16.h>
+
+#include "mxs_device.cuh"
+#include "mxs_internal.h"
+
+namespace mxs {
+
+constexpr int kMaxDevices = 64;
+constexpr int kStageBlocks = 16;                 // 16 MX blocks = 512 k per stage
+constexpr int kBoxBytes = 128;                   // inner extent of one nibble box (256 k)
+constexpr int kFragBytesPerBlockTile = 512;      // one 32-k block x 8 rows of X as fp16 fragments
+constexpr int kMaxSplit = 32;
+constexpr int64_t kMaxSplitItems = 2048;         // bound on tiles x splits when K is split
+
+struct GemmParams {
+    const uint16_t* xf;  // fragments [nblk][NT][32 lanes][8 fp16]
+    const float* xun;    // [8*NT] per-row unscale
+    float* y;            // [M, N]
+    float* part;         // split-K partial tiles [items][M][BN]
+    int* counters;       // split-K arrival counters [ntiles]
+    int64_t N;
+    int M;
+    int nblk;            // K / 32
+    int ntiles;
+    int nsplit;
+    int stages_per_split;
+    int items;           // ntiles * nsplit
+    int sc_from_prep;    // scales were realigned by the preparation kernel
+    int32_t* status;
+};
+
+template <int NT, int NWC, int STAGES>
+struct GemmCfg {
+    static constexpr int BN = 16 * NWC;
+    static constexpr int kConsumers = 32 * NWC;
+    static constexpr int kThreads = kConsumers + 32;
+    static constexpr int kBoxW = BN * kBoxBytes;            // one nibble box
+    static constexpr int kWBytes = 2 * kBoxW;
+    static constexpr int kSBytes = BN * 16;
+    static constexpr int kXBytes = kStageBlocks * NT * kFragBytesPerBlockTile;
+    static constexpr int kStageBytes = kWBytes + kSBytes + kXBytes;
+    static constexpr int kPartPitch = 8 * NT + 1;            // floats per row of the partial tile
+    static constexpr int kPartOffset = STAGES * kStageBytes;
+    static constexpr int kBarOffset = kPartOffset + ((BN * kPartPitch * 4 + 15) / 16) * 16;
+    static constexpr int kMiscOffset = kBarOffset + 2 * STAGES * 8;
+    static constexpr int kSmemBytes = kMiscOffset + 16 + 1024;  // + alignment slack
+    static_assert(kStageBytes % 1024 == 0, "128-byte swizzled boxes need 1 KB aligned stages");
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1, const float (&c)[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%10, %11, %12, %13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+          "f"(c[3]));
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                       uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void consumer_bar(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// One stage of 16 blocks (or the first nb of them) for one consumer warp.
+// lm[j]: swizzled byte offset of this lane's ldmatrix row chunk for block
+// pair j (j = 0..3 inside a nibble box; box 1 is BOXW bytes further).
+template <int NT, int BOXW, bool FULL>
+__device__ __forceinline__ void consume_stage(float (&acc)[NT][4], uint32_t w_row,
+                                              const uint32_t (&lm)[4], uint4 sg, uint4 sg8,
+                                              const uint4* __restrict__ xs, int lane, int nb) {
+    const uint32_t sgw[4] = {sg.x, sg.y, sg.z, sg.w};
+    const uint32_t sg8w[4] = {sg8.x, sg8.y, sg8.z, sg8.w};
+    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int bp = 0; bp < kStageBlocks / 2; ++bp) {
+        if (!FULL && 2 * bp >= nb) break;
+        uint32_t r0, r1, r2, r3;
+        // r0: rows 0-7 blk 2bp, r1: rows 8-15 blk 2bp, r2/r3: blk 2bp+1
+        ldmatrix_x4(w_row + (bp >> 2) * BOXW + lm[bp & 3], r0, r1, r2, r3);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int blk = 2 * bp + h;
+            if (!FULL && blk >= nb) break;
+            uint32_t ag[4], ag8[4];
+            e2m1x8_to_f16x2x4(h ? r2 : r0, ag[0], ag[1], ag[2], ag[3]);
+            e2m1x8_to_f16x2x4(h ? r3 : r1, ag8[0], ag8[1], ag8[2], ag8[3]);
+            const uint32_t sel = (blk & 3) | ((4 + (blk & 3)) << 4);
+            float s_g, s_g8;
+            e8m0x2_to_f32x2(__byte_perm(sgw[blk >> 2], sg8w[blk >> 2], sel), s_g, s_g8);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint4 xv = xs[(blk * NT + nt) * 32 + lane];
+                float d[4];
+                mma_16816(d, ag[0], ag8[0], ag[1], ag8[1], xv.x, xv.y, zero);
+                mma_16816(d, ag[2], ag8[2], ag[3], ag8[3], xv.z, xv.w, d);
+                acc[nt][0] = fmaf(d[0], s_g, acc[nt][0]);
+                acc[nt][1] = fmaf(d[1], s_g, acc[nt][1]);
+                acc[nt][2] = fmaf(d[2], s_g8, acc[nt][2]);
+                acc[nt][3] = fmaf(d[3], s_g8, acc[nt][3]);
+            }
+        }
+    }
+}
+
+struct ItemRange {
+    int tile, split, kb0, kb1, nst;
+};
+
+__device__ __forceinline__ ItemRange item_range(const GemmParams& P, int w) {
+    ItemRange r;
+    r.tile = w % P.ntiles;
+    r.split = w / P.ntiles;
+    r.kb0 = r.split * P.stages_per_split * kStageBlocks;
+    r.kb1 = min(P.nblk, r.kb0 + P.stages_per_split * kStageBlocks);
+    r.nst = r.kb1 > r.kb0 ? (r.kb1 - r.kb0 + kStageBlocks - 1) / kStageBlocks : 0;
+    return r;
+}
+
+template <int NT, int NWC, int STAGES>
+__global__ void __launch_bounds__(32 * (NWC + 1))
+    mxfp4_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
+                      const __grid_constant__ CUtensorMap tm_s, const GemmParams P) {
+    using C = GemmCfg<NT, NWC, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte-swizzled TMA destinations need 1 KB alignment
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
+    uint8_t* smem = smem_raw + pad;
+    const uint32_t smem_base = raw_base + pad;
+    const uint32_t full_bar = smem_base + C::kBarOffset;
+    const uint32_t empty_bar = full_bar + STAGES * 8;
+    float* part = reinterpret_cast<float*>(smem + C::kPartOffset);
+    int* sh_last = reinterpret_cast<int*>(smem + C::kMiscOffset);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar + 8 * s, 1);
+            mbar_init(empty_bar + 8 * s, NWC);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    pdl_trigger();
+
+    if (warp == NWC) {
+        // ------------------------------------------------------- producer
+        if (lane != 0) return;
+        prefetch_tmap(&tm_w);
+        prefetch_tmap(&tm_s);
+        const uint64_t pol_w = policy_evict_first();
+        const uint64_t pol_x = policy_evict_last();
+        // copies that depend on the preparation kernel are deferred until
+        // the first STAGES stages of weights are in flight
+        int def_slot[STAGES], def_kb[STAGES], def_nb[STAGES], def_n0[STAGES];
+        int ndef = 0;
+        bool waited = false;
+        auto issue_dep = [&](int slot, int kb, int nb, int n0) {
+            const uint32_t stage = smem_base + slot * C::kStageBytes;
+            const uint32_t bar = full_bar + 8 * slot;
+            if (P.sc_from_prep) tma_2d(stage + C::kWBytes, &tm_s, kb, n0, bar, pol_w);
+            bulk_g2s(stage + C::kWBytes + C::kSBytes,
+                     P.xf + int64_t(kb) * NT * (kFragBytesPerBlockTile / 2),
+                     uint32_t(nb) * NT * kFragBytesPerBlockTile, bar, pol_x);
+        };
+        int it = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; ok && w < P.items; w += gridDim.x) {
+            const ItemRange R = item_range(P, w);
+            const int n0 = R.tile * C::BN;
+            for (int i = 0; i < R.nst; ++i, ++it) {
+                const int slot = it % STAGES;
+                if (it >= STAGES &&
+                    !mbar_wait(empty_bar + 8 * slot, ((it / STAGES) - 1) & 1, P.status)) {
+                    ok = false;
+                    break;
+                }
+                const int kb = R.kb0 + i * kStageBlocks;
+                const int nb = min(kStageBlocks, R.kb1 - kb);
+                const uint32_t stage = smem_base + slot * C::kStageBytes;
+                const uint32_t bar = full_bar + 8 * slot;
+                mbar_arrive_expect_tx(bar, uint32_t(C::kWBytes + C::kSBytes) +
+                                               uint32_t(nb) * NT * kFragBytesPerBlockTile);
+                tma_2d(stage, &tm_w, kb * 16, n0, bar, pol_w);
+                tma_2d(stage + C::kBoxW, &tm_w, kb * 16 + kBoxBytes, n0, bar, pol_w);
+                if (!P.sc_from_prep) tma_2d(stage + C::kWBytes, &tm_s, kb, n0, bar, pol_w);
+                if (waited) {
+                    issue_dep(slot, kb, nb, n0);
+                } else {
+                    def_slot[ndef] = slot;
+                    def_kb[ndef] = kb;
+                    def_nb[ndef] = nb;
+                    def_n0[ndef] = n0;
+                    ++ndef;
+                    if (ndef == STAGES) {
+                        pdl_wait();
+                        waited = true;
+                        for (int d = 0; d < ndef; ++d)
+                            issue_dep(def_slot[d], def_kb[d], def_nb[d], def_n0[d]);
+                    }
+                }
+            }
+        }
+        if (!waited) {
+            pdl_wait();
+            for (int d = 0; d < ndef; ++d) issue_dep(def_slot[d], def_kb[d], def_nb[d], def_n0[d]);
+        }
+        // never leave a copy in flight: wait (bounded) for the last phase of
+        // every slot filled
+        for (int j = max(0, it - STAGES); j < it; ++j)
+            mbar_wait(full_bar + 8 * (j % STAGES), (j / STAGES) & 1, P.status);
+        return;
+    }
+
+    // ----------------------------------------------------------- consumers
+    const int g = lane >> 2, t = lane & 3;
+    const int rbase = warp * 16;
+    const int mi = lane >> 3, ri = lane & 7;
+    const int lrow = rbase + ri + 8 * (mi & 1);
+    uint32_t lm[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) lm[j] = uint32_t(((2 * j + (mi >> 1)) ^ ri) << 4);
+    const int M = P.M;
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    bool waited = false;
+    int it = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < P.items; w += gridDim.x) {
+        const ItemRange R = item_range(P, w);
+        const int64_t n0 = int64_t(R.tile) * C::BN;
+        const int rows = int(P.N - n0 < int64_t(C::BN) ? P.N - n0 : int64_t(C::BN));
+        for (int i = 0; ok && i < R.nst; ++i, ++it) {
+            const int slot = it % STAGES;
+            if (!mbar_wait(full_bar + 8 * slot, (it / STAGES) & 1, P.status)) {
+                ok = false;
+                break;
+            }
+            const int nb = min(kStageBlocks, R.kb1 - (R.kb0 + i * kStageBlocks));
+            const uint8_t* stage = smem + slot * C::kStageBytes;
+            const uint4 sg = *reinterpret_cast<const uint4*>(stage + C::kWBytes + (rbase + g) * 16);
+            const uint4 sg8 =
+                *reinterpret_cast<const uint4*>(stage + C::kWBytes + (rbase + g + 8) * 16);
+            const uint4* xs = reinterpret_cast<const uint4*>(stage + C::kWBytes + C::kSBytes);
+            const uint32_t w_row = smem_base + slot * C::kStageBytes + uint32_t(lrow) * kBoxBytes;
+            if (nb == kStageBlocks)
+                consume_stage<NT, C::kBoxW, true>(acc, w_row, lm, sg, sg8, xs, lane, nb);
+            else
+                consume_stage<NT, C::kBoxW, false>(acc, w_row, lm, sg, sg8, xs, lane, nb);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar + 8 * slot);
+        }
+
+        // --------------------------------------------- epilogue of one item
+        consumer_bar(C::kConsumers);  // the previous item's partial tile is consumed
+        {
+            const int r = rbase + g;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                part[r * C::kPartPitch + nt * 8 + 2 * t] = acc[nt][0];
+                part[r * C::kPartPitch + nt * 8 + 2 * t + 1] = acc[nt][1];
+                part[(r + 8) * C::kPartPitch + nt * 8 + 2 * t] = acc[nt][2];
+                part[(r + 8) * C::kPartPitch + nt * 8 + 2 * t + 1] = acc[nt][3];
+                acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+            }
+        }
+        consumer_bar(C::kConsumers);
+        if (!waited) {
+            pdl_wait();  // Y, the counters and xun belong to the preceding kernels until now
+            waited = true;
+        }
+        if (P.nsplit == 1) {
+            for (int o = threadIdx.x; o < C::BN * M; o += C::kConsumers) {
+                const int r = o % C::BN, m = o / C::BN;
+                if (r < rows) P.y[int64_t(m) * P.N + n0 + r] = part[r * C::kPartPitch + m] * P.xun[m];
+            }
+        } else {
+            float* mine = P.part + int64_t(w) * M * C::BN;
+            for (int o = threadIdx.x; o < C::BN * M; o += C::kConsumers) {
+                const int r = o % C::BN, m = o / C::BN;
+                __stcg(mine + int64_t(m) * C::BN + r, part[r * C::kPartPitch + m]);
+            }
+            __threadfence();
+            consumer_bar(C::kConsumers);
+            if (threadIdx.x == 0) *sh_last = (atomicAdd(P.counters + R.tile, 1) == P.nsplit - 1);
+            consumer_bar(C::kConsumers);
+            if (*sh_last) {
+                __threadfence();
+                for (int o = threadIdx.x; o < C::BN * M; o += C::kConsumers) {
+                    const int r = o % C::BN, m = o / C::BN;
+                    if (r < rows) {
+                        float s = 0.f;
+                        for (int q = 0; q < P.nsplit; ++q)
+                            s += __ldcg(P.part + (int64_t(q) * P.ntiles + R.tile) * M * C::BN +
+                                        int64_t(m) * C::BN + r);
+                        P.y[int64_t(m) * P.N + n0 + r] = s * P.xun[m];
+                    }
+                }
+                if (threadIdx.x == 0) P.counters[R.tile] = 0;  // ready for the next call
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Preparation: X bf16 [M, K] -> fp16 fragments and per-row unscale factors;
+// zeroed split-K counters; optional copy of the scale rows into 16-byte
+// aligned rows.
+//
+// Row m is multiplied by 2^sh with sh = 142 - (biased exponent of max|x|),
+// which puts max|x| in [2^15, 2^16): fp16 then holds every element within
+// 2^29 of the maximum exactly.  The GEMM multiplies its output by 2^-sh.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float pow2f_exact(int e) {
+    // 2^e as fp32 for e in [-149, 127]
+    if (e >= -126) return __uint_as_float(uint32_t(e + 127) << 23);
+    return __uint_as_float(1u << (e + 149));
+}
+
+__global__ void __launch_bounds__(256)
+    mxfp4_gemm_prep_kernel(const uint16_t* __restrict__ x, int M, int K, int NT,
+                           uint16_t* __restrict__ xf, float* __restrict__ xun, int* counters,
+                           int ncounters, const uint8_t* __restrict__ sc_in, int64_t N, int nblk,
+                           int sc_pitch, uint8_t* __restrict__ sc_out, int repack_ctas) {
+    pdl_trigger();
+    pdl_wait();  // the workspace may still be in use by the previous GEMM
+    const int mpad = 8 * NT;
+    if (int(blockIdx.x) < mpad) {
+        const int m = blockIdx.x;
+        __shared__ uint32_t smax;
+        if (threadIdx.x == 0) smax = 0;
+        __syncthreads();
+        uint32_t mx = 0;
+        if (m < M)
+            for (int k = threadIdx.x; k < K; k += blockDim.x)
+                mx = max(mx, uint32_t(x[int64_t(m) * K + k] & 0x7FFFu));
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if ((threadIdx.x & 31) == 0) atomicMax(&smax, mx);
+        __syncthreads();
+        int emax = int(smax >> 7);  // biased exponent of max|x| (NaN/Inf -> 255)
+        if (emax < 1) emax = 1;
+        const int sh = 142 - emax;  // in [-113, 141]
+        const float f1 = pow2f_exact(sh / 2), f2 = pow2f_exact(sh - sh / 2);
+        if (threadIdx.x == 0) xun[m] = (m < M) ? pow2f_exact(-sh) : 0.f;
+        const int nt = m >> 3, gg = m & 7;
+        for (int k = threadIdx.x; k < K; k += blockDim.x) {
+            float v = 0.f;
+            if (m < M) {
+                const float xv = __uint_as_float(uint32_t(x[int64_t(m) * K + k]) << 16);
+                v = (xv * f1) * f2;
+            }
+            const int blk = k >> 5, w = k & 31, tt = w >> 3, j = w & 7;
+            const int64_t idx = ((int64_t(blk) * NT + nt) * 32 + gg * 4 + tt) * 8 + j;
+            xf[idx] = __half_as_ushort(__float2half_rn(v));
+        }
+    } else if (int(blockIdx.x) == mpad) {
+        for (int i = threadIdx.x; i < ncounters; i += blockDim.x) counters[i] = 0;
+    } else if (repack_ctas > 0) {
+        // realign scale rows: sc_out[n][0..sc_pitch) = sc_in[n][0..nblk), zero padded
+        const int64_t total = N * sc_pitch;
+        const int64_t stride = int64_t(repack_ctas) * blockDim.x;
+        for (int64_t i = int64_t(blockIdx.x - mpad - 1) * blockDim.x + threadIdx.x; i < total;
+             i += stride) {
+            const int64_t n = i / sc_pitch;
+            const int c = int(i - n * sc_pitch);
+            sc_out[i] = c < nblk ? sc_in[n * nblk + c] : uint8_t(0);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static int tiles_nt(int mc) {  // fragment tiles of 8 rows used for a pass of mc rows
+    const int nt = (mc + 7) / 8;
+    return nt > 4 ? 8 : nt;
+}
+static int bn_for_nt(int nt) { return (nt == 3 || nt == 4) ? 128 : 64; }
+
+// Largest split-K work-item count the launcher may pick (0 if it never splits).
+static int64_t split_items_cap(int64_t N, int64_t K, int bn) {
+    const int64_t ntiles = (N + bn - 1) / bn;
+    const int64_t stages = (K / 32 + kStageBlocks - 1) / kStageBlocks;
+    const int64_t ns = std::min<int64_t>(
+        {int64_t(kMaxSplit), stages, std::max<int64_t>(1, kMaxSplitItems / ntiles)});
+    return ns > 1 ? ntiles * ns : 0;
+}
+
+GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales_aligned) {
+    GemmWorkspace w{};
+    const int64_t nblk = K / 32;
+    const int64_t mc = std::min<int64_t>(M, kGemmMaxRowsPerPass);
+    w.repack_scales = !(K % 512 == 0 && scales_aligned);
+    w.sc_pitch = w.repack_scales ? int(align_up(size_t(nblk), 16)) : int(nblk);
+    size_t off = 0;
+    w.xf_off = off;
+    off = align_up(off + size_t(kGemmMaxRowsPerPass) * size_t(K) * 2, 256);
+    w.xun_off = off;
+    off = align_up(off + kGemmMaxRowsPerPass * sizeof(float), 256);
+    // counters and partial tiles, sized for either tile height a pass may use
+    int64_t ncnt = 0, part = 0;
+    for (int bn : {64, 128}) {
+        const int64_t cap = split_items_cap(N, K, bn);
+        if (cap > 0) {
+            ncnt = std::max<int64_t>(ncnt, (N + bn - 1) / bn);
+            part = std::max<int64_t>(part, cap * mc * bn);
+        }
+    }
+    w.cnt_off = off;
+    w.n_counters = int(ncnt);
+    off = align_up(off + size_t(ncnt) * sizeof(int), 256);
+    w.part_off = off;
+    off = align_up(off + size_t(part) * sizeof(float), 256);
+    w.sc_off = off;
+    if (w.repack_scales) off = align_up(off + size_t(N) * size_t(w.sc_pitch), 256);
+    w.bytes = off;
+    return w;
+}
+
+static int env_int(const char* name, int dflt) {
+    const char* v = std::getenv(name);
+    return v ? std::atoi(v) : dflt;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        f = reinterpret_cast<EncodeTiledFn>(p);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
+// 2-D uint8 tensor map over a [rows, cols] byte matrix with the given row pitch.
+static bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                     int64_t pitch, uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(pitch)};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    std::memset(map, 0, sizeof(*map));
+    return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Per-device launch facts of one kernel instantiation, computed on first use.
+struct LaunchFacts {
+    std::atomic<int> sms[kMaxDevices];
+    std::atomic<int> occ[kMaxDevices];
+};
+
+// Split of K: the count whose busiest CTA streams the fewest stages, with a
+// small charge per extra work item for its partial-tile round trip.
+static void choose_split(int64_t ntiles, int stages_total, int64_t grid_cap, int64_t items_cap,
+                         int& nsplit, int& per_split) {
+    double best = 1e300;
+    nsplit = 1;
+    per_split = stages_total;
+    const int max_ns = int(std::min<int64_t>(kMaxSplit, stages_total));
+    for (int ns = 1; ns <= max_ns; ++ns) {
+        const int sps = (stages_total + ns - 1) / ns;
+        const int nse = (stages_total + sps - 1) / sps;  // splits actually used
+        if (nse != ns) continue;
+        const int64_t items = ntiles * ns;
+        if (ns > 1 && items > items_cap) break;
+        const int64_t grid = std::min<int64_t>(items, grid_cap);
+        const double per_cta = double((items + grid - 1) / grid);
+        const double cost = per_cta * (sps + (ns > 1 ? 0.35 : 0.0));
+        if (cost < best - 1e-9) {
+            best = cost;
+            nsplit = ns;
+            per_split = sps;
+        }
+    }
+}
+
+template <int NT, int NWC, int STAGES>
+static cudaError_t launch_main(GemmParams P, const uint8_t* nib, const uint8_t* sc, int sc_pitch,
+                               int64_t K, int64_t items_cap, cudaStream_t stream) {
+    using C = GemmCfg<NT, NWC, STAGES>;
+    auto kern = mxfp4_gemm_kernel<NT, NWC, STAGES>;
+    static LaunchFacts facts;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int sms = facts.sms[dev].load(std::memory_order_acquire);
+    int occ = facts.occ[dev].load(std::memory_order_acquire);
+    if (sms <= 0 || occ <= 0) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   C::kSmemBytes);
+        if (err != cudaSuccess) return err;
+        err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess) return err;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::kThreads,
+                                                            C::kSmemBytes);
+        if (err != cudaSuccess) return err;
+        if (occ < 1) occ = 1;
+        facts.occ[dev].store(occ, std::memory_order_release);
+        facts.sms[dev].store(sms, std::memory_order_release);
+    }
+
+    P.ntiles = int((P.N + C::BN - 1) / C::BN);
+    const int stages_total = (P.nblk + kStageBlocks - 1) / kStageBlocks;
+    const int64_t resident = int64_t(sms) * occ;
+    choose_split(P.ntiles, stages_total, resident, items_cap, P.nsplit, P.stages_per_split);
+    const int forced = env_int("MXS_GEMM_SPLITS", 0);
+    if (forced > 0) {
+        int ns = std::min(forced, stages_total);
+        const int sps = (stages_total + ns - 1) / ns;
+        ns = (stages_total + sps - 1) / sps;
+        if (ns == 1 || int64_t(P.ntiles) * ns <= items_cap) {
+            P.nsplit = ns;
+            P.stages_per_split = sps;
+        }
+    }
+    P.items = P.ntiles * P.nsplit;
+    const int64_t grid = std::min<int64_t>(P.items, resident);
+
+    CUtensorMap tm_w, tm_s;
+    if (!make_map(&tm_w, nib, P.N, K / 2, K / 2, kBoxBytes, C::BN, true))
+        return cudaErrorInvalidValue;
+    if (!make_map(&tm_s, sc, P.N, P.nblk, sc_pitch, 16, C::BN, false))
+        return cudaErrorInvalidValue;
+
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(grid), 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_s, P);
+}
+
+static cudaError_t launch_prep(const uint16_t* x, int M, int K, int NT, uint16_t* xf, float* xun,
+                               int* counters, int ncounters, const uint8_t* sc_in, int64_t N,
+                               int nblk, int sc_pitch, uint8_t* sc_out, bool repack,
+                               cudaStream_t stream) {
+    int repack_ctas = 0;
+    if (repack) {
+        const int64_t total = N * sc_pitch;
+        repack_ctas = int(std::min<int64_t>((total + 255) / 256, 1024));
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(8 * NT + 1 + repack_ctas), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mxfp4_gemm_prep_kernel, x, M, K, NT, xf, xun, counters,
+                              ncounters, sc_in, N, nblk, sc_pitch, sc_out, repack_ctas);
+}
+
+cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* scales, float* y,
+                     int64_t M, int64_t N, int64_t K, void* workspace, const GemmWorkspace& ws,
+                     int32_t* dev_status, cudaStream_t stream) {
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    uint16_t* xf = reinterpret_cast<uint16_t*>(wsb + ws.xf_off);
+    float* xun = reinterpret_cast<float*>(wsb + ws.xun_off);
+    int* counters = reinterpret_cast<int*>(wsb + ws.cnt_off);
+    float* part = reinterpret_cast<float*>(wsb + ws.part_off);
+    uint8_t* sc_aligned = ws.repack_scales ? wsb + ws.sc_off : nullptr;
+    const int nblk = int(K / 32);
+    const int64_t mc0 = std::min<int64_t>(M, kGemmMaxRowsPerPass);
+    for (int64_t m0 = 0; m0 < M; m0 += kGemmMaxRowsPerPass) {
+        const int mc = int(std::min<int64_t>(kGemmMaxRowsPerPass, M - m0));
+        const int NT = tiles_nt(mc);
+        const int bn = bn_for_nt(NT);
+        // the workspace holds partial tiles for mc0 rows and tile height bn
+        int64_t items_cap = split_items_cap(N, K, bn);
+        if (ws.n_counters < (N + bn - 1) / bn || mc > mc0) items_cap = 0;
+        // the scales are realigned once, by the first pass
+        const bool repack = ws.repack_scales && m0 == 0;
+        cudaError_t err = launch_prep(x + m0 * K, mc, int(K), NT, xf, xun, counters,
+                                      ws.n_counters, scales, N, nblk, ws.sc_pitch, sc_aligned,
+                                      repack, stream);
+        if (err != cudaSuccess) return err;
+        GemmParams P{};
+        P.xf = xf;
+        P.xun = xun;
+        P.y = y + m0 * N;
+        P.part = part;
+        P.counters = counters;
+        P.N = N;
+        P.M = mc;
+        P.nblk = nblk;
+        P.sc_from_prep = repack ? 1 : 0;
+        P.status = dev_status;
+        const uint8_t* sc = ws.repack_scales ? sc_aligned : scales;
+        switch (NT) {
+            case 1: err = launch_main<1, 4, 4>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
+            case 2: err = launch_main<2, 4, 3>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
+            case 3: err = launch_main<3, 8, 3>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
+            case 4: err = launch_main<4, 8, 3>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
+            default: err = launch_main<8, 4, 2>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
+        }
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace mxs

@@ -1,0 +1,50 @@
+// Host-side launchers behind the C ABI.  Arguments are validated by the
+// entry points in api.cu before any of these is called.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mxs {
+
+// ---------------------------------------------------------------- GEMM
+// Largest number of X rows handled by one pass over W (8 tiles of 8).
+constexpr int kGemmMaxRowsPerPass = 64;
+
+struct GemmWorkspace {
+    size_t bytes;        // total
+    size_t xf_off;       // fragment-ordered fp16 X, kGemmMaxRowsPerPass rows max
+    size_t xun_off;      // per-row unscale factors (fp32)
+    size_t cnt_off;      // split-K arrival counters (int32)
+    int n_counters;
+    size_t part_off;     // split-K partial tiles (fp32)
+    size_t sc_off;       // realigned scales (only when needed)
+    int sc_pitch;        // bytes per realigned scale row
+    bool repack_scales;  // scales must be copied to the workspace first
+};
+
+GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales_aligned);
+
+cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* scales, float* y,
+                     int64_t M, int64_t N, int64_t K, void* workspace,
+                     const GemmWorkspace& ws, int32_t* dev_status, cudaStream_t stream);
+
+// ---------------------------------------------------------- acceptance
+constexpr int kAcceptMaxK = 32;
+constexpr int64_t kAcceptMaxV = int64_t(1) << 21;
+
+cudaError_t accept_run(const float* p, const float* q, const int32_t* draft, const float* u,
+                       int64_t B, int64_t K, int64_t V, int32_t* out_tokens,
+                       int32_t* n_emitted, int32_t* row_flags, int32_t* dev_status,
+                       cudaStream_t stream);
+
+// ---------------------------------------------------------------- pack
+cudaError_t pack_run(const void* w, int w_dtype, int64_t N, int64_t K, uint8_t* nibbles,
+                     uint8_t* scales, int32_t* dev_status, cudaStream_t stream);
+
+// --------------------------------------------------------------- probe
+cudaError_t hbm_read_probe_run(const void* src, size_t bytes, uint64_t* sink,
+                               cudaStream_t stream);
+
+}  // namespace mxs

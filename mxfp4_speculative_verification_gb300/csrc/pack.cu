@@ -1,0 +1,128 @@
+// mxfp4_pack on sm_103a: real weights -> E2M1 nibbles + E8M0 block scales.
+//
+// Format: "Module 11. Speculative Decoding and Quantization", §12 (E2M1 grid
+// 0,0.5,1,1.5,2,3,4,6 with a sign bit; 32 values share one E8M0 power of two)
+// and the teaching quantizer of §13 (one scale per group, an all-zero group
+// gets scale 1).  Rule: e = smallest integer with amax <= 6 * 2^e (clamped to
+// [-127, 127]), each element rounded to the nearest grid value of w / 2^e
+// with ties to the even fraction bit, sign bit kept.
+//
+// One thread per 32-element block; element-wise and bandwidth-bound, off the
+// verification path.
+#include "mxs_device.cuh"
+#include "mxs_internal.h"
+
+namespace mxs {
+
+template <typename T>
+__device__ __forceinline__ float load_elem(const T* w, int64_t i);
+template <>
+__device__ __forceinline__ float load_elem<float>(const float* w, int64_t i) { return w[i]; }
+template <>
+__device__ __forceinline__ float load_elem<uint16_t>(const uint16_t* w, int64_t i) {
+    return __uint_as_float(uint32_t(w[i]) << 16);
+}
+
+__device__ __forceinline__ float exact_pow2(int e) {  // e in [-149, 127]
+    if (e >= -126) return __uint_as_float(uint32_t(e + 127) << 23);
+    return __uint_as_float(1u << (e + 149));
+}
+
+// Grid code (0..7) of a in [0, 6]: count of decision boundaries passed.
+// Midpoints 0.25, 1.25, 2.5, 5 tie to the lower (even) code, midpoints
+// 0.75, 1.75, 3.5 tie to the upper (even) code.
+__device__ __forceinline__ uint32_t e2m1_magnitude_code(float a) {
+    return uint32_t(a > 0.25f) + uint32_t(a >= 0.75f) + uint32_t(a > 1.25f) +
+           uint32_t(a >= 1.75f) + uint32_t(a > 2.5f) + uint32_t(a >= 3.5f) + uint32_t(a > 5.0f);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+    mxfp4_pack_kernel(const T* __restrict__ w, int64_t N, int64_t K, uint8_t* __restrict__ nib,
+                      uint8_t* __restrict__ sc, int32_t* status) {
+    const int64_t nblk = K / 32;
+    const int64_t total = N * nblk;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t n = i / nblk, blk = i - n * nblk;
+        const int64_t base = n * K + blk * 32;
+        float v[32];
+        float amax = 0.f;
+        bool finite = true;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            v[k] = load_elem<T>(w, base + k);
+            const float a = fabsf(v[k]);
+            if (!(a <= 3.402823466e38f)) finite = false;  // Inf or NaN
+            else amax = fmaxf(amax, a);
+        }
+        uint8_t* out = nib + n * (K / 2) + blk * 16;
+        if (!finite) {
+            sc[i] = 255;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) out[k] = 0;
+            report(status, MXS_DEV_NONFINITE);
+            continue;
+        }
+        int e = 0;
+        if (amax > 0.f) {
+            const uint32_t bits = __float_as_uint(amax);
+            const int ex = int(bits >> 23);
+            const uint32_t man = bits & 0x7FFFFFu;
+            e = (ex == 0) ? -127 : ex - 129 + (man > 0x400000u ? 1 : 0);
+            e = max(-127, min(127, e));
+        }
+        sc[i] = uint8_t(e + 127);
+        const float inv = exact_pow2(-e);
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+            const uint32_t c0 = e2m1_magnitude_code(fabsf(v[k]) * inv) |
+                                ((__float_as_uint(v[k]) >> 31) << 3);
+            const uint32_t c1 = e2m1_magnitude_code(fabsf(v[k + 1]) * inv) |
+                                ((__float_as_uint(v[k + 1]) >> 31) << 3);
+            out[k / 2] = uint8_t(c0 | (c1 << 4));
+        }
+    }
+}
+
+cudaError_t pack_run(const void* w, int w_dtype, int64_t N, int64_t K, uint8_t* nibbles,
+                     uint8_t* scales, int32_t* dev_status, cudaStream_t stream) {
+    const int64_t total = N * (K / 32);
+    if (total == 0) return cudaSuccess;
+    const int threads = 256;
+    const int64_t want = (total + threads - 1) / threads;
+    const unsigned grid = unsigned(want < 65535 * 16 ? want : 65535 * 16);
+    if (w_dtype == MXS_F32)
+        mxfp4_pack_kernel<float><<<grid, threads, 0, stream>>>(static_cast<const float*>(w), N, K,
+                                                                nibbles, scales, dev_status);
+    else
+        mxfp4_pack_kernel<uint16_t><<<grid, threads, 0, stream>>>(
+            static_cast<const uint16_t*>(w), N, K, nibbles, scales, dev_status);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Read-only streaming probe: the HBM roofline of a pure read.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(512) hbm_read_probe_kernel(const uint4* __restrict__ src,
+                                                             size_t n16, unsigned long long* sink) {
+    uint32_t acc = 0;
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+         i += size_t(gridDim.x) * blockDim.x) {
+        const uint4 v = __ldcs(src + i);
+        acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+    if (acc == 0x9E3779B9u) atomicXor(sink, 1ull);  // keeps the loads live
+}
+
+cudaError_t hbm_read_probe_run(const void* src, size_t bytes, uint64_t* sink,
+                               cudaStream_t stream) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    hbm_read_probe_kernel<<<unsigned(sms * 4), 512, 0, stream>>>(
+        static_cast<const uint4*>(src), bytes / 16, reinterpret_cast<unsigned long long*>(sink));
+    return cudaGetLastError();
+}
+
+}  // namespace mxs

@@ -1,0 +1,151 @@
+"""GPU parity of spec_accept against the CPU oracle.
+
+Bar: accepted counts (n_emitted) bit-exact on every row; emitted tokens
+bit-exact except on rows where the oracle's uniform u[b,K] lies within 1e-5
+of an edge of the chosen inverse-CDF bin (counted and reported, not failed).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from helpers import compare_accept, cuda_or_skip
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    return cuda_or_skip()
+
+
+def _gpu(env, p, q, d, u, with_flags=True):
+    torch, mxs = env
+    dev = torch.device("cuda:0")
+    P = torch.from_numpy(np.ascontiguousarray(p, np.float32)).to(dev)
+    Q = torch.from_numpy(np.ascontiguousarray(q, np.float32)).to(dev)
+    D = torch.from_numpy(np.ascontiguousarray(d, np.int32)).to(dev)
+    U = torch.from_numpy(np.ascontiguousarray(u, np.float32)).to(dev)
+    flags = torch.full((P.shape[0],), -7, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    tok, n = mxs.spec_accept(P, Q, D, U, row_flags=flags, dev_status=status)
+    torch.cuda.synchronize()
+    return tok.cpu().numpy(), n.cpu().numpy(), flags.cpu().numpy(), int(status.item())
+
+
+def _check(env, p, q, d, u):
+    tok, n, flags, status = _gpu(env, p, q, d, u)
+    ref = oracle.spec_accept(p, q, d, u)
+    near, mism, bad = compare_accept((tok, n), ref)
+    assert bad.size == 0, f"rows {bad[:10]} differ: gpu {tok[bad[:3]]} vs ref {ref[0][bad[:3]]}"
+    # the row flags agree with the oracle's on the bits both sides define
+    assert np.array_equal(flags & 0xF, ref[2] & 0xF)
+    print(f"rows={len(n)} near_edge={near} token_mismatch={mism}")
+    return near, tok, n, flags, status
+
+
+def test_tiny_config_many_seeds(env):
+    t = workloads.TINY
+    for seed in range(20):
+        p, q, d, u = workloads.spec_inputs(64, t["K_spec"], t["V"], seed, logit_std=t["logit_std"])
+        _check(env, p, q, d, u)
+
+
+@pytest.mark.parametrize("B", [1, 4, 16, 64])
+def test_llama8b_vocab(env, B):
+    p, q, d, u = workloads.spec_inputs(B, 4, workloads.VOCAB_LLAMA, seed=B, logit_std=2.0)
+    _check(env, p, q, d, u)
+
+
+@pytest.mark.parametrize("K", [1, 3, 7])
+def test_acceptance_heavy(env, K):
+    sigma = workloads.tune_draft_noise(0.86, 4096, 3.0, seed=0, samples=8)
+    p, q, d, u = workloads.spec_inputs(64, K, workloads.VOCAB_LLAMA, seed=K, logit_std=3.0,
+                                       draft_noise=sigma)
+    near, tok, n, flags, status = _check(env, p, q, d, u)
+    assert n.mean() > 1.0
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 5, 127, 128, 129, 1000, 4097])
+def test_small_and_ragged_vocab(env, V):
+    p, q, d, u = workloads.spec_inputs(32, 3, V, seed=V, logit_std=1.0)
+    _check(env, p, q, d, u)
+
+
+def test_no_drafts_and_max_drafts(env):
+    p, q, d, u = workloads.spec_inputs(16, 0, 1000, seed=1)
+    _check(env, p, q, d, u)
+    p, q, d, u = workloads.spec_inputs(8, 32, 1000, seed=2, logit_std=0.3)
+    _check(env, p, q, d, u)
+
+
+def test_p_equals_q_accepts_everything(env):
+    p, q, d, u = workloads.spec_inputs(16, 5, 3000, seed=3)
+    q = p[:, :5, :].copy()
+    near, tok, n, flags, status = _check(env, p, q, d, u)
+    assert np.all(n == 6)
+
+
+def test_bad_draft_zero_q_and_zero_residual(env):
+    p, q, d, u = workloads.spec_inputs(8, 3, 64, seed=4)
+    d[0, 2] = 64          # out of range -> error row
+    d[1, 0] = -1
+    q[2, 0, d[2, 0]] = 0.0  # zero-mass proposal -> rejection, flag
+    # row 3: p below q everywhere at position 0 (unnormalised) -> zero residual
+    p[3, 0] = q[3, 0] * 0.5
+    u[3, 0] = 0.99
+    near, tok, n, flags, status = _check(env, p, q, d, u)
+    assert n[0] == 0 and n[1] == 0 and np.all(tok[0] == -1)
+    assert flags[0] & 1 and flags[2] & 2 and flags[3] & 4
+    assert status & 1 and status & 2 and status & 4
+
+
+def test_law_without_mass_is_error_row(env):
+    p, q, d, u = workloads.spec_inputs(4, 2, 100, seed=5)
+    q[0] = p[0, :2]
+    p[0, 2] = 0.0  # bonus law empty
+    tok, n, flags, status = _gpu(env, p, q, d, u)
+    ref = oracle.spec_accept(p, q, d, u)
+    assert n[0] == 0 and ref[1][0] == 0 and flags[0] & 8 and ref[2][0] & 8
+
+
+def test_extreme_uniforms(env):
+    p, q, d, u = workloads.spec_inputs(64, 3, 5000, seed=6)
+    u[:32] = 0.0
+    u[32:] = np.float32(np.nextafter(np.float32(1), np.float32(0)))
+    _check(env, p, q, d, u)
+
+
+def test_misaligned_rows_use_scalar_path(env):
+    torch, mxs = env
+    dev = torch.device("cuda:0")
+    p, q, d, u = workloads.spec_inputs(8, 2, 1024, seed=7)
+    ref = oracle.spec_accept(p, q, d, u)
+    bp = torch.zeros(p.size + 1, dtype=torch.float32, device=dev)
+    bp[1:] = torch.from_numpy(p.ravel()).to(dev)
+    P = bp[1:].view(p.shape)
+    tok, n = mxs.spec_accept(P, torch.from_numpy(q).to(dev), torch.from_numpy(d).to(dev),
+                             torch.from_numpy(u).to(dev))
+    torch.cuda.synchronize()
+    near, mism, bad = compare_accept((tok.cpu().numpy(), n.cpu().numpy()), ref)
+    assert bad.size == 0
+
+
+def test_near_edge_rows_are_flagged(env):
+    # uniform placed exactly on a CDF edge of the bonus law
+    V = 8
+    p = np.zeros((1, 1, V), np.float32)
+    p[0, 0] = [0.125] * 8
+    q = np.zeros((1, 0, V), np.float32)
+    d = np.zeros((1, 0), np.int32)
+    u = np.array([[0.5]], np.float32)
+    tok, n, flags, status = _gpu(env, p, q, d, u)
+    ref = oracle.spec_accept(p, q, d, u)
+    assert ref[3][0] < 1e-5 and flags[0] & 0x10
+    assert tok[0, 0] == ref[0][0, 0] == 4
+
+
+def test_large_vocab_limit(env):
+    V = 1 << 21
+    p, q, d, u = workloads.spec_inputs(2, 1, V, seed=8, logit_std=1.0)
+    _check(env, p, q, d, u)

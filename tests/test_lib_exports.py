@@ -1,0 +1,74 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+The library must build for sm_103a, load, export every function declared in
+include/mxs.h, and reject bad arguments on the host before any launch.
+"""
+import ctypes
+
+import pytest
+
+import mxfp4_speculative_verification_gb300 as mxs
+
+
+@pytest.fixture(scope="module")
+def L():
+    mxs.build()
+    return mxs.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = mxs.declared_symbols()
+    assert {"mxfp4_pack", "mxfp4_verify_gemm", "spec_accept",
+            "mxfp4_verify_gemm_workspace_size"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_version_and_status_strings(L):
+    assert L.mxs_version() == 100
+    assert L.mxs_status_string(0) == b"MXS_OK"
+    assert L.mxs_status_string(5) == b"MXS_ERR_WORKSPACE"
+    assert L.mxs_status_string(99) == b"MXS_ERR_UNKNOWN"
+
+
+def test_workspace_size_rules(L):
+    assert L.mxfp4_verify_gemm_workspace_size(5, 4096, 4096) > 0
+    assert L.mxfp4_verify_gemm_workspace_size(0, 4096, 4096) == 0
+    assert L.mxfp4_verify_gemm_workspace_size(5, 4096, 4100) == 0  # K % 32
+    # K % 512 != 0 adds room for realigned scale rows
+    a = L.mxfp4_verify_gemm_workspace_size(5, 1000, 544)
+    b = L.mxfp4_verify_gemm_workspace_size(5, 1000, 512)
+    assert a >= b + 1000 * 32
+
+
+FAKE = 0x100000  # never dereferenced: validation fails first
+
+
+def test_gemm_rejects_bad_arguments_on_host(L):
+    ws = 1 << 30
+    f = L.mxfp4_verify_gemm
+    assert f(None, FAKE, FAKE, FAKE, 5, 64, 512, FAKE, ws, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, 0, 64, 512, FAKE, ws, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, 5, 64, 500, FAKE, ws, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, 1 << 20, 64, 512, FAKE, ws, None, None) == 3
+    assert f(FAKE, FAKE + 8, FAKE, FAKE, 5, 64, 512, FAKE, ws, None, None) == 2   # nibbles 16B
+    assert f(FAKE, FAKE, FAKE + 1, FAKE, 5, 64, 512, FAKE, ws, None, None) == 2   # scales, K%512==0
+    assert f(FAKE, FAKE, FAKE, FAKE, 5, 64, 512, None, ws, None, None) == 5
+    assert f(FAKE, FAKE, FAKE, FAKE, 5, 64, 512, FAKE, 16, None, None) == 5
+
+
+def test_accept_rejects_bad_arguments_on_host(L):
+    f = L.spec_accept
+    assert f(FAKE, FAKE, FAKE, FAKE, 0, 3, 8, FAKE, FAKE, None, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, 1, 33, 8, FAKE, FAKE, None, None, None) == 3
+    assert f(FAKE, FAKE, FAKE, FAKE, 1, 3, (1 << 21) + 1, FAKE, FAKE, None, None, None) == 3
+    assert f(FAKE, None, FAKE, FAKE, 1, 3, 8, FAKE, FAKE, None, None, None) == 1
+    assert f(FAKE + 2, FAKE, FAKE, FAKE, 1, 3, 8, FAKE, FAKE, None, None, None) == 2
+
+
+def test_pack_rejects_bad_arguments_on_host(L):
+    f = L.mxfp4_pack
+    assert f(FAKE, 0, 4, 33, FAKE, FAKE, None, None) == 1
+    assert f(FAKE, 7, 4, 32, FAKE, FAKE, None, None) == 1
+    assert f(FAKE + 2, 0, 4, 32, FAKE, FAKE, None, None) == 2
+    assert f(None, 0, 0, 32, None, None, None, None) == 0  # empty: nothing to do
