@@ -65,9 +65,12 @@ struct GemmParams {
     int32_t* status;
 };
 
-template <int NT, int NWC, int STAGES>
+// RG groups of 16 weight rows; KW consumer warps share each group, each
+// taking 16/KW of a stage's blocks (KW = 2: one nibble box per warp).
+template <int NT, int RG, int KW, int STAGES>
 struct GemmCfg {
-    static constexpr int BN = 16 * NWC;
+    static constexpr int BN = 16 * RG;
+    static constexpr int NWC = RG * KW;
     static constexpr int kConsumers = 32 * NWC;
     static constexpr int kThreads = kConsumers + 32;
     static constexpr int kBoxW = BN * kBoxBytes;            // one nibble box
@@ -77,7 +80,8 @@ struct GemmCfg {
     static constexpr int kStageBytes = kWBytes + kSBytes + kXBytes;
     static constexpr int kPartPitch = 8 * NT + 1;            // floats per row of the partial tile
     static constexpr int kPartOffset = STAGES * kStageBytes;
-    static constexpr int kBarOffset = kPartOffset + ((BN * kPartPitch * 4 + 15) / 16) * 16;
+    static constexpr int kPartFloats = KW * BN * kPartPitch;  // one partial tile per k-warp
+    static constexpr int kBarOffset = kPartOffset + ((kPartFloats * 4 + 15) / 16) * 16;
     static constexpr int kMiscOffset = kBarOffset + 2 * STAGES * 8;
     static constexpr int kSmemBytes = kMiscOffset + 16 + 1024;  // + alignment slack
     static_assert(kStageBytes % 1024 == 0, "128-byte swizzled boxes need 1 KB aligned stages");
@@ -118,26 +122,30 @@ __device__ __forceinline__ void consumer_bar(int nthreads) {
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-// One stage of 16 blocks (or the first nb of them) for one consumer warp.
-// lm[j]: swizzled byte offset of this lane's ldmatrix row chunk for block
-// pair j (j = 0..3 inside a nibble box; box 1 is BOXW bytes further).
-template <int NT, int BOXW, bool FULL>
+// One consumer warp's share of a stage: 16/KW consecutive blocks (the first
+// nbl of them when the stage is short).  w_row: shared address of this
+// lane's ldmatrix row in the warp's first nibble box; lm[j]: swizzled
+// offset of the lane's 16-byte chunk for block pair j; sgw/sg8w: the scale
+// bytes of the warp's blocks for rows g and g+8; xs: the X fragments of the
+// warp's first block.
+template <int NT, int BOXW, int KW, bool FULL>
 __device__ __forceinline__ void consume_stage(float (&acc)[NT][4], uint32_t w_row,
-                                              const uint32_t (&lm)[4], uint4 sg, uint4 sg8,
-                                              const uint4* __restrict__ xs, int lane, int nb) {
-    const uint32_t sgw[4] = {sg.x, sg.y, sg.z, sg.w};
-    const uint32_t sg8w[4] = {sg8.x, sg8.y, sg8.z, sg8.w};
+                                              const uint32_t (&lm)[4],
+                                              const uint32_t (&sgw)[4 / KW],
+                                              const uint32_t (&sg8w)[4 / KW],
+                                              const uint4* __restrict__ xs, int lane, int nbl) {
     const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+    constexpr int kPairs = kStageBlocks / 2 / KW;  // block pairs per k-warp
 #pragma unroll
-    for (int bp = 0; bp < kStageBlocks / 2; ++bp) {
-        if (!FULL && 2 * bp >= nb) break;
+    for (int bq = 0; bq < kPairs; ++bq) {
+        if (!FULL && 2 * bq >= nbl) break;
         uint32_t r0, r1, r2, r3;
-        // r0: rows 0-7 blk 2bp, r1: rows 8-15 blk 2bp, r2/r3: blk 2bp+1
-        ldmatrix_x4(w_row + (bp >> 2) * BOXW + lm[bp & 3], r0, r1, r2, r3);
+        // r0: rows 0-7 blk 2bq, r1: rows 8-15 blk 2bq, r2/r3: blk 2bq+1
+        ldmatrix_x4(w_row + (bq >> 2) * BOXW + lm[bq & 3], r0, r1, r2, r3);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int blk = 2 * bp + h;
-            if (!FULL && blk >= nb) break;
+            const int blk = 2 * bq + h;
+            if (!FULL && blk >= nbl) break;
             uint32_t ag[4], ag8[4];
             e2m1x8_to_f16x2x4(h ? r2 : r0, ag[0], ag[1], ag[2], ag[3]);
             e2m1x8_to_f16x2x4(h ? r3 : r1, ag8[0], ag8[1], ag8[2], ag8[3]);
@@ -173,11 +181,12 @@ __device__ __forceinline__ ItemRange item_range(const GemmParams& P, int w) {
     return r;
 }
 
-template <int NT, int NWC, int STAGES>
-__global__ void __launch_bounds__(32 * (NWC + 1))
+template <int NT, int RG, int KW, int STAGES>
+__global__ void __launch_bounds__(32 * (RG * KW + 1))
     mxfp4_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_s, const GemmParams P) {
-    using C = GemmCfg<NT, NWC, STAGES>;
+    using C = GemmCfg<NT, RG, KW, STAGES>;
+    constexpr int NWC = C::NWC;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte-swizzled TMA destinations need 1 KB alignment
     const uint32_t raw_base = smem_u32(smem_raw);
@@ -273,7 +282,8 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
 
     // ----------------------------------------------------------- consumers
     const int g = lane >> 2, t = lane & 3;
-    const int rbase = warp * 16;
+    const int rbase = (warp % RG) * 16;
+    const int kw = warp / RG;
     const int mi = lane >> 3, ri = lane & 7;
     const int lrow = rbase + ri + 8 * (mi & 1);
     uint32_t lm[4];
@@ -298,15 +308,25 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
             }
             const int nb = min(kStageBlocks, R.kb1 - (R.kb0 + i * kStageBlocks));
             const uint8_t* stage = smem + slot * C::kStageBytes;
-            const uint4 sg = *reinterpret_cast<const uint4*>(stage + C::kWBytes + (rbase + g) * 16);
-            const uint4 sg8 =
-                *reinterpret_cast<const uint4*>(stage + C::kWBytes + (rbase + g + 8) * 16);
-            const uint4* xs = reinterpret_cast<const uint4*>(stage + C::kWBytes + C::kSBytes);
-            const uint32_t w_row = smem_base + slot * C::kStageBytes + uint32_t(lrow) * kBoxBytes;
+            constexpr int kWords = 4 / KW;  // scale words (4 blocks each) per k-warp
+            const uint32_t* s_row = reinterpret_cast<const uint32_t*>(stage + C::kWBytes);
+            uint32_t sgw[kWords], sg8w[kWords];
+#pragma unroll
+            for (int q = 0; q < kWords; ++q) {
+                sgw[q] = s_row[(rbase + g) * 4 + kw * kWords + q];
+                sg8w[q] = s_row[(rbase + g + 8) * 4 + kw * kWords + q];
+            }
+            constexpr int kBlocksPerWarp = kStageBlocks / KW;
+            const uint4* xs = reinterpret_cast<const uint4*>(stage + C::kWBytes + C::kSBytes) +
+                              kw * kBlocksPerWarp * NT * 32;
+            // k-warp kw starts at block kw*16/KW: box (kw*16/KW)/8, chunk pairs from 0
+            const uint32_t w_row = smem_base + slot * C::kStageBytes + uint32_t(lrow) * kBoxBytes +
+                                   uint32_t((kw * kBlocksPerWarp) / 8) * C::kBoxW;
+            const int nbl = nb - kw * kBlocksPerWarp;
             if (nb == kStageBlocks)
-                consume_stage<NT, C::kBoxW, true>(acc, w_row, lm, sg, sg8, xs, lane, nb);
+                consume_stage<NT, C::kBoxW, KW, true>(acc, w_row, lm, sgw, sg8w, xs, lane, nbl);
             else
-                consume_stage<NT, C::kBoxW, false>(acc, w_row, lm, sg, sg8, xs, lane, nb);
+                consume_stage<NT, C::kBoxW, KW, false>(acc, w_row, lm, sgw, sg8w, xs, lane, nbl);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar + 8 * slot);
         }
@@ -315,16 +335,24 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
         consumer_bar(C::kConsumers);  // the previous item's partial tile is consumed
         {
             const int r = rbase + g;
+            float* pk = part + kw * (C::BN * C::kPartPitch);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                part[r * C::kPartPitch + nt * 8 + 2 * t] = acc[nt][0];
-                part[r * C::kPartPitch + nt * 8 + 2 * t + 1] = acc[nt][1];
-                part[(r + 8) * C::kPartPitch + nt * 8 + 2 * t] = acc[nt][2];
-                part[(r + 8) * C::kPartPitch + nt * 8 + 2 * t + 1] = acc[nt][3];
+                pk[r * C::kPartPitch + nt * 8 + 2 * t] = acc[nt][0];
+                pk[r * C::kPartPitch + nt * 8 + 2 * t + 1] = acc[nt][1];
+                pk[(r + 8) * C::kPartPitch + nt * 8 + 2 * t] = acc[nt][2];
+                pk[(r + 8) * C::kPartPitch + nt * 8 + 2 * t + 1] = acc[nt][3];
                 acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
             }
         }
         consumer_bar(C::kConsumers);
+        // the item's sum over its k-warps, in a fixed order
+        auto tile_val = [&](int r, int m) {
+            float v = part[r * C::kPartPitch + m];
+#pragma unroll
+            for (int q = 1; q < KW; ++q) v += part[q * (C::BN * C::kPartPitch) + r * C::kPartPitch + m];
+            return v;
+        };
         if (!waited) {
             pdl_wait();  // Y, the counters and xun belong to the preceding kernels until now
             waited = true;
@@ -332,13 +360,13 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
         if (P.nsplit == 1) {
             for (int o = threadIdx.x; o < C::BN * M; o += C::kConsumers) {
                 const int r = o % C::BN, m = o / C::BN;
-                if (r < rows) P.y[int64_t(m) * P.N + n0 + r] = part[r * C::kPartPitch + m] * P.xun[m];
+                if (r < rows) P.y[int64_t(m) * P.N + n0 + r] = tile_val(r, m) * P.xun[m];
             }
         } else {
             float* mine = P.part + int64_t(w) * M * C::BN;
             for (int o = threadIdx.x; o < C::BN * M; o += C::kConsumers) {
                 const int r = o % C::BN, m = o / C::BN;
-                __stcg(mine + int64_t(m) * C::BN + r, part[r * C::kPartPitch + m]);
+                __stcg(mine + int64_t(m) * C::BN + r, tile_val(r, m));
             }
             __threadfence();
             consumer_bar(C::kConsumers);
@@ -377,7 +405,22 @@ __device__ __forceinline__ float pow2f_exact(int e) {
     return __uint_as_float(1u << (e + 149));
 }
 
-__global__ void __launch_bounds__(256)
+constexpr int kPrepThreads = 512;
+constexpr int kPrepChunks = 8;  // 16-byte chunks of one X row kept in registers per thread
+
+__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t w, uint32_t m) {
+    return max(m, max(w & 0x7FFFu, (w >> 16) & 0x7FFFu));
+}
+
+// fp16 image of x * 2^sh for two bf16 values (f1 * f2 = 2^sh, both exact)
+__device__ __forceinline__ uint32_t scale_bf16x2_to_f16x2(uint32_t w, float f1, float f2) {
+    const float lo = (__uint_as_float(w << 16) * f1) * f2;
+    const float hi = (__uint_as_float(w & 0xFFFF0000u) * f1) * f2;
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(kPrepThreads)
     mxfp4_gemm_prep_kernel(const uint16_t* __restrict__ x, int M, int K, int NT,
                            uint16_t* __restrict__ xf, float* __restrict__ xun, int* counters,
                            int ncounters, const uint8_t* __restrict__ sc_in, int64_t N, int nblk,
@@ -387,13 +430,32 @@ __global__ void __launch_bounds__(256)
     const int mpad = 8 * NT;
     if (int(blockIdx.x) < mpad) {
         const int m = blockIdx.x;
+        const int nt = m >> 3, gg = m & 7;
         __shared__ uint32_t smax;
         if (threadIdx.x == 0) smax = 0;
         __syncthreads();
+        const uint16_t* row = x + int64_t(m) * K;
+        const int nchunks = K / 8;  // 8 consecutive k: one 16-byte piece of a fragment
+        const bool fast = (K <= kPrepThreads * kPrepChunks * 8) &&
+                          (reinterpret_cast<uintptr_t>(row) % 16 == 0);
+        uint4 v[kPrepChunks];
         uint32_t mx = 0;
-        if (m < M)
-            for (int k = threadIdx.x; k < K; k += blockDim.x)
-                mx = max(mx, uint32_t(x[int64_t(m) * K + k] & 0x7FFFu));
+        if (m < M) {
+            if (fast) {
+#pragma unroll
+                for (int i = 0; i < kPrepChunks; ++i) {
+                    const int c = threadIdx.x + i * kPrepThreads;
+                    v[i] = c < nchunks ? __ldg(reinterpret_cast<const uint4*>(row) + c)
+                                       : make_uint4(0, 0, 0, 0);
+                    mx = max_abs_bf16x2(v[i].x, mx);
+                    mx = max_abs_bf16x2(v[i].y, mx);
+                    mx = max_abs_bf16x2(v[i].z, mx);
+                    mx = max_abs_bf16x2(v[i].w, mx);
+                }
+            } else {
+                for (int k = threadIdx.x; k < K; k += kPrepThreads) mx = max(mx, uint32_t(row[k] & 0x7FFFu));
+            }
+        }
         for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if ((threadIdx.x & 31) == 0) atomicMax(&smax, mx);
         __syncthreads();
@@ -402,24 +464,46 @@ __global__ void __launch_bounds__(256)
         const int sh = 142 - emax;  // in [-113, 141]
         const float f1 = pow2f_exact(sh / 2), f2 = pow2f_exact(sh - sh / 2);
         if (threadIdx.x == 0) xun[m] = (m < M) ? pow2f_exact(-sh) : 0.f;
-        const int nt = m >> 3, gg = m & 7;
-        for (int k = threadIdx.x; k < K; k += blockDim.x) {
-            float v = 0.f;
-            if (m < M) {
-                const float xv = __uint_as_float(uint32_t(x[int64_t(m) * K + k]) << 16);
-                v = (xv * f1) * f2;
+        auto frag = [&](int c) -> uint4* {
+            const int k0 = c * 8;
+            const int blk = k0 >> 5, tt = (k0 & 31) >> 3;
+            return reinterpret_cast<uint4*>(xf + ((int64_t(blk) * NT + nt) * 32 + gg * 4 + tt) * 8);
+        };
+        if (m >= M) {  // padding rows of the fragment tile
+            for (int c = threadIdx.x; c < nchunks; c += kPrepThreads) *frag(c) = make_uint4(0, 0, 0, 0);
+        } else if (fast) {
+#pragma unroll
+            for (int i = 0; i < kPrepChunks; ++i) {
+                const int c = threadIdx.x + i * kPrepThreads;
+                if (c >= nchunks) break;
+                uint4 o;
+                o.x = scale_bf16x2_to_f16x2(v[i].x, f1, f2);
+                o.y = scale_bf16x2_to_f16x2(v[i].y, f1, f2);
+                o.z = scale_bf16x2_to_f16x2(v[i].z, f1, f2);
+                o.w = scale_bf16x2_to_f16x2(v[i].w, f1, f2);
+                *frag(c) = o;
             }
-            const int blk = k >> 5, w = k & 31, tt = w >> 3, j = w & 7;
-            const int64_t idx = ((int64_t(blk) * NT + nt) * 32 + gg * 4 + tt) * 8 + j;
-            xf[idx] = __half_as_ushort(__float2half_rn(v));
+        } else {
+            for (int c = threadIdx.x; c < nchunks; c += kPrepThreads) {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    w[q] = uint32_t(row[c * 8 + 2 * q]) | (uint32_t(row[c * 8 + 2 * q + 1]) << 16);
+                uint4 o;
+                o.x = scale_bf16x2_to_f16x2(w[0], f1, f2);
+                o.y = scale_bf16x2_to_f16x2(w[1], f1, f2);
+                o.z = scale_bf16x2_to_f16x2(w[2], f1, f2);
+                o.w = scale_bf16x2_to_f16x2(w[3], f1, f2);
+                *frag(c) = o;
+            }
         }
     } else if (int(blockIdx.x) == mpad) {
-        for (int i = threadIdx.x; i < ncounters; i += blockDim.x) counters[i] = 0;
+        for (int i = threadIdx.x; i < ncounters; i += kPrepThreads) counters[i] = 0;
     } else if (repack_ctas > 0) {
         // realign scale rows: sc_out[n][0..sc_pitch) = sc_in[n][0..nblk), zero padded
         const int64_t total = N * sc_pitch;
-        const int64_t stride = int64_t(repack_ctas) * blockDim.x;
-        for (int64_t i = int64_t(blockIdx.x - mpad - 1) * blockDim.x + threadIdx.x; i < total;
+        const int64_t stride = int64_t(repack_ctas) * kPrepThreads;
+        for (int64_t i = int64_t(blockIdx.x - mpad - 1) * kPrepThreads + threadIdx.x; i < total;
              i += stride) {
             const int64_t n = i / sc_pitch;
             const int c = int(i - n * sc_pitch);
@@ -553,11 +637,11 @@ static void choose_split(int64_t ntiles, int stages_total, int64_t grid_cap, int
     }
 }
 
-template <int NT, int NWC, int STAGES>
+template <int NT, int RG, int KW, int STAGES>
 static cudaError_t launch_main(GemmParams P, const uint8_t* nib, const uint8_t* sc, int sc_pitch,
                                int64_t K, int64_t items_cap, cudaStream_t stream) {
-    using C = GemmCfg<NT, NWC, STAGES>;
-    auto kern = mxfp4_gemm_kernel<NT, NWC, STAGES>;
+    using C = GemmCfg<NT, RG, KW, STAGES>;
+    auto kern = mxfp4_gemm_kernel<NT, RG, KW, STAGES>;
     static LaunchFacts facts;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -622,11 +706,11 @@ static cudaError_t launch_prep(const uint16_t* x, int M, int K, int NT, uint16_t
     int repack_ctas = 0;
     if (repack) {
         const int64_t total = N * sc_pitch;
-        repack_ctas = int(std::min<int64_t>((total + 255) / 256, 1024));
+        repack_ctas = int(std::min<int64_t>((total + kPrepThreads - 1) / kPrepThreads, 1024));
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(8 * NT + 1 + repack_ctas), 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(kPrepThreads, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -674,11 +758,11 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
         P.status = dev_status;
         const uint8_t* sc = ws.repack_scales ? sc_aligned : scales;
         switch (NT) {
-            case 1: err = launch_main<1, 4, 4>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
-            case 2: err = launch_main<2, 4, 3>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
-            case 3: err = launch_main<3, 8, 3>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
-            case 4: err = launch_main<4, 8, 3>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
-            default: err = launch_main<8, 4, 2>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
+            case 1: err = launch_main<1, 4, 2, 4>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
+            case 2: err = launch_main<2, 4, 2, 3>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
+            case 3: err = launch_main<3, 8, 2, 3>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
+            case 4: err = launch_main<4, 8, 2, 2>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
+            default: err = launch_main<8, 4, 2, 2>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
         }
         if (err != cudaSuccess) return err;
     }
