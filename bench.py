@@ -43,10 +43,10 @@ FALLBACK_HBM_GBS = 6800.0
 
 # Per-launch DRAM traffic of the verify GEMM (read + write bytes) divided by
 # its algorithmic bytes, from the ncu capture summarised in
-# profiles/mxfp4_gemm_kernel_llama8b.md, valid for the gemm.cu source whose
-# sha256 prefix is recorded beside it.  None until a capture exists.
-GEMM_TRAFFIC_RATIO = None
-GEMM_TRAFFIC_SRC_SHA = None
+# profiles/mxfp4_gemm_kernel_lm_head_4096x128256_M5.md, valid for the gemm.cu source whose
+# sha256 prefix is recorded beside it (traffic is reported as null otherwise).
+GEMM_TRAFFIC_RATIO = 1.006
+GEMM_TRAFFIC_SRC_SHA = "a617d484c78ae73e"
 
 WORKLOADS = {
     # name: (model, B, K_spec)
