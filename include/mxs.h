@@ -125,6 +125,38 @@ mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles,
                              void* stream);
 
 /* ------------------------------------------------------------------------
+ * mxfp4_verify_gemm_noalloc -- the same GEMM for callers that cannot
+ * allocate device memory.  (The pages have no counterpart: this is an
+ * interface addition, not part of the method.)
+ *
+ * mxfp4_verify_gemm needs a workspace from its caller.  Some callers cannot
+ * provide one: a plugin inside a host framework that owns every device
+ * allocation and offers no scratch allocator, or a latency-critical path
+ * where cudaMalloc's implicit device-wide synchronisation is not acceptable.
+ * This entry point allocates nothing: its scratch is a file-scope device
+ * array of MXS_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU loading this
+ * part of the library holds until the process exits.
+ *
+ *   Arguments, layouts and accuracy as for mxfp4_verify_gemm, minus the
+ *   workspace.  A shape whose scratch need
+ *   (mxfp4_verify_gemm_workspace_size) exceeds MXS_NOALLOC_SCRATCH_BYTES is
+ *   rejected with MXS_ERR_WORKSPACE before any launch.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make
+ *   that first call before any stream capture.
+ *   All calls on a device share the one array and it keeps the last call's
+ *   contents (the kernels clear what must start at zero).  Calls that
+ *   overlap on the GPU -- on different streams, or from different host
+ *   threads -- race on it and must not be issued.
+ * ---------------------------------------------------------------------- */
+#define MXS_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+mxs_status mxfp4_verify_gemm_noalloc(const void* x, const uint8_t* nibbles,
+                                     const uint8_t* scales, float* y,
+                                     int64_t M, int64_t N, int64_t K,
+                                     int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * spec_accept
  *
  * Exact speculative acceptance for B sequences with K draft tokens each

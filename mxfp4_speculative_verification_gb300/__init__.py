@@ -201,3 +201,28 @@ def hbm_read_probe(src: torch.Tensor, sink: torch.Tensor) -> None:
     dev = _need_cuda(src, sink)
     _check(lib().mxs_hbm_read_probe(_ptr(src), src.numel() * src.element_size() // 16 * 16,
                                     _ptr(sink), _stream(dev)))
+
+
+# ------------------------------------------------------- no-allocation GEMM
+def mxfp4_verify_gemm_noalloc(x: torch.Tensor, nibbles: torch.Tensor, scales: torch.Tensor, *,
+                              out: torch.Tensor | None = None,
+                              dev_status: torch.Tensor | None = None) -> torch.Tensor:
+    """mxfp4_verify_gemm without a workspace, for callers that cannot allocate
+    device memory (e.g. a plugin whose host framework owns every device
+    allocation).  The library's fixed 16 MiB device scratch is used instead;
+    calls must not overlap on the GPU.  ``out`` should be preallocated by such
+    callers (it is allocated here only when omitted)."""
+    L = lib()
+    fn = L.mxfp4_verify_gemm_noalloc
+    if fn.restype is not ctypes.c_int32:
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        fn.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp]
+        fn.restype = ctypes.c_int32
+    M, K = x.shape
+    N = nibbles.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    dev = _need_cuda(x, nibbles, scales, out, dev_status)
+    _check(fn(_ptr(x), _ptr(nibbles), _ptr(scales), _ptr(out), M, N, K, _ptr(dev_status),
+              _stream(dev)))
+    return out
