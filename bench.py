@@ -275,11 +275,13 @@ def run_mxs(args, world, rank, local):
     x_host = {K: torch.from_numpy(workloads.bf16_normal(M, K, seed=rank, tensor_id=K).view(np.int16))
               .view(torch.bfloat16).pin_memory() for K in ks}
     x_dev = {K: x_host[K].to(dev) for K in ks}
-    ys = {}
-    for _, K, N in shapes:
-        ys.setdefault(N, torch.empty((M, N), dtype=torch.float32, device=dev))
+    # one output per GEMM (they are independent problems of the step)
+    ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _, _, N in shapes]
     ws_bytes = max(mxs.mxfp4_verify_gemm_workspace_size(M, N, K) for _, K, N in shapes)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    problems = [(x_dev[K], nib, sc, y) for (_, K, _), (nib, sc), y in zip(shapes, weights, ys)]
+    gws = torch.empty(mxs.mxfp4_verify_gemm_grouped_workspace_size(problems), dtype=torch.uint8,
+                      device=dev)
     p, q, d, u = workloads.spec_inputs(B, K_spec, V, seed=rank, logit_std=2.0)
     acc_host = [torch.from_numpy(a).pin_memory() for a in (p, q, d, u)]
     acc_dev = [a.to(dev) for a in acc_host]
@@ -288,31 +290,39 @@ def run_mxs(args, world, rank, local):
     tok_host = torch.empty_like(out_tok, device="cpu").pin_memory()
     n_host = torch.empty_like(n_emit, device="cpu").pin_memory()
 
-    def gemms():
-        for (_, K, N), (nib, sc) in zip(shapes, weights):
-            mxs.mxfp4_verify_gemm(x_dev[K], nib, sc, out=ys[N], workspace=ws)
+    def gemms_grouped():
+        mxs.mxfp4_verify_gemm_grouped(problems, workspace=gws)
+
+    def gemms_per_call():
+        for (_, K, N), (nib, sc), y in zip(shapes, weights, ys):
+            mxs.mxfp4_verify_gemm(x_dev[K], nib, sc, out=y, workspace=ws)
 
     def accept(reps=1):
         for _ in range(reps):
             mxs.spec_accept(*acc_dev, out_tokens=out_tok, n_emitted=n_emit)
 
     def step():
-        gemms()
+        gemms_grouped()
+        accept()
+
+    def step_per_call():
+        gemms_per_call()
         accept()
 
     stream = torch.cuda.Stream(device=dev)
+    ACC_REPS = 20
+    graphs = {}
     with torch.cuda.stream(stream):
         step()  # eager warm-up: kernel attributes, first launches
+        step_per_call()
         torch.cuda.synchronize(dev)
         n_emitted = n_emit.cpu().numpy()
-        g_step, g_gemm, g_acc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        ACC_REPS = 20
-        with torch.cuda.graph(g_step, stream=stream):
-            step()
-        with torch.cuda.graph(g_gemm, stream=stream):
-            gemms()
-        with torch.cuda.graph(g_acc, stream=stream):
-            accept(ACC_REPS)
+        for name, fn in (("step", step), ("step_pc", step_per_call), ("gemm", gemms_grouped),
+                         ("gemm_pc", gemms_per_call), ("acc", lambda: accept(ACC_REPS))):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            graphs[name] = g
     torch.cuda.synchronize(dev)
 
     gemm_b = sum(gemm_bytes(M, N, K) for _, K, N in shapes)
@@ -341,9 +351,11 @@ def run_mxs(args, world, rank, local):
 
     clocks = ClockSampler(local)
     clocks.start()
-    ms_step = timed(g_step, args.steps)
-    ms_gemm = timed(g_gemm, args.steps)
-    ms_acc = timed(g_acc, args.steps) / ACC_REPS
+    ms_step = timed(graphs["step"], args.steps)
+    ms_gemm = timed(graphs["gemm"], args.steps)
+    ms_step_pc = timed(graphs["step_pc"], args.steps)
+    ms_gemm_pc = timed(graphs["gemm_pc"], args.steps)
+    ms_acc = timed(graphs["acc"], args.steps) / ACC_REPS
     clk = clocks.stop()
 
     # end to end through the public API: pinned host inputs in, tokens out
@@ -377,12 +389,13 @@ def run_mxs(args, world, rank, local):
     peak, peak_kind = load_peaks()
     achieved_gbs = gemm_b / (ms_gemm * 1e-3) / 1e9
     launches = len(shapes)
+    n_main = (len(shapes) + 63) // 64  # grouped launches of at most 64 GEMMs
     traffic = None
     if GEMM_TRAFFIC_RATIO is not None and GEMM_TRAFFIC_SRC_SHA == src_sha():
-        traffic = GEMM_TRAFFIC_RATIO * gemm_b / launches
+        traffic = GEMM_TRAFFIC_RATIO * gemm_b / n_main
 
     if args.detail and rank == 0:
-        per_shape_detail(mxs, torch, stream, dev, shapes, weights, x_dev, ys, ws, M)
+        per_shape_detail(mxs, torch, stream, dev, shapes, weights, x_dev, ws, M)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -405,17 +418,22 @@ def run_mxs(args, world, rank, local):
         "data": "synthetic",
         "config": config_block(args.workload, model, B, K_spec),
         "pct_of_peak": value * 1e3 / peak / world,
-        "roofline": {"bound": "hbm", "kernel": "mxfp4_verify_gemm (prep + mxfp4_gemm_kernel)",
+        "roofline": {"bound": "hbm", "kernel": "mxfp4_gemm_kernel (grouped launches, incl. X preparation)",
                      "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
-                     "bytes_per_launch": gemm_b / launches, "launches_per_step": launches,
-                     "avg_launch_us": ms_gemm * 1e3 / launches, "traffic": traffic},
+                     "bytes_per_launch": gemm_b / n_main, "launches_per_step": n_main,
+                     "avg_launch_us": ms_gemm * 1e3 / n_main, "traffic": traffic},
+        "per_call": {"value": world * step_b / (ms_step_pc * 1e-3) / 1e12, "unit": "TB/s",
+                     "ms_per_step": ms_step_pc,
+                     "gemm_gbs": gemm_b / (ms_gemm_pc * 1e-3) / 1e9,
+                     "path": "one mxfp4_verify_gemm call per GEMM (prep + main kernel each), "
+                             "CUDA graph with programmatic dependent launch"},
         "spec_accept": {"rows_per_s": B / (ms_acc * 1e-3), "us_per_call": ms_acc * 1e3,
                         "bytes_per_call": acc_b, "mean_emitted": float(np.mean(n_emitted))},
         "e2e": {"value": world * step_b / e2e_s / 1e12, "unit": "TB/s",
                 "ms_per_step": e2e_s * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "public Python API -> C ABI, eager launches, pinned host copies"},
-        "gpu_launches": args.steps * (2 * len(shapes) + 1),
+        "gpu_launches": args.steps * (1 + n_main + 1),
         "clocks": clk,
         "cpu_baseline": cpu,
     }
@@ -424,17 +442,18 @@ def run_mxs(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
-def per_shape_detail(mxs, torch, stream, dev, shapes, weights, x_dev, ys, ws, M):
+def per_shape_detail(mxs, torch, stream, dev, shapes, weights, x_dev, ws, M):
     """Per-shape GEMM bandwidth (stderr), each shape timed over all its layers."""
     seen = {}
     for i, (name, K, N) in enumerate(shapes):
         seen.setdefault((K, N), []).append(i)
     for (K, N), idx in seen.items():
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream):
                 for i in idx:
-                    mxs.mxfp4_verify_gemm(x_dev[K], *weights[i], out=ys[N], workspace=ws)
+                    mxs.mxfp4_verify_gemm(x_dev[K], *weights[i], out=y, workspace=ws)
             for _ in range(3):
                 g.replay()
             torch.cuda.synchronize(dev)

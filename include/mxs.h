@@ -125,6 +125,46 @@ mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles,
                              void* stream);
 
 /* ------------------------------------------------------------------------
+ * mxfp4_verify_gemm_grouped -- many independent verify GEMMs in one go
+ *
+ * The verification pass runs every weight matrix of the target model over
+ * the same M candidate positions ("Module 11 ...", §10).  When several of
+ * those GEMMs are independent (Q, K, V or gate and up projections of one
+ * layer, or any set whose outputs feed none of the others' inputs), one
+ * grouped call converts each distinct X once and streams all of their
+ * weights through persistent kernels, instead of paying two launches and a
+ * pipeline fill per GEMM.
+ *
+ *   problems   HOST array of `count` descriptors, read during the call only.
+ *              Per problem: x [M, K] bf16 (problems may share the same x),
+ *              nibbles [N, K/2] (16-byte aligned), scales [N, K/32]
+ *              (16-byte aligned, K % 512 == 0), y [M, N] fp32 written.
+ *              No y may overlap any problem's x, nibbles, scales or another y.
+ *   1 <= count <= 4096, 1 <= M <= 64
+ *   workspace  device, >= mxfp4_verify_gemm_grouped_workspace_size(...)
+ *              bytes, 16-byte aligned.
+ * Results are bit-identical to calling mxfp4_verify_gemm on each problem
+ * whenever that call does not split K (splitting changes only the order
+ * of fp32 additions).
+ * ---------------------------------------------------------------------- */
+typedef struct mxs_gemm_problem {
+    const void* x;
+    const uint8_t* nibbles;
+    const uint8_t* scales;
+    float* y;
+    int64_t N;
+    int64_t K;
+} mxs_gemm_problem;
+
+size_t mxfp4_verify_gemm_grouped_workspace_size(const mxs_gemm_problem* problems,
+                                                int32_t count, int64_t M);
+
+mxs_status mxfp4_verify_gemm_grouped(const mxs_gemm_problem* problems,
+                                     int32_t count, int64_t M, void* workspace,
+                                     size_t workspace_bytes,
+                                     int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * mxfp4_verify_gemm_noalloc -- the same GEMM for callers that cannot
  * allocate device memory.  (The pages have no counterpart: this is an
  * interface addition, not part of the method.)

@@ -23,6 +23,7 @@ import torch
 from . import _build
 
 __all__ = ["build", "lib", "mxfp4_pack", "mxfp4_verify_gemm", "mxfp4_verify_gemm_workspace_size",
+           "mxfp4_verify_gemm_grouped", "mxfp4_verify_gemm_grouped_workspace_size",
            "spec_accept", "hbm_read_probe", "MxsError", "DEV_FLAGS", "declared_symbols"]
 
 MXS_F32, MXS_BF16 = 0, 1
@@ -66,6 +67,10 @@ def lib():
     L.mxfp4_verify_gemm_workspace_size.restype = sz
     L.mxfp4_verify_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, sz, vp, vp]
     L.mxfp4_verify_gemm.restype = i32
+    L.mxfp4_verify_gemm_grouped_workspace_size.argtypes = [vp, i32, i64]
+    L.mxfp4_verify_gemm_grouped_workspace_size.restype = sz
+    L.mxfp4_verify_gemm_grouped.argtypes = [vp, i32, i64, vp, sz, vp, vp]
+    L.mxfp4_verify_gemm_grouped.restype = i32
     L.spec_accept.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, vp, vp, vp]
     L.spec_accept.restype = i32
     L.mxs_hbm_read_probe.argtypes = [vp, sz, vp, vp]
@@ -167,6 +172,54 @@ def mxfp4_verify_gemm(x: torch.Tensor, nibbles: torch.Tensor, scales: torch.Tens
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _ptr(dev_status), _stream(dev)))
     return out
+
+
+class GemmProblem(ctypes.Structure):
+    """C layout of mxs_gemm_problem."""
+    _fields_ = [("x", ctypes.c_void_p), ("nibbles", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+def _problem_array(problems):
+    arr = (GemmProblem * len(problems))()
+    M = None
+    for i, (x, nib, sc, y) in enumerate(problems):
+        if x.dtype != torch.bfloat16 or nib.dtype != torch.uint8 or sc.dtype != torch.uint8 \
+                or y.dtype != torch.float32:
+            raise MxsError("grouped problem dtypes: x bf16, nibbles/scales uint8, y fp32")
+        m, K = x.shape
+        N = nib.shape[0]
+        if nib.shape != (N, K // 2) or sc.shape != (N, K // 32) or y.shape != (m, N):
+            raise MxsError("grouped problem shapes: x [M,K], nibbles [N,K/2], scales [N,K/32], y [M,N]")
+        if M is None:
+            M = m
+        elif m != M:
+            raise MxsError("all grouped problems must share M")
+        arr[i] = GemmProblem(x.data_ptr(), nib.data_ptr(), sc.data_ptr(), y.data_ptr(), N, K)
+    return arr, M
+
+
+def mxfp4_verify_gemm_grouped_workspace_size(problems) -> int:
+    arr, M = _problem_array(problems)
+    return int(lib().mxfp4_verify_gemm_grouped_workspace_size(arr, len(problems), M))
+
+
+def mxfp4_verify_gemm_grouped(problems, *, workspace: torch.Tensor | None = None,
+                              dev_status: torch.Tensor | None = None) -> None:
+    """Independent GEMMs sharing M: problems is a list of (x, nibbles, scales, y)
+    device tensors; each y [M, N] is written with X . dequant(W)^T."""
+    if not problems:
+        return
+    arr, M = _problem_array(problems)
+    dev = _need_cuda(*[t for p in problems for t in p], workspace, dev_status)
+    need = int(lib().mxfp4_verify_gemm_grouped_workspace_size(arr, len(problems), M))
+    if need == 0:
+        raise MxsError("unsupported grouped GEMM (need 1 <= M <= 64, K % 512 == 0, aligned W)")
+    if workspace is None:
+        workspace = _workspace(dev, need)
+    _check(lib().mxfp4_verify_gemm_grouped(arr, len(problems), M, _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(),
+                                           _ptr(dev_status), _stream(dev)))
 
 
 # ---------------------------------------------------------- acceptance

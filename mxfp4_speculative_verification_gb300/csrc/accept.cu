@@ -6,30 +6,38 @@
 // first rejection draw the replacement from norm((p - q)+); when every
 // proposal survives draw the bonus token from the next position's law) and
 // §5 (block B18: the draw is accepted iff draw < acceptance, acceptance 0
-// where q = 0).  The page-3 diagram of "Next-Gen Speculative Decoding and FP4
-// Quantization ..." names this step the "Parallel Softmax & Acceptance
-// Evaluation Mask" of the batched verification kernel.
+// where q = 0).  The pipeline diagram of "Next-Gen Speculative Decoding and
+// FP4 Quantization Shake Up LLM Inference Economics" names this step the
+// "Parallel Softmax & Acceptance Evaluation Mask" of the batched
+// verification kernel.
 //
-// One CTA (1024 threads) per sequence:
-//  * warp 0 gathers p_i(x_i), q_i(x_i), u_i for the K drafts, tests
-//    u*q < p exactly (an fp32 x fp32 product is exact in double) and finds the
-//    first rejection j with one ballot;
-//  * all 32 warps stream the one law that is sampled (residual row j, or p_K),
-//    128 elements per warp step with float4 loads, forming fp32 sums of each
-//    128-element sub-tile (warp shuffle tree) in shared memory;
-//  * a block-wide double scan over the sub-tile sums gives S and the sub-tile
-//    where the CDF crosses u_K * S; warp 0 rescans that sub-tile in double to
-//    find the token: the smallest t with r_t > 0 and C_t > u_K * S.
+// One thread-block cluster of C CTAs per sequence (C = 1..8 by vocabulary
+// size), each CTA owning a contiguous slice of the vocabulary:
+//  * warp 0 of every CTA gathers p_i(x_i), q_i(x_i), u_i for the K drafts,
+//    tests u*q < p exactly (an fp32 x fp32 product is exact in double) and
+//    finds the first rejection j with one ballot (all CTAs agree);
+//  * all warps stream their slice of the one law that is sampled (residual
+//    row pair j, or p_K) with float4 loads, forming fp32 sums of 128-element
+//    sub-tiles in shared memory and the slice total in double;
+//  * the slice totals are exchanged through distributed shared memory and
+//    summed in rank order by every CTA (identical S everywhere); the CTA
+//    whose slice holds the crossing C_t > u_K * S locates the sub-tile with a
+//    double scan and rescans it in double to pick the token.
+#include <cooperative_groups.h>
+
 #include <climits>
 
 #include "mxs_device.cuh"
 #include "mxs_internal.h"
 
+namespace cg = cooperative_groups;
+
 namespace mxs {
 
-constexpr int kAcceptThreads = 1024;
+constexpr int kAcceptThreads = 512;
 constexpr int kAcceptWarps = kAcceptThreads / 32;
 constexpr int kSubTile = 128;  // elements per warp step (float4 per lane)
+constexpr int kMaxCluster = 8;
 constexpr double kNearEdge = 1e-5;
 
 struct AcceptParams {
@@ -39,11 +47,18 @@ struct AcceptParams {
     const float* u;
     int64_t V;
     int K;
-    int nsub;  // ceil(V / kSubTile)
+    int nsub;       // ceil(V / kSubTile)
+    int per_cta;    // sub-tiles per CTA of the cluster
     int32_t* out_tokens;
     int32_t* n_emitted;
     int32_t* row_flags;
     int32_t* status;
+};
+
+// What each CTA publishes to the others of its cluster.
+struct SliceSummary {
+    double total;  // sum of the slice's sub-tile sums (double, fixed order)
+    int lastpos;   // last index with positive mass in the slice (-1 if none)
 };
 
 // Residual (or bonus) mass of 4 consecutive elements starting at e.
@@ -53,9 +68,8 @@ __device__ __forceinline__ void load_law4(const float* __restrict__ prow,
                                           int64_t V, float (&r)[4]) {
     if (VEC && e + 3 < V) {
         const float4 pv = __ldcs(reinterpret_cast<const float4*>(prow + e));
-        float4 qv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (use_res) qv = __ldcs(reinterpret_cast<const float4*>(qrow + e));
         if (use_res) {
+            const float4 qv = __ldcs(reinterpret_cast<const float4*>(qrow + e));
             r[0] = fmaxf(pv.x - qv.x, 0.f);
             r[1] = fmaxf(pv.y - qv.y, 0.f);
             r[2] = fmaxf(pv.z - qv.z, 0.f);
@@ -98,20 +112,20 @@ __device__ __forceinline__ double warp_scan_d(double v, int lane) {
     return v;
 }
 
-// Stream the law once: per-sub-tile fp32 sums into subsum[], and the last
-// index with positive mass into *lastpos.
+// Stream sub-tiles [s0, s1) of the law once: fp32 sums into subsum[st - s0],
+// the last positive index into *lastpos.
 template <bool VEC>
 __device__ void sum_pass(const float* __restrict__ prow, const float* __restrict__ qrow,
-                         bool use_res, int64_t V, int nsub, float* subsum, int* lastpos) {
+                         bool use_res, int64_t V, int s0, int s1, float* subsum, int* lastpos) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int lp = -1;
     constexpr int U = 4;
-    for (int st0 = warp; st0 < nsub; st0 += U * kAcceptWarps) {
+    for (int st0 = s0 + warp; st0 < s1; st0 += U * kAcceptWarps) {
         float r[U][4];
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const int st = st0 + k * kAcceptWarps;
-            if (st < nsub) {
+            if (st < s1) {
                 load_law4<VEC>(prow, qrow, use_res, int64_t(st) * kSubTile + 4 * lane, V, r[k]);
             } else {
                 r[k][0] = r[k][1] = r[k][2] = r[k][3] = 0.f;
@@ -120,9 +134,9 @@ __device__ void sum_pass(const float* __restrict__ prow, const float* __restrict
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const int st = st0 + k * kAcceptWarps;
-            if (st >= nsub) break;
+            if (st >= s1) break;
             const float s = warp_sum_f((r[k][0] + r[k][1]) + (r[k][2] + r[k][3]));
-            if (lane == 0) subsum[st] = s;
+            if (lane == 0) subsum[st - s0] = s;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 if (r[k][i] > 0.f) lp = max(lp, st * kSubTile + 4 * lane + i);
@@ -133,11 +147,11 @@ __device__ void sum_pass(const float* __restrict__ prow, const float* __restrict
     if (lane == 0 && lp >= 0) atomicMax(lastpos, lp);
 }
 
-// S = sum of the sub-tile sums, in a fixed order (thread-strided, then tree).
-__device__ double block_total(const float* subsum, int nsub, double* wtot) {
+// Sum of the slice's sub-tile sums in a fixed order (thread-strided, then tree).
+__device__ double slice_total(const float* subsum, int n, double* wtot) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     double s = 0.0;
-    for (int i = threadIdx.x; i < nsub; i += kAcceptThreads) s += double(subsum[i]);
+    for (int i = threadIdx.x; i < n; i += kAcceptThreads) s += double(subsum[i]);
     s = warp_sum_d(s);
     if (lane == 0) wtot[warp] = s;
     __syncthreads();
@@ -152,9 +166,13 @@ __global__ void __launch_bounds__(kAcceptThreads) spec_accept_kernel(const Accep
     extern __shared__ float subsum[];
     __shared__ double wtot[kAcceptWarps];
     __shared__ double sh_prefix;
+    __shared__ SliceSummary sh_mine;
     __shared__ int sh_j, sh_flags, sh_err, sh_lastpos, sh_tstar;
 
-    const int64_t b = blockIdx.x;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = int(cluster.num_blocks());
+    const int rank = int(cluster.block_rank());
+    const int64_t b = blockIdx.x / C;
     const int K = P.K;
     const int64_t V = P.V;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -200,12 +218,14 @@ __global__ void __launch_bounds__(kAcceptThreads) spec_accept_kernel(const Accep
 
     const int j = sh_j;
     int32_t* tok = P.out_tokens + b * (K + 1);
-    if (sh_err) {
-        if (threadIdx.x <= K) tok[threadIdx.x] = -1;
-        if (threadIdx.x == 0) {
-            P.n_emitted[b] = 0;
-            if (P.row_flags) P.row_flags[b] = sh_flags;
-            report(P.status, sh_flags);
+    if (sh_err) {  // uniform across the cluster: no cluster barrier is reached
+        if (rank == 0) {
+            for (int i = threadIdx.x; i <= K; i += blockDim.x) tok[i] = -1;
+            if (threadIdx.x == 0) {
+                P.n_emitted[b] = 0;
+                if (P.row_flags) P.row_flags[b] = sh_flags;
+                report(P.status, sh_flags);
+            }
         }
         return;
     }
@@ -214,9 +234,35 @@ __global__ void __launch_bounds__(kAcceptThreads) spec_accept_kernel(const Accep
     bool use_res = j < K;
     const float* prow = P.p + (b * (K + 1) + j) * V;
     const float* qrow = use_res ? P.q + (b * K + j) * V : nullptr;
-    sum_pass<VEC>(prow, qrow, use_res, V, P.nsub, subsum, &sh_lastpos);
-    __syncthreads();
-    double S = block_total(subsum, P.nsub, wtot);
+    const int s0 = min(P.nsub, rank * P.per_cta);
+    const int s1 = min(P.nsub, s0 + P.per_cta);
+    const int nloc = s1 - s0;
+
+    // Sum this CTA's slice, publish it, and read every slice of the cluster.
+    // Returns S (identical bits in every CTA) and this slice's prefix.
+    auto exchange = [&](double& S, double& prefix, int& lastpos) {
+        sum_pass<VEC>(prow, qrow, use_res, V, s0, s1, subsum, &sh_lastpos);
+        __syncthreads();
+        const double tot = slice_total(subsum, nloc, wtot);
+        if (threadIdx.x == 0) {
+            sh_mine.total = tot;
+            sh_mine.lastpos = sh_lastpos;
+        }
+        cluster.sync();
+        S = 0.0;
+        prefix = 0.0;
+        lastpos = -1;
+        for (int c = 0; c < C; ++c) {
+            const SliceSummary o = *cluster.map_shared_rank(&sh_mine, c);
+            if (c == rank) prefix = S;
+            S += o.total;
+            lastpos = max(lastpos, o.lastpos);
+        }
+        cluster.sync();  // every CTA has read every summary
+    };
+    double S, prefix;
+    int lastpos;
+    exchange(S, prefix, lastpos);
     if (!(S > 0.0)) {
         // A positive residual exists whenever rejection is possible; only the
         // rounding of the inputs gets here.  Sample p_j instead.
@@ -226,12 +272,33 @@ __global__ void __launch_bounds__(kAcceptThreads) spec_accept_kernel(const Accep
         }
         __syncthreads();
         use_res = false;
-        sum_pass<VEC>(prow, nullptr, false, V, P.nsub, subsum, &sh_lastpos);
-        __syncthreads();
-        S = block_total(subsum, P.nsub, wtot);
+        qrow = nullptr;
+        exchange(S, prefix, lastpos);
     }
-    if (!(S > 0.0) || isinf(S) || isnan(S)) {
-        if (threadIdx.x <= K) tok[threadIdx.x] = -1;
+    const bool no_law = !(S > 0.0) || isinf(S) || isnan(S);
+    const double uK = double(P.u[b * (K + 1) + K]);
+    const double thr = uK * S;
+
+    // The slice holding the first crossing, computed identically everywhere.
+    int owner = -1;
+    if (!no_law) {
+        double run = 0.0;
+        for (int c = 0; c < C; ++c) {
+            const double t = cluster.map_shared_rank(&sh_mine, c)->total;
+            if (t > 0.0 && run + t > thr) {
+                owner = c;
+                break;
+            }
+            run += t;
+        }
+    }
+    // Summaries stay readable until every CTA has located the owner.
+    cluster.sync();
+    const int writer = (no_law || owner < 0) ? 0 : owner;
+    if (rank != writer) return;
+
+    if (no_law) {
+        for (int i = threadIdx.x; i <= K; i += blockDim.x) tok[i] = -1;
         if (threadIdx.x == 0) {
             const int f = sh_flags | MXS_DEV_NO_LAW;
             P.n_emitted[b] = 0;
@@ -240,27 +307,25 @@ __global__ void __launch_bounds__(kAcceptThreads) spec_accept_kernel(const Accep
         }
         return;
     }
-    const double uK = double(P.u[b * (K + 1) + K]);
-    const double thr = uK * S;
 
     // --------------------------- locate the sub-tile where C crosses thr
-    {
-        const int per = (P.nsub + kAcceptThreads - 1) / kAcceptThreads;
-        const int s0 = min(P.nsub, int(threadIdx.x) * per);
-        const int s1 = min(P.nsub, s0 + per);
+    if (owner >= 0) {
+        const int per = (nloc + kAcceptThreads - 1) / kAcceptThreads;
+        const int a0 = min(nloc, int(threadIdx.x) * per);
+        const int a1 = min(nloc, a0 + per);
         double local = 0.0;
-        for (int st = s0; st < s1; ++st) local += double(subsum[st]);
+        for (int st = a0; st < a1; ++st) local += double(subsum[st]);
         const double inc = warp_scan_d(local, lane);
         if (lane == 31) wtot[warp] = inc;
         __syncthreads();
         if (warp == 0) {
-            const double wt = wtot[lane];
+            const double wt = lane < kAcceptWarps ? wtot[lane] : 0.0;
             const double winc = warp_scan_d(wt, lane);
-            wtot[lane] = winc - wt;  // exclusive prefix of warp totals
+            if (lane < kAcceptWarps) wtot[lane] = winc - wt;  // exclusive prefix of warp totals
         }
         __syncthreads();
-        double run = wtot[warp] + (inc - local);
-        for (int st = s0; st < s1; ++st) {
+        double run = prefix + wtot[warp] + (inc - local);
+        for (int st = a0; st < a1; ++st) {
             const float s = subsum[st];
             const double end = run + double(s);
             if (s > 0.f && end > thr) {
@@ -271,10 +336,19 @@ __global__ void __launch_bounds__(kAcceptThreads) spec_accept_kernel(const Accep
         }
         __syncthreads();
         // the owner of the first crossing publishes its starting prefix
-        run = wtot[warp] + (inc - local);
-        for (int st = s0; st < s1; ++st) {
+        run = prefix + wtot[warp] + (inc - local);
+        for (int st = a0; st < a1; ++st) {
             if (st == sh_tstar) sh_prefix = run;
             run += double(subsum[st]);
+        }
+        __syncthreads();
+        if (sh_tstar == INT_MAX && threadIdx.x == 0) {
+            // Summed in this order the slice ends at or below u*S (a rounding
+            // tie with its total): continue the rescan after the slice.
+            double end = prefix;
+            for (int st = 0; st < nloc; ++st) end += double(subsum[st]);
+            sh_prefix = end;
+            sh_tstar = nloc;
         }
         __syncthreads();
     }
@@ -283,9 +357,9 @@ __global__ void __launch_bounds__(kAcceptThreads) spec_accept_kernel(const Accep
     if (warp == 0) {
         int pick = -1;
         double before = 0.0, after = 0.0;
-        if (sh_tstar != INT_MAX) {
+        if (owner >= 0 && sh_tstar != INT_MAX) {
             double run = sh_prefix;
-            for (int st = sh_tstar; st < P.nsub && pick < 0; ++st) {
+            for (int st = s0 + sh_tstar; st < P.nsub && pick < 0; ++st) {
                 float r[4];
                 load_law4<VEC>(prow, qrow, use_res, int64_t(st) * kSubTile + 4 * lane, V, r);
                 double c[4];
@@ -319,7 +393,7 @@ __global__ void __launch_bounds__(kAcceptThreads) spec_accept_kernel(const Accep
         }
         if (pick < 0) {
             // rounding put u*S at or beyond the last positive mass
-            pick = sh_lastpos;
+            pick = lastpos;
             float rl[4];
             const int64_t e = int64_t(pick) & ~int64_t(3);
             load_law4<false>(prow, qrow, use_res, e, V, rl);
@@ -354,26 +428,34 @@ cudaError_t accept_run(const float* p, const float* q, const int32_t* draft, con
     P.V = V;
     P.K = int(K);
     P.nsub = int((V + kSubTile - 1) / kSubTile);
+    // cluster size: about 64 sub-tiles (8192 elements) or more per CTA
+    int C = (P.nsub + 63) / 64;
+    C = C < 1 ? 1 : (C > kMaxCluster ? kMaxCluster : C);
+    while (int64_t(B) * C > int64_t(INT32_MAX)) C >>= 1;
+    P.per_cta = (P.nsub + C - 1) / C;
     P.out_tokens = out_tokens;
     P.n_emitted = n_emitted;
     P.row_flags = row_flags;
     P.status = dev_status;
     const bool vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
                      (K == 0 || reinterpret_cast<uintptr_t>(q) % 16 == 0);
-    const size_t smem = size_t(P.nsub) * sizeof(float);
-    cudaError_t err;
-    if (vec) {
-        err = cudaFuncSetAttribute(spec_accept_kernel<true>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (err != cudaSuccess) return err;
-        spec_accept_kernel<true><<<unsigned(B), kAcceptThreads, smem, stream>>>(P);
-    } else {
-        err = cudaFuncSetAttribute(spec_accept_kernel<false>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (err != cudaSuccess) return err;
-        spec_accept_kernel<false><<<unsigned(B), kAcceptThreads, smem, stream>>>(P);
-    }
-    return cudaGetLastError();
+    const size_t smem = size_t(P.per_cta) * sizeof(float);
+    auto kern = vec ? spec_accept_kernel<true> : spec_accept_kernel<false>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(B * C), 1, 1);
+    cfg.blockDim = dim3(kAcceptThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = unsigned(C);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
 }  // namespace mxs

@@ -1,6 +1,7 @@
 // The C ABI of libmxs (declared in include/mxs.h): host-side validation,
 // then the launchers in gemm.cu, accept.cu and pack.cu.
 #include <cstdint>
+#include <vector>
 
 #include "mxs.h"
 #include "mxs_internal.h"
@@ -16,6 +17,29 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 mxs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MXS_OK : MXS_ERR_CUDA; }
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+bool grouped_valid(const mxs_gemm_problem* problems, int32_t count, int64_t M,
+                          std::vector<mxs::GroupedGemm>& out, mxs_status& st) {
+    st = MXS_OK;
+    if (!problems || count < 1 || M < 1) { st = MXS_ERR_INVALID_ARG; return false; }
+    if (count > 4096 || M > mxs::kGemmMaxRowsPerPass) { st = MXS_ERR_UNSUPPORTED; return false; }
+    out.resize(size_t(count));
+    for (int32_t i = 0; i < count; ++i) {
+        const mxs_gemm_problem& p = problems[i];
+        if (!p.x || !p.nibbles || !p.scales || !p.y || p.N < 1 || p.K < 32 || p.K % 32 != 0) {
+            st = MXS_ERR_INVALID_ARG;
+            return false;
+        }
+        if (p.N > kMaxN || p.K > kMaxK || p.K % 512 != 0) { st = MXS_ERR_UNSUPPORTED; return false; }
+        if (!aligned(p.x, 2) || !aligned(p.nibbles, 16) || !aligned(p.scales, 16) || !aligned(p.y, 4)) {
+            st = MXS_ERR_MISALIGNED;
+            return false;
+        }
+        out[size_t(i)] = mxs::GroupedGemm{static_cast<const uint16_t*>(p.x), p.nibbles, p.scales,
+                                          p.y, p.N, p.K};
+    }
+    return true;
+}
 
 }  // namespace
 
@@ -55,6 +79,28 @@ mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles, const uint8_
     if (!aligned(workspace, 16)) return MXS_ERR_MISALIGNED;
     return cuda_status(mxs::gemm_run(static_cast<const uint16_t*>(x), nibbles, scales, y, M, N, K,
                                      workspace, ws, dev_status, as_stream(stream)));
+}
+
+size_t mxfp4_verify_gemm_grouped_workspace_size(const mxs_gemm_problem* problems, int32_t count,
+                                                int64_t M) {
+    std::vector<mxs::GroupedGemm> gs;
+    mxs_status st;
+    if (!grouped_valid(problems, count, M, gs, st)) return 0;
+    return mxs::gemm_grouped_workspace(gs.data(), count, M);
+}
+
+mxs_status mxfp4_verify_gemm_grouped(const mxs_gemm_problem* problems, int32_t count, int64_t M,
+                                     void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                     void* stream) {
+    std::vector<mxs::GroupedGemm> gs;
+    mxs_status st;
+    if (!grouped_valid(problems, count, M, gs, st)) return st;
+    if (!aligned(dev_status, 4)) return MXS_ERR_MISALIGNED;
+    const size_t need = mxs::gemm_grouped_workspace(gs.data(), count, M);
+    if (!workspace || workspace_bytes < need) return MXS_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return MXS_ERR_MISALIGNED;
+    return cuda_status(mxs::gemm_grouped_run(gs.data(), count, M, workspace, dev_status,
+                                             as_stream(stream)));
 }
 
 mxs_status spec_accept(const float* p, const float* q, const int32_t* draft, const float* u,

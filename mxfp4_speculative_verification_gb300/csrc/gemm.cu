@@ -33,6 +33,7 @@
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
+#include <vector>
 
 #include <cuda_fp16.h>
 
@@ -48,20 +49,32 @@ constexpr int kFragBytesPerBlockTile = 512;      // one 32-k block x 8 rows of X
 constexpr int kMaxSplit = 32;
 constexpr int64_t kMaxSplitItems = 2048;         // bound on tiles x splits when K is split
 
-struct GemmParams {
-    const uint16_t* xf;  // fragments [nblk][NT][32 lanes][8 fp16]
-    const float* xun;    // [8*NT] per-row unscale
-    float* y;            // [M, N]
-    float* part;         // split-K partial tiles [items][M][BN]
-    int* counters;       // split-K arrival counters [ntiles]
+// One GEMM of a launch.  Tensor maps first: they need 64-byte alignment.
+struct Problem {
+    CUtensorMap tm_w;      // nibbles [N, K/2]: boxes of 128 B x BN rows, 128-byte swizzle
+    CUtensorMap tm_s;      // scales [N, nblk] (16-byte row pitch): boxes of 16 B x BN rows
+    const uint16_t* xf;    // X fragments [nblk][NT][32 lanes][8 fp16]
+    const float* xun;      // [8*NT] per-row unscale
+    float* y;              // [M, N]
+    float* part;           // split-K partial tiles [ntiles*nsplit][M][BN]
+    int* counters;         // split-K arrival counters [ntiles]
     int64_t N;
-    int M;
-    int nblk;            // K / 32
+    int nblk;              // K / 32
     int ntiles;
     int nsplit;
     int stages_per_split;
-    int items;           // ntiles * nsplit
-    int sc_from_prep;    // scales were realigned by the preparation kernel
+    int item_begin;        // first work item of this GEMM within the launch
+    int sc_from_prep;      // scales were realigned by the preparation kernel
+};
+
+// The GEMMs of one launch (a kernel parameter, read in place).  They share
+// the row count M of X and are independent of one another.
+template <int G>
+struct ProblemSet {
+    Problem p[G];
+    int count;
+    int items;  // total work items
+    int M;
     int32_t* status;
 };
 
@@ -171,7 +184,7 @@ struct ItemRange {
     int tile, split, kb0, kb1, nst;
 };
 
-__device__ __forceinline__ ItemRange item_range(const GemmParams& P, int w) {
+__device__ __forceinline__ ItemRange item_range(const Problem& P, int w) {
     ItemRange r;
     r.tile = w % P.ntiles;
     r.split = w / P.ntiles;
@@ -181,10 +194,22 @@ __device__ __forceinline__ ItemRange item_range(const GemmParams& P, int w) {
     return r;
 }
 
-template <int NT, int RG, int KW, int STAGES>
+// The GEMM that work item w belongs to (binary search over item_begin).
+template <int G>
+__device__ __forceinline__ int find_problem(const ProblemSet<G>& S, int w) {
+    if (G == 1) return 0;
+    int lo = 0, hi = S.count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (S.p[mid].item_begin <= w) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <int NT, int RG, int KW, int STAGES, int G>
 __global__ void __launch_bounds__(32 * (RG * KW + 1))
-    mxfp4_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
-                      const __grid_constant__ CUtensorMap tm_s, const GemmParams P) {
+    mxfp4_gemm_kernel(const __grid_constant__ ProblemSet<G> S) {
     using C = GemmCfg<NT, RG, KW, STAGES>;
     constexpr int NWC = C::NWC;
     extern __shared__ uint8_t smem_raw[];
@@ -214,32 +239,39 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
     if (warp == NWC) {
         // ------------------------------------------------------- producer
         if (lane != 0) return;
-        prefetch_tmap(&tm_w);
-        prefetch_tmap(&tm_s);
         const uint64_t pol_w = policy_evict_first();
         const uint64_t pol_x = policy_evict_last();
         // copies that depend on the preparation kernel are deferred until
         // the first STAGES stages of weights are in flight
-        int def_slot[STAGES], def_kb[STAGES], def_nb[STAGES], def_n0[STAGES];
+        int def_slot[STAGES], def_kb[STAGES], def_nb[STAGES], def_n0[STAGES], def_pi[STAGES];
         int ndef = 0;
         bool waited = false;
-        auto issue_dep = [&](int slot, int kb, int nb, int n0) {
+        auto issue_dep = [&](int slot, int kb, int nb, int n0, int pi) {
+            const Problem& pb = S.p[pi];
             const uint32_t stage = smem_base + slot * C::kStageBytes;
             const uint32_t bar = full_bar + 8 * slot;
-            if (P.sc_from_prep) tma_2d(stage + C::kWBytes, &tm_s, kb, n0, bar, pol_w);
+            if (pb.sc_from_prep) tma_2d(stage + C::kWBytes, &pb.tm_s, kb, n0, bar, pol_w);
             bulk_g2s(stage + C::kWBytes + C::kSBytes,
-                     P.xf + int64_t(kb) * NT * (kFragBytesPerBlockTile / 2),
+                     pb.xf + int64_t(kb) * NT * (kFragBytesPerBlockTile / 2),
                      uint32_t(nb) * NT * kFragBytesPerBlockTile, bar, pol_x);
         };
         int it = 0;
+        int last_pi = -1;
         bool ok = true;
-        for (int w = blockIdx.x; ok && w < P.items; w += gridDim.x) {
-            const ItemRange R = item_range(P, w);
+        for (int w = blockIdx.x; ok && w < S.items; w += gridDim.x) {
+            const int pi = find_problem(S, w);
+            const Problem& pb = S.p[pi];
+            if (pi != last_pi) {
+                prefetch_tmap(&pb.tm_w);
+                prefetch_tmap(&pb.tm_s);
+                last_pi = pi;
+            }
+            const ItemRange R = item_range(pb, w - pb.item_begin);
             const int n0 = R.tile * C::BN;
             for (int i = 0; i < R.nst; ++i, ++it) {
                 const int slot = it % STAGES;
                 if (it >= STAGES &&
-                    !mbar_wait(empty_bar + 8 * slot, ((it / STAGES) - 1) & 1, P.status)) {
+                    !mbar_wait(empty_bar + 8 * slot, ((it / STAGES) - 1) & 1, S.status)) {
                     ok = false;
                     break;
                 }
@@ -249,34 +281,36 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
                 const uint32_t bar = full_bar + 8 * slot;
                 mbar_arrive_expect_tx(bar, uint32_t(C::kWBytes + C::kSBytes) +
                                                uint32_t(nb) * NT * kFragBytesPerBlockTile);
-                tma_2d(stage, &tm_w, kb * 16, n0, bar, pol_w);
-                tma_2d(stage + C::kBoxW, &tm_w, kb * 16 + kBoxBytes, n0, bar, pol_w);
-                if (!P.sc_from_prep) tma_2d(stage + C::kWBytes, &tm_s, kb, n0, bar, pol_w);
+                tma_2d(stage, &pb.tm_w, kb * 16, n0, bar, pol_w);
+                tma_2d(stage + C::kBoxW, &pb.tm_w, kb * 16 + kBoxBytes, n0, bar, pol_w);
+                if (!pb.sc_from_prep) tma_2d(stage + C::kWBytes, &pb.tm_s, kb, n0, bar, pol_w);
                 if (waited) {
-                    issue_dep(slot, kb, nb, n0);
+                    issue_dep(slot, kb, nb, n0, pi);
                 } else {
                     def_slot[ndef] = slot;
                     def_kb[ndef] = kb;
                     def_nb[ndef] = nb;
                     def_n0[ndef] = n0;
+                    def_pi[ndef] = pi;
                     ++ndef;
                     if (ndef == STAGES) {
                         pdl_wait();
                         waited = true;
                         for (int d = 0; d < ndef; ++d)
-                            issue_dep(def_slot[d], def_kb[d], def_nb[d], def_n0[d]);
+                            issue_dep(def_slot[d], def_kb[d], def_nb[d], def_n0[d], def_pi[d]);
                     }
                 }
             }
         }
         if (!waited) {
             pdl_wait();
-            for (int d = 0; d < ndef; ++d) issue_dep(def_slot[d], def_kb[d], def_nb[d], def_n0[d]);
+            for (int d = 0; d < ndef; ++d)
+                issue_dep(def_slot[d], def_kb[d], def_nb[d], def_n0[d], def_pi[d]);
         }
         // never leave a copy in flight: wait (bounded) for the last phase of
         // every slot filled
         for (int j = max(0, it - STAGES); j < it; ++j)
-            mbar_wait(full_bar + 8 * (j % STAGES), (j / STAGES) & 1, P.status);
+            mbar_wait(full_bar + 8 * (j % STAGES), (j / STAGES) & 1, S.status);
         return;
     }
 
@@ -289,20 +323,22 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
     uint32_t lm[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) lm[j] = uint32_t(((2 * j + (mi >> 1)) ^ ri) << 4);
-    const int M = P.M;
+    const int M = S.M;
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     bool waited = false;
     int it = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < P.items; w += gridDim.x) {
-        const ItemRange R = item_range(P, w);
+    for (int w = blockIdx.x; w < S.items; w += gridDim.x) {
+        const Problem& P = S.p[find_problem(S, w)];
+        const int wl = w - P.item_begin;  // item index within its GEMM
+        const ItemRange R = item_range(P, wl);
         const int64_t n0 = int64_t(R.tile) * C::BN;
         const int rows = int(P.N - n0 < int64_t(C::BN) ? P.N - n0 : int64_t(C::BN));
         for (int i = 0; ok && i < R.nst; ++i, ++it) {
             const int slot = it % STAGES;
-            if (!mbar_wait(full_bar + 8 * slot, (it / STAGES) & 1, P.status)) {
+            if (!mbar_wait(full_bar + 8 * slot, (it / STAGES) & 1, S.status)) {
                 ok = false;
                 break;
             }
@@ -363,7 +399,7 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
                 if (r < rows) P.y[int64_t(m) * P.N + n0 + r] = tile_val(r, m) * P.xun[m];
             }
         } else {
-            float* mine = P.part + int64_t(w) * M * C::BN;
+            float* mine = P.part + int64_t(wl) * M * C::BN;
             for (int o = threadIdx.x; o < C::BN * M; o += C::kConsumers) {
                 const int r = o % C::BN, m = o / C::BN;
                 __stcg(mine + int64_t(m) * C::BN + r, tile_val(r, m));
@@ -420,16 +456,44 @@ __device__ __forceinline__ uint32_t scale_bf16x2_to_f16x2(uint32_t w, float f1, 
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__global__ void __launch_bounds__(kPrepThreads)
-    mxfp4_gemm_prep_kernel(const uint16_t* __restrict__ x, int M, int K, int NT,
-                           uint16_t* __restrict__ xf, float* __restrict__ xun, int* counters,
-                           int ncounters, const uint8_t* __restrict__ sc_in, int64_t N, int nblk,
-                           int sc_pitch, uint8_t* __restrict__ sc_out, int repack_ctas) {
+// One distinct X of a launch.
+struct PrepJob {
+    const uint16_t* x;  // [M, K] bf16
+    uint16_t* xf;       // fragments out
+    float* xun;         // [8*NT] unscale factors out
+    int K;
+};
+
+constexpr int kPrepMaxJobs = 16;
+
+struct PrepSet {
+    PrepJob job[kPrepMaxJobs];
+    int njobs;
+    int M;
+    int NT;
+    int* counters;        // split-K counters to zero (may be null)
+    int ncounters;
+    const uint8_t* sc_in;  // scale realignment (single GEMM only; null otherwise)
+    int64_t N;
+    int nblk;
+    int sc_pitch;
+    uint8_t* sc_out;
+    int repack_ctas;
+};
+
+__global__ void __launch_bounds__(kPrepThreads) mxfp4_gemm_prep_kernel(const __grid_constant__ PrepSet Q) {
     pdl_trigger();
     pdl_wait();  // the workspace may still be in use by the previous GEMM
+    const int NT = Q.NT, M = Q.M;
     const int mpad = 8 * NT;
-    if (int(blockIdx.x) < mpad) {
-        const int m = blockIdx.x;
+    const int nrow_ctas = Q.njobs * mpad;
+    if (int(blockIdx.x) < nrow_ctas) {
+        const PrepJob& J = Q.job[blockIdx.x / mpad];
+        const int K = J.K;
+        const uint16_t* __restrict__ x = J.x;
+        uint16_t* __restrict__ xf = J.xf;
+        float* __restrict__ xun = J.xun;
+        const int m = blockIdx.x % mpad;
         const int nt = m >> 3, gg = m & 7;
         __shared__ uint32_t smax;
         if (threadIdx.x == 0) smax = 0;
@@ -497,17 +561,17 @@ __global__ void __launch_bounds__(kPrepThreads)
                 *frag(c) = o;
             }
         }
-    } else if (int(blockIdx.x) == mpad) {
-        for (int i = threadIdx.x; i < ncounters; i += kPrepThreads) counters[i] = 0;
-    } else if (repack_ctas > 0) {
+    } else if (int(blockIdx.x) == nrow_ctas) {
+        for (int i = threadIdx.x; i < Q.ncounters; i += kPrepThreads) Q.counters[i] = 0;
+    } else if (Q.repack_ctas > 0) {
         // realign scale rows: sc_out[n][0..sc_pitch) = sc_in[n][0..nblk), zero padded
-        const int64_t total = N * sc_pitch;
-        const int64_t stride = int64_t(repack_ctas) * kPrepThreads;
-        for (int64_t i = int64_t(blockIdx.x - mpad - 1) * kPrepThreads + threadIdx.x; i < total;
-             i += stride) {
-            const int64_t n = i / sc_pitch;
-            const int c = int(i - n * sc_pitch);
-            sc_out[i] = c < nblk ? sc_in[n * nblk + c] : uint8_t(0);
+        const int64_t total = Q.N * Q.sc_pitch;
+        const int64_t stride = int64_t(Q.repack_ctas) * kPrepThreads;
+        for (int64_t i = int64_t(blockIdx.x - nrow_ctas - 1) * kPrepThreads + threadIdx.x;
+             i < total; i += stride) {
+            const int64_t n = i / Q.sc_pitch;
+            const int c = int(i - n * Q.sc_pitch);
+            Q.sc_out[i] = c < Q.nblk ? Q.sc_in[n * Q.nblk + c] : uint8_t(0);
         }
     }
 }
@@ -637,11 +701,26 @@ static void choose_split(int64_t ntiles, int stages_total, int64_t grid_cap, int
     }
 }
 
-template <int NT, int RG, int KW, int STAGES>
-static cudaError_t launch_main(GemmParams P, const uint8_t* nib, const uint8_t* sc, int sc_pitch,
-                               int64_t K, int64_t items_cap, cudaStream_t stream) {
+// One GEMM as the host describes it before the launch is planned.
+struct HostGemm {
+    const uint8_t* nib;
+    const uint8_t* sc;   // the scale rows actually streamed (in place or realigned)
+    int sc_pitch;
+    bool sc_from_prep;
+    const uint16_t* xf;
+    const float* xun;
+    float* y;
+    float* part;
+    int* counters;
+    int64_t N, K;
+    int64_t items_cap;   // 0: never split K
+};
+
+template <int NT, int RG, int KW, int STAGES, int G>
+static cudaError_t launch_main(const HostGemm* gs, int count, int M, int32_t* status,
+                               cudaStream_t stream) {
     using C = GemmCfg<NT, RG, KW, STAGES>;
-    auto kern = mxfp4_gemm_kernel<NT, RG, KW, STAGES>;
+    auto kern = mxfp4_gemm_kernel<NT, RG, KW, STAGES, G>;
     static LaunchFacts facts;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -662,29 +741,55 @@ static cudaError_t launch_main(GemmParams P, const uint8_t* nib, const uint8_t* 
         facts.occ[dev].store(occ, std::memory_order_release);
         facts.sms[dev].store(sms, std::memory_order_release);
     }
-
-    P.ntiles = int((P.N + C::BN - 1) / C::BN);
-    const int stages_total = (P.nblk + kStageBlocks - 1) / kStageBlocks;
     const int64_t resident = int64_t(sms) * occ;
-    choose_split(P.ntiles, stages_total, resident, items_cap, P.nsplit, P.stages_per_split);
-    const int forced = env_int("MXS_GEMM_SPLITS", 0);
-    if (forced > 0) {
-        int ns = std::min(forced, stages_total);
-        const int sps = (stages_total + ns - 1) / ns;
-        ns = (stages_total + sps - 1) / sps;
-        if (ns == 1 || int64_t(P.ntiles) * ns <= items_cap) {
-            P.nsplit = ns;
-            P.stages_per_split = sps;
-        }
-    }
-    P.items = P.ntiles * P.nsplit;
-    const int64_t grid = std::min<int64_t>(P.items, resident);
 
-    CUtensorMap tm_w, tm_s;
-    if (!make_map(&tm_w, nib, P.N, K / 2, K / 2, kBoxBytes, C::BN, true))
-        return cudaErrorInvalidValue;
-    if (!make_map(&tm_s, sc, P.N, P.nblk, sc_pitch, 16, C::BN, false))
-        return cudaErrorInvalidValue;
+    // the problem table lives in the (large) kernel parameter block
+    static thread_local ProblemSet<G>* S_buf = nullptr;
+    if (!S_buf) S_buf = new ProblemSet<G>;
+    ProblemSet<G>& S = *S_buf;
+    std::memset(&S, 0, sizeof(S));
+    S.count = count;
+    S.M = M;
+    S.status = status;
+    int64_t items = 0;
+    const int forced = env_int("MXS_GEMM_SPLITS", 0);
+    for (int i = 0; i < count; ++i) {
+        const HostGemm& h = gs[i];
+        Problem& p = S.p[i];
+        p.xf = h.xf;
+        p.xun = h.xun;
+        p.y = h.y;
+        p.part = h.part;
+        p.counters = h.counters;
+        p.N = h.N;
+        p.nblk = int(h.K / 32);
+        p.ntiles = int((h.N + C::BN - 1) / C::BN);
+        p.sc_from_prep = h.sc_from_prep ? 1 : 0;
+        const int stages_total = (p.nblk + kStageBlocks - 1) / kStageBlocks;
+        p.nsplit = 1;
+        p.stages_per_split = stages_total;
+        if (h.items_cap > 0) {
+            choose_split(p.ntiles, stages_total, resident, h.items_cap, p.nsplit, p.stages_per_split);
+            if (forced > 0) {
+                int ns = std::min(forced, stages_total);
+                const int sps = (stages_total + ns - 1) / ns;
+                ns = (stages_total + sps - 1) / sps;
+                if (ns == 1 || int64_t(p.ntiles) * ns <= h.items_cap) {
+                    p.nsplit = ns;
+                    p.stages_per_split = sps;
+                }
+            }
+        }
+        p.item_begin = int(items);
+        items += int64_t(p.ntiles) * p.nsplit;
+        if (items > INT32_MAX) return cudaErrorInvalidValue;
+        if (!make_map(&p.tm_w, h.nib, h.N, h.K / 2, h.K / 2, kBoxBytes, C::BN, true))
+            return cudaErrorInvalidValue;
+        if (!make_map(&p.tm_s, h.sc, h.N, p.nblk, h.sc_pitch, 16, C::BN, false))
+            return cudaErrorInvalidValue;
+    }
+    S.items = int(items);
+    const int64_t grid = std::min<int64_t>(items, resident);
 
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(grid), 1, 1);
@@ -696,20 +801,25 @@ static cudaError_t launch_main(GemmParams P, const uint8_t* nib, const uint8_t* 
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_s, P);
+    return cudaLaunchKernelEx(&cfg, kern, S);
 }
 
-static cudaError_t launch_prep(const uint16_t* x, int M, int K, int NT, uint16_t* xf, float* xun,
-                               int* counters, int ncounters, const uint8_t* sc_in, int64_t N,
-                               int nblk, int sc_pitch, uint8_t* sc_out, bool repack,
-                               cudaStream_t stream) {
-    int repack_ctas = 0;
-    if (repack) {
-        const int64_t total = N * sc_pitch;
-        repack_ctas = int(std::min<int64_t>((total + kPrepThreads - 1) / kPrepThreads, 1024));
+// Kernel shape for a pass of M <= 64 rows: NT fragment tiles of 8 rows.
+template <int G>
+static cudaError_t launch_main_nt(int NT, const HostGemm* gs, int count, int M, int32_t* status,
+                                  cudaStream_t stream) {
+    switch (NT) {
+        case 1: return launch_main<1, 4, 2, 4, G>(gs, count, M, status, stream);
+        case 2: return launch_main<2, 4, 2, 3, G>(gs, count, M, status, stream);
+        case 3: return launch_main<3, 8, 2, 3, G>(gs, count, M, status, stream);
+        case 4: return launch_main<4, 8, 2, 2, G>(gs, count, M, status, stream);
+        default: return launch_main<8, 4, 2, 2, G>(gs, count, M, status, stream);
     }
+}
+
+static cudaError_t launch_prep(const PrepSet& Q, cudaStream_t stream) {
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(unsigned(8 * NT + 1 + repack_ctas), 1, 1);
+    cfg.gridDim = dim3(unsigned(Q.njobs * 8 * Q.NT + 1 + Q.repack_ctas), 1, 1);
     cfg.blockDim = dim3(kPrepThreads, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr;
@@ -717,8 +827,7 @@ static cudaError_t launch_prep(const uint16_t* x, int M, int K, int NT, uint16_t
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mxfp4_gemm_prep_kernel, x, M, K, NT, xf, xun, counters,
-                              ncounters, sc_in, N, nblk, sc_pitch, sc_out, repack_ctas);
+    return cudaLaunchKernelEx(&cfg, mxfp4_gemm_prep_kernel, Q);
 }
 
 cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* scales, float* y,
@@ -741,29 +850,117 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
         if (ws.n_counters < (N + bn - 1) / bn || mc > mc0) items_cap = 0;
         // the scales are realigned once, by the first pass
         const bool repack = ws.repack_scales && m0 == 0;
-        cudaError_t err = launch_prep(x + m0 * K, mc, int(K), NT, xf, xun, counters,
-                                      ws.n_counters, scales, N, nblk, ws.sc_pitch, sc_aligned,
-                                      repack, stream);
-        if (err != cudaSuccess) return err;
-        GemmParams P{};
-        P.xf = xf;
-        P.xun = xun;
-        P.y = y + m0 * N;
-        P.part = part;
-        P.counters = counters;
-        P.N = N;
-        P.M = mc;
-        P.nblk = nblk;
-        P.sc_from_prep = repack ? 1 : 0;
-        P.status = dev_status;
-        const uint8_t* sc = ws.repack_scales ? sc_aligned : scales;
-        switch (NT) {
-            case 1: err = launch_main<1, 4, 2, 4>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
-            case 2: err = launch_main<2, 4, 2, 3>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
-            case 3: err = launch_main<3, 8, 2, 3>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
-            case 4: err = launch_main<4, 8, 2, 2>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
-            default: err = launch_main<8, 4, 2, 2>(P, nibbles, sc, ws.sc_pitch, K, items_cap, stream); break;
+        PrepSet Q{};
+        Q.job[0].x = x + m0 * K;
+        Q.job[0].xf = xf;
+        Q.job[0].xun = xun;
+        Q.job[0].K = int(K);
+        Q.njobs = 1;
+        Q.M = mc;
+        Q.NT = NT;
+        Q.counters = counters;
+        Q.ncounters = ws.n_counters;
+        if (repack) {
+            Q.sc_in = scales;
+            Q.N = N;
+            Q.nblk = nblk;
+            Q.sc_pitch = ws.sc_pitch;
+            Q.sc_out = sc_aligned;
+            Q.repack_ctas = int(std::min<int64_t>((N * ws.sc_pitch + kPrepThreads - 1) / kPrepThreads, 1024));
         }
+        cudaError_t err = launch_prep(Q, stream);
+        if (err != cudaSuccess) return err;
+        HostGemm h{};
+        h.nib = nibbles;
+        h.sc = ws.repack_scales ? sc_aligned : scales;
+        h.sc_pitch = ws.sc_pitch;
+        h.sc_from_prep = repack;
+        h.xf = xf;
+        h.xun = xun;
+        h.y = y + m0 * N;
+        h.part = part;
+        h.counters = counters;
+        h.N = N;
+        h.K = K;
+        h.items_cap = items_cap;
+        err = launch_main_nt<1>(NT, &h, 1, mc, dev_status, stream);
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+// ------------------------------------------------------------------ grouped
+// Independent GEMMs sharing M <= 64: each distinct X is converted once, then
+// persistent launches of up to kGroupMax GEMMs stream every weight matrix
+// through the same shared-memory ring.
+constexpr int kGroupMax = 64;
+
+size_t gemm_grouped_workspace(const GroupedGemm* gs, int count, int64_t M) {
+    const int NT = tiles_nt(int(M));
+    size_t off = 0;
+    for (int i = 0; i < count; ++i) {
+        bool seen = false;
+        for (int j = 0; j < i && !seen; ++j) seen = gs[j].x == gs[i].x && gs[j].K == gs[i].K;
+        if (seen) continue;
+        off = align_up(off + size_t(8 * NT) * size_t(gs[i].K) * 2, 256);
+        off = align_up(off + kGemmMaxRowsPerPass * sizeof(float), 256);
+    }
+    return off;
+}
+
+cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* workspace,
+                             int32_t* dev_status, cudaStream_t stream) {
+    const int NT = tiles_nt(int(M));
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    // distinct activations, in first-use order
+    std::vector<int> xid(count);
+    std::vector<PrepJob> jobs;
+    size_t off = 0;
+    for (int i = 0; i < count; ++i) {
+        int found = -1;
+        for (int j = 0; j < int(jobs.size()); ++j)
+            if (jobs[j].x == gs[i].x && jobs[j].K == int(gs[i].K)) found = j;
+        if (found < 0) {
+            PrepJob J{};
+            J.x = gs[i].x;
+            J.K = int(gs[i].K);
+            J.xf = reinterpret_cast<uint16_t*>(wsb + off);
+            off = align_up(off + size_t(8 * NT) * size_t(gs[i].K) * 2, 256);
+            J.xun = reinterpret_cast<float*>(wsb + off);
+            off = align_up(off + kGemmMaxRowsPerPass * sizeof(float), 256);
+            found = int(jobs.size());
+            jobs.push_back(J);
+        }
+        xid[i] = found;
+    }
+    for (size_t j0 = 0; j0 < jobs.size(); j0 += kPrepMaxJobs) {
+        PrepSet Q{};
+        Q.njobs = int(std::min<size_t>(kPrepMaxJobs, jobs.size() - j0));
+        for (int q = 0; q < Q.njobs; ++q) Q.job[q] = jobs[j0 + q];
+        Q.M = int(M);
+        Q.NT = NT;
+        cudaError_t err = launch_prep(Q, stream);
+        if (err != cudaSuccess) return err;
+    }
+    std::vector<HostGemm> hs(count);
+    for (int i = 0; i < count; ++i) {
+        HostGemm& h = hs[i];
+        h.nib = gs[i].nibbles;
+        h.sc = gs[i].scales;
+        h.sc_pitch = int(gs[i].K / 32);
+        h.sc_from_prep = false;
+        h.xf = jobs[xid[i]].xf;
+        h.xun = jobs[xid[i]].xun;
+        h.y = gs[i].y;
+        h.N = gs[i].N;
+        h.K = gs[i].K;
+        h.items_cap = 0;
+    }
+    // balanced launches of at most kGroupMax GEMMs
+    const int nlaunch = (count + kGroupMax - 1) / kGroupMax;
+    for (int l = 0; l < nlaunch; ++l) {
+        const int b = int(int64_t(count) * l / nlaunch), e = int(int64_t(count) * (l + 1) / nlaunch);
+        cudaError_t err = launch_main_nt<kGroupMax>(NT, hs.data() + b, e - b, int(M), dev_status, stream);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;

@@ -30,6 +30,20 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
                      int64_t M, int64_t N, int64_t K, void* workspace,
                      const GemmWorkspace& ws, int32_t* dev_status, cudaStream_t stream);
 
+// One GEMM of a grouped call (independent GEMMs sharing M <= 64).
+struct GroupedGemm {
+    const uint16_t* x;
+    const uint8_t* nibbles;
+    const uint8_t* scales;
+    float* y;
+    int64_t N, K;
+};
+
+size_t gemm_grouped_workspace(const GroupedGemm* gs, int count, int64_t M);
+
+cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* workspace,
+                             int32_t* dev_status, cudaStream_t stream);
+
 // ---------------------------------------------------------- acceptance
 constexpr int kAcceptMaxK = 32;
 constexpr int64_t kAcceptMaxV = int64_t(1) << 21;

@@ -72,3 +72,20 @@ def test_pack_rejects_bad_arguments_on_host(L):
     assert f(FAKE, 7, 4, 32, FAKE, FAKE, None, None) == 1
     assert f(FAKE + 2, 0, 4, 32, FAKE, FAKE, None, None) == 2
     assert f(None, 0, 0, 32, None, None, None, None) == 0  # empty: nothing to do
+
+
+def test_grouped_rejects_bad_arguments_on_host(L):
+    import mxfp4_speculative_verification_gb300 as m
+    arr = (m.GemmProblem * 2)()
+    arr[0] = m.GemmProblem(FAKE, FAKE, FAKE, FAKE, 64, 512)
+    arr[1] = m.GemmProblem(FAKE, FAKE, FAKE, FAKE, 64, 4096)
+    f = L.mxfp4_verify_gemm_grouped
+    assert L.mxfp4_verify_gemm_grouped_workspace_size(arr, 2, 5) > 0
+    assert f(None, 2, 5, FAKE, 1 << 30, None, None) == 1
+    assert f(arr, 0, 5, FAKE, 1 << 30, None, None) == 1
+    assert f(arr, 2, 65, FAKE, 1 << 30, None, None) == 3
+    assert f(arr, 2, 5, FAKE, 16, None, None) == 5
+    arr[1] = m.GemmProblem(FAKE, FAKE, FAKE, FAKE, 64, 544)   # K % 512 != 0
+    assert f(arr, 2, 5, FAKE, 1 << 30, None, None) == 3
+    arr[1] = m.GemmProblem(FAKE, FAKE + 4, FAKE, FAKE, 64, 512)  # nibbles not 16-byte aligned
+    assert f(arr, 2, 5, FAKE, 1 << 30, None, None) == 2
