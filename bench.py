@@ -17,7 +17,8 @@ back inside the timed region.  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mxs|reference]
-                       [--workload llama8b|llama8b_b4|llama8b_b16|llama8b_b64|llama70b]
+                       [--workload llama8b|llama8b_b4|llama8b_b16|llama8b_b64|
+                                   llama70b|llama70b_b1|llama70b_b4]
 """
 from __future__ import annotations
 
@@ -55,6 +56,8 @@ WORKLOADS = {
     "llama8b_b16": ("llama8b", 16, 4),
     "llama8b_b64": ("llama8b", 64, 4),
     "llama70b": ("llama70b", 16, 4),
+    "llama70b_b1": ("llama70b", 1, 4),
+    "llama70b_b4": ("llama70b", 4, 4),
 }
 
 

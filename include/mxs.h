@@ -140,7 +140,8 @@ mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles,
  *              nibbles [N, K/2] (16-byte aligned), scales [N, K/32]
  *              (16-byte aligned, K % 512 == 0), y [M, N] fp32 written.
  *              No y may overlap any problem's x, nibbles, scales or another y.
- *   1 <= count <= 4096, 1 <= M <= 64
+ *   1 <= count <= 4096, 1 <= M <= 65536 (rows are processed 64 at a time,
+ *   each group of rows one pass over every weight matrix)
  *   workspace  device, >= mxfp4_verify_gemm_grouped_workspace_size(...)
  *              bytes, 16-byte aligned.
  * Results are bit-identical to calling mxfp4_verify_gemm on each problem

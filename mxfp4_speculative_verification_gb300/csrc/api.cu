@@ -22,7 +22,7 @@ bool grouped_valid(const mxs_gemm_problem* problems, int32_t count, int64_t M,
                           std::vector<mxs::GroupedGemm>& out, mxs_status& st) {
     st = MXS_OK;
     if (!problems || count < 1 || M < 1) { st = MXS_ERR_INVALID_ARG; return false; }
-    if (count > 4096 || M > mxs::kGemmMaxRowsPerPass) { st = MXS_ERR_UNSUPPORTED; return false; }
+    if (count > 4096 || M > kMaxM) { st = MXS_ERR_UNSUPPORTED; return false; }
     out.resize(size_t(count));
     for (int32_t i = 0; i < count; ++i) {
         const mxs_gemm_problem& p = problems[i];

@@ -896,7 +896,7 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
 constexpr int kGroupMax = 64;
 
 size_t gemm_grouped_workspace(const GroupedGemm* gs, int count, int64_t M) {
-    const int NT = tiles_nt(int(M));
+    const int NT = tiles_nt(int(std::min<int64_t>(M, kGemmMaxRowsPerPass)));
     size_t off = 0;
     for (int i = 0; i < count; ++i) {
         bool seen = false;
@@ -910,9 +910,9 @@ size_t gemm_grouped_workspace(const GroupedGemm* gs, int count, int64_t M) {
 
 cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* workspace,
                              int32_t* dev_status, cudaStream_t stream) {
-    const int NT = tiles_nt(int(M));
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
-    // distinct activations, in first-use order
+    const int NT0 = tiles_nt(int(std::min<int64_t>(M, kGemmMaxRowsPerPass)));
+    // distinct activations, in first-use order; fragment space sized for NT0
     std::vector<int> xid(count);
     std::vector<PrepJob> jobs;
     size_t off = 0;
@@ -925,7 +925,7 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
             J.x = gs[i].x;
             J.K = int(gs[i].K);
             J.xf = reinterpret_cast<uint16_t*>(wsb + off);
-            off = align_up(off + size_t(8 * NT) * size_t(gs[i].K) * 2, 256);
+            off = align_up(off + size_t(8 * NT0) * size_t(gs[i].K) * 2, 256);
             J.xun = reinterpret_cast<float*>(wsb + off);
             off = align_up(off + kGemmMaxRowsPerPass * sizeof(float), 256);
             found = int(jobs.size());
@@ -933,35 +933,47 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
         }
         xid[i] = found;
     }
-    for (size_t j0 = 0; j0 < jobs.size(); j0 += kPrepMaxJobs) {
-        PrepSet Q{};
-        Q.njobs = int(std::min<size_t>(kPrepMaxJobs, jobs.size() - j0));
-        for (int q = 0; q < Q.njobs; ++q) Q.job[q] = jobs[j0 + q];
-        Q.M = int(M);
-        Q.NT = NT;
-        cudaError_t err = launch_prep(Q, stream);
-        if (err != cudaSuccess) return err;
-    }
     std::vector<HostGemm> hs(count);
-    for (int i = 0; i < count; ++i) {
-        HostGemm& h = hs[i];
-        h.nib = gs[i].nibbles;
-        h.sc = gs[i].scales;
-        h.sc_pitch = int(gs[i].K / 32);
-        h.sc_from_prep = false;
-        h.xf = jobs[xid[i]].xf;
-        h.xun = jobs[xid[i]].xun;
-        h.y = gs[i].y;
-        h.N = gs[i].N;
-        h.K = gs[i].K;
-        h.items_cap = 0;
-    }
-    // balanced launches of at most kGroupMax GEMMs
-    const int nlaunch = (count + kGroupMax - 1) / kGroupMax;
-    for (int l = 0; l < nlaunch; ++l) {
-        const int b = int(int64_t(count) * l / nlaunch), e = int(int64_t(count) * (l + 1) / nlaunch);
-        cudaError_t err = launch_main_nt<kGroupMax>(NT, hs.data() + b, e - b, int(M), dev_status, stream);
-        if (err != cudaSuccess) return err;
+    // rows are processed 64 at a time; each pass converts its rows of every
+    // distinct X, then streams every weight matrix once
+    for (int64_t m0 = 0; m0 < M; m0 += kGemmMaxRowsPerPass) {
+        const int mc = int(std::min<int64_t>(kGemmMaxRowsPerPass, M - m0));
+        const int NT = tiles_nt(mc);
+        for (size_t j0 = 0; j0 < jobs.size(); j0 += kPrepMaxJobs) {
+            PrepSet Q{};
+            Q.njobs = int(std::min<size_t>(kPrepMaxJobs, jobs.size() - j0));
+            for (int q = 0; q < Q.njobs; ++q) {
+                Q.job[q] = jobs[j0 + q];
+                Q.job[q].x = jobs[j0 + q].x + m0 * jobs[j0 + q].K;
+            }
+            Q.M = mc;
+            Q.NT = NT;
+            cudaError_t err = launch_prep(Q, stream);
+            if (err != cudaSuccess) return err;
+        }
+        for (int i = 0; i < count; ++i) {
+            HostGemm& h = hs[i];
+            h = HostGemm{};
+            h.nib = gs[i].nibbles;
+            h.sc = gs[i].scales;
+            h.sc_pitch = int(gs[i].K / 32);
+            h.sc_from_prep = false;
+            h.xf = jobs[xid[i]].xf;
+            h.xun = jobs[xid[i]].xun;
+            h.y = gs[i].y + m0 * gs[i].N;
+            h.N = gs[i].N;
+            h.K = gs[i].K;
+            h.items_cap = 0;
+        }
+        // balanced launches of at most kGroupMax GEMMs
+        const int nlaunch = (count + kGroupMax - 1) / kGroupMax;
+        for (int l = 0; l < nlaunch; ++l) {
+            const int b = int(int64_t(count) * l / nlaunch);
+            const int e = int(int64_t(count) * (l + 1) / nlaunch);
+            cudaError_t err =
+                launch_main_nt<kGroupMax>(NT, hs.data() + b, e - b, mc, dev_status, stream);
+            if (err != cudaSuccess) return err;
+        }
     }
     return cudaSuccess;
 }

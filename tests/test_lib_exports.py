@@ -83,7 +83,7 @@ def test_grouped_rejects_bad_arguments_on_host(L):
     assert L.mxfp4_verify_gemm_grouped_workspace_size(arr, 2, 5) > 0
     assert f(None, 2, 5, FAKE, 1 << 30, None, None) == 1
     assert f(arr, 0, 5, FAKE, 1 << 30, None, None) == 1
-    assert f(arr, 2, 65, FAKE, 1 << 30, None, None) == 3
+    assert f(arr, 2, 65537, FAKE, 1 << 30, None, None) == 3
     assert f(arr, 2, 5, FAKE, 16, None, None) == 5
     arr[1] = m.GemmProblem(FAKE, FAKE, FAKE, FAKE, 64, 544)   # K % 512 != 0
     assert f(arr, 2, 5, FAKE, 1 << 30, None, None) == 3
