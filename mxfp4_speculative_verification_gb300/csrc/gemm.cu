@@ -65,6 +65,8 @@ struct Problem {
     int stages_per_split;
     int item_begin;        // first work item of this GEMM within the launch
     int sc_from_prep;      // scales were realigned by the preparation kernel
+    const uint8_t* sc;     // the scale rows that tm_s streams (row pitch sc_pitch bytes)
+    int64_t sc_pitch;
 };
 
 // The GEMMs of one launch (a kernel parameter, read in place).  They share
@@ -441,6 +443,8 @@ __device__ __forceinline__ float pow2f_exact(int e) {
     return __uint_as_float(1u << (e + 149));
 }
 
+#include "gemm_umma.cuh"
+
 constexpr int kPrepThreads = 512;
 constexpr int kPrepChunks = 8;  // 16-byte chunks of one X row kept in registers per thread
 
@@ -471,6 +475,7 @@ struct PrepSet {
     int njobs;
     int M;
     int NT;
+    int umma_npad;        // 0: mma.sync fragments; else swizzled tcgen05 tiles of this many rows
     int* counters;        // split-K counters to zero (may be null)
     int ncounters;
     const uint8_t* sc_in;  // scale realignment (single GEMM only; null otherwise)
@@ -485,7 +490,8 @@ __global__ void __launch_bounds__(kPrepThreads) mxfp4_gemm_prep_kernel(const __g
     pdl_trigger();
     pdl_wait();  // the workspace may still be in use by the previous GEMM
     const int NT = Q.NT, M = Q.M;
-    const int mpad = 8 * NT;
+    const int npad = Q.umma_npad;
+    const int mpad = npad > 0 ? npad : 8 * NT;
     const int nrow_ctas = Q.njobs * mpad;
     if (int(blockIdx.x) < nrow_ctas) {
         const PrepJob& J = Q.job[blockIdx.x / mpad];
@@ -530,6 +536,13 @@ __global__ void __launch_bounds__(kPrepThreads) mxfp4_gemm_prep_kernel(const __g
         if (threadIdx.x == 0) xun[m] = (m < M) ? pow2f_exact(-sh) : 0.f;
         auto frag = [&](int c) -> uint4* {
             const int k0 = c * 8;
+            if (npad > 0) {
+                // [stage of 512 k][chunk of 64 k][row][128 B, 16-byte units swizzled by row % 8]
+                const int st = k0 >> 9, ch = (k0 >> 6) & 7, u = (k0 >> 3) & 7;
+                const int64_t byte = int64_t(st) * npad * 1024 + int64_t(ch) * npad * 128 + m * 128 +
+                                     ((u ^ (m & 7)) << 4);
+                return reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(xf) + byte);
+            }
             const int blk = k0 >> 5, tt = (k0 & 31) >> 3;
             return reinterpret_cast<uint4*>(xf + ((int64_t(blk) * NT + nt) * 32 + gg * 4 + tt) * 8);
         };
@@ -604,7 +617,7 @@ GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales
     w.sc_pitch = w.repack_scales ? int(align_up(size_t(nblk), 16)) : int(nblk);
     size_t off = 0;
     w.xf_off = off;
-    off = align_up(off + size_t(kGemmMaxRowsPerPass) * size_t(K) * 2, 256);
+    off = align_up(off + size_t(kGemmMaxRowsPerPass) * align_up(size_t(K), 512) * 2, 256);
     w.xun_off = off;
     off = align_up(off + kGemmMaxRowsPerPass * sizeof(float), 256);
     // counters and partial tiles, sized for either tile height a pass may use
@@ -716,37 +729,10 @@ struct HostGemm {
     int64_t items_cap;   // 0: never split K
 };
 
-template <int NT, int RG, int KW, int STAGES, int G>
-static cudaError_t launch_main(const HostGemm* gs, int count, int M, int32_t* status,
-                               cudaStream_t stream) {
-    using C = GemmCfg<NT, RG, KW, STAGES>;
-    auto kern = mxfp4_gemm_kernel<NT, RG, KW, STAGES, G>;
-    static LaunchFacts facts;
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    int sms = facts.sms[dev].load(std::memory_order_acquire);
-    int occ = facts.occ[dev].load(std::memory_order_acquire);
-    if (sms <= 0 || occ <= 0) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   C::kSmemBytes);
-        if (err != cudaSuccess) return err;
-        err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (err != cudaSuccess) return err;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::kThreads,
-                                                            C::kSmemBytes);
-        if (err != cudaSuccess) return err;
-        if (occ < 1) occ = 1;
-        facts.occ[dev].store(occ, std::memory_order_release);
-        facts.sms[dev].store(sms, std::memory_order_release);
-    }
-    const int64_t resident = int64_t(sms) * occ;
-
-    // the problem table lives in the (large) kernel parameter block
-    static thread_local ProblemSet<G>* S_buf = nullptr;
-    if (!S_buf) S_buf = new ProblemSet<G>;
-    ProblemSet<G>& S = *S_buf;
+// Fill the launch's problem table for tiles of BN rows.
+template <int G>
+static cudaError_t build_problems(ProblemSet<G>& S, const HostGemm* gs, int count, int M,
+                                  int32_t* status, int BN, int64_t resident) {
     std::memset(&S, 0, sizeof(S));
     S.count = count;
     S.M = M;
@@ -763,8 +749,10 @@ static cudaError_t launch_main(const HostGemm* gs, int count, int M, int32_t* st
         p.counters = h.counters;
         p.N = h.N;
         p.nblk = int(h.K / 32);
-        p.ntiles = int((h.N + C::BN - 1) / C::BN);
+        p.ntiles = int((h.N + BN - 1) / BN);
         p.sc_from_prep = h.sc_from_prep ? 1 : 0;
+        p.sc = h.sc;
+        p.sc_pitch = h.sc_pitch;
         const int stages_total = (p.nblk + kStageBlocks - 1) / kStageBlocks;
         p.nsplit = 1;
         p.stages_per_split = stages_total;
@@ -783,18 +771,46 @@ static cudaError_t launch_main(const HostGemm* gs, int count, int M, int32_t* st
         p.item_begin = int(items);
         items += int64_t(p.ntiles) * p.nsplit;
         if (items > INT32_MAX) return cudaErrorInvalidValue;
-        if (!make_map(&p.tm_w, h.nib, h.N, h.K / 2, h.K / 2, kBoxBytes, C::BN, true))
+        if (!make_map(&p.tm_w, h.nib, h.N, h.K / 2, h.K / 2, kBoxBytes, uint32_t(BN), true))
             return cudaErrorInvalidValue;
-        if (!make_map(&p.tm_s, h.sc, h.N, p.nblk, h.sc_pitch, 16, C::BN, false))
+        if (!make_map(&p.tm_s, h.sc, h.N, p.nblk, h.sc_pitch, 16, uint32_t(BN), false))
             return cudaErrorInvalidValue;
     }
     S.items = int(items);
-    const int64_t grid = std::min<int64_t>(items, resident);
+    return cudaSuccess;
+}
 
+// SM count and resident CTAs per SM of one kernel, cached per device.
+template <typename Kern>
+static cudaError_t launch_facts(LaunchFacts& facts, Kern kern, int threads, int smem, int& sms,
+                                int& occ) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    sms = facts.sms[dev].load(std::memory_order_acquire);
+    occ = facts.occ[dev].load(std::memory_order_acquire);
+    if (sms > 0 && occ > 0) return cudaSuccess;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+    if (err != cudaSuccess) return err;
+    if (occ < 1) occ = 1;
+    facts.occ[dev].store(occ, std::memory_order_release);
+    facts.sms[dev].store(sms, std::memory_order_release);
+    return cudaSuccess;
+}
+
+// Persistent launch with programmatic dependent launch enabled.
+template <typename Kern, typename Set>
+static cudaError_t launch_persistent(Kern kern, const Set& S, int threads, int smem, int64_t grid,
+                                     cudaStream_t stream) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(grid), 1, 1);
-    cfg.blockDim = dim3(C::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.blockDim = dim3(unsigned(threads), 1, 1);
+    cfg.dynamicSmemBytes = size_t(smem);
     cfg.stream = stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -802,6 +818,25 @@ static cudaError_t launch_main(const HostGemm* gs, int count, int M, int32_t* st
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, S);
+}
+
+template <int NT, int RG, int KW, int STAGES, int G>
+static cudaError_t launch_main(const HostGemm* gs, int count, int M, int32_t* status,
+                               cudaStream_t stream) {
+    using C = GemmCfg<NT, RG, KW, STAGES>;
+    auto kern = mxfp4_gemm_kernel<NT, RG, KW, STAGES, G>;
+    static LaunchFacts facts;
+    int sms = 0, occ = 0;
+    cudaError_t err = launch_facts(facts, kern, C::kThreads, C::kSmemBytes, sms, occ);
+    if (err != cudaSuccess) return err;
+    const int64_t resident = int64_t(sms) * occ;
+    // the problem table lives in the (large) kernel parameter block
+    static thread_local ProblemSet<G>* S_buf = nullptr;
+    if (!S_buf) S_buf = new ProblemSet<G>;
+    err = build_problems(*S_buf, gs, count, M, status, C::BN, resident);
+    if (err != cudaSuccess) return err;
+    const int64_t grid = std::min<int64_t>(S_buf->items, resident);
+    return launch_persistent(kern, *S_buf, C::kThreads, C::kSmemBytes, grid, stream);
 }
 
 // Kernel shape for a pass of M <= 64 rows: NT fragment tiles of 8 rows.
@@ -817,9 +852,59 @@ static cudaError_t launch_main_nt(int NT, const HostGemm* gs, int count, int M, 
     }
 }
 
+// tcgen05 kernel: one CTA per SM, whole 128-row tiles (K is never split).
+template <int NPAD, int STAGES, int G>
+static cudaError_t launch_umma(const HostGemm* gs, int count, int M, int32_t* status,
+                               cudaStream_t stream) {
+    using C = UCfg<NPAD, STAGES>;
+    auto kern = mxfp4_gemm_umma_kernel<NPAD, STAGES, G>;
+    static LaunchFacts facts;
+    int sms = 0, occ = 0;
+    cudaError_t err = launch_facts(facts, kern, kUThreads, C::kSmemBytes, sms, occ);
+    if (err != cudaSuccess) return err;
+    static thread_local ProblemSet<G>* S_buf = nullptr;
+    if (!S_buf) S_buf = new ProblemSet<G>;
+    HostGemm tmp[G];
+    for (int i = 0; i < count; ++i) {
+        tmp[i] = gs[i];
+        tmp[i].items_cap = 0;
+    }
+    err = build_problems(*S_buf, tmp, count, M, status, kUBN, int64_t(sms));
+    if (err != cudaSuccess) return err;
+    const int64_t grid = std::min<int64_t>(S_buf->items, int64_t(sms));
+    return launch_persistent(kern, *S_buf, kUThreads, C::kSmemBytes, grid, stream);
+}
+
+// Rows of the X tile fed to the tensor cores for a pass of mc rows (MMA N).
+static int umma_npad(int mc) { return std::max(16, (mc + 15) / 16 * 16); }
+
+template <int G>
+static cudaError_t launch_umma_np(int npad, const HostGemm* gs, int count, int M, int32_t* status,
+                                  cudaStream_t stream) {
+    switch (npad) {
+        case 16: return launch_umma<16, 4, G>(gs, count, M, status, stream);
+        case 32: return launch_umma<32, 3, G>(gs, count, M, status, stream);
+        case 48: return launch_umma<48, 2, G>(gs, count, M, status, stream);
+        default: return launch_umma<64, 2, G>(gs, count, M, status, stream);
+    }
+}
+
+// Which kernel a pass of mc rows uses.  mma.sync (legacy tensor path) is
+// faster up to 32 rows; beyond that its m16n8k16 issue rate, not HBM,
+// bounds it and the tcgen05 kernel takes over.  MXS_GEMM_PATH=mma|umma
+// forces one (umma needs more than 8 rows).
+static bool use_umma(int mc, int64_t tiles128, bool grouped) {
+    const char* path = std::getenv("MXS_GEMM_PATH");
+    if (path && std::strcmp(path, "mma") == 0) return false;
+    if (path && std::strcmp(path, "umma") == 0) return mc > 8;
+    // the tcgen05 kernel never splits K: a lone GEMM needs enough 128-row tiles
+    return mc > 32 && (grouped || tiles128 >= 64);
+}
+
 static cudaError_t launch_prep(const PrepSet& Q, cudaStream_t stream) {
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(unsigned(Q.njobs * 8 * Q.NT + 1 + Q.repack_ctas), 1, 1);
+    const int rows = Q.umma_npad > 0 ? Q.umma_npad : 8 * Q.NT;
+    cfg.gridDim = dim3(unsigned(Q.njobs * rows + 1 + Q.repack_ctas), 1, 1);
     cfg.blockDim = dim3(kPrepThreads, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr;
@@ -848,6 +933,7 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
         // the workspace holds partial tiles for mc0 rows and tile height bn
         int64_t items_cap = split_items_cap(N, K, bn);
         if (ws.n_counters < (N + bn - 1) / bn || mc > mc0) items_cap = 0;
+        const bool umma = use_umma(mc, (N + kUBN - 1) / kUBN, false);
         // the scales are realigned once, by the first pass
         const bool repack = ws.repack_scales && m0 == 0;
         PrepSet Q{};
@@ -858,6 +944,7 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
         Q.njobs = 1;
         Q.M = mc;
         Q.NT = NT;
+        Q.umma_npad = umma ? umma_npad(mc) : 0;
         Q.counters = counters;
         Q.ncounters = ws.n_counters;
         if (repack) {
@@ -883,7 +970,8 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
         h.N = N;
         h.K = K;
         h.items_cap = items_cap;
-        err = launch_main_nt<1>(NT, &h, 1, mc, dev_status, stream);
+        err = umma ? launch_umma_np<1>(umma_npad(mc), &h, 1, mc, dev_status, stream)
+                   : launch_main_nt<1>(NT, &h, 1, mc, dev_status, stream);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
@@ -895,14 +983,20 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
 // through the same shared-memory ring.
 constexpr int kGroupMax = 64;
 
+// Bytes of one prepared X (either layout) for passes of at most mc0 rows.
+static size_t xf_bytes(int mc0, int64_t K) {
+    const int rows = std::max(8 * tiles_nt(mc0), umma_npad(mc0));
+    return size_t(rows) * align_up(size_t(K), 512) * 2;
+}
+
 size_t gemm_grouped_workspace(const GroupedGemm* gs, int count, int64_t M) {
-    const int NT = tiles_nt(int(std::min<int64_t>(M, kGemmMaxRowsPerPass)));
+    const int mc0 = int(std::min<int64_t>(M, kGemmMaxRowsPerPass));
     size_t off = 0;
     for (int i = 0; i < count; ++i) {
         bool seen = false;
         for (int j = 0; j < i && !seen; ++j) seen = gs[j].x == gs[i].x && gs[j].K == gs[i].K;
         if (seen) continue;
-        off = align_up(off + size_t(8 * NT) * size_t(gs[i].K) * 2, 256);
+        off = align_up(off + xf_bytes(mc0, gs[i].K), 256);
         off = align_up(off + kGemmMaxRowsPerPass * sizeof(float), 256);
     }
     return off;
@@ -911,8 +1005,8 @@ size_t gemm_grouped_workspace(const GroupedGemm* gs, int count, int64_t M) {
 cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* workspace,
                              int32_t* dev_status, cudaStream_t stream) {
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
-    const int NT0 = tiles_nt(int(std::min<int64_t>(M, kGemmMaxRowsPerPass)));
-    // distinct activations, in first-use order; fragment space sized for NT0
+    const int mc0 = int(std::min<int64_t>(M, kGemmMaxRowsPerPass));
+    // distinct activations, in first-use order; X space sized for passes of mc0 rows
     std::vector<int> xid(count);
     std::vector<PrepJob> jobs;
     size_t off = 0;
@@ -925,7 +1019,7 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
             J.x = gs[i].x;
             J.K = int(gs[i].K);
             J.xf = reinterpret_cast<uint16_t*>(wsb + off);
-            off = align_up(off + size_t(8 * NT0) * size_t(gs[i].K) * 2, 256);
+            off = align_up(off + xf_bytes(mc0, gs[i].K), 256);
             J.xun = reinterpret_cast<float*>(wsb + off);
             off = align_up(off + kGemmMaxRowsPerPass * sizeof(float), 256);
             found = int(jobs.size());
@@ -939,6 +1033,7 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
     for (int64_t m0 = 0; m0 < M; m0 += kGemmMaxRowsPerPass) {
         const int mc = int(std::min<int64_t>(kGemmMaxRowsPerPass, M - m0));
         const int NT = tiles_nt(mc);
+        const bool umma = use_umma(mc, 0, true);
         for (size_t j0 = 0; j0 < jobs.size(); j0 += kPrepMaxJobs) {
             PrepSet Q{};
             Q.njobs = int(std::min<size_t>(kPrepMaxJobs, jobs.size() - j0));
@@ -948,6 +1043,7 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
             }
             Q.M = mc;
             Q.NT = NT;
+            Q.umma_npad = umma ? umma_npad(mc) : 0;
             cudaError_t err = launch_prep(Q, stream);
             if (err != cudaSuccess) return err;
         }
@@ -971,7 +1067,8 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
             const int b = int(int64_t(count) * l / nlaunch);
             const int e = int(int64_t(count) * (l + 1) / nlaunch);
             cudaError_t err =
-                launch_main_nt<kGroupMax>(NT, hs.data() + b, e - b, mc, dev_status, stream);
+                umma ? launch_umma_np<kGroupMax>(umma_npad(mc), hs.data() + b, e - b, mc, dev_status, stream)
+                     : launch_main_nt<kGroupMax>(NT, hs.data() + b, e - b, mc, dev_status, stream);
             if (err != cudaSuccess) return err;
         }
     }

@@ -79,6 +79,29 @@ def test_grouped_equals_single_call_without_split(env, monkeypatch):
         assert torch.equal(single.view(torch.int32), y.view(torch.int32))
 
 
+def test_grouped_equals_single_call_tcgen05(env, monkeypatch):
+    torch, mxs = env
+    # both entry points on the tcgen05 kernel (K is never split there)
+    monkeypatch.setenv("MXS_GEMM_PATH", "umma")
+    probs, host = _problems(env, 40, [(4096, 28672), (14336, 4096)], n_x=1)
+    mxs.mxfp4_verify_gemm_grouped(probs)
+    for x, nib, sc, y in probs:
+        single = mxs.mxfp4_verify_gemm(x, nib, sc)
+        torch.cuda.synchronize()
+        assert torch.equal(single.view(torch.int32), y.view(torch.int32))
+
+
+def test_grouped_many_problems_several_launches_wide(env):
+    torch, mxs = env
+    shapes = [(512 * (1 + i % 3), 64 + 7 * i) for i in range(150)]
+    probs, host = _problems(env, 40, shapes, n_x=3)
+    mxs.mxfp4_verify_gemm_grouped(probs)
+    torch.cuda.synchronize()
+    for (x, nib, sc), (_, _, _, y) in zip(host, probs):
+        err = gemm_row_rel_err(y.cpu().numpy(), oracle.gemm(x, nib, sc))
+        assert np.all(err <= GEMM_REL_TOL)
+
+
 def test_grouped_rejects_unsupported(env):
     torch, mxs = env
     probs, _ = _problems(env, 5, [(544, 64)])
