@@ -890,7 +890,7 @@ static cudaError_t launch_umma_np(int npad, const HostGemm* gs, int count, int M
 }
 
 // Which kernel a pass of mc rows uses.  mma.sync (legacy tensor path) is
-// faster up to 32 rows; beyond that its m16n8k16 issue rate, not HBM,
+// faster up to 24 rows; beyond that its m16n8k16 issue rate, not HBM,
 // bounds it and the tcgen05 kernel takes over.  MXS_GEMM_PATH=mma|umma
 // forces one (umma needs more than 8 rows).
 static bool use_umma(int mc, int64_t tiles128, bool grouped) {
@@ -898,7 +898,7 @@ static bool use_umma(int mc, int64_t tiles128, bool grouped) {
     if (path && std::strcmp(path, "mma") == 0) return false;
     if (path && std::strcmp(path, "umma") == 0) return mc > 8;
     // the tcgen05 kernel never splits K: a lone GEMM needs enough 128-row tiles
-    return mc > 32 && (grouped || tiles128 >= 64);
+    return mc > 24 && (grouped || tiles128 >= 64);
 }
 
 static cudaError_t launch_prep(const PrepSet& Q, cudaStream_t stream) {

@@ -1,6 +1,6 @@
 // Wide-M verify GEMM on sm_103a tensor cores (tcgen05 / UMMA), included by gemm.cu.
 //
-// For M > 32 candidate positions the legacy mma.sync path runs out of tensor
+// For M > 24 candidate positions the legacy mma.sync path runs out of tensor
 // throughput before HBM does, so this kernel issues tcgen05.mma (kind::f16,
 // fp32 accumulate in tensor memory) with
 //   * A = 128 weight rows x 16 k, decoded by CUDA-core warps straight into
@@ -24,6 +24,13 @@
 // reaches TMEM lane quadrant warp % 4; the four decoders of a quadrant take
 // blocks 4j..4j+3 (j = 0..3) of every 16-block stage.  The j = 0 decoders
 // also run the rare exact path and read D back.
+//
+// Hand-offs: the MMA warp waits once per stage (all 16 decoders arrive on
+// the slot's `sready`), then issues the stage's 32 MMAs back to back and
+// frees each quarter's A columns with its own commit.  A satisfied mbarrier
+// wait costs a few hundred cycles during which the tensor pipe starves, so
+// per-stage rather than per-quarter waits matter more than anything else
+// in this kernel.
 
 constexpr int kUBN = 128;                    // weight rows per tile (MMA M)
 constexpr int kUDecodeWarps = 16;
@@ -47,10 +54,11 @@ struct UCfg {
     static constexpr int kStageBytes = kWBytes + kSBytes + kXBytes;
     static constexpr int kMaskOffset = STAGES * kStageBytes;      // uint8 [STAGES][4][128]
     static constexpr int kErefOffset = kMaskOffset + STAGES * 4 * kUBN;  // int32 [2][128]
-    static constexpr int kBarOffset = kErefOffset + 2 * kUBN * 4;
-    // full[S], empty[S], maskfull[S], afull[5], afree[5], dready[2], dfree[2],
+    static constexpr int kLowOffset = kErefOffset + 2 * kUBN * 4;        // int32 [2]: tile has low blocks
+    static constexpr int kBarOffset = kLowOffset + 16;
+    // full[S], empty[S], maskfull[S], sready[S], afree[5], dready[2], dfree[2],
     // efull[2], efree[2], fin
-    static constexpr int kNumBars = 3 * STAGES + 2 * kUASets + 9;
+    static constexpr int kNumBars = 4 * STAGES + kUASets + 9;
     static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOffset + 16 + 1024;
     static_assert(kStageBytes % 1024 == 0, "swizzled tiles need 1 KB alignment");
@@ -164,6 +172,13 @@ __device__ __forceinline__ uint32_t scale_word_max(uint32_t acc, uint32_t w, int
     return __vmaxu4(acc, w & ~nan & keep);
 }
 
+// Byte-wise minimum of acc and w over the bytes below `valid`.  NaN scales
+// (255) never lower the minimum.
+__device__ __forceinline__ uint32_t scale_word_min(uint32_t acc, uint32_t w, int valid) {
+    const uint32_t keep = valid >= 4 ? 0xFFFFFFFFu : (valid <= 0 ? 0u : (1u << (8 * valid)) - 1u);
+    return __vminu4(acc, w | ~keep);
+}
+
 // Decode one 32-k block of a weight row (16 bytes of nibbles) into 16 fp16x2.
 __device__ __forceinline__ void decode_block(uint4 nib, uint32_t (&v)[16]) {
     e2m1x8_to_f16x2x4(nib.x, v[0], v[1], v[2], v[3]);
@@ -215,10 +230,13 @@ __global__ void __launch_bounds__(kUThreads, 1)
     // j = 1..3 -> j = 0 hand-off of the out-of-window masks of one stage slot;
     // its next phase needs the slot refilled, so it never runs ahead of its waiter
     auto maskfull_b = [&](int s) { return bars + 8u * (2 * STAGES + s); };
-    // quarter stage t = 4 * it + j decodes into A set t % 5 (u-th use: parity (t / 5) & 1)
-    auto afull_b = [&](int a) { return bars + 8u * (3 * STAGES + a); };
-    auto afree_b = [&](int a) { return bars + 8u * (3 * STAGES + kUASets + a); };
-    constexpr int kB2 = 3 * STAGES + 2 * kUASets;
+    // all four quarters of the stage in a slot are decoded (one wait per stage for
+    // the MMA warp: each wait costs a few hundred cycles of tensor-pipe idle time)
+    auto sready_b = [&](int s) { return bars + 8u * (3 * STAGES + s); };
+    // quarter stage t = 4 * it + j decodes into A set t % 5, freed by the MMA's
+    // commit (u-th use: parity (t / 5) & 1)
+    auto afree_b = [&](int a) { return bars + 8u * (4 * STAGES + a); };
+    constexpr int kB2 = 4 * STAGES + kUASets;
     auto dready_b = [&](int d) { return bars + 8u * (kB2 + d); };
     auto dfree_b = [&](int d) { return bars + 8u * (kB2 + 2 + d); };
     auto efull_b = [&](int d) { return bars + 8u * (kB2 + 4 + d); };
@@ -228,6 +246,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOffset + 4);
     uint8_t* masks = smem + C::kMaskOffset;
     int* eref_s = reinterpret_cast<int*>(smem + C::kErefOffset);
+    volatile int* tlow_s = reinterpret_cast<volatile int*>(smem + C::kLowOffset);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -237,11 +256,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
             mbar_init(full_b(s), 1);
             mbar_init(empty_b(s), 1 + kUDecodeWarps);  // MMA commit + every decoder warp
             mbar_init(maskfull_b(s), 12);              // the j = 1..3 decoders
+            mbar_init(sready_b(s), kUDecodeWarps);
         }
-        for (int a = 0; a < kUASets; ++a) {
-            mbar_init(afull_b(a), 4);
-            mbar_init(afree_b(a), 1);
-        }
+        for (int a = 0; a < kUASets; ++a) mbar_init(afree_b(a), 1);
         for (int d = 0; d < 2; ++d) {
             mbar_init(dready_b(d), 1);
             mbar_init(dfree_b(d), 4);
@@ -261,19 +278,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
     const int M = S.M;
 
     // Bounded wait that gives up for the whole CTA after the first timeout.
-    // Called by whole warps: lane 0 polls the barrier and the warp then goes
-    // on together (the shuffle orders the other lanes after lane 0's
-    // acquire), which keeps 32x fewer polls off the shared-memory pipe.
+    // Every lane polls: on a completed phase that returns in about half the
+    // time of one lane polling and broadcasting the result.
     auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
-        int good = 0;
-        if (lane == 0 && !*abort_flag) {
-            good = mbar_wait(bar, parity, S.status) ? 1 : 0;
-            if (!good) *abort_flag = 1;
-        }
-        return __shfl_sync(0xffffffffu, good, 0) != 0;
-    };
-    // the same for a single thread (the TMA producer)
-    auto wait_one = [&](uint32_t bar, uint32_t parity) -> bool {
         if (*abort_flag) return false;
         if (mbar_wait(bar, parity, S.status)) return true;
         *abort_flag = 1;
@@ -315,7 +322,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
                 const int n0 = R.tile * kUBN;
                 for (int i = 0; i < R.nst; ++i, ++it) {
                     const int slot = it % STAGES;
-                    if (it >= STAGES && !wait_one(empty_b(slot), ((it / STAGES) - 1) & 1)) {
+                    if (it >= STAGES && !wait(empty_b(slot), ((it / STAGES) - 1) & 1)) {
                         ok = false;
                         break;
                     }
@@ -357,18 +364,18 @@ __global__ void __launch_bounds__(kUThreads, 1)
                 const int slot = it % STAGES;
                 const int nb = min(kStageBlocks, R.kb1 - (R.kb0 + i * kStageBlocks));
                 if (!wait(full_b(slot), (it / STAGES) & 1)) { ok = false; break; }
+                if (!wait(sready_b(slot), (it / STAGES) & 1)) { ok = false; break; }
+                tc_fence_after();
                 // descriptor of the stage's X tile; block b, k-step jj starts
                 // (b >> 1) * NPAD * 128 + ((b & 1) * 2 + jj) * 32 bytes further
                 const uint64_t xd = umma_desc_sw128(sbase + slot * C::kStageBytes + C::kWBytes + C::kSBytes);
-                for (int j = 0; j < 4; ++j) {
-                    const int t = 4 * it + j;
-                    const int set = t % kUASets;
-                    if (!wait(afull_b(set), (t / kUASets) & 1)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t a0 = tbase + kUASetCols * set;
-                    const uint64_t xq = xd + uint64_t((j * 2 * NPAD * 128) >> 4);
-                    const int nbq = min(4, nb - 4 * j);
-                    if (elect_one()) {
+                if (elect_one()) {
+                    for (int j = 0; j < 4; ++j) {
+                        const int t = 4 * it + j;
+                        const int set = t % kUASets;
+                        const uint32_t a0 = tbase + kUASetCols * set;
+                        const uint64_t xq = xd + uint64_t((j * 2 * NPAD * 128) >> 4);
+                        const int nbq = min(4, nb - 4 * j);
                         if (nbq == 4) {
 #pragma unroll
                             for (int bb = 0; bb < 4; ++bb)
@@ -386,10 +393,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
                         }
                         tc_commit(afree_b(set));
                     }
-                    __syncwarp();
+                    tc_commit(empty_b(slot));
                 }
-                if (!ok) break;
-                if (elect_one()) tc_commit(empty_b(slot));
                 __syncwarp();
             }
             if (ok && elect_one()) tc_commit(dready_b(db));
@@ -398,8 +403,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
         // every issued MMA has completed before the allocation is released
         if (elect_one()) tc_commit(fin_b);
         __syncwarp();
-        if (lane == 0) mbar_wait(fin_b, 0, S.status);
-        __syncwarp();
+        mbar_wait(fin_b, 0, S.status);
     } else if (warp == 2) {
         // ---------------------------------------------- row exponents e_ref
         bool waited = false;
@@ -416,10 +420,25 @@ __global__ void __launch_bounds__(kUThreads, 1)
             const int64_t n0 = int64_t(R.tile) * kUBN;
             const int nchunk = (pb.nblk + 15) >> 4;
             const int tail = pb.nblk - 16 * (nchunk - 1);  // bytes of the row in its last chunk
+            // pull the next tile's scale rows into L2 now, so that reading them a
+            // tile from now waits on L2 rather than HBM
+            const int wn = w + int(gridDim.x);
+            if (wn < S.items) {
+                const Problem& pn = S.p[find_problem(S, wn)];
+                const int64_t nn0 = int64_t(item_range(pn, wn - pn.item_begin).tile) * kUBN;
+                const int lines = int((pn.nblk + 127) >> 7);
+                for (int rr = 0; rr < 4; ++rr) {
+                    const int64_t n = nn0 + lane + 32 * rr;
+                    if (n < pn.N)
+                        for (int l = 0; l < lines; ++l)
+                            asm volatile("prefetch.global.L2 [%0];" ::"l"(pn.sc + n * pn.sc_pitch + 128 * l));
+                }
+            }
+            bool low = false;  // some row has a block below its fp16 window
 #pragma unroll 1
             for (int rr = 0; rr < 4; ++rr) {
                 const int r = lane + 32 * rr;
-                uint32_t mx = 0;
+                uint32_t mx = 0, mn = 0xFFFFFFFFu;
                 if (n0 + r < pb.N) {
                     const uint4* row = reinterpret_cast<const uint4*>(pb.sc + (n0 + r) * pb.sc_pitch);
 #pragma unroll 4
@@ -429,17 +448,28 @@ __global__ void __launch_bounds__(kUThreads, 1)
                         mx = scale_word_max(mx, v.y, 4);
                         mx = scale_word_max(mx, v.z, 4);
                         mx = scale_word_max(mx, v.w, 4);
+                        mn = __vminu4(__vminu4(mn, v.x), __vminu4(v.y, __vminu4(v.z, v.w)));
                     }
                     const uint4 v = __ldg(row + nchunk - 1);
                     mx = scale_word_max(mx, v.x, tail);
                     mx = scale_word_max(mx, v.y, tail - 4);
                     mx = scale_word_max(mx, v.z, tail - 8);
                     mx = scale_word_max(mx, v.w, tail - 12);
+                    mn = scale_word_min(mn, v.x, tail);
+                    mn = scale_word_min(mn, v.y, tail - 4);
+                    mn = scale_word_min(mn, v.z, tail - 8);
+                    mn = scale_word_min(mn, v.w, tail - 12);
                 }
                 mx = __vmaxu4(mx, mx >> 16);
                 mx = __vmaxu4(mx, mx >> 8);
+                mn = __vminu4(mn, mn >> 16);
+                mn = __vminu4(mn, mn >> 8);
                 eref_s[es * kUBN + r] = int(mx & 0xFFu);
+                low |= int(mn & 0xFFu) < int(mx & 0xFFu) - kUWindow;
             }
+            low = __any_sync(0xffffffffu, low);
+            if (lane == 0) tlow_s[es] = low ? 1 : 0;
+            __syncwarp();
             mbar_arrive(efull_b(es));
         }
     } else {
@@ -503,6 +533,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
             const int es = tc & 1;
             if (!wait(efull_b(es), (tc >> 1) & 1)) { ok = false; break; }
             const int eref = eref_s[es * kUBN + r];
+            // without blocks below the fp16 window anywhere in the tile, the j = 0
+            // warps neither wait for the others' masks nor run the exact path
+            const bool tile_low = tlow_s[es] != 0;
             for (int i = 0; i < R.nst; ++i, ++it) {
                 const int slot = it % STAGES;
                 const int nb = min(kStageBlocks, R.kb1 - (R.kb0 + i * kStageBlocks));
@@ -537,12 +570,12 @@ __global__ void __launch_bounds__(kUThreads, 1)
                     for (int c = 0; c < 16; ++c) v[c] = hmul2_u32(v[c], mul[bb]);
                     tmem_st16(tbase + lane_addr + kUASetCols * set + 16u * bb, v);
                 }
-                if (j > 0) masks[(slot * 4 + j) * kUBN + r] = uint8_t(om);
+                if (j > 0 && tile_low) masks[(slot * 4 + j) * kUBN + r] = uint8_t(om);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(afull_b(set));
+                    mbar_arrive(sready_b(slot));
                     if (j > 0) {
                         mbar_arrive(maskfull_b(slot));
                         mbar_arrive(empty_b(slot));
@@ -552,11 +585,16 @@ __global__ void __launch_bounds__(kUThreads, 1)
                     // the previous tile's D is complete once this tile's first quarter is out
                     if (pd_tc >= 0 && !drain()) { ok = false; break; }
                     // blocks below the fp16 window (rare), all 16 of the stage: exact on
-                    // the CUDA cores while the stage is still resident, summed into E
-                    if (!wait(maskfull_b(slot), (it / STAGES) & 1)) { ok = false; break; }
-                    const uint32_t om16 = om | (uint32_t(masks[(slot * 4 + 1) * kUBN + r]) << 4) |
-                                          (uint32_t(masks[(slot * 4 + 2) * kUBN + r]) << 8) |
-                                          (uint32_t(masks[(slot * 4 + 3) * kUBN + r]) << 12);
+                    // the CUDA cores while the stage is still resident, summed into E.
+                    // (The j = 1..3 warps arrive on maskfull at every use of the slot;
+                    // waiting only in flagged tiles keeps the phases aligned, since no
+                    // arrival of a slot's next use precedes this warp's empty arrival.)
+                    if (tile_low && !wait(maskfull_b(slot), (it / STAGES) & 1)) { ok = false; break; }
+                    const uint32_t om16 =
+                        !tile_low ? 0u
+                                  : om | (uint32_t(masks[(slot * 4 + 1) * kUBN + r]) << 4) |
+                                        (uint32_t(masks[(slot * 4 + 2) * kUBN + r]) << 8) |
+                                        (uint32_t(masks[(slot * 4 + 3) * kUBN + r]) << 12);
                     if (__any_sync(0xffffffffu, om16 != 0)) {
                         const uint4 srow = *reinterpret_cast<const uint4*>(stage + C::kWBytes + r * 16);
                         const uint32_t sws[4] = {srow.x, srow.y, srow.z, srow.w};

@@ -1,4 +1,4 @@
-"""GPU parity of the tcgen05 (tensor memory) verify-GEMM path used for M > 32.
+"""GPU parity of the tcgen05 (tensor memory) verify-GEMM path used for M > 24.
 
 The entry points pick this path on their own only for wide passes (and, for
 a single GEMM, wide outputs); here it is forced (MXS_GEMM_PATH=umma) so that
