@@ -11,8 +11,12 @@
 // "Parallel Softmax & Acceptance Evaluation Mask" of the batched
 // verification kernel.
 //
-// One thread-block cluster of C CTAs per sequence (C = 1..8 by vocabulary
-// size), each CTA owning a contiguous slice of the vocabulary:
+// Two kernels.  For V <= 131072 (the pages' vocabularies) the register-
+// resident kernel further down holds each CTA's slice of the sampled law in
+// registers and carries the CDF in float-float arithmetic.  Above that, the
+// streaming kernel below: one thread-block cluster of C CTAs per sequence
+// (C = 1..8 by vocabulary size), each CTA owning a contiguous slice of the
+// vocabulary:
 //  * warp 0 of every CTA gathers p_i(x_i), q_i(x_i), u_i for the K drafts,
 //    tests u*q < p exactly (an fp32 x fp32 product is exact in double) and
 //    finds the first rejection j with one ballot (all CTAs agree);
@@ -26,6 +30,7 @@
 #include <cooperative_groups.h>
 
 #include <climits>
+#include <cstdlib>
 
 #include "mxs_device.cuh"
 #include "mxs_internal.h"
@@ -161,6 +166,48 @@ __device__ double slice_total(const float* subsum, int n, double* wtot) {
     return S;
 }
 
+// The left-to-right acceptance test of row b, run by one warp: lane i < K
+// gathers p_i(x_i), q_i(x_i) and u_i, tests u*q < p exactly (an fp32 x fp32
+// product is exact in double) and one ballot finds the first rejection j (K if
+// every draft survives).  Lane 0 stores j and the row's flags.
+__device__ __forceinline__ void accept_drafts(const AcceptParams& P, int64_t b, int lane, int* sh_j,
+                                              int* sh_flags, int* sh_err) {
+    const int K = P.K;
+    const int64_t V = P.V;
+    const bool active = lane < K;
+    const int x = active ? P.draft[b * K + lane] : 0;
+    const bool bad = active && (x < 0 || int64_t(x) >= V);
+    const unsigned badm = __ballot_sync(0xffffffffu, bad);
+    int j = K, flags = 0;
+    if (badm) {
+        flags = MXS_DEV_BAD_DRAFT;
+    } else {
+        bool rej = false, zq = false;
+        if (active) {
+            const float qx = P.q[(b * K + lane) * V + x];
+            const float px = P.p[(b * (K + 1) + lane) * V + x];
+            const float ui = P.u[b * (K + 1) + lane];
+            if (qx > 0.f) {
+                rej = !(double(ui) * double(qx) < double(px));
+            } else {
+                rej = true;
+                zq = true;
+            }
+        }
+        const unsigned rm = __ballot_sync(0xffffffffu, rej);
+        const unsigned zm = __ballot_sync(0xffffffffu, zq);
+        if (rm) {
+            j = __ffs(int(rm)) - 1;
+            if ((zm >> j) & 1u) flags |= MXS_DEV_ZERO_Q;
+        }
+    }
+    if (lane == 0) {
+        *sh_j = j;
+        *sh_flags = flags;
+        *sh_err = badm ? 1 : 0;
+    }
+}
+
 template <bool VEC>
 __global__ void __launch_bounds__(kAcceptThreads) spec_accept_kernel(const AcceptParams P) {
     extern __shared__ float subsum[];
@@ -179,37 +226,8 @@ __global__ void __launch_bounds__(kAcceptThreads) spec_accept_kernel(const Accep
 
     // ---------------------------------------------- acceptance (warp 0)
     if (warp == 0) {
-        const bool active = lane < K;
-        const int x = active ? P.draft[b * K + lane] : 0;
-        const bool bad = active && (x < 0 || int64_t(x) >= V);
-        const unsigned badm = __ballot_sync(0xffffffffu, bad);
-        int j = K, flags = 0;
-        if (badm) {
-            flags = MXS_DEV_BAD_DRAFT;
-        } else {
-            bool rej = false, zq = false;
-            if (active) {
-                const float qx = P.q[(b * K + lane) * V + x];
-                const float px = P.p[(b * (K + 1) + lane) * V + x];
-                const float ui = P.u[b * (K + 1) + lane];
-                if (qx > 0.f) {
-                    rej = !(double(ui) * double(qx) < double(px));
-                } else {
-                    rej = true;
-                    zq = true;
-                }
-            }
-            const unsigned rm = __ballot_sync(0xffffffffu, rej);
-            const unsigned zm = __ballot_sync(0xffffffffu, zq);
-            if (rm) {
-                j = __ffs(int(rm)) - 1;
-                if ((zm >> j) & 1u) flags |= MXS_DEV_ZERO_Q;
-            }
-        }
+        accept_drafts(P, b, lane, &sh_j, &sh_flags, &sh_err);
         if (lane == 0) {
-            sh_j = j;
-            sh_flags = flags;
-            sh_err = badm ? 1 : 0;
             sh_lastpos = -1;
             sh_tstar = INT_MAX;
         }
@@ -417,6 +435,338 @@ __global__ void __launch_bounds__(kAcceptThreads) spec_accept_kernel(const Accep
     }
 }
 
+// ---------------------------------------------------------------------------
+// Register-resident variant for V <= kRegMaxV (every vocabulary of the pages'
+// models).  CTA `rank` of the cluster owns elements [rank * 16384, ...) and
+// loads them once, 8 float4 per thread with every load in flight; element
+// v0 + 4 (i * 512 + t) + e sits in chunk i of thread t, so chunk i of warp w
+// is the 128-element sub-tile i * 16 + w and its fp32 sum is formed exactly
+// as in the streaming kernel.  After one exchange of slice totals (two
+// cluster barriers) the CTA holding the crossing locates the sub-tile and the
+// warp that loaded it rescans it from its registers.
+//
+// Above the sub-tile sums the running CDF is carried in float-float (an fp32
+// pair added with error-free transformations, about 44 significant bits):
+// dependent double additions cost hundreds of cycles each on this GPU's
+// FP64 unit and dominated the latency of a call; the pair arithmetic runs on
+// the fp32 pipes and keeps the CDF error many orders below the 1e-5 band in
+// which a sampled token may legitimately differ from the oracle's.
+// ---------------------------------------------------------------------------
+struct ff {
+    float hi, lo;
+};
+__device__ __forceinline__ ff ff_make(float a) { return ff{a, 0.f}; }
+// Knuth's two-sum of the high parts, then the low parts folded in.
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+    const float s = __fadd_rn(a.hi, b.hi);
+    const float v = __fsub_rn(s, a.hi);
+    float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, v)), __fsub_rn(b.hi, v));
+    e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+    const float hi = __fadd_rn(s, e);
+    return ff{hi, __fsub_rn(e, __fsub_rn(hi, s))};
+}
+__device__ __forceinline__ ff ff_neg(ff a) { return ff{-a.hi, -a.lo}; }
+// sign of a - b (compared through the pair difference)
+__device__ __forceinline__ bool ff_gt(ff a, ff b) {
+    const ff d = ff_add(a, ff_neg(b));
+    return d.hi > 0.f || (d.hi == 0.f && d.lo > 0.f);
+}
+// u * a for an fp32 u: the product of the high parts split exactly by an fma
+__device__ __forceinline__ ff ff_mul_f(ff a, float u) {
+    const float p = __fmul_rn(a.hi, u);
+    const float e = __fmaf_rn(a.hi, u, -p);
+    return ff_add(ff{p, 0.f}, ff{e, __fmul_rn(a.lo, u)});
+}
+__device__ __forceinline__ ff ff_shfl_up(ff v, int o) {
+    return ff{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+}
+__device__ __forceinline__ ff ff_shfl(ff v, int src) {
+    return ff{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+__device__ __forceinline__ ff ff_shfl_xor(ff v, int o) {
+    return ff{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+}
+// inclusive warp scan in lane order
+__device__ __forceinline__ ff warp_scan_ff(ff v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const ff n = ff_shfl_up(v, o);
+        if (lane >= o) v = ff_add(n, v);
+    }
+    return v;
+}
+// exclusive prefix from an inclusive scan (lane 0 gets zero)
+__device__ __forceinline__ ff warp_excl_ff(ff inc, int lane) {
+    const ff e = ff_shfl_up(inc, 1);
+    return lane == 0 ? ff{0.f, 0.f} : e;
+}
+
+struct SliceSummaryFF {
+    ff total;
+    int lastpos;
+};
+
+constexpr int kRegChunks = 8;
+constexpr int kRegSlice = kAcceptThreads * 4 * kRegChunks;      // 16384 elements per CTA
+constexpr int kRegSub = kRegChunks * kAcceptWarps;               // 128 sub-tiles per CTA
+constexpr int64_t kRegMaxV = int64_t(kMaxCluster) * kRegSlice;   // 131072
+
+template <bool VEC>
+__global__ void __launch_bounds__(kAcceptThreads) spec_accept_reg_kernel(const AcceptParams P) {
+    __shared__ float subsum[kRegSub];
+    __shared__ ff wsum[kRegSub / 32];
+    __shared__ SliceSummaryFF sh_mine;
+    __shared__ ff sh_S, sh_slice_prefix, sh_prefix;
+    __shared__ int sh_j, sh_flags, sh_err, sh_lastpos, sh_all_lastpos, sh_owner, sh_tstar;
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = int(cluster.num_blocks());
+    const int rank = int(cluster.block_rank());
+    const int64_t b = blockIdx.x / C;
+    const int K = P.K;
+    const int64_t V = P.V;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (warp == 0) {
+        accept_drafts(P, b, lane, &sh_j, &sh_flags, &sh_err);
+        if (lane == 0) sh_tstar = INT_MAX;
+    }
+    __syncthreads();
+
+    const int j = sh_j;
+    int32_t* tok = P.out_tokens + b * (K + 1);
+    if (sh_err) {  // uniform across the cluster: no cluster barrier is reached
+        if (rank == 0) {
+            for (int i = threadIdx.x; i <= K; i += blockDim.x) tok[i] = -1;
+            if (threadIdx.x == 0) {
+                P.n_emitted[b] = 0;
+                if (P.row_flags) P.row_flags[b] = sh_flags;
+                report(P.status, sh_flags);
+            }
+        }
+        return;
+    }
+
+    bool use_res = j < K;
+    const float* prow = P.p + (b * (K + 1) + j) * V;
+    const float* qrow = use_res ? P.q + (b * K + j) * V : nullptr;
+    const int64_t v0 = int64_t(rank) * kRegSlice;
+    const float uK = P.u[b * (K + 1) + K];
+    float r[kRegChunks][4];
+
+    // Load the slice, form the sub-tile sums and exchange the slice totals.
+    // Afterwards sh_S (identical bits in every CTA), sh_slice_prefix,
+    // sh_all_lastpos and sh_owner are set.
+    auto load_and_exchange = [&]() {
+#pragma unroll
+        for (int i = 0; i < kRegChunks; ++i)
+            load_law4<VEC>(prow, qrow, use_res, v0 + 4 * (int64_t(i) * kAcceptThreads + threadIdx.x), V, r[i]);
+        int lp = -1;
+#pragma unroll
+        for (int i = 0; i < kRegChunks; ++i) {
+            const float sm = warp_sum_f((r[i][0] + r[i][1]) + (r[i][2] + r[i][3]));
+            if (lane == 0) subsum[i * kAcceptWarps + warp] = sm;
+            const int e0 = int(v0) + 4 * (i * kAcceptThreads + int(threadIdx.x));
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (r[i][e] > 0.f) lp = max(lp, e0 + e);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+        if (threadIdx.x == 0) sh_lastpos = -1;
+        __syncthreads();
+        if (lane == 0 && lp >= 0) atomicMax(&sh_lastpos, lp);
+        // slice total: sub-tile st in thread st, a fixed-order pair reduction
+        if (threadIdx.x < kRegSub) {
+            ff v = ff_make(subsum[threadIdx.x]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = ff_add(v, ff_shfl_xor(v, o));
+            if (lane == 0) wsum[warp] = v;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            ff tot = wsum[0];
+#pragma unroll
+            for (int w = 1; w < kRegSub / 32; ++w) tot = ff_add(tot, wsum[w]);
+            sh_mine.total = tot;
+            sh_mine.lastpos = sh_lastpos;
+        }
+        cluster.sync();
+        if (threadIdx.x == 0) {
+            SliceSummaryFF o[kMaxCluster];
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c)
+                if (c < C) o[c] = *cluster.map_shared_rank(&sh_mine, c);
+            ff S{0.f, 0.f}, prefix{0.f, 0.f};
+            int last = -1;
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c)
+                if (c < C) {
+                    if (c == rank) prefix = S;
+                    S = ff_add(S, o[c].total);
+                    last = max(last, o[c].lastpos);
+                }
+            // the slice holding the first crossing, found identically everywhere
+            int owner = -1;
+            if (S.hi > 0.f && isfinite(S.hi)) {
+                const ff thr = ff_mul_f(S, uK);
+                ff run{0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < kMaxCluster; ++c)
+                    if (c < C && owner < 0) {
+                        const ff end = ff_add(run, o[c].total);
+                        if (o[c].total.hi > 0.f && ff_gt(end, thr)) owner = c;
+                        run = end;
+                    }
+            }
+            sh_S = S;
+            sh_slice_prefix = prefix;
+            sh_all_lastpos = last;
+            sh_owner = owner;
+        }
+        cluster.sync();  // every CTA has read every summary
+    };
+    load_and_exchange();
+    if (!(sh_S.hi > 0.f)) {
+        // A positive residual exists whenever rejection is possible; only the
+        // rounding of the inputs gets here.  Sample p_j instead.
+        if (threadIdx.x == 0) sh_flags |= MXS_DEV_ZERO_RESIDUAL;
+        use_res = false;
+        qrow = nullptr;
+        load_and_exchange();
+    }
+    const ff S = sh_S;
+    const bool no_law = !(S.hi > 0.f) || !isfinite(S.hi);
+    const ff thr = ff_mul_f(S, uK);
+    const int owner = sh_owner;
+    const int writer = (no_law || owner < 0) ? 0 : owner;
+    if (rank != writer) return;
+
+    if (no_law) {
+        for (int i = threadIdx.x; i <= K; i += blockDim.x) tok[i] = -1;
+        if (threadIdx.x == 0) {
+            const int f = sh_flags | MXS_DEV_NO_LAW;
+            P.n_emitted[b] = 0;
+            if (P.row_flags) P.row_flags[b] = f;
+            report(P.status, f);
+        }
+        return;
+    }
+
+    // --------------------------- locate the sub-tile where C crosses thr
+    if (owner >= 0) {
+        // thread st < 128 holds sub-tile st: pair scan over them (every shuffle
+        // with its whole warp; the crossing thread only copies its start out)
+        ff local{0.f, 0.f}, excl{0.f, 0.f}, start{0.f, 0.f};
+        if (threadIdx.x < kRegSub) {
+            local = ff_make(subsum[threadIdx.x]);
+            const ff inc = warp_scan_ff(local, lane);
+            excl = warp_excl_ff(inc, lane);
+            if (lane == 31) wsum[warp] = inc;
+        }
+        __syncthreads();
+        if (threadIdx.x < kRegSub) {
+            start = sh_slice_prefix;
+            for (int w = 0; w < warp; ++w) start = ff_add(start, wsum[w]);
+            start = ff_add(start, excl);
+            if (local.hi > 0.f && ff_gt(ff_add(start, local), thr)) atomicMin(&sh_tstar, int(threadIdx.x));
+        }
+        __syncthreads();
+        if (threadIdx.x < kRegSub && int(threadIdx.x) == sh_tstar) sh_prefix = start;
+        __syncthreads();
+    }
+
+    // ------------------- exact position, from the registers that hold it
+    const int tstar = sh_tstar;
+    const int rescan_warp = (owner >= 0 && tstar != INT_MAX) ? (tstar % kAcceptWarps) : 0;
+    if (warp == rescan_warp) {
+        int pick = -1;
+        ff before{0.f, 0.f}, after{0.f, 0.f};
+        bool edge_known = false;
+        int flags = sh_flags;
+        if (owner >= 0 && tstar != INT_MAX) {
+            const int ci = tstar / kAcceptWarps;
+            float rr[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < kRegChunks; ++i)
+                if (i == ci) {
+                    rr[0] = r[i][0]; rr[1] = r[i][1]; rr[2] = r[i][2]; rr[3] = r[i][3];
+                }
+            ff c[4];
+            c[0] = ff_make(rr[0]);
+            c[1] = ff_add(c[0], ff_make(rr[1]));
+            c[2] = ff_add(c[1], ff_make(rr[2]));
+            c[3] = ff_add(c[2], ff_make(rr[3]));
+            const ff lane_inc = warp_scan_ff(c[3], lane);
+            const ff base = ff_add(sh_prefix, warp_excl_ff(lane_inc, lane));
+            int first = 4;
+#pragma unroll
+            for (int i = 3; i >= 0; --i)
+                if (rr[i] > 0.f && ff_gt(ff_add(base, c[i]), thr)) first = i;
+            const int e0 = int(v0) + 4 * (ci * kAcceptThreads + warp * 32);
+            const unsigned hit = __ballot_sync(0xffffffffu, first < 4);
+            if (hit) {
+                const int L = __ffs(int(hit)) - 1;
+                const int fi = __shfl_sync(0xffffffffu, first, L);
+                ff cv{0.f, 0.f};
+                float rv = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (i == fi) { cv = c[i]; rv = rr[i]; }
+                const ff cb = ff_shfl(base, L);
+                cv = ff_shfl(cv, L);
+                rv = __shfl_sync(0xffffffffu, rv, L);
+                pick = e0 + 4 * L + fi;
+                after = ff_add(cb, cv);
+                before = ff_add(after, ff_make(-rv));
+            } else {
+                // the sub-tile ends at or below u*S when summed in pairs (a
+                // rounding tie with its fp32 sum): its last positive element
+                int lp = -1;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (rr[i] > 0.f) lp = 4 * lane + i;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+                pick = e0 + lp;
+                flags |= MXS_DEV_NEAR_EDGE;
+                edge_known = true;
+            }
+        } else if (owner >= 0) {
+            // the slice ends at or below u*S in this summation order (a rounding
+            // tie with its total): its last positive element
+            pick = sh_lastpos;
+            flags |= MXS_DEV_NEAR_EDGE;
+            edge_known = true;
+        } else {
+            // rounding put u*S at or beyond the last positive mass
+            pick = sh_all_lastpos;
+            float rl[4];
+            const int64_t e = int64_t(pick) & ~int64_t(3);
+            load_law4<false>(prow, qrow, use_res, e, V, rl);
+            after = S;
+            before = ff_add(S, ff_make(-rl[pick - e]));
+        }
+        if (lane == 0) {
+            if (!edge_known) {
+                // |u - C/S| for the two CDF values around the pick
+                const ff d0 = ff_add(before, ff_neg(thr)), d1 = ff_add(after, ff_neg(thr));
+                const float e0 = fabsf(d0.hi + d0.lo) / S.hi, e1 = fabsf(d1.hi + d1.lo) / S.hi;
+                if (fminf(e0, e1) < float(kNearEdge)) flags |= MXS_DEV_NEAR_EDGE;
+            }
+            tok[j] = pick;
+            P.n_emitted[b] = j + 1;
+            if (P.row_flags) P.row_flags[b] = flags;
+            report(P.status, flags);
+        }
+    }
+    // emitted drafts, then padding
+    for (int i = threadIdx.x; i <= K; i += blockDim.x) {
+        if (i < j) tok[i] = P.draft[b * K + i];
+        else if (i > j) tok[i] = -1;
+    }
+}
+
 cudaError_t accept_run(const float* p, const float* q, const int32_t* draft, const float* u,
                        int64_t B, int64_t K, int64_t V, int32_t* out_tokens, int32_t* n_emitted,
                        int32_t* row_flags, int32_t* dev_status, cudaStream_t stream) {
@@ -439,8 +789,15 @@ cudaError_t accept_run(const float* p, const float* q, const int32_t* draft, con
     P.status = dev_status;
     const bool vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
                      (K == 0 || reinterpret_cast<uintptr_t>(q) % 16 == 0);
-    const size_t smem = size_t(P.per_cta) * sizeof(float);
-    auto kern = vec ? spec_accept_kernel<true> : spec_accept_kernel<false>;
+    size_t smem = size_t(P.per_cta) * sizeof(float);
+    void (*kern)(AcceptParams) = vec ? spec_accept_kernel<true> : spec_accept_kernel<false>;
+    const bool reg = V <= kRegMaxV && std::getenv("MXS_ACCEPT_STREAMING") == nullptr;
+    if (reg) {
+        // one 16384-element slice per CTA, held in registers
+        C = int((V + kRegSlice - 1) / kRegSlice);
+        kern = vec ? spec_accept_reg_kernel<true> : spec_accept_reg_kernel<false>;
+        smem = 0;
+    }
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg{};
