@@ -42,12 +42,18 @@ import workloads  # noqa: E402
 METRIC = "MXFP4 verify-GEMM achieved HBM TB/s (% of peak); spec_accept rows/sec"
 FALLBACK_HBM_GBS = 6800.0
 
-# Per-launch DRAM traffic of the verify GEMM (read + write bytes) divided by
-# its algorithmic bytes, from the ncu capture summarised in
-# profiles/mxfp4_gemm_kernel_lm_head_4096x128256_M5.md, valid for the gemm.cu source whose
-# sha256 prefix is recorded beside it (traffic is reported as null otherwise).
-GEMM_TRAFFIC_RATIO = 1.006
-GEMM_TRAFFIC_SRC_SHA = "a617d484c78ae73e"
+# Per-launch DRAM traffic of each verify-GEMM kernel (read + write bytes)
+# divided by its algorithmic bytes, from the ncu captures summarised in
+# profiles/ (lm_head shape), valid for the GEMM sources (gemm.cu and
+# gemm_umma.cuh) whose sha256 prefix is recorded beside it; traffic is
+# reported as null otherwise.
+GEMM_TRAFFIC = {
+    # mxfp4_gemm_kernel, passes of <= 24 rows (lm_head, M=5)
+    "mma": {"ratio": 1.0074, "sha": "ec43777a6639162d"},
+    # mxfp4_gemm_umma_kernel, passes of 25..64 rows (lm_head, M=64; Y is still in L2 at exit)
+    "umma": {"ratio": 0.9140, "sha": "ec43777a6639162d"},
+}
+UMMA_MIN_ROWS = 25  # passes of at least this many rows run on the tcgen05 kernel
 
 WORKLOADS = {
     # name: (model, B, K_spec)
@@ -155,8 +161,17 @@ def dist_setup(args):
 
 
 def src_sha() -> str:
-    with open(os.path.join(ROOT, "mxfp4_speculative_verification_gb300", "csrc", "gemm.cu"), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "gemm_umma.cuh"):
+        with open(os.path.join(ROOT, "mxfp4_speculative_verification_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def gemm_passes(M: int):
+    """Row passes of the grouped GEMM (64 rows at most each) and the kernel of each."""
+    rows = [min(64, M - m0) for m0 in range(0, M, 64)]
+    return [(r, "umma" if r >= UMMA_MIN_ROWS else "mma") for r in rows]
 
 
 # ----------------------------------------------------------------------------
@@ -391,11 +406,17 @@ def run_mxs(args, world, rank, local):
 
     peak, peak_kind = load_peaks()
     achieved_gbs = gemm_b / (ms_gemm * 1e-3) / 1e9
-    launches = len(shapes)
-    n_main = (len(shapes) + 63) // 64  # grouped launches of at most 64 GEMMs
+    passes = gemm_passes(M)
+    n_main = len(passes) * ((len(shapes) + 63) // 64)  # grouped launches of at most 64 GEMMs
+    n_prep = len(passes) * ((len(ks) + 15) // 16)      # one X preparation per pass
+    kinds = sorted({k for _, k in passes})
+    kernel_name = {"mma": "mxfp4_gemm_kernel (mma.sync)",
+                   "umma": "mxfp4_gemm_umma_kernel (tcgen05)"}
     traffic = None
-    if GEMM_TRAFFIC_RATIO is not None and GEMM_TRAFFIC_SRC_SHA == src_sha():
-        traffic = GEMM_TRAFFIC_RATIO * gemm_b / n_main
+    if len(kinds) == 1:
+        t = GEMM_TRAFFIC[kinds[0]]
+        if t["ratio"] is not None and t["sha"] == src_sha():
+            traffic = t["ratio"] * gemm_b / n_main
 
     if args.detail and rank == 0:
         per_shape_detail(mxs, torch, stream, dev, shapes, weights, x_dev, ws, M)
@@ -417,11 +438,14 @@ def run_mxs(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32",
         "compute": "E2M1 weights decoded exactly to fp16, X rows power-of-two scaled to fp16, "
-                   "fp16 tensor-core products, fp32 accumulation; acceptance predicate exact (f64)",
+                   "fp16 tensor-core products, fp32 accumulation; acceptance predicate exact (f64), "
+                   "sampling CDF in float-float above fp32 128-element sums",
         "data": "synthetic",
         "config": config_block(args.workload, model, B, K_spec),
         "pct_of_peak": value * 1e3 / peak / world,
-        "roofline": {"bound": "hbm", "kernel": "mxfp4_gemm_kernel (grouped launches, incl. X preparation)",
+        "roofline": {"bound": "hbm",
+                     "kernel": " + ".join(f"{kernel_name[k]} for {r} rows" for r, k in passes)
+                               + " (grouped launches, incl. X preparation)",
                      "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": gemm_b / n_main, "launches_per_step": n_main,
@@ -436,7 +460,7 @@ def run_mxs(args, world, rank, local):
         "e2e": {"value": world * step_b / e2e_s / 1e12, "unit": "TB/s",
                 "ms_per_step": e2e_s * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "public Python API -> C ABI, eager launches, pinned host copies"},
-        "gpu_launches": args.steps * (1 + n_main + 1),
+        "gpu_launches": args.steps * (n_prep + n_main + 1),
         "clocks": clk,
         "cpu_baseline": cpu,
     }
