@@ -37,16 +37,28 @@ constexpr int kUDecodeWarps = 16;
 constexpr int kUFirstDecoder = 3;
 constexpr int kUThreads = 32 * (kUFirstDecoder + kUDecodeWarps);
 constexpr uint32_t kUTmemCols = 512;
-constexpr int kUASets = 5;                   // A ring: quarter stages of 4 blocks x 16 columns
-constexpr uint32_t kUASetCols = 64;
-constexpr uint32_t kUDCol0 = 320;            // D buffers at columns 320 and 384
-constexpr uint32_t kUDColStride = 64;
-constexpr uint32_t kUECol = 448;             // exact-path accumulator E
+constexpr uint32_t kUASetCols = 64;          // one A set: a quarter stage, 4 blocks x 16 columns
 constexpr int kUWindow = 26;                 // binades below the row maximum kept in fp16
 constexpr int kUBias = 13;                   // A = e2m1 * 2^(e_b - e_ref + kUBias)
 
+// Tensor-memory map.  The A ring takes what D leaves: 7 quarter-stage sets
+// (1.75 stages) for N_pad <= 32, 6 for 48, 5 for 64.  The exact-path
+// accumulator E lives in shared memory where it fits (N_pad <= 48) and in
+// the last 64 columns otherwise.
+template <int NPAD>
+struct UTmem {
+    static constexpr bool kESmem = NPAD <= 48;
+    static constexpr int kASets = NPAD <= 32 ? 7 : (NPAD <= 48 ? 6 : 5);
+    static constexpr uint32_t kDCol0 = uint32_t(kASets) * kUASetCols;
+    static constexpr uint32_t kDStride = NPAD <= 32 ? 32 : 64;
+    static constexpr uint32_t kECol = 448;  // used only when !kESmem
+    static_assert(kDCol0 + 2 * kDStride <= (kESmem ? kUTmemCols : kECol), "TMEM map");
+    static_assert(kESmem || kECol + 64 <= kUTmemCols, "TMEM map");
+};
+
 template <int NPAD, int STAGES>
 struct UCfg {
+    using T = UTmem<NPAD>;
     static constexpr int kBoxW = kUBN * kBoxBytes;               // 16 KB nibble box
     static constexpr int kWBytes = 2 * kBoxW;
     static constexpr int kSBytes = kUBN * 16;
@@ -55,17 +67,18 @@ struct UCfg {
     static constexpr int kMaskOffset = STAGES * kStageBytes;      // uint8 [STAGES][4][128]
     static constexpr int kErefOffset = kMaskOffset + STAGES * 4 * kUBN;  // int32 [2][128]
     static constexpr int kLowOffset = kErefOffset + 2 * kUBN * 4;        // int32 [2]: tile has low blocks
-    static constexpr int kBarOffset = kLowOffset + 16;
+    static constexpr int kEPitch = NPAD + 1;                              // floats per row of E
+    static constexpr int kEOffset = kLowOffset + 16;                      // fp32 [128][NPAD + 1] if in smem
+    static constexpr int kBarOffset = kEOffset + (T::kESmem ? kUBN * kEPitch * 4 : 0);
     // full[S], empty[S], maskfull[S], sready[S], afree[5], dready[2], dfree[2],
     // efull[2], efree[2], fin
-    static constexpr int kNumBars = 4 * STAGES + kUASets + 9;
+    static constexpr int kNumBars = 4 * STAGES + T::kASets + 9;
     static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOffset + 16 + 1024;
     static_assert(kStageBytes % 1024 == 0, "swizzled tiles need 1 KB alignment");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 64, "MMA N");
-    static_assert(kUDCol0 + 2 * kUDColStride <= kUECol && kUECol + 64 <= kUTmemCols, "TMEM map");
-    static_assert(kUASets * kUASetCols <= kUDCol0, "TMEM map");
+    static_assert(kBarOffset % 8 == 0, "mbarrier alignment");
 };
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -236,7 +249,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
     // quarter stage t = 4 * it + j decodes into A set t % 5, freed by the MMA's
     // commit (u-th use: parity (t / 5) & 1)
     auto afree_b = [&](int a) { return bars + 8u * (4 * STAGES + a); };
-    constexpr int kB2 = 4 * STAGES + kUASets;
+    constexpr int kASets = C::T::kASets;
+    constexpr int kB2 = 4 * STAGES + kASets;
     auto dready_b = [&](int d) { return bars + 8u * (kB2 + d); };
     auto dfree_b = [&](int d) { return bars + 8u * (kB2 + 2 + d); };
     auto efull_b = [&](int d) { return bars + 8u * (kB2 + 4 + d); };
@@ -258,7 +272,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
             mbar_init(maskfull_b(s), 12);              // the j = 1..3 decoders
             mbar_init(sready_b(s), kUDecodeWarps);
         }
-        for (int a = 0; a < kUASets; ++a) mbar_init(afree_b(a), 1);
+        for (int a = 0; a < kASets; ++a) mbar_init(afree_b(a), 1);
         for (int d = 0; d < 2; ++d) {
             mbar_init(dready_b(d), 1);
             mbar_init(dfree_b(d), 4);
@@ -359,7 +373,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
             const ItemRange R = item_range(pb, w - pb.item_begin);
             const int db = tc & 1;
             if (tc >= 2 && !wait(dfree_b(db), ((tc >> 1) - 1) & 1)) { ok = false; break; }
-            const uint32_t d_t = tbase + kUDCol0 + kUDColStride * db;
+            const uint32_t d_t = tbase + C::T::kDCol0 + C::T::kDStride * db;
             for (int i = 0; ok && i < R.nst; ++i, ++it) {
                 const int slot = it % STAGES;
                 const int nb = min(kStageBlocks, R.kb1 - (R.kb0 + i * kStageBlocks));
@@ -372,7 +386,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
                 if (elect_one()) {
                     for (int j = 0; j < 4; ++j) {
                         const int t = 4 * it + j;
-                        const int set = t % kUASets;
+                        const int set = t % kASets;
                         const uint32_t a0 = tbase + kUASetCols * set;
                         const uint64_t xq = xd + uint64_t((j * 2 * NPAD * 128) >> 4);
                         const int nbq = min(4, nb - 4 * j);
@@ -478,6 +492,25 @@ __global__ void __launch_bounds__(kUThreads, 1)
         const int j = (warp - kUFirstDecoder) >> 2;          // blocks 4j..4j+3 of a stage
         const int r = 32 * q + lane;                         // weight row within the tile
         const uint32_t lane_addr = uint32_t(32 * q) << 16;
+        // the exact-path accumulator E of this thread's row: 16 columns at a time
+        float* erow = reinterpret_cast<float*>(smem + C::kEOffset) + r * C::kEPitch;
+        auto e_load16 = [&](int c0, uint32_t (&ev)[16]) {
+            if constexpr (C::T::kESmem) {
+#pragma unroll
+                for (int c = 0; c < 16; ++c) ev[c] = c0 + c < NPAD ? __float_as_uint(erow[c0 + c]) : 0u;
+            } else {
+                tmem_ld16(tbase + lane_addr + C::T::kECol + c0, ev);
+            }
+        };
+        auto e_store16 = [&](int c0, const uint32_t (&ev)[16]) {
+            if constexpr (C::T::kESmem) {
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    if (c0 + c < NPAD) erow[c0 + c] = __uint_as_float(ev[c]);
+            } else {
+                tmem_st16(tbase + lane_addr + C::T::kECol + c0, ev);
+            }
+        };
         bool waited_pdl = false;
         bool e_used = false;                                 // E holds exact-path sums (j = 0)
         int it = 0, tc = 0;
@@ -504,8 +537,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
 #pragma unroll
             for (int c0 = 0; c0 < NPAD; c0 += 16) {
                 uint32_t dv[16], ev[16];
-                tmem_ld16(tbase + lane_addr + kUDCol0 + kUDColStride * db + c0, dv);
-                if (e_used) tmem_ld16(tbase + lane_addr + kUECol + c0, ev);
+                tmem_ld16(tbase + lane_addr + C::T::kDCol0 + C::T::kDStride * db + c0, dv);
+                if (e_used) e_load16(c0, ev);
                 tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
@@ -542,8 +575,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
                 if (!wait(full_b(slot), (it / STAGES) & 1)) { ok = false; break; }
                 const uint8_t* stage = smem + slot * C::kStageBytes;
                 const int t = 4 * it + j;
-                const int set = t % kUASets;
-                if (t >= kUASets && !wait(afree_b(set), ((t / kUASets) - 1) & 1)) { ok = false; break; }
+                const int set = t % kASets;
+                if (t >= kASets && !wait(afree_b(set), ((t / kASets) - 1) & 1)) { ok = false; break; }
                 // per-block fp16 multipliers 2^(e - e_ref + 13): 0 takes a block out of
                 // the MMA (beyond the stage's blocks, or below the fp16 window), NaN
                 // for a NaN scale
@@ -604,14 +637,14 @@ __global__ void __launch_bounds__(kUThreads, 1)
 #pragma unroll
                             for (int c = 0; c < 16; ++c) z[c] = 0u;
 #pragma unroll
-                            for (int c0 = 0; c0 < NPAD; c0 += 16) tmem_st16(tbase + lane_addr + kUECol + c0, z);
+                            for (int c0 = 0; c0 < NPAD; c0 += 16) e_store16(c0, z);
                             tmem_wait_st();
                             e_used = true;
                         }
 #pragma unroll 1
                         for (int c0 = 0; c0 < NPAD; c0 += 16) {
                             uint32_t ev[16];
-                            tmem_ld16(tbase + lane_addr + kUECol + c0, ev);
+                            e_load16(c0, ev);
                             tmem_wait_ld();
                             float ea[16];
 #pragma unroll
@@ -629,7 +662,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
                             __syncwarp();
 #pragma unroll
                             for (int c = 0; c < 16; ++c) ev[c] = __float_as_uint(ea[c]);
-                            tmem_st16(tbase + lane_addr + kUECol + c0, ev);
+                            e_store16(c0, ev);
                         }
                         tmem_wait_st();
                     }
