@@ -44,14 +44,14 @@ FALLBACK_HBM_GBS = 6800.0
 
 # Per-launch DRAM traffic of each verify-GEMM kernel (read + write bytes)
 # divided by its algorithmic bytes, from the ncu captures summarised in
-# profiles/ (lm_head shape), valid for the GEMM sources (gemm.cu and
-# gemm_umma.cuh) whose sha256 prefix is recorded beside it; traffic is
-# reported as null otherwise.
+# profiles/ (lm_head shape), valid for the sources of that kernel (gemm.cu
+# for mma.sync, gemm.cu + gemm_umma.cuh for tcgen05) whose sha256 prefix is
+# recorded beside it; traffic is reported as null otherwise.
 GEMM_TRAFFIC = {
     # mxfp4_gemm_kernel, passes of <= 24 rows (lm_head, M=5)
-    "mma": {"ratio": 1.0074, "sha": "ec43777a6639162d"},
+    "mma": {"ratio": 1.0074, "sha": "1f42c35c94e7af4f"},
     # mxfp4_gemm_umma_kernel, passes of 25..64 rows (lm_head, M=64; Y is still in L2 at exit)
-    "umma": {"ratio": 0.9140, "sha": "ec43777a6639162d"},
+    "umma": {"ratio": None, "sha": None},
 }
 UMMA_MIN_ROWS = 25  # passes of at least this many rows run on the tcgen05 kernel
 
@@ -160,9 +160,9 @@ def dist_setup(args):
     return world, rank, local
 
 
-def src_sha() -> str:
+def src_sha(kind: str) -> str:
     h = hashlib.sha256()
-    for name in ("gemm.cu", "gemm_umma.cuh"):
+    for name in ("gemm.cu",) + (("gemm_umma.cuh",) if kind == "umma" else ()):
         with open(os.path.join(ROOT, "mxfp4_speculative_verification_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -415,7 +415,7 @@ def run_mxs(args, world, rank, local):
     traffic = None
     if len(kinds) == 1:
         t = GEMM_TRAFFIC[kinds[0]]
-        if t["ratio"] is not None and t["sha"] == src_sha():
+        if t["ratio"] is not None and t["sha"] == src_sha(kinds[0]):
             traffic = t["ratio"] * gemm_b / n_main
 
     if args.detail and rank == 0:
