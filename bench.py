@@ -51,7 +51,7 @@ GEMM_TRAFFIC = {
     # mxfp4_gemm_kernel, passes of <= 24 rows (lm_head, M=5)
     "mma": {"ratio": 1.0074, "sha": "1f42c35c94e7af4f"},
     # mxfp4_gemm_umma_kernel, passes of 25..64 rows (lm_head, M=64; Y is still in L2 at exit)
-    "umma": {"ratio": None, "sha": None},
+    "umma": {"ratio": 0.9139, "sha": "05c65604455520d6"},
 }
 UMMA_MIN_ROWS = 25  # passes of at least this many rows run on the tcgen05 kernel
 
@@ -91,6 +91,31 @@ def load_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def in_process_peaks(mxs, torch, dev, nbytes: int = 2 << 30, reps: int = 5):
+    """HBM figures measured in this process: a device copy (read + write
+    bytes) and the library's read-only probe, each over buffers far larger
+    than L2.  Reported beside the MEASURED_PEAKS.json denominator."""
+    src = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
+    src.fill_(1.0)
+    dst = torch.empty_like(src)
+    sink = torch.zeros(4096, dtype=torch.int64, device=dev)
+    out = {}
+    for name, fn, moved in (("copy_gbs", lambda: dst.copy_(src), 2 * nbytes),
+                            ("read_gbs", lambda: mxs.hbm_read_probe(src, sink), nbytes)):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        out[name] = moved * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del src, dst
+    return out
 
 
 class ClockSampler:
@@ -405,6 +430,7 @@ def run_mxs(args, world, rank, local):
     d2h = tok_host.numel() * 4 + n_host.numel() * 4
 
     peak, peak_kind = load_peaks()
+    inproc = in_process_peaks(mxs, torch, dev) if rank == 0 else None
     achieved_gbs = gemm_b / (ms_gemm * 1e-3) / 1e9
     passes = gemm_passes(M)
     n_main = len(passes) * ((len(shapes) + 63) // 64)  # grouped launches of at most 64 GEMMs
@@ -456,13 +482,15 @@ def run_mxs(args, world, rank, local):
                      "path": "one mxfp4_verify_gemm call per GEMM (prep + main kernel each), "
                              "CUDA graph with programmatic dependent launch"},
         "spec_accept": {"rows_per_s": B / (ms_acc * 1e-3), "us_per_call": ms_acc * 1e3,
-                        "bytes_per_call": acc_b, "mean_emitted": float(np.mean(n_emitted))},
+                        "bytes_per_call": acc_b, "mean_emitted": float(np.mean(n_emitted)),
+                        "pct_of_peak": acc_b / (ms_acc * 1e-3) / 1e9 / peak},
         "e2e": {"value": world * step_b / e2e_s / 1e12, "unit": "TB/s",
                 "ms_per_step": e2e_s * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "public Python API -> C ABI, eager launches, pinned host copies"},
         "gpu_launches": args.steps * (n_prep + n_main + 1),
         "clocks": clk,
         "cpu_baseline": cpu,
+        "peaks_in_process": inproc,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -521,6 +549,81 @@ def profile_target(args):
     torch.cuda.synchronize()
 
 
+def accept_sweep(args):
+    """Acceptance-heavy sweep: B=64, K in {1,3,7}, V=128256, target logits N(0,3),
+    draft logits = target + N(0, sigma) with sigma bisected so that the mean
+    overlap sum_t min(p_t, q_t) is about 0.86.  p and q are drawn once per K;
+    drafts and uniforms are redrawn every round until the standard error of the
+    mean emitted count is below 0.01.  Reports the mean against the closed form
+    (1 - a^(K+1)) / (1 - a) at the mean overlap a, and against the exact tail
+    sum over each row's own overlaps, E_b = sum_k prod_{i<k} a_{b,i}."""
+    import torch
+
+    import mxfp4_speculative_verification_gb300 as mxs
+
+    mxs.build()
+    dev = torch.device("cuda:0")
+    B, V, std = 64, workloads.VOCAB_LLAMA, 3.0
+    peak, peak_kind = load_peaks()
+    sigma = workloads.tune_draft_noise(0.86, 4096, std, seed=0, samples=8)
+    rows = []
+    for K in (1, 3, 7):
+        p, q, _, _ = workloads.spec_inputs(B, K, V, seed=100 + K, logit_std=std, draft_noise=sigma)
+        alpha = np.minimum(p[:, :K, :].astype(np.float64), q.astype(np.float64)).sum(axis=-1)  # [B, K]
+        tail = np.concatenate([np.ones((B, 1)), np.cumprod(alpha, axis=1)], axis=1).sum(axis=1)
+        a_mean = float(alpha.mean())
+        closed = (1.0 - a_mean ** (K + 1)) / (1.0 - a_mean)
+        cdf = np.cumsum(q.astype(np.float64), axis=-1)
+        p_d, q_d = torch.from_numpy(p).to(dev), torch.from_numpy(q).to(dev)
+        out_tok = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+        n_emit = torch.empty((B,), dtype=torch.int32, device=dev)
+        rng = workloads.host_rng(200 + K, 0)
+        counts = []
+        rounds = 0
+        while True:
+            rounds += 1
+            uni = rng.random((B, K))
+            d = np.empty((B, K), dtype=np.int32)
+            for b in range(B):
+                for i in range(K):
+                    c = cdf[b, i]
+                    d[b, i] = min(int(np.searchsorted(c, uni[b, i] * c[-1], side="right")), V - 1)
+            u = rng.random((B, K + 1), dtype=np.float32)
+            mxs.spec_accept(p_d, q_d, torch.from_numpy(d).to(dev), torch.from_numpy(u).to(dev),
+                            out_tokens=out_tok, n_emitted=n_emit)
+            counts.append(n_emit.cpu().numpy().astype(np.float64))
+            allc = np.concatenate(counts)
+            se = float(allc.std(ddof=1) / np.sqrt(allc.size))
+            if (se < 0.01 and rounds >= 4) or rounds >= 1500:
+                break
+        # timing on the last round's inputs (one call, CUDA events, after warm-up)
+        for _ in range(5):
+            mxs.spec_accept(p_d, q_d, torch.from_numpy(d).to(dev), torch.from_numpy(u).to(dev),
+                            out_tokens=out_tok, n_emitted=n_emit)
+        d_d, u_d = torch.from_numpy(d).to(dev), torch.from_numpy(u).to(dev)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 50
+        e0.record()
+        for _ in range(reps):
+            mxs.spec_accept(p_d, q_d, d_d, u_d, out_tokens=out_tok, n_emitted=n_emit)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        nb = accept_bytes(B, K, V, n_emit.cpu().numpy())
+        rows.append({"K": K, "rows": int(allc.size), "rounds": rounds,
+                     "mean_emitted": float(allc.mean()), "std_error": se,
+                     "mean_overlap": a_mean, "closed_form": closed,
+                     "exact_tail_sum": float(tail.mean()),
+                     "z_vs_tail_sum": float((allc.mean() - tail.mean()) / se),
+                     "us_per_call": us, "rows_per_s": B / (us * 1e-6),
+                     "hbm_gbs": nb / (us * 1e-6) / 1e9, "pct_of_peak": nb / (us * 1e-6) / 1e9 / peak})
+    print(json.dumps({"metric": "spec_accept acceptance-heavy sweep (mean emitted tokens per step)",
+                      "B": B, "V": V, "logit_std": std, "draft_noise_sigma": sigma,
+                      "peak_gbs": peak, "peak_source": f"{peak_kind} hbm_gbs", "data": "synthetic",
+                      "rows": rows}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -536,12 +639,18 @@ def main():
                          "and exit; a small target for ncu captures")
     ap.add_argument("--profile-accept", action="store_true",
                     help="only run spec_accept of the workload 4 times and exit (ncu target)")
+    ap.add_argument("--accept-sweep", action="store_true",
+                    help="acceptance-heavy sweep (B=64, K in 1/3/7): mean emitted tokens vs the closed "
+                         "form and the per-row tail sum, plus timing; prints its own JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup(args)
     if args.profile_gemm or args.profile_accept:
         profile_target(args)
+        return
+    if args.accept_sweep:
+        accept_sweep(args)
         return
     if args.impl == "reference":
         run_reference(args, world, rank)
