@@ -511,8 +511,14 @@ constexpr int kRegSlice = kAcceptThreads * 4 * kRegChunks;      // 16384 element
 constexpr int kRegSub = kRegChunks * kAcceptWarps;               // 128 sub-tiles per CTA
 constexpr int64_t kRegMaxV = int64_t(kMaxCluster) * kRegSlice;   // 131072
 
-template <bool VEC>
-__global__ void __launch_bounds__(kAcceptThreads) spec_accept_reg_kernel(const AcceptParams P) {
+// RELOAD = false keeps the slice in registers until the rescan (one CTA per SM:
+// best while every row's cluster is resident at once).  RELOAD = true lets the
+// registers go after the sub-tile sums and re-reads the one crossing sub-tile
+// from L2 for the rescan; at half the registers two CTAs share an SM, so twice
+// as many rows are in flight when a batch needs several waves.
+template <bool VEC, bool RELOAD>
+__global__ void __launch_bounds__(kAcceptThreads, RELOAD ? 2 : 1)
+    spec_accept_reg_kernel(const AcceptParams P) {
     __shared__ float subsum[kRegSub];
     __shared__ ff wsum[kRegSub / 32];
     __shared__ SliceSummaryFF sh_mine;
@@ -558,18 +564,24 @@ __global__ void __launch_bounds__(kAcceptThreads) spec_accept_reg_kernel(const A
     // Afterwards sh_S (identical bits in every CTA), sh_slice_prefix,
     // sh_all_lastpos and sh_owner are set.
     auto load_and_exchange = [&]() {
-#pragma unroll
-        for (int i = 0; i < kRegChunks; ++i)
-            load_law4<VEC>(prow, qrow, use_res, v0 + 4 * (int64_t(i) * kAcceptThreads + threadIdx.x), V, r[i]);
         int lp = -1;
+        // all chunks in flight at once, or (RELOAD) two batches of half as many
+        constexpr int kBatch = RELOAD ? kRegChunks / 2 : kRegChunks;
 #pragma unroll
-        for (int i = 0; i < kRegChunks; ++i) {
-            const float sm = warp_sum_f((r[i][0] + r[i][1]) + (r[i][2] + r[i][3]));
-            if (lane == 0) subsum[i * kAcceptWarps + warp] = sm;
-            const int e0 = int(v0) + 4 * (i * kAcceptThreads + int(threadIdx.x));
+        for (int i0 = 0; i0 < kRegChunks; i0 += kBatch) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (r[i][e] > 0.f) lp = max(lp, e0 + e);
+            for (int i = i0; i < i0 + kBatch; ++i)
+                load_law4<VEC>(prow, qrow, use_res, v0 + 4 * (int64_t(i) * kAcceptThreads + threadIdx.x), V,
+                               r[i]);
+#pragma unroll
+            for (int i = i0; i < i0 + kBatch; ++i) {
+                const float sm = warp_sum_f((r[i][0] + r[i][1]) + (r[i][2] + r[i][3]));
+                if (lane == 0) subsum[i * kAcceptWarps + warp] = sm;
+                const int e0 = int(v0) + 4 * (i * kAcceptThreads + int(threadIdx.x));
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (r[i][e] > 0.f) lp = max(lp, e0 + e);
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
@@ -687,11 +699,16 @@ __global__ void __launch_bounds__(kAcceptThreads) spec_accept_reg_kernel(const A
         if (owner >= 0 && tstar != INT_MAX) {
             const int ci = tstar / kAcceptWarps;
             float rr[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (RELOAD) {
+                // the crossing sub-tile again, from L2 (read moments ago)
+                load_law4<VEC>(prow, qrow, use_res, v0 + 4 * (int64_t(ci) * kAcceptThreads + threadIdx.x), V, rr);
+            } else {
 #pragma unroll
-            for (int i = 0; i < kRegChunks; ++i)
-                if (i == ci) {
-                    rr[0] = r[i][0]; rr[1] = r[i][1]; rr[2] = r[i][2]; rr[3] = r[i][3];
-                }
+                for (int i = 0; i < kRegChunks; ++i)
+                    if (i == ci) {
+                        rr[0] = r[i][0]; rr[1] = r[i][1]; rr[2] = r[i][2]; rr[3] = r[i][3];
+                    }
+            }
             ff c[4];
             c[0] = ff_make(rr[0]);
             c[1] = ff_add(c[0], ff_make(rr[1]));
@@ -795,7 +812,17 @@ cudaError_t accept_run(const float* p, const float* q, const int32_t* draft, con
     if (reg) {
         // one 16384-element slice per CTA, held in registers
         C = int((V + kRegSlice - 1) / kRegSlice);
-        kern = vec ? spec_accept_reg_kernel<true> : spec_accept_reg_kernel<false>;
+        // once the clusters would take more than half the SMs, trade the registers
+        // for a second CTA per SM (measured: B = 16 19.3 -> 12.0 us, B = 64
+        // 47.5 -> 25.3 us; B <= 4 is ~0.4 us faster keeping them)
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        const char* rl = std::getenv("MXS_ACCEPT_RELOAD");
+        const bool reload = rl ? std::atoi(rl) != 0 : 2 * int64_t(B) * C > int64_t(sms);
+        if (reload) kern = vec ? spec_accept_reg_kernel<true, true> : spec_accept_reg_kernel<false, true>;
+        else kern = vec ? spec_accept_reg_kernel<true, false> : spec_accept_reg_kernel<false, false>;
         smem = 0;
     }
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
