@@ -506,19 +506,22 @@ struct SliceSummaryFF {
     int lastpos;
 };
 
-constexpr int kRegChunks = 8;
-constexpr int kRegSlice = kAcceptThreads * 4 * kRegChunks;      // 16384 elements per CTA
-constexpr int kRegSub = kRegChunks * kAcceptWarps;               // 128 sub-tiles per CTA
-constexpr int64_t kRegMaxV = int64_t(kMaxCluster) * kRegSlice;   // 131072
+constexpr int64_t kRegMaxV = int64_t(kMaxCluster) * kAcceptThreads * 4 * 8;  // 131072
 
-// RELOAD = false keeps the slice in registers until the rescan (one CTA per SM:
-// best while every row's cluster is resident at once).  RELOAD = true lets the
-// registers go after the sub-tile sums and re-reads the one crossing sub-tile
-// from L2 for the rescan; at half the registers two CTAs share an SM, so twice
-// as many rows are in flight when a batch needs several waves.
-template <bool VEC, bool RELOAD>
+// RELOAD = false keeps the slice in registers until the rescan (one CTA per SM,
+// CH = 8 float4 chunks per thread: 16384-element slices; best while every row's
+// cluster is resident at once).  RELOAD = true lets the registers go after the
+// sub-tile sums (formed in batches of 4 chunks) and re-reads the one crossing
+// sub-tile from L2 for the rescan: two CTAs share an SM, and with CH = 16
+// (32768-element slices, clusters of 4 at V = 128256) four times as many rows
+// are in flight when a batch would otherwise need several waves.
+template <bool VEC, bool RELOAD, int CH>
 __global__ void __launch_bounds__(kAcceptThreads, RELOAD ? 2 : 1)
     spec_accept_reg_kernel(const AcceptParams P) {
+    constexpr int kRegChunks = CH;
+    constexpr int kRegSlice = kAcceptThreads * 4 * kRegChunks;  // elements per CTA
+    constexpr int kRegSub = kRegChunks * kAcceptWarps;           // 128-element sub-tiles per CTA
+    static_assert(kRegSub <= kAcceptThreads, "one sub-tile per thread in the scan");
     __shared__ float subsum[kRegSub];
     __shared__ ff wsum[kRegSub / 32];
     __shared__ SliceSummaryFF sh_mine;
@@ -566,7 +569,7 @@ __global__ void __launch_bounds__(kAcceptThreads, RELOAD ? 2 : 1)
     auto load_and_exchange = [&]() {
         int lp = -1;
         // all chunks in flight at once, or (RELOAD) two batches of half as many
-        constexpr int kBatch = RELOAD ? kRegChunks / 2 : kRegChunks;
+        constexpr int kBatch = RELOAD ? 4 : kRegChunks;
 #pragma unroll
         for (int i0 = 0; i0 < kRegChunks; i0 += kBatch) {
 #pragma unroll
@@ -811,18 +814,30 @@ cudaError_t accept_run(const float* p, const float* q, const int32_t* draft, con
     const bool reg = V <= kRegMaxV && std::getenv("MXS_ACCEPT_STREAMING") == nullptr;
     if (reg) {
         // one 16384-element slice per CTA, held in registers
-        C = int((V + kRegSlice - 1) / kRegSlice);
-        // once the clusters would take more than half the SMs, trade the registers
-        // for a second CTA per SM (measured: B = 16 19.3 -> 12.0 us, B = 64
-        // 47.5 -> 25.3 us; B <= 4 is ~0.4 us faster keeping them)
+        C = int((V + kAcceptThreads * 32 - 1) / (kAcceptThreads * 32));
+        // Three forms, by how many CTAs the batch needs (C8 = CTAs per row at
+        // 16384 elements each):
+        //  * B C8 <= SMs / 2: registers kept until the rescan (one CTA per SM);
+        //  * B C8 <= 2 SMs: reload form, two CTAs per SM, one wave;
+        //  * beyond: reload form with 32768-element slices (clusters of 4 at
+        //    V = 128256), so every row is in flight at once.
+        // Measured at V = 128256: B <= 4 ~0.4 us faster with registers; B = 16
+        // 19.3 -> 11.9 us (reload); B = 64 47.5 -> 25.3 (reload) -> 19.9 us (wide).
         int dev = 0, sms = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        const char* rl = std::getenv("MXS_ACCEPT_RELOAD");
-        const bool reload = rl ? std::atoi(rl) != 0 : 2 * int64_t(B) * C > int64_t(sms);
-        if (reload) kern = vec ? spec_accept_reg_kernel<true, true> : spec_accept_reg_kernel<false, true>;
-        else kern = vec ? spec_accept_reg_kernel<true, false> : spec_accept_reg_kernel<false, false>;
+        const int64_t ctas = int64_t(B) * C;
+        int form = 2 * ctas <= int64_t(sms) ? 0 : (ctas <= 2 * int64_t(sms) ? 1 : 2);
+        if (const char* f = std::getenv("MXS_ACCEPT_FORM")) form = std::atoi(f) == 1 ? 1 : (std::atoi(f) == 2 ? 2 : 0);
+        if (form == 2) {
+            C = int((V + kAcceptThreads * 64 - 1) / (kAcceptThreads * 64));
+            kern = vec ? spec_accept_reg_kernel<true, true, 16> : spec_accept_reg_kernel<false, true, 16>;
+        } else if (form == 1) {
+            kern = vec ? spec_accept_reg_kernel<true, true, 8> : spec_accept_reg_kernel<false, true, 8>;
+        } else {
+            kern = vec ? spec_accept_reg_kernel<true, false, 8> : spec_accept_reg_kernel<false, false, 8>;
+        }
         smem = 0;
     }
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));

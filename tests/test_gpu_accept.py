@@ -149,3 +149,18 @@ def test_large_vocab_limit(env):
     V = 1 << 21
     p, q, d, u = workloads.spec_inputs(2, 1, V, seed=8, logit_std=1.0)
     _check(env, p, q, d, u)
+
+
+@pytest.mark.parametrize("form", ["0", "1", "2"])
+@pytest.mark.parametrize("V,B", [(workloads.VOCAB_LLAMA, 6), (50000, 9), (4097, 5), (40000, 3)])
+def test_every_kernel_form(env, monkeypatch, form, V, B):
+    # the register-resident kernel's three forms (registers kept; registers released
+    # and the crossing sub-tile re-read; the same with twice the slice per CTA),
+    # forced on the same inputs whatever the batch size would pick
+    monkeypatch.setenv("MXS_ACCEPT_FORM", form)
+    p, q, d, u = workloads.spec_inputs(B, 4, V, seed=V + B, logit_std=2.0)
+    _check(env, p, q, d, u)
+    # an error row (a draft id out of range) through the same form
+    d2 = d.copy()
+    d2[0, 1] = V + 3
+    _check(env, p, q, d2, u)
