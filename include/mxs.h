@@ -115,6 +115,14 @@ mxs_status mxfp4_pack(const void* w, int32_t w_dtype, int64_t N, int64_t K,
  * power of two so that its largest |x| lies in [2^15, 2^16) before it is
  * rounded to fp16 for the tensor cores: exact for every element within 2^29
  * of that row's largest magnitude.
+ *
+ * Kernels: a pass of at most 24 rows runs on mma.sync (each 32-k block summed
+ * and scaled by its E8M0 factor in fp32, split-K when N is small); a pass of
+ * 25..64 rows on 128-row tiles of N >= 8192 runs on the tcgen05 tensor-memory
+ * kernel (weights pre-scaled to exact fp16 against each row's largest
+ * exponent, whole-tile fp32 accumulation).  The two add in different orders,
+ * so their results differ in the last bits, both within the stated accuracy.
+ * MXS_GEMM_PATH=mma or =umma in the environment forces one of them.
  * ---------------------------------------------------------------------- */
 size_t mxfp4_verify_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
@@ -145,8 +153,10 @@ mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles,
  *   workspace  device, >= mxfp4_verify_gemm_grouped_workspace_size(...)
  *              bytes, 16-byte aligned.
  * Results are bit-identical to calling mxfp4_verify_gemm on each problem
- * whenever that call does not split K (splitting changes only the order
- * of fp32 additions).
+ * whenever both take the same kernel and the single call does not split K
+ * (splitting changes only the order of fp32 additions).  Passes of at most
+ * 24 rows use mma.sync in both; passes of more rows use the tcgen05 kernel
+ * here for every problem, but in a single call only for N >= 8192.
  * ---------------------------------------------------------------------- */
 typedef struct mxs_gemm_problem {
     const void* x;

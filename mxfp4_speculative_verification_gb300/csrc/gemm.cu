@@ -26,7 +26,10 @@
 //    exponent;
 //  * when K is split, each work item writes its partial tile to the
 //    workspace and bumps a per-tile counter; the item that completes the
-//    count sums all partials in split order (deterministic) and writes Y.
+//    count sums all partials in split order (deterministic) and writes Y;
+//  * passes of more than 24 rows (and, for a single GEMM, N >= 8192) run
+//    instead on the tcgen05 kernel of gemm_umma.cuh, fed by the same
+//    preparation kernel in its swizzled tile layout (`use_umma`).
 #include <cuda.h>  // CUtensorMap and the tensor-map enums (types only)
 
 #include <algorithm>
