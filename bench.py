@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -45,13 +46,14 @@ FALLBACK_HBM_GBS = 6800.0
 # Per-launch DRAM traffic of each verify-GEMM kernel (read + write bytes)
 # divided by its algorithmic bytes, from the ncu captures summarised in
 # profiles/ (lm_head shape), valid for the sources of that kernel (gemm.cu
-# for mma.sync, gemm.cu + gemm_umma.cuh for tcgen05) whose sha256 prefix is
-# recorded beside it; traffic is reported as null otherwise.
+# for mma.sync, gemm.cu + gemm_umma.cuh for tcgen05) whose sha256 prefix,
+# taken over the code with comments removed, is recorded beside it; traffic
+# is reported as null otherwise.
 GEMM_TRAFFIC = {
     # mxfp4_gemm_kernel, passes of <= 24 rows (lm_head, M=5)
-    "mma": {"ratio": 1.0074, "sha": "1f42c35c94e7af4f"},
+    "mma": {"ratio": 1.0074, "sha": "e6d8c71d70c4ae89"},
     # mxfp4_gemm_umma_kernel, passes of 25..64 rows (lm_head, M=64; Y is still in L2 at exit)
-    "umma": {"ratio": 0.9139, "sha": "05c65604455520d6"},
+    "umma": {"ratio": 0.9139, "sha": "502faf98fca7049a"},
 }
 UMMA_MIN_ROWS = 25  # passes of at least this many rows run on the tcgen05 kernel
 
@@ -185,11 +187,18 @@ def dist_setup(args):
     return world, rank, local
 
 
-def src_sha(kind: str) -> str:
+def code_only(src: str) -> str:
+    """C++ source without comments and blank lines (comment edits keep a kernel's key)."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in src.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
+def src_sha(kind: str, root: str = ROOT) -> str:
     h = hashlib.sha256()
     for name in ("gemm.cu",) + (("gemm_umma.cuh",) if kind == "umma" else ()):
-        with open(os.path.join(ROOT, "mxfp4_speculative_verification_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(root, "mxfp4_speculative_verification_gb300", "csrc", name)) as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
