@@ -29,6 +29,7 @@
 //    double scan and rescans it in double to pick the token.
 #include <cooperative_groups.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdlib>
 
@@ -787,6 +788,20 @@ __global__ void __launch_bounds__(kAcceptThreads, RELOAD ? 2 : 1)
     }
 }
 
+// Multiprocessor count of the current device, queried once per device.
+static cudaError_t sm_count(int& sms) {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    sms = cache[dev].load(std::memory_order_relaxed);
+    if (sms > 0) return cudaSuccess;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) cache[dev].store(sms, std::memory_order_relaxed);
+    return e;
+}
+
 cudaError_t accept_run(const float* p, const float* q, const int32_t* draft, const float* u,
                        int64_t B, int64_t K, int64_t V, int32_t* out_tokens, int32_t* n_emitted,
                        int32_t* row_flags, int32_t* dev_status, cudaStream_t stream) {
@@ -823,9 +838,8 @@ cudaError_t accept_run(const float* p, const float* q, const int32_t* draft, con
         //    V = 128256), so every row is in flight at once.
         // Measured at V = 128256: B <= 4 ~0.4 us faster with registers; B = 16
         // 19.3 -> 11.9 us (reload); B = 64 47.5 -> 25.3 (reload) -> 19.9 us (wide).
-        int dev = 0, sms = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        int sms = 0;
+        cudaError_t e = sm_count(sms);
         if (e != cudaSuccess) return e;
         const int64_t ctas = int64_t(B) * C;
         int form = 2 * ctas <= int64_t(sms) ? 0 : (ctas <= 2 * int64_t(sms) ? 1 : 2);
