@@ -12,10 +12,13 @@
 //    fragments (each row scaled by a power of two so that it fits fp16
 //    exactly), zeroes the split-K counters and, when needed, realigns the
 //    scale rows;
-//  * the main kernel is persistent: each CTA walks a list of work items
-//    (a tile of BN weight rows x one K range) and streams them through one
-//    continuous shared-memory ring, so the pipeline never drains between
-//    tiles.  One producer thread issues per 512-k stage two 2-D TMA tensor
+//  * the main kernel is persistent: each CTA claims work items (a tile of
+//    BN weight rows x one K range) one at a time from a counter in global
+//    memory and streams them through one continuous shared-memory ring, so
+//    the pipeline never drains between tiles.  Grouped launches order their
+//    GEMMs longest item first, which makes the claims a longest-first list
+//    schedule: items of different K (e.g. a layer's down projection against
+//    its other projections) end close together on every SM.  One producer thread issues per 512-k stage two 2-D TMA tensor
 //    copies of nibbles (128-byte swizzle, evict-first), one of scales and
 //    one bulk copy of the stage's X fragments, all completing on one
 //    mbarrier.  Consumer warps each own 16 weight rows: ldmatrix fetches
@@ -81,6 +84,7 @@ struct ProblemSet {
     int items;  // total work items
     int M;
     int32_t* status;
+    int* sched;  // item claim counter, zeroed before the launch (null: static round robin)
 };
 
 // RG groups of 16 weight rows; KW consumer warps share each group, each
@@ -101,7 +105,8 @@ struct GemmCfg {
     static constexpr int kPartFloats = KW * BN * kPartPitch;  // one partial tile per k-warp
     static constexpr int kBarOffset = kPartOffset + ((kPartFloats * 4 + 15) / 16) * 16;
     static constexpr int kMiscOffset = kBarOffset + 2 * STAGES * 8;
-    static constexpr int kSmemBytes = kMiscOffset + 16 + 1024;  // + alignment slack
+    static constexpr int kItemOffset = kMiscOffset + 16;     // work item of each ring slot
+    static constexpr int kSmemBytes = kItemOffset + 16 * ((4 * STAGES + 15) / 16) + 1024;
     static_assert(kStageBytes % 1024 == 0, "128-byte swizzled boxes need 1 KB aligned stages");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
@@ -138,6 +143,21 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 
 __device__ __forceinline__ void consumer_bar(int nthreads) {
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Barrier over the consumer threads that also returns whether v held on any
+// of them: the consumers leave their item loop together or not at all.
+__device__ __forceinline__ bool consumer_any(int nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pv, pr;\n\t"
+        "setp.ne.u32 pv, %1, 0;\n\t"
+        "barrier.cta.red.or.pred pr, 2, %2, pv;\n\t"
+        "selp.u32 %0, 1, 0, pr;\n\t}"
+        : "=r"(r)
+        : "r"(uint32_t(v)), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // One consumer warp's share of a stage: 16/KW consecutive blocks (the first
@@ -227,6 +247,9 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
     const uint32_t empty_bar = full_bar + STAGES * 8;
     float* part = reinterpret_cast<float*>(smem + C::kPartOffset);
     int* sh_last = reinterpret_cast<int*>(smem + C::kMiscOffset);
+    // item whose first stage a slot holds (-1: no items left), written by the
+    // producer before the slot's full barrier completes
+    volatile int* sh_item = reinterpret_cast<volatile int*>(smem + C::kItemOffset);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -263,7 +286,12 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
         int it = 0;
         int last_pi = -1;
         bool ok = true;
-        for (int w = blockIdx.x; ok && w < S.items; w += gridDim.x) {
+        int w = blockIdx.x;
+        while (ok && w < S.items) {
+            // the next item is claimed one item ahead, once the preceding
+            // kernels are done (they zero the counter)
+            int next = -1;
+            auto claim = [&]() { next = S.sched ? int(gridDim.x) + atomicAdd(S.sched, 1) : w + int(gridDim.x); };
             const int pi = find_problem(S, w);
             const Problem& pb = S.p[pi];
             if (pi != last_pi) {
@@ -284,6 +312,7 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
                 const int nb = min(kStageBlocks, R.kb1 - kb);
                 const uint32_t stage = smem_base + slot * C::kStageBytes;
                 const uint32_t bar = full_bar + 8 * slot;
+                if (i == 0) sh_item[slot] = w;
                 mbar_arrive_expect_tx(bar, uint32_t(C::kWBytes + C::kSBytes) +
                                                uint32_t(nb) * NT * kFragBytesPerBlockTile);
                 tma_2d(stage, &pb.tm_w, kb * 16, n0, bar, pol_w);
@@ -305,7 +334,19 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
                             issue_dep(def_slot[d], def_kb[d], def_nb[d], def_n0[d], def_pi[d]);
                     }
                 }
+                if (next < 0 && (waited || !S.sched)) claim();
             }
+            if (!ok) break;
+            if (next < 0) {
+                if (!waited) {
+                    pdl_wait();
+                    waited = true;
+                    for (int d = 0; d < ndef; ++d)
+                        issue_dep(def_slot[d], def_kb[d], def_nb[d], def_n0[d], def_pi[d]);
+                }
+                claim();
+            }
+            w = next;
         }
         if (!waited) {
             pdl_wait();
@@ -316,6 +357,15 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
         // every slot filled
         for (int j = max(0, it - STAGES); j < it; ++j)
             mbar_wait(full_bar + 8 * (j % STAGES), (j / STAGES) & 1, S.status);
+        // end of the item stream (after the waits above, which read the
+        // slots' current phases): a slot whose barrier completes without copies
+        if (ok) {
+            const int slot = it % STAGES;
+            if (it < STAGES || mbar_wait(empty_bar + 8 * slot, ((it / STAGES) - 1) & 1, S.status)) {
+                sh_item[slot] = -1;
+                mbar_arrive(full_bar + 8 * slot);
+            }
+        }
         return;
     }
 
@@ -335,7 +385,16 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
     bool waited = false;
     int it = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < S.items; w += gridDim.x) {
+    for (;;) {
+        // the next item, from the slot of its first stage
+        int w = -1;
+        if (ok) {
+            const int slot = it % STAGES;
+            if (mbar_wait(full_bar + 8 * slot, (it / STAGES) & 1, S.status)) w = sh_item[slot];
+            else ok = false;
+        }
+        __syncwarp();
+        if (consumer_any(C::kConsumers, w < 0)) break;
         const Problem& P = S.p[find_problem(S, w)];
         const int wl = w - P.item_begin;  // item index within its GEMM
         const ItemRange R = item_range(P, wl);
@@ -632,9 +691,10 @@ GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales
             part = std::max<int64_t>(part, cap * mc * bn);
         }
     }
+    // the main kernel's item claim counter, then one split-K counter per tile
     w.cnt_off = off;
     w.n_counters = int(ncnt);
-    off = align_up(off + size_t(ncnt) * sizeof(int), 256);
+    off = align_up(off + size_t(1 + ncnt) * sizeof(int), 256);
     w.part_off = off;
     off = align_up(off + size_t(part) * sizeof(float), 256);
     w.sc_off = off;
@@ -735,11 +795,12 @@ struct HostGemm {
 // Fill the launch's problem table for tiles of BN rows.
 template <int G>
 static cudaError_t build_problems(ProblemSet<G>& S, const HostGemm* gs, int count, int M,
-                                  int32_t* status, int BN, int64_t resident) {
+                                  int32_t* status, int BN, int64_t resident, int* sched) {
     std::memset(&S, 0, sizeof(S));
     S.count = count;
     S.M = M;
     S.status = status;
+    S.sched = sched;
     int64_t items = 0;
     const int forced = env_int("MXS_GEMM_SPLITS", 0);
     for (int i = 0; i < count; ++i) {
@@ -825,7 +886,7 @@ static cudaError_t launch_persistent(Kern kern, const Set& S, int threads, int s
 
 template <int NT, int RG, int KW, int STAGES, int G>
 static cudaError_t launch_main(const HostGemm* gs, int count, int M, int32_t* status,
-                               cudaStream_t stream) {
+                               int* sched, cudaStream_t stream) {
     using C = GemmCfg<NT, RG, KW, STAGES>;
     auto kern = mxfp4_gemm_kernel<NT, RG, KW, STAGES, G>;
     static LaunchFacts facts;
@@ -836,7 +897,7 @@ static cudaError_t launch_main(const HostGemm* gs, int count, int M, int32_t* st
     // the problem table lives in the (large) kernel parameter block
     static thread_local ProblemSet<G>* S_buf = nullptr;
     if (!S_buf) S_buf = new ProblemSet<G>;
-    err = build_problems(*S_buf, gs, count, M, status, C::BN, resident);
+    err = build_problems(*S_buf, gs, count, M, status, C::BN, resident, sched);
     if (err != cudaSuccess) return err;
     const int64_t grid = std::min<int64_t>(S_buf->items, resident);
     return launch_persistent(kern, *S_buf, C::kThreads, C::kSmemBytes, grid, stream);
@@ -845,13 +906,13 @@ static cudaError_t launch_main(const HostGemm* gs, int count, int M, int32_t* st
 // Kernel shape for a pass of M <= 64 rows: NT fragment tiles of 8 rows.
 template <int G>
 static cudaError_t launch_main_nt(int NT, const HostGemm* gs, int count, int M, int32_t* status,
-                                  cudaStream_t stream) {
+                                  int* sched, cudaStream_t stream) {
     switch (NT) {
-        case 1: return launch_main<1, 4, 2, 4, G>(gs, count, M, status, stream);
-        case 2: return launch_main<2, 4, 2, 3, G>(gs, count, M, status, stream);
-        case 3: return launch_main<3, 8, 2, 3, G>(gs, count, M, status, stream);
-        case 4: return launch_main<4, 8, 2, 2, G>(gs, count, M, status, stream);
-        default: return launch_main<8, 4, 2, 2, G>(gs, count, M, status, stream);
+        case 1: return launch_main<1, 4, 2, 4, G>(gs, count, M, status, sched, stream);
+        case 2: return launch_main<2, 4, 2, 3, G>(gs, count, M, status, sched, stream);
+        case 3: return launch_main<3, 8, 2, 3, G>(gs, count, M, status, sched, stream);
+        case 4: return launch_main<4, 8, 2, 2, G>(gs, count, M, status, sched, stream);
+        default: return launch_main<8, 4, 2, 2, G>(gs, count, M, status, sched, stream);
     }
 }
 
@@ -872,7 +933,7 @@ static cudaError_t launch_umma(const HostGemm* gs, int count, int M, int32_t* st
         tmp[i] = gs[i];
         tmp[i].items_cap = 0;
     }
-    err = build_problems(*S_buf, tmp, count, M, status, kUBN, int64_t(sms));
+    err = build_problems(*S_buf, tmp, count, M, status, kUBN, int64_t(sms), nullptr);
     if (err != cudaSuccess) return err;
     const int64_t grid = std::min<int64_t>(S_buf->items, int64_t(sms));
     return launch_persistent(kern, *S_buf, kUThreads, C::kSmemBytes, grid, stream);
@@ -904,6 +965,13 @@ static bool use_umma(int mc, int64_t tiles128, bool grouped) {
     return mc > 24 && (grouped || tiles128 >= 64);
 }
 
+// The claim counter a launch of the mma.sync kernel uses, or null for the
+// static round-robin order (MXS_GEMM_SCHED=static, for comparison).
+static int* sched_or_null(int* counter) {
+    const char* v = std::getenv("MXS_GEMM_SCHED");
+    return (v && std::strcmp(v, "static") == 0) ? nullptr : counter;
+}
+
 static cudaError_t launch_prep(const PrepSet& Q, cudaStream_t stream) {
     cudaLaunchConfig_t cfg{};
     const int rows = Q.umma_npad > 0 ? Q.umma_npad : 8 * Q.NT;
@@ -924,7 +992,8 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
     uint16_t* xf = reinterpret_cast<uint16_t*>(wsb + ws.xf_off);
     float* xun = reinterpret_cast<float*>(wsb + ws.xun_off);
-    int* counters = reinterpret_cast<int*>(wsb + ws.cnt_off);
+    int* sched = reinterpret_cast<int*>(wsb + ws.cnt_off);
+    int* counters = sched + 1;
     float* part = reinterpret_cast<float*>(wsb + ws.part_off);
     uint8_t* sc_aligned = ws.repack_scales ? wsb + ws.sc_off : nullptr;
     const int nblk = int(K / 32);
@@ -948,8 +1017,8 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
         Q.M = mc;
         Q.NT = NT;
         Q.umma_npad = umma ? umma_npad(mc) : 0;
-        Q.counters = counters;
-        Q.ncounters = ws.n_counters;
+        Q.counters = sched;  // the claim counter and the split-K counters
+        Q.ncounters = 1 + ws.n_counters;
         if (repack) {
             Q.sc_in = scales;
             Q.N = N;
@@ -974,7 +1043,7 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
         h.K = K;
         h.items_cap = items_cap;
         err = umma ? launch_umma_np<1>(umma_npad(mc), &h, 1, mc, dev_status, stream)
-                   : launch_main_nt<1>(NT, &h, 1, mc, dev_status, stream);
+                   : launch_main_nt<1>(NT, &h, 1, mc, dev_status, sched_or_null(sched), stream);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
@@ -1002,7 +1071,8 @@ size_t gemm_grouped_workspace(const GroupedGemm* gs, int count, int64_t M) {
         off = align_up(off + xf_bytes(mc0, gs[i].K), 256);
         off = align_up(off + kGemmMaxRowsPerPass * sizeof(float), 256);
     }
-    return off;
+    // one item claim counter per launch of a pass
+    return align_up(off + size_t((count + kGroupMax - 1) / kGroupMax) * sizeof(int), 256);
 }
 
 cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* workspace,
@@ -1030,6 +1100,8 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
         }
         xid[i] = found;
     }
+    int* sched = reinterpret_cast<int*>(wsb + off);  // one claim counter per launch of a pass
+    const int nlaunch = (count + kGroupMax - 1) / kGroupMax;
     std::vector<HostGemm> hs(count);
     // rows are processed 64 at a time; each pass converts its rows of every
     // distinct X, then streams every weight matrix once
@@ -1047,6 +1119,10 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
             Q.M = mc;
             Q.NT = NT;
             Q.umma_npad = umma ? umma_npad(mc) : 0;
+            if (j0 == 0) {
+                Q.counters = sched;
+                Q.ncounters = nlaunch;
+            }
             cudaError_t err = launch_prep(Q, stream);
             if (err != cudaSuccess) return err;
         }
@@ -1065,13 +1141,17 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
             h.items_cap = 0;
         }
         // balanced launches of at most kGroupMax GEMMs
-        const int nlaunch = (count + kGroupMax - 1) / kGroupMax;
         for (int l = 0; l < nlaunch; ++l) {
             const int b = int(int64_t(count) * l / nlaunch);
             const int e = int(int64_t(count) * (l + 1) / nlaunch);
+            int* claim = umma ? nullptr : sched_or_null(sched + l);
+            // claimed in table order: longest items (largest K) first
+            if (claim)
+                std::stable_sort(hs.begin() + b, hs.begin() + e,
+                                 [](const HostGemm& u, const HostGemm& v) { return u.K > v.K; });
             cudaError_t err =
                 umma ? launch_umma_np<kGroupMax>(umma_npad(mc), hs.data() + b, e - b, mc, dev_status, stream)
-                     : launch_main_nt<kGroupMax>(NT, hs.data() + b, e - b, mc, dev_status, stream);
+                     : launch_main_nt<kGroupMax>(NT, hs.data() + b, e - b, mc, dev_status, claim, stream);
             if (err != cudaSuccess) return err;
         }
     }

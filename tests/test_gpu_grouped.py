@@ -107,3 +107,22 @@ def test_grouped_rejects_unsupported(env):
     probs, _ = _problems(env, 5, [(544, 64)])
     with pytest.raises(mxs.MxsError):
         mxs.mxfp4_verify_gemm_grouped(probs)
+
+
+@pytest.mark.parametrize("M", [5, 20])
+def test_grouped_claim_order_does_not_change_results(env, monkeypatch, M):
+    torch, mxs = env
+    # items claimed from the counter (longest first) vs the static round robin:
+    # every output element is computed by one item in a fixed order either way
+    shapes = [(K, N) for _, K, N in workloads.LLAMA8B_LAYER] * 3 + [(512, 300), (14336, 70)]
+    probs, _ = _problems(env, M, shapes, n_x=1)
+    mxs.mxfp4_verify_gemm_grouped(probs)
+    torch.cuda.synchronize()
+    dyn = [y.clone() for *_, y in probs]
+    monkeypatch.setenv("MXS_GEMM_SCHED", "static")
+    for *_, y in probs:
+        y.fill_(float("nan"))
+    mxs.mxfp4_verify_gemm_grouped(probs)
+    torch.cuda.synchronize()
+    for a, (*_, b) in zip(dyn, probs):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
