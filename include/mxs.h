@@ -104,8 +104,9 @@ mxs_status mxfp4_pack(const void* w, int32_t w_dtype, int64_t N, int64_t K,
  *   1 <= M <= 65536, 1 <= N <= 4194240, 32 <= K <= 1048576, K % 32 == 0;
  *              rows are processed 64 at a time, each group one pass over W
  *   workspace  device, >= mxfp4_verify_gemm_workspace_size(M, N, K) bytes,
- *              16-byte aligned; scratch for the converted X (and the
- *              realigned scales).  Two calls in flight at the same time must
+ *              16-byte aligned; scratch for the converted X, the split-K
+ *              counters (zeroed by the call itself) and, when needed, the
+ *              realigned scales.  Two calls in flight at the same time must
  *              not share a workspace.  The scales need no workspace copy when
  *              K % 512 == 0 and `scales` is 16-byte aligned; with K % 512 == 0
  *              a misaligned `scales` is rejected (MXS_ERR_MISALIGNED) because
@@ -157,6 +158,12 @@ mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles,
  * (splitting changes only the order of fp32 additions).  Passes of at most
  * 24 rows use mma.sync in both; passes of more rows use the tcgen05 kernel
  * here for every problem, but in a single call only for N >= 8192.
+ * Within each mma.sync launch the problems are ordered by K, largest first,
+ * and the CTAs claim work items (a 64- or 128-row tile) from a counter in
+ * the workspace, zeroed by the call itself: a longest-first list schedule.
+ * Every output element is still summed by one item in a fixed order, so the
+ * results do not depend on which SM takes which item (MXS_GEMM_SCHED=static
+ * selects a fixed round robin, for comparison).
  * ---------------------------------------------------------------------- */
 typedef struct mxs_gemm_problem {
     const void* x;

@@ -12,13 +12,15 @@
 //    fragments (each row scaled by a power of two so that it fits fp16
 //    exactly), zeroes the split-K counters and, when needed, realigns the
 //    scale rows;
-//  * the main kernel is persistent: each CTA claims work items (a tile of
-//    BN weight rows x one K range) one at a time from a counter in global
-//    memory and streams them through one continuous shared-memory ring, so
-//    the pipeline never drains between tiles.  Grouped launches order their
-//    GEMMs longest item first, which makes the claims a longest-first list
-//    schedule: items of different K (e.g. a layer's down projection against
-//    its other projections) end close together on every SM.  One producer thread issues per 512-k stage two 2-D TMA tensor
+//  * the main kernel is persistent: each CTA streams its work items (a tile
+//    of BN weight rows x one K range) through one continuous shared-memory
+//    ring, so the pipeline never drains between tiles.  A single GEMM's
+//    items go round robin over the CTAs.  A grouped launch orders its GEMMs
+//    longest item first and, after a round-robin prefix that fills every
+//    ring, its CTAs claim further items one at a time from a counter in
+//    global memory: a longest-first list schedule, so that items of
+//    different K (a layer's down projection against its other projections)
+//    end close together on every SM.  One producer thread issues per 512-k stage two 2-D TMA tensor
 //    copies of nibbles (128-byte swizzle, evict-first), one of scales and
 //    one bulk copy of the stage's X fragments, all completing on one
 //    mbarrier.  Consumer warps each own 16 weight rows: ldmatrix fetches
@@ -85,6 +87,7 @@ struct ProblemSet {
     int M;
     int32_t* status;
     int* sched;  // item claim counter, zeroed before the launch (null: static round robin)
+    int nstatic; // items each CTA takes in round-robin order before it claims
 };
 
 // RG groups of 16 weight rows; KW consumer warps share each group, each
@@ -107,6 +110,9 @@ struct GemmCfg {
     static constexpr int kMiscOffset = kBarOffset + 2 * STAGES * 8;
     static constexpr int kItemOffset = kMiscOffset + 16;     // work item of each ring slot
     static constexpr int kSmemBytes = kItemOffset + 16 * ((4 * STAGES + 15) / 16) + 1024;
+    // Two CTAs per SM when the shared memory allows them (228 KB per SM, 1 KB
+    // reserved per CTA), else 0 (the register budget left to the compiler)
+    static constexpr int kMinBlocks = 2 * (kSmemBytes + 1024) <= 233472 ? 2 : 0;
     static_assert(kStageBytes % 1024 == 0, "128-byte swizzled boxes need 1 KB aligned stages");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
@@ -232,8 +238,13 @@ __device__ __forceinline__ int find_problem(const ProblemSet<G>& S, int w) {
     return lo;
 }
 
+// Register budget, measured (same GB300, A/B): a single GEMM's short split-K
+// items run fastest with the budget set for the CTAs per SM that fit (no
+// spills in the per-item path); the grouped launches' long items with the
+// compiler's own budget.
 template <int NT, int RG, int KW, int STAGES, int G>
-__global__ void __launch_bounds__(32 * (RG * KW + 1))
+__global__ void __launch_bounds__(GemmCfg<NT, RG, KW, STAGES>::kThreads,
+                                  G == 1 ? GemmCfg<NT, RG, KW, STAGES>::kMinBlocks : 0)
     mxfp4_gemm_kernel(const __grid_constant__ ProblemSet<G> S) {
     using C = GemmCfg<NT, RG, KW, STAGES>;
     constexpr int NWC = C::NWC;
@@ -287,11 +298,17 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
         int last_pi = -1;
         bool ok = true;
         int w = blockIdx.x;
+        int taken = 1;  // items this CTA has started
         while (ok && w < S.items) {
-            // the next item is claimed one item ahead, once the preceding
-            // kernels are done (they zero the counter)
+            // The next item, one item ahead: the first nstatic of a CTA in
+            // round-robin order (enough stages to fill the ring before the
+            // preceding kernels finish), then from the counter, which the
+            // preceding kernels zero (so only after griddepcontrol.wait).
             int next = -1;
-            auto claim = [&]() { next = S.sched ? int(gridDim.x) + atomicAdd(S.sched, 1) : w + int(gridDim.x); };
+            const bool by_counter = G > 1 && S.sched != nullptr && taken >= S.nstatic;
+            auto claim = [&]() {
+                next = by_counter ? S.nstatic * int(gridDim.x) + atomicAdd(S.sched, 1) : w + int(gridDim.x);
+            };
             const int pi = find_problem(S, w);
             const Problem& pb = S.p[pi];
             if (pi != last_pi) {
@@ -312,7 +329,7 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
                 const int nb = min(kStageBlocks, R.kb1 - kb);
                 const uint32_t stage = smem_base + slot * C::kStageBytes;
                 const uint32_t bar = full_bar + 8 * slot;
-                if (i == 0) sh_item[slot] = w;
+                if (G > 1 && i == 0) sh_item[slot] = w;
                 mbar_arrive_expect_tx(bar, uint32_t(C::kWBytes + C::kSBytes) +
                                                uint32_t(nb) * NT * kFragBytesPerBlockTile);
                 tma_2d(stage, &pb.tm_w, kb * 16, n0, bar, pol_w);
@@ -334,7 +351,7 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
                             issue_dep(def_slot[d], def_kb[d], def_nb[d], def_n0[d], def_pi[d]);
                     }
                 }
-                if (next < 0 && (waited || !S.sched)) claim();
+                if (next < 0 && (waited || !by_counter)) claim();
             }
             if (!ok) break;
             if (next < 0) {
@@ -347,6 +364,7 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
                 claim();
             }
             w = next;
+            ++taken;
         }
         if (!waited) {
             pdl_wait();
@@ -359,7 +377,7 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
             mbar_wait(full_bar + 8 * (j % STAGES), (j / STAGES) & 1, S.status);
         // end of the item stream (after the waits above, which read the
         // slots' current phases): a slot whose barrier completes without copies
-        if (ok) {
+        if (G > 1 && ok) {
             const int slot = it % STAGES;
             if (it < STAGES || mbar_wait(empty_bar + 8 * slot, ((it / STAGES) - 1) & 1, S.status)) {
                 sh_item[slot] = -1;
@@ -385,16 +403,22 @@ __global__ void __launch_bounds__(32 * (RG * KW + 1))
     bool waited = false;
     int it = 0;
     bool ok = true;
-    for (;;) {
-        // the next item, from the slot of its first stage
-        int w = -1;
-        if (ok) {
-            const int slot = it % STAGES;
-            if (mbar_wait(full_bar + 8 * slot, (it / STAGES) & 1, S.status)) w = sh_item[slot];
-            else ok = false;
+    // a single GEMM: the static round robin; grouped: the item each first
+    // stage's slot names
+    for (int ws = blockIdx.x;; ws += gridDim.x) {
+        int w = ws;
+        if constexpr (G == 1) {
+            if (w >= S.items) break;
+        } else {
+            w = -1;
+            if (ok) {
+                const int slot = it % STAGES;
+                if (mbar_wait(full_bar + 8 * slot, (it / STAGES) & 1, S.status)) w = sh_item[slot];
+                else ok = false;
+            }
+            __syncwarp();
+            if (consumer_any(C::kConsumers, w < 0)) break;
         }
-        __syncwarp();
-        if (consumer_any(C::kConsumers, w < 0)) break;
         const Problem& P = S.p[find_problem(S, w)];
         const int wl = w - P.item_begin;  // item index within its GEMM
         const ItemRange R = item_range(P, wl);
@@ -691,10 +715,9 @@ GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales
             part = std::max<int64_t>(part, cap * mc * bn);
         }
     }
-    // the main kernel's item claim counter, then one split-K counter per tile
     w.cnt_off = off;
     w.n_counters = int(ncnt);
-    off = align_up(off + size_t(1 + ncnt) * sizeof(int), 256);
+    off = align_up(off + size_t(ncnt) * sizeof(int), 256);
     w.part_off = off;
     off = align_up(off + size_t(part) * sizeof(float), 256);
     w.sc_off = off;
@@ -899,6 +922,15 @@ static cudaError_t launch_main(const HostGemm* gs, int count, int M, int32_t* st
     if (!S_buf) S_buf = new ProblemSet<G>;
     err = build_problems(*S_buf, gs, count, M, status, C::BN, resident, sched);
     if (err != cudaSuccess) return err;
+    // round-robin items per CTA before claiming: enough for STAGES stages
+    int min_nst = STAGES;
+    for (int i = 0; i < count; ++i) {
+        const Problem& p = S_buf->p[i];
+        const int total = (p.nblk + kStageBlocks - 1) / kStageBlocks;
+        const int last = total - (p.nsplit - 1) * p.stages_per_split;
+        min_nst = std::min(min_nst, std::min(p.stages_per_split, last));
+    }
+    S_buf->nstatic = (STAGES + min_nst - 1) / min_nst;
     const int64_t grid = std::min<int64_t>(S_buf->items, resident);
     return launch_persistent(kern, *S_buf, C::kThreads, C::kSmemBytes, grid, stream);
 }
@@ -965,8 +997,10 @@ static bool use_umma(int mc, int64_t tiles128, bool grouped) {
     return mc > 24 && (grouped || tiles128 >= 64);
 }
 
-// The claim counter a launch of the mma.sync kernel uses, or null for the
-// static round-robin order (MXS_GEMM_SCHED=static, for comparison).
+// The claim counter a grouped launch of the mma.sync kernel uses, or null for
+// the static round-robin order (MXS_GEMM_SCHED=static, for comparison).  A
+// single GEMM always takes the static order: its items are uniform, and its
+// split-K items (one or two stages) would expose the claim's latency.
 static int* sched_or_null(int* counter) {
     const char* v = std::getenv("MXS_GEMM_SCHED");
     return (v && std::strcmp(v, "static") == 0) ? nullptr : counter;
@@ -992,8 +1026,7 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
     uint16_t* xf = reinterpret_cast<uint16_t*>(wsb + ws.xf_off);
     float* xun = reinterpret_cast<float*>(wsb + ws.xun_off);
-    int* sched = reinterpret_cast<int*>(wsb + ws.cnt_off);
-    int* counters = sched + 1;
+    int* counters = reinterpret_cast<int*>(wsb + ws.cnt_off);
     float* part = reinterpret_cast<float*>(wsb + ws.part_off);
     uint8_t* sc_aligned = ws.repack_scales ? wsb + ws.sc_off : nullptr;
     const int nblk = int(K / 32);
@@ -1017,8 +1050,8 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
         Q.M = mc;
         Q.NT = NT;
         Q.umma_npad = umma ? umma_npad(mc) : 0;
-        Q.counters = sched;  // the claim counter and the split-K counters
-        Q.ncounters = 1 + ws.n_counters;
+        Q.counters = counters;
+        Q.ncounters = ws.n_counters;
         if (repack) {
             Q.sc_in = scales;
             Q.N = N;
@@ -1043,7 +1076,7 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
         h.K = K;
         h.items_cap = items_cap;
         err = umma ? launch_umma_np<1>(umma_npad(mc), &h, 1, mc, dev_status, stream)
-                   : launch_main_nt<1>(NT, &h, 1, mc, dev_status, sched_or_null(sched), stream);
+                   : launch_main_nt<1>(NT, &h, 1, mc, dev_status, nullptr, stream);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;

@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
             float* yrow = pd_pb->y + pd_n0 + r;
             const float* xun = pd_pb->xun;
             const int64_t N = pd_pb->N;
-#pragma unroll
+#pragma unroll 1
             for (int c0 = 0; c0 < NPAD; c0 += 16) {
                 uint32_t dv[16], ev[16];
                 tmem_ld16(tbase + lane_addr + C::T::kDCol0 + C::T::kDStride * db + c0, dv);

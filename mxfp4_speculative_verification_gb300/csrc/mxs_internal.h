@@ -16,8 +16,7 @@ struct GemmWorkspace {
     size_t bytes;        // total
     size_t xf_off;       // fragment-ordered fp16 X, kGemmMaxRowsPerPass rows max
     size_t xun_off;      // per-row unscale factors (fp32)
-    size_t cnt_off;      // the main kernel's item claim counter, then n_counters split-K
-                         // arrival counters (int32)
+    size_t cnt_off;      // split-K arrival counters (int32)
     int n_counters;
     size_t part_off;     // split-K partial tiles (fp32)
     size_t sc_off;       // realigned scales (only when needed)
