@@ -51,9 +51,9 @@ FALLBACK_HBM_GBS = 6800.0
 # is reported as null otherwise.
 GEMM_TRAFFIC = {
     # mxfp4_gemm_kernel, passes of <= 24 rows (lm_head, M=5)
-    "mma": {"ratio": None, "sha": None},
+    "mma": {"ratio": 1.0058, "sha": "5a68f06976607d73"},
     # mxfp4_gemm_umma_kernel, passes of 25..64 rows (lm_head, M=64; Y is still in L2 at exit)
-    "umma": {"ratio": None, "sha": None},
+    "umma": {"ratio": 0.9140, "sha": "4dc2e3af11e73292"},
 }
 UMMA_MIN_ROWS = 25  # passes of at least this many rows run on the tcgen05 kernel
 
