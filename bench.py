@@ -51,11 +51,12 @@ FALLBACK_HBM_GBS = 6800.0
 # is reported as null otherwise.
 GEMM_TRAFFIC = {
     # mxfp4_gemm_kernel, passes of <= 24 rows (lm_head, M=5)
-    "mma": {"ratio": 1.0058, "sha": "5a68f06976607d73"},
+    "mma": {"ratio": 1.0058, "sha": "bac806f7faf8e884"},
     # mxfp4_gemm_umma_kernel, passes of 25..64 rows (lm_head, M=64; Y is still in L2 at exit)
-    "umma": {"ratio": 0.9140, "sha": "4dc2e3af11e73292"},
+    "umma": {"ratio": 0.9140, "sha": "714ca1cc92223745"},
 }
 UMMA_MIN_ROWS = 25  # passes of at least this many rows run on the tcgen05 kernel
+GROUP_MAX = 84      # GEMMs per grouped launch at most (the problem table is a kernel parameter)
 
 WORKLOADS = {
     # name: (model, B, K_spec)
@@ -194,9 +195,16 @@ def code_only(src: str) -> str:
     return "\n".join(ln for ln in lines if ln)
 
 
+# Device code each GEMM kernel is built from (the host launchers in gemm.cu are not part of it).
+KERNEL_SOURCES = {
+    "mma": ("mxs_device.cuh", "gemm_common.cuh", "gemm_prep.cuh", "gemm_mma.cuh"),
+    "umma": ("mxs_device.cuh", "gemm_common.cuh", "gemm_prep.cuh", "gemm_umma.cuh"),
+}
+
+
 def src_sha(kind: str, root: str = ROOT) -> str:
     h = hashlib.sha256()
-    for name in ("gemm.cu",) + (("gemm_umma.cuh",) if kind == "umma" else ()):
+    for name in KERNEL_SOURCES[kind]:
         with open(os.path.join(root, "mxfp4_speculative_verification_gb300", "csrc", name)) as f:
             h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
@@ -442,7 +450,7 @@ def run_mxs(args, world, rank, local):
     inproc = in_process_peaks(mxs, torch, dev) if rank == 0 else None
     achieved_gbs = gemm_b / (ms_gemm * 1e-3) / 1e9
     passes = gemm_passes(M)
-    n_main = len(passes) * ((len(shapes) + 63) // 64)  # grouped launches of at most 64 GEMMs
+    n_main = len(passes) * ((len(shapes) + GROUP_MAX - 1) // GROUP_MAX)  # grouped launches
     n_prep = len(passes) * ((len(ks) + 15) // 16)      # one X preparation per pass
     kinds = sorted({k for _, k in passes})
     kernel_name = {"mma": "mxfp4_gemm_kernel (mma.sync)",
