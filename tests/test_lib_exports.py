@@ -89,3 +89,21 @@ def test_grouped_rejects_bad_arguments_on_host(L):
     assert f(arr, 2, 5, FAKE, 1 << 30, None, None) == 3
     arr[1] = m.GemmProblem(FAKE, FAKE + 4, FAKE, FAKE, 64, 512)  # nibbles not 16-byte aligned
     assert f(arr, 2, 5, FAKE, 1 << 30, None, None) == 2
+
+
+def test_grouped_workspace_layout(L):
+    # problems sharing one X: the X space is counted once (16 rows of fp16 for a
+    # 5-row pass, the wider of the two kernels' layouts, plus 64 unscale
+    # factors), then one int claim counter per launch of up to 84 GEMMs, each
+    # area rounded up to 256 bytes (4096 problems need 49 counters: one unit)
+    import mxfp4_speculative_verification_gb300 as m
+
+    def size(count, K=4096):
+        arr = (m.GemmProblem * count)()
+        for i in range(count):
+            arr[i] = m.GemmProblem(FAKE, FAKE, FAKE, FAKE, 64, K)
+        return L.mxfp4_verify_gemm_grouped_workspace_size(arr, count, 5)
+
+    assert size(1) == 16 * 4096 * 2 + 256 + 256
+    assert size(1) == size(84) == size(85) == size(4096)
+    assert size(1, K=14336) == 16 * 14336 * 2 + 256 + 256
