@@ -188,6 +188,21 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (the whole job is as slow as its slowest rank)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tbps(world: int, bytes_per_rank: float, seconds: float) -> float:
+    """Whole-job throughput: every rank processes bytes_per_rank in the (max) time."""
+    return world * bytes_per_rank / seconds / 1e12
+
+
 def code_only(src: str) -> str:
     """C++ source without comments and blank lines (comment edits keep a kernel's key)."""
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
@@ -402,12 +417,7 @@ def run_mxs(args, world, rank, local):
                 graph.replay()
             ev1.record(stream)
         torch.cuda.synchronize(dev)
-        ms = ev0.elapsed_time(ev1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms / steps
+        return max_over_ranks(ev0.elapsed_time(ev1), world, dev) / steps
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -439,10 +449,7 @@ def run_mxs(args, world, rank, local):
             e2e_step()
         torch.cuda.synchronize(dev)
         e2e_s = (time.perf_counter() - t0) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, world, dev)
     h2d = sum(x_host[K].numel() * 2 for K in ks) + sum(a.numel() * a.element_size() for a in acc_host)
     d2h = tok_host.numel() * 4 + n_host.numel() * 4
 
@@ -474,7 +481,7 @@ def run_mxs(args, world, rank, local):
         if world > 1:
             torch.distributed.destroy_process_group()
         return
-    value = world * step_b / (ms_step * 1e-3) / 1e12
+    value = job_tbps(world, step_b, ms_step * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -493,7 +500,7 @@ def run_mxs(args, world, rank, local):
                      "frac": achieved_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": gemm_b / n_main, "launches_per_step": n_main,
                      "avg_launch_us": ms_gemm * 1e3 / n_main, "traffic": traffic},
-        "per_call": {"value": world * step_b / (ms_step_pc * 1e-3) / 1e12, "unit": "TB/s",
+        "per_call": {"value": job_tbps(world, step_b, ms_step_pc * 1e-3), "unit": "TB/s",
                      "ms_per_step": ms_step_pc,
                      "gemm_gbs": gemm_b / (ms_gemm_pc * 1e-3) / 1e9,
                      "path": "one mxfp4_verify_gemm call per GEMM (prep + main kernel each), "
@@ -501,7 +508,7 @@ def run_mxs(args, world, rank, local):
         "spec_accept": {"rows_per_s": B / (ms_acc * 1e-3), "us_per_call": ms_acc * 1e3,
                         "bytes_per_call": acc_b, "mean_emitted": float(np.mean(n_emitted)),
                         "pct_of_peak": acc_b / (ms_acc * 1e-3) / 1e9 / peak},
-        "e2e": {"value": world * step_b / e2e_s / 1e12, "unit": "TB/s",
+        "e2e": {"value": job_tbps(world, step_b, e2e_s), "unit": "TB/s",
                 "ms_per_step": e2e_s * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "public Python API -> C ABI, eager launches, pinned host copies"},
         "gpu_launches": args.steps * (n_prep + n_main + 1),
