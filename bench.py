@@ -45,17 +45,17 @@ FALLBACK_HBM_GBS = 6800.0
 
 # Per-launch DRAM traffic of each verify-GEMM kernel (read + write bytes)
 # divided by its algorithmic bytes, from the ncu captures summarised in
-# profiles/ (lm_head shape), valid for the sources of that kernel (gemm.cu
-# for mma.sync, gemm.cu + gemm_umma.cuh for tcgen05) whose sha256 prefix,
+# profiles/, valid for the device sources of that kernel whose sha256 prefix,
 # taken over the code with comments removed, is recorded beside it; traffic
-# is reported as null otherwise.
+# is reported as null otherwise (ratio None: not yet captured on the current
+# sources).
 GEMM_TRAFFIC = {
-    # mxfp4_gemm_kernel, passes of <= 24 rows (lm_head, M=5)
-    "mma": {"ratio": 1.0058, "sha": "bac806f7faf8e884"},
-    # mxfp4_gemm_umma_kernel, passes of 25..64 rows (lm_head, M=64; Y is still in L2 at exit)
-    "umma": {"ratio": 0.9140, "sha": "714ca1cc92223745"},
+    # mxfp4_gemm_kernel, passes of <= 24 rows
+    "mma": {"ratio": None, "sha": None},
+    # mxfp4_gemm_bs_kernel, passes of 25..64 rows
+    "bs": {"ratio": None, "sha": None},
 }
-UMMA_MIN_ROWS = 25  # passes of at least this many rows run on the tcgen05 kernel
+BS_MIN_ROWS = 25    # passes of at least this many rows run on the block-scaled kernel
 GROUP_MAX = 84      # GEMMs per grouped launch at most (the problem table is a kernel parameter)
 
 WORKLOADS = {
@@ -210,10 +210,11 @@ def code_only(src: str) -> str:
     return "\n".join(ln for ln in lines if ln)
 
 
-# Device code each GEMM kernel is built from (the host launchers in gemm.cu are not part of it).
+# Device code each GEMM main kernel is built from (the host launchers in
+# gemm.cu and the preparation kernel, a launch of its own, are not part of it).
 KERNEL_SOURCES = {
-    "mma": ("mxs_device.cuh", "gemm_common.cuh", "gemm_prep.cuh", "gemm_mma.cuh"),
-    "umma": ("mxs_device.cuh", "gemm_common.cuh", "gemm_prep.cuh", "gemm_umma.cuh"),
+    "mma": ("mxs_device.cuh", "gemm_common.cuh", "gemm_mma.cuh"),
+    "bs": ("mxs_device.cuh", "gemm_common.cuh", "gemm_bs.cuh"),
 }
 
 
@@ -225,10 +226,23 @@ def src_sha(kind: str, root: str = ROOT) -> str:
     return h.hexdigest()[:16]
 
 
+def compute_desc(kinds) -> str:
+    """What the step computes in, for the kernels its passes use."""
+    parts = []
+    if "mma" in kinds:
+        parts.append("E2M1 weights decoded exactly to fp16, X rows power-of-two scaled to fp16, "
+                     "fp16 tensor-core products, fp32 accumulation")
+    if "bs" in kinds:
+        parts.append("E2M1 weights x X as two E4M3 terms with UE8M0 block factors on the block-scaled "
+                     "tensor core (exact for bf16 X within 2^16 of its block maximum), fp32 accumulation")
+    parts.append("acceptance predicate exact (f64), sampling CDF in float-float above fp32 128-element sums")
+    return "; ".join(parts)
+
+
 def gemm_passes(M: int):
     """Row passes of the grouped GEMM (64 rows at most each) and the kernel of each."""
     rows = [min(64, M - m0) for m0 in range(0, M, 64)]
-    return [(r, "umma" if r >= UMMA_MIN_ROWS else "mma") for r in rows]
+    return [(r, "bs" if r >= BS_MIN_ROWS else "mma") for r in rows]
 
 
 # ----------------------------------------------------------------------------
@@ -461,7 +475,7 @@ def run_mxs(args, world, rank, local):
     n_prep = len(passes) * ((len(ks) + 15) // 16)      # one X preparation per pass
     kinds = sorted({k for _, k in passes})
     kernel_name = {"mma": "mxfp4_gemm_kernel (mma.sync)",
-                   "umma": "mxfp4_gemm_umma_kernel (tcgen05)"}
+                   "bs": "mxfp4_gemm_bs_kernel (tcgen05 kind::mxf8f6f4 block-scaled)"}
     traffic = None
     if len(kinds) == 1:
         t = GEMM_TRAFFIC[kinds[0]]
@@ -487,9 +501,7 @@ def run_mxs(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32",
-        "compute": "E2M1 weights decoded exactly to fp16, X rows power-of-two scaled to fp16, "
-                   "fp16 tensor-core products, fp32 accumulation; acceptance predicate exact (f64), "
-                   "sampling CDF in float-float above fp32 128-element sums",
+        "compute": compute_desc(kinds),
         "data": "synthetic",
         "config": config_block(args.workload, model, B, K_spec),
         "pct_of_peak": value * 1e3 / peak / world,

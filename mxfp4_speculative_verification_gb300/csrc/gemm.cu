@@ -43,6 +43,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <vector>
@@ -55,13 +56,16 @@
 namespace mxs {
 
 constexpr int kMaxDevices = 64;
+constexpr int kBsSmemAttr = 232448;             // dynamic shared memory the block-scaled kernel may ask for
 constexpr int kMaxSplit = 32;
 constexpr int64_t kMaxSplitItems = 2048;         // bound on tiles x splits when K is split
+constexpr int64_t kBsMaxSplitItems = 304;        // the same for the block-scaled kernel (2 per SM)
 
 #include "gemm_common.cuh"
 #include "gemm_mma.cuh"
 #include "gemm_prep.cuh"
 #include "gemm_umma.cuh"
+#include "gemm_bs.cuh"
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -83,24 +87,55 @@ static int64_t split_items_cap(int64_t N, int64_t K, int bn) {
     return ns > 1 ? ntiles * ns : 0;
 }
 
+// Largest split-K work-item count of the block-scaled kernel (0 if it never splits).
+static int64_t bs_split_items_cap(int64_t N, int64_t K) {
+    const int64_t ntiles = (N + kBsRows - 1) / kBsRows;
+    const int64_t stages = (K / 32 + kBsStageBlocks - 1) / kBsStageBlocks;
+    const int64_t ns = std::min<int64_t>(
+        {int64_t(kMaxSplit), stages, std::max<int64_t>(1, kBsMaxSplitItems / ntiles)});
+    return ns > 1 ? ntiles * ns : 0;
+}
+
+static bool use_bs(int64_t rows_left, bool eligible);
+
+// Whether a call of M rows may run a block-scaled pass (sizes its workspace).
+static bool bs_may_run(int64_t M, int64_t K) { return use_bs(M, K % 128 == 0); }
+
+// Bytes of X prepared for the block-scaled kernel (passes of at most mc rows).
+static size_t bs_x_bytes(int64_t mc, int64_t K) {
+    const int npad = bs_npad(int(std::min<int64_t>(mc, kBsMaxNpad)));
+    return size_t((K + 255) / 256) * size_t(bs_bstage_bytes(npad) + bs_sfbstage_bytes(npad));
+}
+
 GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales_aligned) {
     GemmWorkspace w{};
     const int64_t nblk = K / 32;
     const int64_t mc = std::min<int64_t>(M, kGemmMaxRowsPerPass);
+    const int64_t mcb = std::min<int64_t>(M, kBsMaxNpad);
     w.repack_scales = !(K % 512 == 0 && scales_aligned);
     w.sc_pitch = w.repack_scales ? int(align_up(size_t(nblk), 16)) : int(nblk);
     size_t off = 0;
     w.xf_off = off;
-    off = align_up(off + size_t(kGemmMaxRowsPerPass) * align_up(size_t(K), 512) * 2, 256);
+    off = align_up(off + std::max(size_t(kGemmMaxRowsPerPass) * align_up(size_t(K), 512) * 2,
+                                  bs_may_run(M, K) ? bs_x_bytes(mcb, K) : size_t(0)),
+                   256);
     w.xun_off = off;
-    off = align_up(off + kGemmMaxRowsPerPass * sizeof(float), 256);
-    // counters and partial tiles, sized for either tile height a pass may use
+    off = align_up(off + kBsMaxNpad * sizeof(float), 256);
+    // counters and partial tiles, sized for any tile height a pass may use
+    // (the block-scaled kernel counts each 32-row quarter of a tile apart)
     int64_t ncnt = 0, part = 0;
     for (int bn : {64, 128}) {
         const int64_t cap = split_items_cap(N, K, bn);
         if (cap > 0) {
             ncnt = std::max<int64_t>(ncnt, (N + bn - 1) / bn);
             part = std::max<int64_t>(part, cap * mc * bn);
+        }
+    }
+    if (bs_may_run(M, K)) {
+        const int64_t cap = bs_split_items_cap(N, K);
+        if (cap > 0) {
+            ncnt = std::max<int64_t>(ncnt, 4 * ((N + kBsRows - 1) / kBsRows));
+            part = std::max<int64_t>(part, cap * mcb * kBsRows);
         }
     }
     w.cnt_off = off;
@@ -157,6 +192,24 @@ static bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D tensor map over packed E2M1 nibbles [rows, K] for the block-scaled
+// kernel: dims (128 codes, rows, K / 128 chunks), each request of the
+// 16U4_ALIGN16B type spreading 16 codes (8 bytes) over 16 bytes of shared
+// memory; boxes of 128 codes x 128 rows x `chunks`, 128-byte swizzle.  Needs
+// K % 128 == 0 and a 32-byte aligned base (the type's rules).
+static bool make_map_e2m1_spread(CUtensorMap* map, const void* base, int64_t rows, int64_t K, uint32_t chunks) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[3] = {128, cuuint64_t(rows), cuuint64_t(K / 128)};
+    cuuint64_t strides[2] = {cuuint64_t(K / 2), 64};
+    cuuint32_t box[3] = {128, uint32_t(kBsRows), chunks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    std::memset(map, 0, sizeof(*map));
+    return f(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Per-device launch facts of one kernel instantiation, computed on first use.
 struct LaunchFacts {
     std::atomic<int> sms[kMaxDevices];
@@ -166,7 +219,7 @@ struct LaunchFacts {
 // Split of K: the count whose busiest CTA streams the fewest stages, with a
 // small charge per extra work item for its partial-tile round trip.
 static void choose_split(int64_t ntiles, int stages_total, int64_t grid_cap, int64_t items_cap,
-                         int& nsplit, int& per_split) {
+                         int& nsplit, int& per_split, double item_cost = 0.35) {
     double best = 1e300;
     nsplit = 1;
     per_split = stages_total;
@@ -179,7 +232,7 @@ static void choose_split(int64_t ntiles, int stages_total, int64_t grid_cap, int
         if (ns > 1 && items > items_cap) break;
         const int64_t grid = std::min<int64_t>(items, grid_cap);
         const double per_cta = double((items + grid - 1) / grid);
-        const double cost = per_cta * (sps + (ns > 1 ? 0.35 : 0.0));
+        const double cost = per_cta * (sps + (ns > 1 ? item_cost : 0.0));
         if (cost < best - 1e-9) {
             best = cost;
             nsplit = ns;
@@ -204,9 +257,11 @@ struct HostGemm {
 };
 
 // Fill the launch's problem table for tiles of BN rows.
+// bs: the block-scaled kernel (256-k stages, scales read in place).
 template <int G>
 static cudaError_t build_problems(ProblemSet<G>& S, const HostGemm* gs, int count, int M,
-                                  int32_t* status, int BN, int64_t resident, int* sched) {
+                                  int32_t* status, int BN, int64_t resident, int* sched,
+                                  bool bs = false) {
     std::memset(&S, 0, sizeof(S));
     S.count = count;
     S.M = M;
@@ -228,11 +283,13 @@ static cudaError_t build_problems(ProblemSet<G>& S, const HostGemm* gs, int coun
         p.sc_from_prep = h.sc_from_prep ? 1 : 0;
         p.sc = h.sc;
         p.sc_pitch = h.sc_pitch;
-        const int stages_total = (p.nblk + kStageBlocks - 1) / kStageBlocks;
+        const int sblk = bs ? kBsStageBlocks : kStageBlocks;
+        const int stages_total = (p.nblk + sblk - 1) / sblk;
         p.nsplit = 1;
         p.stages_per_split = stages_total;
         if (h.items_cap > 0) {
-            choose_split(p.ntiles, stages_total, resident, h.items_cap, p.nsplit, p.stages_per_split);
+            choose_split(p.ntiles, stages_total, resident, h.items_cap, p.nsplit, p.stages_per_split,
+                         bs ? 0.7 : 0.35);
             if (forced > 0) {
                 int ns = std::min(forced, stages_total);
                 const int sps = (stages_total + ns - 1) / ns;
@@ -246,6 +303,13 @@ static cudaError_t build_problems(ProblemSet<G>& S, const HostGemm* gs, int coun
         p.item_begin = int(items);
         items += int64_t(p.ntiles) * p.nsplit;
         if (items > INT32_MAX) return cudaErrorInvalidValue;
+        if (bs) {
+            // both 128-k chunks of a stage per request, and one chunk for the last of an odd count
+            if (!make_map_e2m1_spread(&p.tm_w, h.nib, h.N, h.K, 2) ||
+                !make_map_e2m1_spread(&p.tm_s, h.nib, h.N, h.K, 1))
+                return cudaErrorInvalidValue;
+            continue;
+        }
         if (!make_map(&p.tm_w, h.nib, h.N, h.K / 2, h.K / 2, kBoxBytes, uint32_t(BN), true))
             return cudaErrorInvalidValue;
         if (!make_map(&p.tm_s, h.sc, h.N, p.nblk, h.sc_pitch, 16, uint32_t(BN), false))
@@ -373,6 +437,64 @@ static cudaError_t launch_umma_np(int npad, const HostGemm* gs, int count, int M
     }
 }
 
+// Stage slots of the block-scaled kernel for a pass of npad rows;
+// MXS_GEMM_BS_RINGS=c overrides it when c slots fit shared and tensor memory.
+static int bs_ring_for(int npad) {
+    const int c = env_int("MXS_GEMM_BS_RINGS", 0);
+    if (c >= 2 && c <= kBsMaxRing && bs_smem_bytes(npad, c) <= kBsSmemAttr && bs_tmem_need(npad, c) <= int(kBsTmemCols))
+        return c;
+    return bs_ring(npad);
+}
+
+// Block-scaled kernel: one CTA per SM, 128-row tiles, K split only for a
+// single GEMM whose tiles leave SMs idle.
+template <int G>
+static cudaError_t launch_bs_np(const HostGemm* gs, int count, int M, int32_t* status,
+                                cudaStream_t stream) {
+    auto kern = mxfp4_gemm_bs_kernel<G>;
+    static LaunchFacts facts;
+    int sms = 0, occ = 0;
+    cudaError_t err = launch_facts(facts, kern, kBsThreads, kBsSmemAttr, sms, occ);
+    if (err != cudaSuccess) return err;
+    static thread_local ProblemSet<G>* S_buf = nullptr;
+    if (!S_buf) S_buf = new ProblemSet<G>;
+    err = build_problems(*S_buf, gs, count, M, status, kBsRows, int64_t(sms), nullptr, true);
+    if (err != cudaSuccess) return err;
+    const int npad = bs_npad(M);
+    S_buf->ring = bs_ring_for(npad);
+    S_buf->pf_stages = std::max(0, std::min(64, env_int("MXS_GEMM_BS_PF", kBsPfStages)));
+    const int64_t grid = std::min<int64_t>(S_buf->items, int64_t(sms));
+    return launch_persistent(kern, *S_buf, kBsThreads, bs_smem_bytes(npad, S_buf->ring), grid, stream);
+}
+
+// Every pass size the block-scaled kernel takes fits its shared and tensor memory.
+static constexpr bool bs_shapes_fit() {
+    for (int m = 1; m <= kBsMaxNpad; ++m) {
+        const int npad = bs_npad(m);
+        const int rc = bs_ring(npad);
+        if (bs_smem_bytes(npad, rc) > kBsSmemAttr || bs_tmem_need(npad, rc) > int(kBsTmemCols) || rc > kBsMaxRing)
+            return false;
+    }
+    return true;
+}
+static_assert(bs_shapes_fit(), "block-scaled kernel: a pass size exceeds shared or tensor memory");
+
+// The block-scaled kernel takes every pass of at least MXS_GEMM_BS_MIN rows
+// (default 25: below that mma.sync streams faster, measured on the lm_head
+// shape) whenever the weights allow it: K % 128 == 0 and 32-byte aligned
+// nibbles (the packed TMA type's rules).  MXS_GEMM_PATH=bs forces it for
+// every pass it can take.
+static bool bs_eligible(int64_t K, const void* nib) {
+    return K % 128 == 0 && (reinterpret_cast<uintptr_t>(nib) & 31) == 0;
+}
+static bool use_bs(int64_t rows_left, bool eligible) {
+    if (!eligible) return false;
+    const char* path = std::getenv("MXS_GEMM_PATH");
+    if (path && std::strcmp(path, "bs") == 0) return true;
+    if (path && (std::strcmp(path, "mma") == 0 || std::strcmp(path, "umma") == 0)) return false;
+    return rows_left >= env_int("MXS_GEMM_BS_MIN", 25);
+}
+
 // Which kernel a pass of mc rows uses.  mma.sync (legacy tensor path) is
 // faster up to 24 rows; beyond that its m16n8k16 issue rate, not HBM,
 // bounds it and the tcgen05 kernel takes over.  MXS_GEMM_PATH=mma|umma
@@ -396,7 +518,7 @@ static int* sched_or_null(int* counter) {
 
 static cudaError_t launch_prep(const PrepSet& Q, cudaStream_t stream) {
     cudaLaunchConfig_t cfg{};
-    const int rows = Q.umma_npad > 0 ? Q.umma_npad : 8 * Q.NT;
+    const int rows = Q.bs_npad > 0 ? Q.bs_npad : (Q.umma_npad > 0 ? Q.umma_npad : 8 * Q.NT);
     cfg.gridDim = dim3(unsigned(Q.njobs * rows + 1 + Q.repack_ctas), 1, 1);
     cfg.blockDim = dim3(kPrepThreads, 1, 1);
     cfg.stream = stream;
@@ -419,25 +541,61 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
     uint8_t* sc_aligned = ws.repack_scales ? wsb + ws.sc_off : nullptr;
     const int nblk = int(K / 32);
     const int64_t mc0 = std::min<int64_t>(M, kGemmMaxRowsPerPass);
-    for (int64_t m0 = 0; m0 < M; m0 += kGemmMaxRowsPerPass) {
-        const int mc = int(std::min<int64_t>(kGemmMaxRowsPerPass, M - m0));
-        const int NT = tiles_nt(mc);
+    const bool bs_ok = bs_eligible(K, nibbles);
+    bool scales_realigned = false;
+    for (int64_t m0 = 0, mc = 0; m0 < M; m0 += mc) {
+        if (use_bs(M - m0, bs_ok)) {
+            // block-scaled pass of up to 128 rows: raw scales, its own X layout
+            mc = std::min<int64_t>(kBsMaxNpad, M - m0);
+            PrepSet Q{};
+            Q.job[0].x = x + m0 * K;
+            Q.job[0].xf = xf;
+            Q.job[0].xun = xun;
+            Q.job[0].K = int(K);
+            Q.njobs = 1;
+            Q.M = int(mc);
+            Q.NT = 1;
+            Q.bs_npad = bs_npad(int(mc));
+            Q.counters = counters;
+            Q.ncounters = ws.n_counters;
+            cudaError_t err = launch_prep(Q, stream);
+            if (err != cudaSuccess) return err;
+            HostGemm h{};
+            h.nib = nibbles;
+            h.sc = scales;
+            h.sc_pitch = nblk;
+            h.xf = xf;
+            h.xun = xun;
+            h.y = y + m0 * N;
+            h.part = part;
+            h.counters = counters;
+            h.N = N;
+            h.K = K;
+            const int64_t cap = bs_split_items_cap(N, K);
+            h.items_cap = (cap > 0 && ws.n_counters >= 4 * ((N + kBsRows - 1) / kBsRows)) ? cap : 0;
+            err = launch_bs_np<1>(&h, 1, int(mc), dev_status, stream);
+            if (err != cudaSuccess) return err;
+            continue;
+        }
+        mc = std::min<int64_t>(kGemmMaxRowsPerPass, M - m0);
+        const int NT = tiles_nt(int(mc));
         const int bn = bn_for_nt(NT);
         // the workspace holds partial tiles for mc0 rows and tile height bn
         int64_t items_cap = split_items_cap(N, K, bn);
         if (ws.n_counters < (N + bn - 1) / bn || mc > mc0) items_cap = 0;
-        const bool umma = use_umma(mc, (N + kUBN - 1) / kUBN, false);
-        // the scales are realigned once, by the first pass
-        const bool repack = ws.repack_scales && m0 == 0;
+        const bool umma = use_umma(int(mc), (N + kUBN - 1) / kUBN, false);
+        // the scales are realigned once, by the first pass that reads them
+        const bool repack = ws.repack_scales && !scales_realigned;
+        scales_realigned = true;
         PrepSet Q{};
         Q.job[0].x = x + m0 * K;
         Q.job[0].xf = xf;
         Q.job[0].xun = xun;
         Q.job[0].K = int(K);
         Q.njobs = 1;
-        Q.M = mc;
+        Q.M = int(mc);
         Q.NT = NT;
-        Q.umma_npad = umma ? umma_npad(mc) : 0;
+        Q.umma_npad = umma ? umma_npad(int(mc)) : 0;
         Q.counters = counters;
         Q.ncounters = ws.n_counters;
         if (repack) {
@@ -463,8 +621,8 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
         h.N = N;
         h.K = K;
         h.items_cap = items_cap;
-        err = umma ? launch_umma_np<1>(umma_npad(mc), &h, 1, mc, dev_status, stream)
-                   : launch_main_nt<1>(NT, &h, 1, mc, dev_status, nullptr, stream);
+        err = umma ? launch_umma_np<1>(umma_npad(int(mc)), &h, 1, int(mc), dev_status, stream)
+                   : launch_main_nt<1>(NT, &h, 1, int(mc), dev_status, nullptr, stream);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
@@ -477,21 +635,22 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
 constexpr int kGroupMax = 84;
 static_assert(sizeof(ProblemSet<kGroupMax>) <= 32764, "the problem table is a kernel parameter (32764 bytes at most)");
 
-// Bytes of one prepared X (either layout) for passes of at most mc0 rows.
-static size_t xf_bytes(int mc0, int64_t K) {
+// Bytes of one prepared X (any layout) for an X of M rows.
+static size_t xf_bytes(int64_t M, int64_t K) {
+    const int mc0 = int(std::min<int64_t>(M, kGemmMaxRowsPerPass));
     const int rows = std::max(8 * tiles_nt(mc0), umma_npad(mc0));
-    return size_t(rows) * align_up(size_t(K), 512) * 2;
+    return std::max(size_t(rows) * align_up(size_t(K), 512) * 2,
+                    bs_may_run(M, K) ? bs_x_bytes(std::min<int64_t>(M, kBsMaxNpad), K) : size_t(0));
 }
 
 size_t gemm_grouped_workspace(const GroupedGemm* gs, int count, int64_t M) {
-    const int mc0 = int(std::min<int64_t>(M, kGemmMaxRowsPerPass));
     size_t off = 0;
     for (int i = 0; i < count; ++i) {
         bool seen = false;
         for (int j = 0; j < i && !seen; ++j) seen = gs[j].x == gs[i].x && gs[j].K == gs[i].K;
         if (seen) continue;
-        off = align_up(off + xf_bytes(mc0, gs[i].K), 256);
-        off = align_up(off + kGemmMaxRowsPerPass * sizeof(float), 256);
+        off = align_up(off + xf_bytes(M, gs[i].K), 256);
+        off = align_up(off + kBsMaxNpad * sizeof(float), 256);
     }
     // one item claim counter per launch of a pass
     return align_up(off + size_t((count + kGroupMax - 1) / kGroupMax) * sizeof(int), 256);
@@ -500,11 +659,12 @@ size_t gemm_grouped_workspace(const GroupedGemm* gs, int count, int64_t M) {
 cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* workspace,
                              int32_t* dev_status, cudaStream_t stream) {
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
-    const int mc0 = int(std::min<int64_t>(M, kGemmMaxRowsPerPass));
-    // distinct activations, in first-use order; X space sized for passes of mc0 rows
+    // distinct activations, in first-use order; X space sized for the largest pass
     std::vector<int> xid(count);
     std::vector<PrepJob> jobs;
     size_t off = 0;
+    bool bs_ok = true;
+    for (int i = 0; i < count; ++i) bs_ok = bs_ok && bs_eligible(gs[i].K, gs[i].nibbles);
     for (int i = 0; i < count; ++i) {
         int found = -1;
         for (int j = 0; j < int(jobs.size()); ++j)
@@ -514,9 +674,9 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
             J.x = gs[i].x;
             J.K = int(gs[i].K);
             J.xf = reinterpret_cast<uint16_t*>(wsb + off);
-            off = align_up(off + xf_bytes(mc0, gs[i].K), 256);
+            off = align_up(off + xf_bytes(M, gs[i].K), 256);
             J.xun = reinterpret_cast<float*>(wsb + off);
-            off = align_up(off + kGemmMaxRowsPerPass * sizeof(float), 256);
+            off = align_up(off + kBsMaxNpad * sizeof(float), 256);
             found = int(jobs.size());
             jobs.push_back(J);
         }
@@ -525,12 +685,15 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
     int* sched = reinterpret_cast<int*>(wsb + off);  // one claim counter per launch of a pass
     const int nlaunch = (count + kGroupMax - 1) / kGroupMax;
     std::vector<HostGemm> hs(count);
-    // rows are processed 64 at a time; each pass converts its rows of every
-    // distinct X, then streams every weight matrix once
-    for (int64_t m0 = 0; m0 < M; m0 += kGemmMaxRowsPerPass) {
-        const int mc = int(std::min<int64_t>(kGemmMaxRowsPerPass, M - m0));
+    // rows are processed up to 128 (block-scaled kernel) or 64 at a time; each
+    // pass converts its rows of every distinct X, then streams every weight
+    // matrix once
+    for (int64_t m0 = 0, mcl = 0; m0 < M; m0 += mcl) {
+        const bool bs = use_bs(M - m0, bs_ok);
+        mcl = std::min<int64_t>(bs ? kBsMaxNpad : kGemmMaxRowsPerPass, M - m0);
+        const int mc = int(mcl);
         const int NT = tiles_nt(mc);
-        const bool umma = use_umma(mc, 0, true);
+        const bool umma = !bs && use_umma(mc, 0, true);
         for (size_t j0 = 0; j0 < jobs.size(); j0 += kPrepMaxJobs) {
             PrepSet Q{};
             Q.njobs = int(std::min<size_t>(kPrepMaxJobs, jobs.size() - j0));
@@ -541,6 +704,7 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
             Q.M = mc;
             Q.NT = NT;
             Q.umma_npad = umma ? umma_npad(mc) : 0;
+            Q.bs_npad = bs ? bs_npad(mc) : 0;
             if (j0 == 0) {
                 Q.counters = sched;
                 Q.ncounters = nlaunch;
@@ -566,14 +730,15 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
         for (int l = 0; l < nlaunch; ++l) {
             const int b = int(int64_t(count) * l / nlaunch);
             const int e = int(int64_t(count) * (l + 1) / nlaunch);
-            int* claim = umma ? nullptr : sched_or_null(sched + l);
+            int* claim = (umma || bs) ? nullptr : sched_or_null(sched + l);
             // claimed in table order: longest items (largest K) first
             if (claim)
                 std::stable_sort(hs.begin() + b, hs.begin() + e,
                                  [](const HostGemm& u, const HostGemm& v) { return u.K > v.K; });
             cudaError_t err =
-                umma ? launch_umma_np<kGroupMax>(umma_npad(mc), hs.data() + b, e - b, mc, dev_status, stream)
-                     : launch_main_nt<kGroupMax>(NT, hs.data() + b, e - b, mc, dev_status, claim, stream);
+                bs     ? launch_bs_np<kGroupMax>(hs.data() + b, e - b, mc, dev_status, stream)
+                : umma ? launch_umma_np<kGroupMax>(umma_npad(mc), hs.data() + b, e - b, mc, dev_status, stream)
+                       : launch_main_nt<kGroupMax>(NT, hs.data() + b, e - b, mc, dev_status, claim, stream);
             if (err != cudaSuccess) return err;
         }
     }

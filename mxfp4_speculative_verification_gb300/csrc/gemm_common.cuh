@@ -37,6 +37,8 @@ struct ProblemSet {
     int32_t* status;
     int* sched;  // item claim counter, zeroed before the launch (null: static round robin)
     int nstatic; // items each CTA takes in round-robin order before it claims
+    int ring;    // block-scaled kernel: stage slots
+    int pf_stages;  // block-scaled kernel: L2 prefetch distance of the weights, in stages
 };
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,

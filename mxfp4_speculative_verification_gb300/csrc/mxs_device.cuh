@@ -74,6 +74,36 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
     }
 }
 
+// The same wait, letting the hardware suspend the thread (up to `hint_ns`
+// per try) until the phase completes, so that a warp waiting a long time
+// takes no issue slots from the warps it shares a scheduler with.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, int32_t* status,
+                                                uint32_t hint_ns = 20000u) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, hint_ns)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            report(status, MXS_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // ------------------------------------------------------------ bulk copies
 // 1-D TMA copy global -> shared, completion counted on an mbarrier.
 // dst, src 16-byte aligned; bytes a multiple of 16.

@@ -15,10 +15,10 @@ spec.loader.exec_module(bench)
 def test_gemm_passes_split_rows_and_pick_kernels():
     assert bench.gemm_passes(5) == [(5, "mma")]
     assert bench.gemm_passes(24) == [(24, "mma")]
-    assert bench.gemm_passes(25) == [(25, "umma")]
-    assert bench.gemm_passes(64) == [(64, "umma")]
-    assert bench.gemm_passes(80) == [(64, "umma"), (16, "mma")]
-    assert bench.gemm_passes(320) == [(64, "umma")] * 5
+    assert bench.gemm_passes(25) == [(25, "bs")]
+    assert bench.gemm_passes(64) == [(64, "bs")]
+    assert bench.gemm_passes(80) == [(64, "bs"), (16, "mma")]
+    assert bench.gemm_passes(320) == [(64, "bs")] * 5
     assert sum(r for r, _ in bench.gemm_passes(1000)) == 1000
 
 
