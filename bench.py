@@ -97,15 +97,15 @@ def load_peaks():
 
 
 def in_process_peaks(mxs, torch, dev, nbytes: int = 2 << 30, reps: int = 5):
-    """HBM figures measured in this process: a device copy (read + write
-    bytes) and the library's read-only probe, each over buffers far larger
+    """HBM figures measured in this process: the library's device copy kernel
+    (read + write bytes) and its read-only probe, each over buffers far larger
     than L2.  Reported beside the MEASURED_PEAKS.json denominator."""
     src = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
     src.fill_(1.0)
     dst = torch.empty_like(src)
     sink = torch.zeros(4096, dtype=torch.int64, device=dev)
     out = {}
-    for name, fn, moved in (("copy_gbs", lambda: dst.copy_(src), 2 * nbytes),
+    for name, fn, moved in (("copy_gbs", lambda: mxs.hbm_copy_probe(dst, src), 2 * nbytes),
                             ("read_gbs", lambda: mxs.hbm_read_probe(src, sink), nbytes)):
         for _ in range(2):
             fn()

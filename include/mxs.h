@@ -256,6 +256,14 @@ mxs_status spec_accept(const float* p, const float* q, const int32_t* draft,
 mxs_status mxs_hbm_read_probe(const void* src, size_t bytes, uint64_t* sink,
                               void* stream);
 
+/* ------------------------------------------------------------------------
+ * mxs_hbm_copy_probe -- measurement helper (not part of the method): copies
+ * `bytes` (multiple of 16) from `src` to `dst` (device, 16-byte aligned, not
+ * overlapping).  Used for the read + write HBM roofline that the verify
+ * GEMM's bandwidth is reported against.
+ * ---------------------------------------------------------------------- */
+mxs_status mxs_hbm_copy_probe(void* dst, const void* src, size_t bytes, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* mxs_status_string(mxs_status status);
 

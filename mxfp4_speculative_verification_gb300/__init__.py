@@ -24,7 +24,9 @@ from . import _build
 
 __all__ = ["build", "lib", "mxfp4_pack", "mxfp4_verify_gemm", "mxfp4_verify_gemm_workspace_size",
            "mxfp4_verify_gemm_grouped", "mxfp4_verify_gemm_grouped_workspace_size",
-           "spec_accept", "hbm_read_probe", "MxsError", "DEV_FLAGS", "declared_symbols"]
+           "mxfp4_verify_gemm_noalloc", "spec_accept", "hbm_read_probe", "hbm_copy_probe", "MxsError",
+           "DEV_FLAGS",
+           "declared_symbols"]
 
 MXS_F32, MXS_BF16 = 0, 1
 DEV_FLAGS = {
@@ -75,6 +77,8 @@ def lib():
     L.spec_accept.restype = i32
     L.mxs_hbm_read_probe.argtypes = [vp, sz, vp, vp]
     L.mxs_hbm_read_probe.restype = i32
+    L.mxs_hbm_copy_probe.argtypes = [vp, vp, sz, vp]
+    L.mxs_hbm_copy_probe.restype = i32
     L.mxs_status_string.argtypes = [i32]
     L.mxs_status_string.restype = ctypes.c_char_p
     L.mxs_version.argtypes = []
@@ -121,6 +125,12 @@ def mxfp4_pack(w: torch.Tensor, *, nibbles: torch.Tensor | None = None,
         dt = MXS_BF16
     else:
         raise MxsError("w must be float32 or bfloat16")
+    if K % 32 != 0:
+        raise MxsError("K must be a multiple of 32")
+    for name, t, shape in (("nibbles", nibbles, (N, K // 2)), ("scales", scales, (N, K // 32))):
+        if t is not None and (t.dtype != torch.uint8 or tuple(t.shape) != shape):
+            raise MxsError(f"{name} must be a uint8 tensor of shape {list(shape)}")
+    _check_status(dev_status)
     if nibbles is None:
         nibbles = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
     if scales is None:
@@ -148,18 +158,35 @@ def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
     return ws
 
 
+def _gemm_shapes(x: torch.Tensor, nibbles: torch.Tensor, scales: torch.Tensor,
+                 out: torch.Tensor | None, dev_status: torch.Tensor | None):
+    """Check the GEMM operands (the C side cannot see buffer extents); returns (M, N, K)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise MxsError("x must be a 2-D bfloat16 tensor [M, K]")
+    if nibbles.dtype != torch.uint8 or scales.dtype != torch.uint8 or nibbles.dim() != 2:
+        raise MxsError("nibbles and scales must be 2-D uint8 tensors")
+    M, K = x.shape
+    N = nibbles.shape[0]
+    if K % 32 != 0 or nibbles.shape != (N, K // 2) or scales.shape != (N, K // 32):
+        raise MxsError("W shapes must be [N, K/2] and [N, K/32] with K % 32 == 0")
+    if out is not None and (out.dtype != torch.float32 or tuple(out.shape) != (M, N)):
+        raise MxsError("out must be a float32 tensor [M, N]")
+    _check_status(dev_status)
+    return M, N, K
+
+
+def _check_status(dev_status: torch.Tensor | None) -> None:
+    if dev_status is not None and (dev_status.dtype != torch.int32 or dev_status.numel() < 1):
+        raise MxsError("dev_status must be an int32 tensor of at least one element")
+
+
 def mxfp4_verify_gemm(x: torch.Tensor, nibbles: torch.Tensor, scales: torch.Tensor, *,
                       out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                       dev_status: torch.Tensor | None = None) -> torch.Tensor:
     """Y[M, N] (fp32) = X[M, K] (bf16) . dequant(W)^T for MXFP4 W ([N, K/2] + [N, K/32])."""
-    if x.dtype != torch.bfloat16 or x.dim() != 2:
-        raise MxsError("x must be a 2-D bfloat16 tensor [M, K]")
-    if nibbles.dtype != torch.uint8 or scales.dtype != torch.uint8:
-        raise MxsError("nibbles and scales must be uint8")
-    M, K = x.shape
-    N = nibbles.shape[0]
-    if nibbles.shape != (N, K // 2) or scales.shape != (N, K // 32):
-        raise MxsError("W shapes must be [N, K/2] and [N, K/32]")
+    M, N, K = _gemm_shapes(x, nibbles, scales, out, dev_status)
+    if workspace is not None and workspace.dtype != torch.uint8:
+        raise MxsError("workspace must be a uint8 tensor")
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=x.device)
     dev = _need_cuda(x, nibbles, scales, out, workspace, dev_status)
@@ -235,10 +262,17 @@ def spec_accept(p: torch.Tensor, q: torch.Tensor, draft: torch.Tensor, u: torch.
         raise MxsError("p, q and u must be float32")
     if draft.dtype != torch.int32:
         raise MxsError("draft must be int32")
+    if p.dim() != 3:
+        raise MxsError("p must be 3-D [B, K+1, V]")
     B, K1, V = p.shape
     K = K1 - 1
     if q.shape != (B, K, V) or draft.shape != (B, K) or u.shape != (B, K + 1):
         raise MxsError("shape mismatch: p [B,K+1,V], q [B,K,V], draft [B,K], u [B,K+1]")
+    for name, t, shape in (("out_tokens", out_tokens, (B, K + 1)), ("n_emitted", n_emitted, (B,)),
+                           ("row_flags", row_flags, (B,))):
+        if t is not None and (t.dtype != torch.int32 or tuple(t.shape) != shape):
+            raise MxsError(f"{name} must be an int32 tensor of shape {list(shape)}")
+    _check_status(dev_status)
     if out_tokens is None:
         out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=p.device)
     if n_emitted is None:
@@ -256,6 +290,15 @@ def hbm_read_probe(src: torch.Tensor, sink: torch.Tensor) -> None:
                                     _ptr(sink), _stream(dev)))
 
 
+def hbm_copy_probe(dst: torch.Tensor, src: torch.Tensor) -> None:
+    """Copy ``src`` into ``dst`` with the library's copy kernel (read + write HBM roofline)."""
+    nbytes = src.numel() * src.element_size() // 16 * 16
+    if dst.numel() * dst.element_size() < nbytes:
+        raise MxsError("dst is smaller than src")
+    dev = _need_cuda(dst, src)
+    _check(lib().mxs_hbm_copy_probe(_ptr(dst), _ptr(src), nbytes, _stream(dev)))
+
+
 # ------------------------------------------------------- no-allocation GEMM
 def mxfp4_verify_gemm_noalloc(x: torch.Tensor, nibbles: torch.Tensor, scales: torch.Tensor, *,
                               out: torch.Tensor | None = None,
@@ -265,14 +308,13 @@ def mxfp4_verify_gemm_noalloc(x: torch.Tensor, nibbles: torch.Tensor, scales: to
     allocation).  The library's fixed 16 MiB device scratch is used instead;
     calls must not overlap on the GPU.  ``out`` should be preallocated by such
     callers (it is allocated here only when omitted)."""
+    M, N, K = _gemm_shapes(x, nibbles, scales, out, dev_status)
     L = lib()
     fn = L.mxfp4_verify_gemm_noalloc
     if fn.restype is not ctypes.c_int32:
         vp, i64 = ctypes.c_void_p, ctypes.c_int64
         fn.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp]
         fn.restype = ctypes.c_int32
-    M, K = x.shape
-    N = nibbles.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=x.device)
     dev = _need_cuda(x, nibbles, scales, out, dev_status)

@@ -124,6 +124,15 @@ mxs_status mxs_hbm_read_probe(const void* src, size_t bytes, uint64_t* sink, voi
     return cuda_status(mxs::hbm_read_probe_run(src, bytes, sink, as_stream(stream)));
 }
 
+mxs_status mxs_hbm_copy_probe(void* dst, const void* src, size_t bytes, void* stream) {
+    if (!dst || !src || bytes == 0 || bytes % 16 != 0) return MXS_ERR_INVALID_ARG;
+    if (!aligned(src, 16) || !aligned(dst, 16)) return MXS_ERR_MISALIGNED;
+    const char* d = static_cast<const char*>(dst);
+    const char* sp = static_cast<const char*>(src);
+    if (d < sp + bytes && sp < d + bytes) return MXS_ERR_INVALID_ARG;  // overlapping buffers
+    return cuda_status(mxs::hbm_copy_probe_run(dst, src, bytes, as_stream(stream)));
+}
+
 const char* mxs_status_string(mxs_status status) {
     switch (status) {
         case MXS_OK: return "MXS_OK";

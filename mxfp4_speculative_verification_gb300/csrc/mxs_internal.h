@@ -60,5 +60,6 @@ cudaError_t pack_run(const void* w, int w_dtype, int64_t N, int64_t K, uint8_t* 
 // --------------------------------------------------------------- probe
 cudaError_t hbm_read_probe_run(const void* src, size_t bytes, uint64_t* sink,
                                cudaStream_t stream);
+cudaError_t hbm_copy_probe_run(void* dst, const void* src, size_t bytes, cudaStream_t stream);
 
 }  // namespace mxs

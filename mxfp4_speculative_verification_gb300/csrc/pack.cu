@@ -125,4 +125,31 @@ cudaError_t hbm_read_probe_run(const void* src, size_t bytes, uint64_t* sink,
     return cudaGetLastError();
 }
 
+// Device copy dst <- src, 16 bytes per access, four accesses in flight per
+// thread and streaming cache hints: the HBM read + write roofline the GEMM is
+// measured against.
+__global__ void __launch_bounds__(512) hbm_copy_probe_kernel(uint4* __restrict__ dst,
+                                                             const uint4* __restrict__ src, size_t n16) {
+    const size_t stride = size_t(gridDim.x) * blockDim.x;
+    size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        const uint4 a = __ldcs(src + i), b = __ldcs(src + i + stride);
+        const uint4 c = __ldcs(src + i + 2 * stride), d = __ldcs(src + i + 3 * stride);
+        __stcs(dst + i, a);
+        __stcs(dst + i + stride, b);
+        __stcs(dst + i + 2 * stride, c);
+        __stcs(dst + i + 3 * stride, d);
+    }
+    for (; i < n16; i += stride) __stcs(dst + i, __ldcs(src + i));
+}
+
+cudaError_t hbm_copy_probe_run(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    hbm_copy_probe_kernel<<<unsigned(sms * 4), 512, 0, stream>>>(static_cast<uint4*>(dst),
+                                                                  static_cast<const uint4*>(src), bytes / 16);
+    return cudaGetLastError();
+}
+
 }  // namespace mxs

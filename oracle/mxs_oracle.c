@@ -27,7 +27,7 @@
  *          Integration": packed nibbles laid out [rows, K/2], scales
  *          [rows, K/32], fp32 accumulation.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - E8M0 value is 2^(e-127); code 255 is NaN.
  *   - element k of a row is in byte k/2, even k in the low nibble.
  *   - the acceptance test u*q(x) < p(x) is evaluated exactly (the product of

@@ -107,3 +107,18 @@ def test_grouped_workspace_layout(L):
     assert size(1) == 16 * 4096 * 2 + 256 + 256
     assert size(1) == size(84) == size(85) == size(4096)
     assert size(1, K=14336) == 16 * 14336 * 2 + 256 + 256
+
+
+def test_hbm_probes_reject_bad_arguments_on_host(L):
+    import ctypes
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    L.mxs_hbm_copy_probe.argtypes = [vp, vp, sz, vp]
+    L.mxs_hbm_read_probe.argtypes = [vp, sz, vp, vp]
+    copy, read = L.mxs_hbm_copy_probe, L.mxs_hbm_read_probe
+    assert copy(FAKE, FAKE + (1 << 20), 0, None) == 1          # no bytes
+    assert copy(FAKE, FAKE + (1 << 20), 1000, None) == 1       # not a multiple of 16
+    assert copy(None, FAKE, 4096, None) == 1
+    assert copy(FAKE + 8, FAKE + (1 << 20), 4096, None) == 2   # misaligned destination
+    assert copy(FAKE, FAKE + 2048, 4096, None) == 1            # overlapping buffers
+    assert read(FAKE, 0, FAKE, None) == 1
+    assert read(FAKE + 4, 4096, FAKE, None) == 2
