@@ -267,6 +267,10 @@ static cudaError_t build_problems(ProblemSet<G>& S, const HostGemm* gs, int coun
     S.M = M;
     S.status = status;
     S.sched = sched;
+    // bounded waits: the limit, and (tests only) a stage CTA 0 leaves out
+    const long long wl = std::atoll(std::getenv("MXS_GEMM_WAIT_LIMIT_NS") ? std::getenv("MXS_GEMM_WAIT_LIMIT_NS") : "0");
+    S.wait_ns = wl > 0 ? (unsigned long long)wl : kWaitLimitNs;
+    S.skip_stage = env_int("MXS_GEMM_TEST_SKIP_STAGE", -1);
     int64_t items = 0;
     const int forced = env_int("MXS_GEMM_SPLITS", 0);
     for (int i = 0; i < count; ++i) {

@@ -38,6 +38,10 @@ struct ProblemSet {
     int* sched;  // item claim counter, zeroed before the launch (null: static round robin)
     int nstatic; // items each CTA takes in round-robin order before it claims
     int ring;    // block-scaled kernel: stage slots
+    // mma.sync kernel, tests of the bounded waits only: the wait limit (ns),
+    // and a stage that CTA 0's producer leaves out entirely (-1: none)
+    unsigned long long wait_ns;
+    int skip_stage;
     int pf_stages;  // block-scaled kernel: L2 prefetch distance of the weights, in stages
 };
 
