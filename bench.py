@@ -50,10 +50,10 @@ FALLBACK_HBM_GBS = 6800.0
 # is reported as null otherwise (ratio None: not yet captured on the current
 # sources).
 GEMM_TRAFFIC = {
-    # mxfp4_gemm_kernel, passes of <= 24 rows
-    "mma": {"ratio": None, "sha": None},
-    # mxfp4_gemm_bs_kernel, passes of 25..64 rows
-    "bs": {"ratio": None, "sha": None},
+    # mxfp4_gemm_kernel, passes of <= 24 rows: lm_head 4096 x 128256 at M=5
+    "mma": {"ratio": 1.0049, "sha": "8dfd894e5619908b"},
+    # mxfp4_gemm_bs_kernel, passes of 25..64 rows: lm_head 4096 x 128256 at M=64
+    "bs": {"ratio": 1.0243, "sha": "9b2ad6d90c7c3a0a"},
 }
 BS_MIN_ROWS = 25    # passes of at least this many rows run on the block-scaled kernel
 GROUP_MAX = 84      # GEMMs per grouped launch at most (the problem table is a kernel parameter)
@@ -226,6 +226,18 @@ def src_sha(kind: str, root: str = ROOT) -> str:
     return h.hexdigest()[:16]
 
 
+ACCEPT_LOGIT_STD = 3.0   # target logits N(0, 3) as in the acceptance-heavy configuration
+ACCEPT_OVERLAP = 0.86    # mean per-token acceptance the pages report for code and math prompts
+_SIGMA = {}
+
+
+def draft_sigma() -> float:
+    """Draft-logit noise giving a mean overlap sum_t min(p_t, q_t) of ACCEPT_OVERLAP."""
+    if "s" not in _SIGMA:
+        _SIGMA["s"] = workloads.tune_draft_noise(ACCEPT_OVERLAP, 4096, ACCEPT_LOGIT_STD, seed=0, samples=8)
+    return _SIGMA["s"]
+
+
 def compute_desc(kinds) -> str:
     """What the step computes in, for the kernels its passes use."""
     parts = []
@@ -237,6 +249,20 @@ def compute_desc(kinds) -> str:
                      "tensor core (exact for bf16 X within 2^16 of its block maximum), fp32 accumulation")
     parts.append("acceptance predicate exact (f64), sampling CDF in float-float above fp32 128-element sums")
     return "; ".join(parts)
+
+
+def pass_traffic(shapes, passes, n_main):
+    """DRAM bytes per grouped launch implied by the captured traffic ratios:
+    every pass streams the whole W again plus its own X and Y rows, so a
+    step of several passes moves more than its algorithmic bytes.  None when
+    a kernel's ratio was not captured on its current sources."""
+    total = 0.0
+    for rows, kind in passes:
+        t = GEMM_TRAFFIC[kind]
+        if t["ratio"] is None or t["sha"] != src_sha(kind):
+            return None
+        total += t["ratio"] * sum(gemm_bytes(rows, N, K) for _, K, N in shapes)
+    return total / n_main
 
 
 def gemm_passes(M: int):
@@ -371,7 +397,11 @@ def run_mxs(args, world, rank, local):
     problems = [(x_dev[K], nib, sc, y) for (_, K, _), (nib, sc), y in zip(shapes, weights, ys)]
     gws = torch.empty(mxs.mxfp4_verify_gemm_grouped_workspace_size(problems), dtype=torch.uint8,
                       device=dev)
-    p, q, d, u = workloads.spec_inputs(B, K_spec, V, seed=rank, logit_std=2.0)
+    # acceptance inputs as in the pages' workloads: draft law = target law with
+    # noise tuned to a mean per-token overlap of 0.86, drafts drawn from it
+    sigma = draft_sigma()
+    p, q, d, u = workloads.spec_inputs(B, K_spec, V, seed=rank, logit_std=ACCEPT_LOGIT_STD, draft_noise=sigma)
+    alpha = float(np.minimum(p[:, :K_spec, :].astype(np.float64), q.astype(np.float64)).sum(axis=-1).mean())
     acc_host = [torch.from_numpy(a).pin_memory() for a in (p, q, d, u)]
     acc_dev = [a.to(dev) for a in acc_host]
     out_tok = torch.empty((B, K_spec + 1), dtype=torch.int32, device=dev)
@@ -476,14 +506,32 @@ def run_mxs(args, world, rank, local):
     kinds = sorted({k for _, k in passes})
     kernel_name = {"mma": "mxfp4_gemm_kernel (mma.sync)",
                    "bs": "mxfp4_gemm_bs_kernel (tcgen05 kind::mxf8f6f4 block-scaled)"}
-    traffic = None
-    if len(kinds) == 1:
-        t = GEMM_TRAFFIC[kinds[0]]
-        if t["ratio"] is not None and t["sha"] == src_sha(kinds[0]):
-            traffic = t["ratio"] * gemm_b / n_main
+    traffic = pass_traffic(shapes, passes, n_main)
 
     if args.detail and rank == 0:
         per_shape_detail(mxs, torch, stream, dev, shapes, weights, x_dev, ws, M)
+
+    # the other configurations, each timed the same way (weights of the same
+    # stack reused; the 70B stack generated once on the device)
+    sweep, acc_sweep = [], None
+    if not args.no_sweep and rank == 0 and world == 1:
+        wcache = {model: weights}
+        clocks2 = ClockSampler(local)
+        clocks2.start()
+        for wl in SWEEP_WORKLOADS:
+            if wl == args.workload:
+                continue
+            m2, b2, k2 = WORKLOADS[wl]
+            if m2 not in wcache:
+                wcache[m2] = [workloads.device_mxfp4_weights(N, K, lo, hi, seed=i, device=dev)
+                              for i, (_, K, N) in enumerate(workloads.stack_shapes(m2))]
+            sweep.append(sweep_point(mxs, torch, dev, stream, wl, wcache[m2], args, peak_for_sweep()))
+        clk2 = clocks2.stop()
+        for rec in sweep:
+            rec["clocks"] = clk2
+        del wcache
+        torch.cuda.empty_cache()
+        acc_sweep = accept_sweep_rows(mxs, torch, dev, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -519,6 +567,10 @@ def run_mxs(args, world, rank, local):
                              "CUDA graph with programmatic dependent launch"},
         "spec_accept": {"rows_per_s": B / (ms_acc * 1e-3), "us_per_call": ms_acc * 1e3,
                         "bytes_per_call": acc_b, "mean_emitted": float(np.mean(n_emitted)),
+                        "mean_overlap": alpha,
+                        "closed_form_emitted": (1.0 - alpha ** (K_spec + 1)) / (1.0 - alpha),
+                        "inputs": f"target logits N(0,{ACCEPT_LOGIT_STD:g}), draft = target + N(0,{sigma:.3f}) "
+                                  f"(mean overlap {ACCEPT_OVERLAP}), drafts drawn from the draft law",
                         "pct_of_peak": acc_b / (ms_acc * 1e-3) / 1e9 / peak},
         "e2e": {"value": job_tbps(world, step_b, e2e_s), "unit": "TB/s",
                 "ms_per_step": e2e_s * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -527,10 +579,93 @@ def run_mxs(args, world, rank, local):
         "clocks": clk,
         "cpu_baseline": cpu,
         "peaks_in_process": inproc,
+        "sweep": sweep,
+        "accept_sweep": acc_sweep,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+# The configurations reported beside the headline (each a sub-record of the
+# same JSON line): the 8B batch sweep and the 70B stack at three batch sizes.
+SWEEP_WORKLOADS = ("llama8b_b4", "llama8b_b16", "llama8b_b64", "llama70b_b1", "llama70b_b4", "llama70b")
+
+
+def peak_for_sweep() -> float:
+    return load_peaks()[0]
+
+
+def sweep_point(mxs, torch, dev, stream, wl, weights, args, peak):
+    """One configuration: its grouped GEMM step and its acceptance call, each
+    captured in a CUDA graph and timed with CUDA events after warm-up."""
+    model, B, K_spec = WORKLOADS[wl]
+    M = B * (K_spec + 1)
+    V = workloads.VOCAB_LLAMA
+    shapes = workloads.stack_shapes(model)
+    ks = sorted({K for _, K, _ in shapes})
+    x_dev = {K: workloads.device_bf16_normal(M, K, seed=K, device=dev) for K in ks}
+    ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _, _, N in shapes]
+    problems = [(x_dev[K], nib, sc, y) for (_, K, _), (nib, sc), y in zip(shapes, weights, ys)]
+    gws = torch.empty(mxs.mxfp4_verify_gemm_grouped_workspace_size(problems), dtype=torch.uint8, device=dev)
+    p, q, d, u = workloads.spec_inputs(B, K_spec, V, seed=1, logit_std=ACCEPT_LOGIT_STD, draft_noise=draft_sigma())
+    acc = [torch.from_numpy(a).to(dev) for a in (p, q, d, u)]
+    out_tok = torch.empty((B, K_spec + 1), dtype=torch.int32, device=dev)
+    n_emit = torch.empty((B,), dtype=torch.int32, device=dev)
+    reps = 10
+    with torch.cuda.stream(stream):
+        mxs.mxfp4_verify_gemm_grouped(problems, workspace=gws)
+        mxs.spec_accept(*acc, out_tokens=out_tok, n_emitted=n_emit)
+        torch.cuda.synchronize(dev)
+        n_emitted = n_emit.cpu().numpy()
+        g_gemm, g_acc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_gemm, stream=stream):
+            mxs.mxfp4_verify_gemm_grouped(problems, workspace=gws)
+        with torch.cuda.graph(g_acc, stream=stream):
+            for _ in range(reps):
+                mxs.spec_accept(*acc, out_tokens=out_tok, n_emitted=n_emit)
+    torch.cuda.synchronize(dev)
+
+    def timed(graph, steps):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                graph.replay()
+            torch.cuda.synchronize(dev)
+            ev0.record(stream)
+            for _ in range(steps):
+                graph.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        return ev0.elapsed_time(ev1) / steps
+
+    steps = max(3, min(args.steps, 10))
+    ms_gemm = timed(g_gemm, steps)
+    ms_acc = timed(g_acc, steps) / reps
+    gemm_b = sum(gemm_bytes(M, N, K) for _, K, N in shapes)
+    acc_b = accept_bytes(B, K_spec, V, n_emitted)
+    passes = gemm_passes(M)
+    n_main = len(passes) * ((len(shapes) + GROUP_MAX - 1) // GROUP_MAX)
+    gbs = gemm_b / (ms_gemm * 1e-3) / 1e9
+    flops = sum(2 * M * N * K for _, K, N in shapes)
+    alpha = float(np.minimum(p[:, :K_spec, :].astype(np.float64), q.astype(np.float64)).sum(axis=-1).mean())
+    kinds = sorted({k for _, k in passes})
+    traffic = pass_traffic(shapes, passes, n_main)
+    del x_dev, ys, problems, gws, acc
+    return {
+        "workload": config_block(wl, model, B, K_spec)["workload"], "M": M,
+        "ms_per_step": ms_gemm + ms_acc, "value": (gemm_b + acc_b) / ((ms_gemm + ms_acc) * 1e-3) / 1e12,
+        "unit": "TB/s", "steps": steps,
+        "passes": [f"{r} rows: {k}" for r, k in passes],
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "bytes_per_launch": gemm_b / n_main, "launches_per_step": n_main,
+                     "avg_launch_us": ms_gemm * 1e3 / n_main, "traffic": traffic,
+                     "useful_tflops": flops / (ms_gemm * 1e-3) / 1e12},
+        "spec_accept": {"B": B, "us_per_call": ms_acc * 1e3, "rows_per_s": B / (ms_acc * 1e-3),
+                        "mean_emitted": float(np.mean(n_emitted)), "mean_overlap": alpha,
+                        "closed_form_emitted": (1.0 - alpha ** (K_spec + 1)) / (1.0 - alpha),
+                        "pct_of_peak": acc_b / (ms_acc * 1e-3) / 1e9 / peak},
+    }
 
 
 def per_shape_detail(mxs, torch, stream, dev, shapes, weights, x_dev, ws, M):
@@ -569,7 +704,7 @@ def profile_target(args):
     mxs.build()
     dev = torch.device("cuda:0")
     model, B, K_spec = WORKLOADS[args.workload]
-    M = B * (K_spec + 1)
+    M = args.profile_m or B * (K_spec + 1)
     if args.profile_gemm:
         K, N = (int(v) for v in args.profile_gemm.split(","))
         nib, sc = workloads.device_mxfp4_weights(N, K, *workloads.LLAMA_EXP_RANGE, seed=0, device=dev)
@@ -579,29 +714,24 @@ def profile_target(args):
             mxs.mxfp4_verify_gemm(x, nib, sc, out=y)
     else:
         V = workloads.VOCAB_LLAMA
-        p, q, d, u = (torch.from_numpy(a).to(dev) for a in workloads.spec_inputs(B, K_spec, V, seed=0))
+        p, q, d, u = (torch.from_numpy(a).to(dev) for a in workloads.spec_inputs(
+            B, K_spec, V, seed=0, logit_std=ACCEPT_LOGIT_STD, draft_noise=draft_sigma()))
         for _ in range(4):
             mxs.spec_accept(p, q, d, u)
     torch.cuda.synchronize()
 
 
-def accept_sweep(args):
+def accept_sweep_rows(mxs, torch, dev, peak, max_rounds=1500):
     """Acceptance-heavy sweep: B=64, K in {1,3,7}, V=128256, target logits N(0,3),
     draft logits = target + N(0, sigma) with sigma bisected so that the mean
     overlap sum_t min(p_t, q_t) is about 0.86.  p and q are drawn once per K;
-    drafts and uniforms are redrawn every round until the standard error of the
-    mean emitted count is below 0.01.  Reports the mean against the closed form
-    (1 - a^(K+1)) / (1 - a) at the mean overlap a, and against the exact tail
-    sum over each row's own overlaps, E_b = sum_k prod_{i<k} a_{b,i}."""
-    import torch
-
-    import mxfp4_speculative_verification_gb300 as mxs
-
-    mxs.build()
-    dev = torch.device("cuda:0")
-    B, V, std = 64, workloads.VOCAB_LLAMA, 3.0
-    peak, peak_kind = load_peaks()
-    sigma = workloads.tune_draft_noise(0.86, 4096, std, seed=0, samples=8)
+    drafts (sampled from q on the device) and uniforms are redrawn every round
+    until the standard error of the mean emitted count is below 0.01.  Reports
+    the mean against the closed form (1 - a^(K+1)) / (1 - a) at the mean overlap
+    a, and against the exact tail sum over each row's own overlaps,
+    E_b = sum_k prod_{i<k} a_{b,i}."""
+    B, V, std = 64, workloads.VOCAB_LLAMA, ACCEPT_LOGIT_STD
+    sigma = draft_sigma()
     rows = []
     for K in (1, 3, 7):
         p, q, _, _ = workloads.spec_inputs(B, K, V, seed=100 + K, logit_std=std, draft_noise=sigma)
@@ -609,42 +739,36 @@ def accept_sweep(args):
         tail = np.concatenate([np.ones((B, 1)), np.cumprod(alpha, axis=1)], axis=1).sum(axis=1)
         a_mean = float(alpha.mean())
         closed = (1.0 - a_mean ** (K + 1)) / (1.0 - a_mean)
-        cdf = np.cumsum(q.astype(np.float64), axis=-1)
         p_d, q_d = torch.from_numpy(p).to(dev), torch.from_numpy(q).to(dev)
+        q_rows = q_d.view(B * K, V)
         out_tok = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
         n_emit = torch.empty((B,), dtype=torch.int32, device=dev)
-        rng = workloads.host_rng(200 + K, 0)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(200 + K)
         counts = []
         rounds = 0
         while True:
             rounds += 1
-            uni = rng.random((B, K))
-            d = np.empty((B, K), dtype=np.int32)
-            for b in range(B):
-                for i in range(K):
-                    c = cdf[b, i]
-                    d[b, i] = min(int(np.searchsorted(c, uni[b, i] * c[-1], side="right")), V - 1)
-            u = rng.random((B, K + 1), dtype=np.float32)
-            mxs.spec_accept(p_d, q_d, torch.from_numpy(d).to(dev), torch.from_numpy(u).to(dev),
-                            out_tokens=out_tok, n_emitted=n_emit)
-            counts.append(n_emit.cpu().numpy().astype(np.float64))
-            allc = np.concatenate(counts)
-            se = float(allc.std(ddof=1) / np.sqrt(allc.size))
-            if (se < 0.01 and rounds >= 4) or rounds >= 1500:
-                break
-        # timing on the last round's inputs (one call, CUDA events, after warm-up)
+            d_d = torch.multinomial(q_rows, 1, generator=gen).view(B, K).to(torch.int32)
+            u_d = torch.rand((B, K + 1), generator=gen, device=dev, dtype=torch.float32)
+            mxs.spec_accept(p_d, q_d, d_d, u_d, out_tokens=out_tok, n_emitted=n_emit)
+            counts.append(n_emit.to(torch.float64))
+            if rounds >= 4 and (rounds % 16 == 0 or rounds >= max_rounds):
+                allc = torch.cat(counts).cpu().numpy()
+                se = float(allc.std(ddof=1) / np.sqrt(allc.size))
+                if se < 0.01 or rounds >= max_rounds:
+                    break
+        # timing on the last round's inputs (CUDA events, after warm-up)
         for _ in range(5):
-            mxs.spec_accept(p_d, q_d, torch.from_numpy(d).to(dev), torch.from_numpy(u).to(dev),
-                            out_tokens=out_tok, n_emitted=n_emit)
-        d_d, u_d = torch.from_numpy(d).to(dev), torch.from_numpy(u).to(dev)
-        torch.cuda.synchronize()
+            mxs.spec_accept(p_d, q_d, d_d, u_d, out_tokens=out_tok, n_emitted=n_emit)
+        torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         reps = 50
         e0.record()
         for _ in range(reps):
             mxs.spec_accept(p_d, q_d, d_d, u_d, out_tokens=out_tok, n_emitted=n_emit)
         e1.record()
-        torch.cuda.synchronize()
+        torch.cuda.synchronize(dev)
         us = e0.elapsed_time(e1) * 1e3 / reps
         nb = accept_bytes(B, K, V, n_emit.cpu().numpy())
         rows.append({"K": K, "rows": int(allc.size), "rounds": rounds,
@@ -654,10 +778,25 @@ def accept_sweep(args):
                      "z_vs_tail_sum": float((allc.mean() - tail.mean()) / se),
                      "us_per_call": us, "rows_per_s": B / (us * 1e-6),
                      "hbm_gbs": nb / (us * 1e-6) / 1e9, "pct_of_peak": nb / (us * 1e-6) / 1e9 / peak})
-    print(json.dumps({"metric": "spec_accept acceptance-heavy sweep (mean emitted tokens per step)",
-                      "B": B, "V": V, "logit_std": std, "draft_noise_sigma": sigma,
-                      "peak_gbs": peak, "peak_source": f"{peak_kind} hbm_gbs", "data": "synthetic",
-                      "rows": rows}), flush=True)
+        del p_d, q_d, q_rows
+    return {"metric": "spec_accept acceptance-heavy sweep (mean emitted tokens per step)",
+            "B": B, "V": V, "logit_std": std, "draft_noise_sigma": sigma,
+            "drafts": "sampled from q on the device (torch.multinomial), uniforms torch.rand",
+            "rows": rows}
+
+
+def accept_sweep(args):
+    """The acceptance-heavy sweep alone, as its own JSON line."""
+    import torch
+
+    import mxfp4_speculative_verification_gb300 as mxs
+
+    mxs.build()
+    dev = torch.device("cuda:0")
+    peak, peak_kind = load_peaks()
+    rec = accept_sweep_rows(mxs, torch, dev, peak)
+    rec.update({"peak_gbs": peak, "peak_source": f"{peak_kind} hbm_gbs", "data": "synthetic"})
+    print(json.dumps(rec), flush=True)
 
 
 def main():
@@ -670,9 +809,13 @@ def main():
     ap.add_argument("--detail", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the sub-records of the other configurations (8B batch sweep, 70B stack)")
     ap.add_argument("--profile-gemm", metavar="K,N",
                     help="only run one verify GEMM of this shape (M from --workload) 4 times "
                          "and exit; a small target for ncu captures")
+    ap.add_argument("--profile-m", type=int, default=0,
+                    help="rows of the --profile-gemm call (default: the workload's M)")
     ap.add_argument("--profile-accept", action="store_true",
                     help="only run spec_accept of the workload 4 times and exit (ncu target)")
     ap.add_argument("--accept-sweep", action="store_true",
