@@ -51,11 +51,14 @@ FALLBACK_HBM_GBS = 6800.0
 # sources).
 GEMM_TRAFFIC = {
     # mxfp4_gemm_kernel, passes of <= 24 rows: lm_head 4096 x 128256 at M=5
-    "mma": {"ratio": 1.0049, "sha": "8dfd894e5619908b"},
-    # mxfp4_gemm_bs_kernel, passes of 25..64 rows: lm_head 4096 x 128256 at M=64
-    "bs": {"ratio": 1.0243, "sha": "9b2ad6d90c7c3a0a"},
+    "mma": {"ratio": None, "sha": None},
+    # mxfp4_gemm_bs_kernel, kind::mxf8f6f4 (passes of 33..64 rows)
+    "bs8": {"ratio": None, "sha": None},
+    # mxfp4_gemm_bs_kernel, kind::mxf4 (passes of 9..32 rows)
+    "bs4": {"ratio": None, "sha": None},
 }
-BS_MIN_ROWS = 25    # passes of at least this many rows run on the block-scaled kernel
+BS_MIN_ROWS = 9     # passes of at least this many rows run on the block-scaled kernel
+BS4_MAX_ROWS = 32   # its mxf4 kind takes passes of up to this many rows
 GROUP_MAX = 84      # GEMMs per grouped launch at most (the problem table is a kernel parameter)
 
 WORKLOADS = {
@@ -214,7 +217,8 @@ def code_only(src: str) -> str:
 # gemm.cu and the preparation kernel, a launch of its own, are not part of it).
 KERNEL_SOURCES = {
     "mma": ("mxs_device.cuh", "gemm_common.cuh", "gemm_mma.cuh"),
-    "bs": ("mxs_device.cuh", "gemm_common.cuh", "gemm_bs.cuh"),
+    "bs8": ("mxs_device.cuh", "gemm_common.cuh", "gemm_bs.cuh"),
+    "bs4": ("mxs_device.cuh", "gemm_common.cuh", "gemm_bs.cuh"),
 }
 
 
@@ -244,9 +248,13 @@ def compute_desc(kinds) -> str:
     if "mma" in kinds:
         parts.append("E2M1 weights decoded exactly to fp16, X rows power-of-two scaled to fp16, "
                      "fp16 tensor-core products, fp32 accumulation")
-    if "bs" in kinds:
+    if "bs8" in kinds:
         parts.append("E2M1 weights x X as two E4M3 terms with UE8M0 block factors on the block-scaled "
-                     "tensor core (exact for bf16 X within 2^16 of its block maximum), fp32 accumulation")
+                     "tensor core (kind::mxf8f6f4; exact for bf16 X within 2^16 of its block maximum), "
+                     "fp32 accumulation")
+    if "bs4" in kinds:
+        parts.append("E2M1 weights x X as six E2M1 terms with UE8M0 block factors on the block-scaled "
+                     "tensor core (kind::mxf4; X to within max|x|/4^6 of each 32-block), fp32 accumulation")
     parts.append("acceptance predicate exact (f64), sampling CDF in float-float above fp32 128-element sums")
     return "; ".join(parts)
 
@@ -266,9 +274,21 @@ def pass_traffic(shapes, passes, n_main):
 
 
 def gemm_passes(M: int):
-    """Row passes of the grouped GEMM (64 rows at most each) and the kernel of each."""
-    rows = [min(64, M - m0) for m0 in range(0, M, 64)]
-    return [(r, "bs" if r >= BS_MIN_ROWS else "mma") for r in rows]
+    """Row passes of the grouped GEMM and the kernel of each, as the library
+    plans them for K % 128 == 0: fewer than BS_MIN_ROWS rows left go to
+    mma.sync, up to BS4_MAX_ROWS to the mxf4 kind, else 64 rows at a time to
+    the mxf8f6f4 kind."""
+    passes, m0 = [], 0
+    while m0 < M:
+        left = M - m0
+        if left < BS_MIN_ROWS:
+            passes.append((min(64, left), "mma"))
+        elif left <= BS4_MAX_ROWS:
+            passes.append((left, "bs4"))
+        else:
+            passes.append((min(64, left), "bs8"))
+        m0 += passes[-1][0]
+    return passes
 
 
 # ----------------------------------------------------------------------------
@@ -505,7 +525,8 @@ def run_mxs(args, world, rank, local):
     n_prep = len(passes) * ((len(ks) + 15) // 16)      # one X preparation per pass
     kinds = sorted({k for _, k in passes})
     kernel_name = {"mma": "mxfp4_gemm_kernel (mma.sync)",
-                   "bs": "mxfp4_gemm_bs_kernel (tcgen05 kind::mxf8f6f4 block-scaled)"}
+                   "bs8": "mxfp4_gemm_bs_kernel (tcgen05 kind::mxf8f6f4 block-scaled)",
+                   "bs4": "mxfp4_gemm_bs_kernel (tcgen05 kind::mxf4 block-scaled)"}
     traffic = pass_traffic(shapes, passes, n_main)
 
     if args.detail and rank == 0:

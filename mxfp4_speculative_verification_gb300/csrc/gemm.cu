@@ -56,16 +56,15 @@
 namespace mxs {
 
 constexpr int kMaxDevices = 64;
-constexpr int kBsSmemAttr = 232448;             // dynamic shared memory the block-scaled kernel may ask for
 constexpr int kMaxSplit = 32;
 constexpr int64_t kMaxSplitItems = 2048;         // bound on tiles x splits when K is split
 constexpr int64_t kBsMaxSplitItems = 304;        // the same for the block-scaled kernel (2 per SM)
 
 #include "gemm_common.cuh"
 #include "gemm_mma.cuh"
-#include "gemm_prep.cuh"
 #include "gemm_umma.cuh"
 #include "gemm_bs.cuh"
+#include "gemm_prep.cuh"
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -96,15 +95,19 @@ static int64_t bs_split_items_cap(int64_t N, int64_t K) {
     return ns > 1 ? ntiles * ns : 0;
 }
 
-static bool use_bs(int64_t rows_left, bool eligible);
+static int bs_kind_for(int64_t rows_left, int64_t K, const void* nib);
 
-// Whether a call of M rows may run a block-scaled pass (sizes its workspace).
-static bool bs_may_run(int64_t M, int64_t K) { return use_bs(M, K % 128 == 0); }
+// Whether a call of M rows may run a block-scaled pass (sizes its workspace;
+// the nibbles' alignment is not known yet, so assume the best).
+static bool bs_may_run(int64_t M, int64_t K) { return bs_kind_for(M, K, nullptr) >= 0; }
 
-// Bytes of X prepared for the block-scaled kernel (passes of at most mc rows).
+// Bytes of X prepared for the block-scaled kernel (passes of at most mc
+// rows, either kind).
 static size_t bs_x_bytes(int64_t mc, int64_t K) {
-    const int npad = bs_npad(int(std::min<int64_t>(mc, kBsMaxNpad)));
-    return size_t((K + 255) / 256) * size_t(bs_bstage_bytes(npad) + bs_sfbstage_bytes(npad));
+    const int m = int(std::min<int64_t>(mc, kBsMaxNpad));
+    const int per_stage = std::max(bs_bstage_bytes(0, bs_npad(0, m)),
+                                   bs_bstage_bytes(1, bs_npad(1, std::min(m, kBsF4MaxRows))));
+    return size_t((K + 255) / 256) * size_t(per_stage);
 }
 
 GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales_aligned) {
@@ -257,11 +260,12 @@ struct HostGemm {
 };
 
 // Fill the launch's problem table for tiles of BN rows.
-// bs: the block-scaled kernel (256-k stages, scales read in place).
+// bs: the block-scaled kernel (256-k stages, scales read in place), 1 for
+// its mxf8f6f4 kind (padded E2M1 boxes), 2 for its mxf4 kind (packed boxes).
 template <int G>
 static cudaError_t build_problems(ProblemSet<G>& S, const HostGemm* gs, int count, int M,
                                   int32_t* status, int BN, int64_t resident, int* sched,
-                                  bool bs = false) {
+                                  int bs = 0) {
     std::memset(&S, 0, sizeof(S));
     S.count = count;
     S.M = M;
@@ -308,9 +312,13 @@ static cudaError_t build_problems(ProblemSet<G>& S, const HostGemm* gs, int coun
         items += int64_t(p.ntiles) * p.nsplit;
         if (items > INT32_MAX) return cudaErrorInvalidValue;
         if (bs) {
-            // both 128-k chunks of a stage per request, and one chunk for the last of an odd count
-            if (!make_map_e2m1_spread(&p.tm_w, h.nib, h.N, h.K, 2) ||
-                !make_map_e2m1_spread(&p.tm_s, h.nib, h.N, h.K, 1))
+            // weights: both 128-k chunks of a stage per request (padded E2M1 for
+            // mxf8f6f4), or the packed bytes of the stage (mxf4); scales: 16
+            // blocks x 128 rows per request (the rows are 16-byte aligned:
+            // K % 512 == 0 in place, else realigned in the workspace)
+            const bool wmap = bs == 1 ? make_map_e2m1_spread(&p.tm_w, h.nib, h.N, h.K, 2)
+                                      : make_map(&p.tm_w, h.nib, h.N, h.K / 2, h.K / 2, kBoxBytes, uint32_t(kBsRows), true);
+            if (!wmap || !make_map(&p.tm_s, h.sc, h.N, p.nblk, h.sc_pitch, 16, uint32_t(kBsRows), false))
                 return cudaErrorInvalidValue;
             continue;
         }
@@ -443,60 +451,77 @@ static cudaError_t launch_umma_np(int npad, const HostGemm* gs, int count, int M
 
 // Stage slots of the block-scaled kernel for a pass of npad rows;
 // MXS_GEMM_BS_RINGS=c overrides it when c slots fit shared and tensor memory.
-static int bs_ring_for(int npad) {
+static int bs_ring_for(int kind, int npad) {
     const int c = env_int("MXS_GEMM_BS_RINGS", 0);
-    if (c >= 2 && c <= kBsMaxRing && bs_smem_bytes(npad, c) <= kBsSmemAttr && bs_tmem_need(npad, c) <= int(kBsTmemCols))
+    if (c >= 2 && c <= kBsMaxRing && bs_smem_bytes(kind, npad, c) <= kBsSmemAttr &&
+        bs_tmem_need(kind, npad, c) <= int(kBsTmemCols))
         return c;
-    return bs_ring(npad);
+    return bs_ring(kind, npad);
 }
 
 // Block-scaled kernel: one CTA per SM, 128-row tiles, K split only for a
 // single GEMM whose tiles leave SMs idle.
-template <int G>
-static cudaError_t launch_bs_np(const HostGemm* gs, int count, int M, int32_t* status,
-                                cudaStream_t stream) {
-    auto kern = mxfp4_gemm_bs_kernel<G>;
+template <int G, int KIND>
+static cudaError_t launch_bs(const HostGemm* gs, int count, int M, int32_t* status, cudaStream_t stream) {
+    auto kern = mxfp4_gemm_bs_kernel<G, KIND>;
     static LaunchFacts facts;
     int sms = 0, occ = 0;
     cudaError_t err = launch_facts(facts, kern, kBsThreads, kBsSmemAttr, sms, occ);
     if (err != cudaSuccess) return err;
     static thread_local ProblemSet<G>* S_buf = nullptr;
     if (!S_buf) S_buf = new ProblemSet<G>;
-    err = build_problems(*S_buf, gs, count, M, status, kBsRows, int64_t(sms), nullptr, true);
+    err = build_problems(*S_buf, gs, count, M, status, kBsRows, int64_t(sms), nullptr, KIND == 0 ? 1 : 2);
     if (err != cudaSuccess) return err;
-    const int npad = bs_npad(M);
-    S_buf->ring = bs_ring_for(npad);
-    S_buf->pf_stages = std::max(0, std::min(64, env_int("MXS_GEMM_BS_PF", kBsPfStages)));
+    const int npad = bs_npad(KIND, M);
+    S_buf->ring = bs_ring_for(KIND, npad);
     const int64_t grid = std::min<int64_t>(S_buf->items, int64_t(sms));
-    return launch_persistent(kern, *S_buf, kBsThreads, bs_smem_bytes(npad, S_buf->ring), grid, stream);
+    return launch_persistent(kern, *S_buf, kBsThreads, bs_smem_bytes(KIND, npad, S_buf->ring), grid, stream);
+}
+
+template <int G>
+static cudaError_t launch_bs_kind(int kind, const HostGemm* gs, int count, int M, int32_t* status,
+                                  cudaStream_t stream) {
+    return kind ? launch_bs<G, 1>(gs, count, M, status, stream) : launch_bs<G, 0>(gs, count, M, status, stream);
 }
 
 // Every pass size the block-scaled kernel takes fits its shared and tensor memory.
 static constexpr bool bs_shapes_fit() {
-    for (int m = 1; m <= kBsMaxNpad; ++m) {
-        const int npad = bs_npad(m);
-        const int rc = bs_ring(npad);
-        if (bs_smem_bytes(npad, rc) > kBsSmemAttr || bs_tmem_need(npad, rc) > int(kBsTmemCols) || rc > kBsMaxRing)
-            return false;
-    }
+    for (int kind = 0; kind < 2; ++kind)
+        for (int m = 1; m <= (kind ? kBsF4MaxRows : kBsMaxNpad); ++m) {
+            const int npad = bs_npad(kind, m);
+            const int rc = bs_ring(kind, npad);
+            if (bs_smem_bytes(kind, npad, rc) > kBsSmemAttr || bs_tmem_need(kind, npad, rc) > int(kBsTmemCols) ||
+                rc > kBsMaxRing || rc < 3 || bs_slot_bytes(kind, npad) % 1024 != 0)
+                return false;
+        }
     return true;
 }
 static_assert(bs_shapes_fit(), "block-scaled kernel: a pass size exceeds shared or tensor memory");
 
-// The block-scaled kernel takes every pass of at least MXS_GEMM_BS_MIN rows
-// (default 25: below that mma.sync streams faster, measured on the lm_head
-// shape) whenever the weights allow it: K % 128 == 0 and 32-byte aligned
-// nibbles (the packed TMA type's rules).  MXS_GEMM_PATH=bs forces it for
-// every pass it can take.
-static bool bs_eligible(int64_t K, const void* nib) {
-    return K % 128 == 0 && (reinterpret_cast<uintptr_t>(nib) & 31) == 0;
-}
-static bool use_bs(int64_t rows_left, bool eligible) {
-    if (!eligible) return false;
+// The kind of block-scaled pass that takes the next rows (rows_left of
+// them), or -1 for the mma.sync / tcgen05 f16 kernels.  Passes of at least
+// MXS_GEMM_BS_MIN rows (default 9) go to the block-scaled kernel: up to 32
+// rows the mxf4 kind (any K, 16-byte aligned nibbles), beyond that
+// mxf8f6f4, which needs K % 128 == 0 and 32-byte aligned nibbles (the padded
+// TMA type's rules) and otherwise leaves the pass to the older kernels.
+// MXS_GEMM_PATH=bs8 or bs4 forces one kind for every pass it can take
+// (bs4: 32 rows at most per pass), bs the default choice at any row count,
+// mma or umma the older kernels.
+static int bs_kind_for(int64_t rows_left, int64_t K, const void* nib) {
+    const bool f8_ok = K % 128 == 0 && (reinterpret_cast<uintptr_t>(nib) & 31) == 0;
+    const bool f4_ok = K % 32 == 0 && (reinterpret_cast<uintptr_t>(nib) & 15) == 0;
     const char* path = std::getenv("MXS_GEMM_PATH");
-    if (path && std::strcmp(path, "bs") == 0) return true;
-    if (path && (std::strcmp(path, "mma") == 0 || std::strcmp(path, "umma") == 0)) return false;
-    return rows_left >= env_int("MXS_GEMM_BS_MIN", 25);
+    if (path && std::strcmp(path, "bs8") == 0) return f8_ok ? 0 : -1;
+    if (path && std::strcmp(path, "bs4") == 0) return f4_ok ? 1 : -1;
+    if (path && (std::strcmp(path, "mma") == 0 || std::strcmp(path, "umma") == 0)) return -1;
+    const bool forced = path && std::strcmp(path, "bs") == 0;
+    if (!forced && rows_left < env_int("MXS_GEMM_BS_MIN", 9)) return -1;
+    if (rows_left <= kBsF4MaxRows) return f4_ok ? 1 : (f8_ok ? 0 : -1);
+    return f8_ok ? 0 : -1;
+}
+// Rows of a block-scaled pass of the given kind.
+static int64_t bs_pass_rows(int kind, int64_t rows_left) {
+    return std::min<int64_t>(kind ? kBsF4MaxRows : kBsMaxNpad, rows_left);
 }
 
 // Which kernel a pass of mc rows uses.  mma.sync (legacy tensor path) is
@@ -524,7 +549,9 @@ static cudaError_t launch_prep(const PrepSet& Q, cudaStream_t stream) {
     cudaLaunchConfig_t cfg{};
     const int rows = Q.bs_npad > 0 ? Q.bs_npad : (Q.umma_npad > 0 ? Q.umma_npad : 8 * Q.NT);
     cfg.gridDim = dim3(unsigned(Q.njobs * rows + 1 + Q.repack_ctas), 1, 1);
-    cfg.blockDim = dim3(kPrepThreads, 1, 1);
+    // block-scaled passes: 256 threads, so that a preparation CTA and a CTA of
+    // the main kernel (launched early through PDL) fit one SM together
+    cfg.blockDim = dim3(Q.bs_npad > 0 ? kPrepThreadsBs : kPrepThreads, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -545,12 +572,18 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
     uint8_t* sc_aligned = ws.repack_scales ? wsb + ws.sc_off : nullptr;
     const int nblk = int(K / 32);
     const int64_t mc0 = std::min<int64_t>(M, kGemmMaxRowsPerPass);
-    const bool bs_ok = bs_eligible(K, nibbles);
     bool scales_realigned = false;
     for (int64_t m0 = 0, mc = 0; m0 < M; m0 += mc) {
-        if (use_bs(M - m0, bs_ok)) {
-            // block-scaled pass of up to 128 rows: raw scales, its own X layout
-            mc = std::min<int64_t>(kBsMaxNpad, M - m0);
+        const int kind = bs_kind_for(M - m0, K, nibbles);
+        // the scales are realigned once, by the first pass that reads them;
+        // every pass that streams the realigned copy waits for the preparation
+        // kernel before its first scale request (its completion implies that
+        // of every earlier kernel of the call)
+        const bool repack = ws.repack_scales && !scales_realigned;
+        scales_realigned = true;
+        if (kind >= 0) {
+            // block-scaled pass: its own X layout
+            mc = bs_pass_rows(kind, M - m0);
             PrepSet Q{};
             Q.job[0].x = x + m0 * K;
             Q.job[0].xf = xf;
@@ -559,15 +592,25 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
             Q.njobs = 1;
             Q.M = int(mc);
             Q.NT = 1;
-            Q.bs_npad = bs_npad(int(mc));
+            Q.bs_npad = bs_npad(kind, int(mc));
+            Q.bs_kind = kind;
             Q.counters = counters;
             Q.ncounters = ws.n_counters;
+            if (repack) {
+                Q.sc_in = scales;
+                Q.N = N;
+                Q.nblk = nblk;
+                Q.sc_pitch = ws.sc_pitch;
+                Q.sc_out = sc_aligned;
+                Q.repack_ctas = int(std::min<int64_t>((N * ws.sc_pitch + kPrepThreadsBs - 1) / kPrepThreadsBs, 1024));
+            }
             cudaError_t err = launch_prep(Q, stream);
             if (err != cudaSuccess) return err;
             HostGemm h{};
             h.nib = nibbles;
-            h.sc = scales;
-            h.sc_pitch = nblk;
+            h.sc = ws.repack_scales ? sc_aligned : scales;
+            h.sc_pitch = ws.repack_scales ? ws.sc_pitch : nblk;
+            h.sc_from_prep = ws.repack_scales;
             h.xf = xf;
             h.xun = xun;
             h.y = y + m0 * N;
@@ -577,7 +620,7 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
             h.K = K;
             const int64_t cap = bs_split_items_cap(N, K);
             h.items_cap = (cap > 0 && ws.n_counters >= 4 * ((N + kBsRows - 1) / kBsRows)) ? cap : 0;
-            err = launch_bs_np<1>(&h, 1, int(mc), dev_status, stream);
+            err = launch_bs_kind<1>(kind, &h, 1, int(mc), dev_status, stream);
             if (err != cudaSuccess) return err;
             continue;
         }
@@ -588,9 +631,6 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
         int64_t items_cap = split_items_cap(N, K, bn);
         if (ws.n_counters < (N + bn - 1) / bn || mc > mc0) items_cap = 0;
         const bool umma = use_umma(int(mc), (N + kUBN - 1) / kUBN, false);
-        // the scales are realigned once, by the first pass that reads them
-        const bool repack = ws.repack_scales && !scales_realigned;
-        scales_realigned = true;
         PrepSet Q{};
         Q.job[0].x = x + m0 * K;
         Q.job[0].xf = xf;
@@ -616,7 +656,7 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
         h.nib = nibbles;
         h.sc = ws.repack_scales ? sc_aligned : scales;
         h.sc_pitch = ws.sc_pitch;
-        h.sc_from_prep = repack;
+        h.sc_from_prep = ws.repack_scales;
         h.xf = xf;
         h.xun = xun;
         h.y = y + m0 * N;
@@ -667,8 +707,6 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
     std::vector<int> xid(count);
     std::vector<PrepJob> jobs;
     size_t off = 0;
-    bool bs_ok = true;
-    for (int i = 0; i < count; ++i) bs_ok = bs_ok && bs_eligible(gs[i].K, gs[i].nibbles);
     for (int i = 0; i < count; ++i) {
         int found = -1;
         for (int j = 0; j < int(jobs.size()); ++j)
@@ -693,8 +731,12 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
     // pass converts its rows of every distinct X, then streams every weight
     // matrix once
     for (int64_t m0 = 0, mcl = 0; m0 < M; m0 += mcl) {
-        const bool bs = use_bs(M - m0, bs_ok);
-        mcl = std::min<int64_t>(bs ? kBsMaxNpad : kGemmMaxRowsPerPass, M - m0);
+        // one kind for every GEMM of the pass, or none if they would differ
+        int kind = count > 0 ? bs_kind_for(M - m0, gs[0].K, gs[0].nibbles) : -1;
+        for (int i = 1; i < count && kind >= 0; ++i)
+            if (bs_kind_for(M - m0, gs[i].K, gs[i].nibbles) != kind) kind = -1;
+        const bool bs = kind >= 0;
+        mcl = bs ? bs_pass_rows(kind, M - m0) : std::min<int64_t>(kGemmMaxRowsPerPass, M - m0);
         const int mc = int(mcl);
         const int NT = tiles_nt(mc);
         const bool umma = !bs && use_umma(mc, 0, true);
@@ -708,7 +750,8 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
             Q.M = mc;
             Q.NT = NT;
             Q.umma_npad = umma ? umma_npad(mc) : 0;
-            Q.bs_npad = bs ? bs_npad(mc) : 0;
+            Q.bs_npad = bs ? bs_npad(kind, mc) : 0;
+            Q.bs_kind = bs ? kind : 0;
             if (j0 == 0) {
                 Q.counters = sched;
                 Q.ncounters = nlaunch;
@@ -740,7 +783,7 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
                 std::stable_sort(hs.begin() + b, hs.begin() + e,
                                  [](const HostGemm& u, const HostGemm& v) { return u.K > v.K; });
             cudaError_t err =
-                bs     ? launch_bs_np<kGroupMax>(hs.data() + b, e - b, mc, dev_status, stream)
+                bs     ? launch_bs_kind<kGroupMax>(kind, hs.data() + b, e - b, mc, dev_status, stream)
                 : umma ? launch_umma_np<kGroupMax>(umma_npad(mc), hs.data() + b, e - b, mc, dev_status, stream)
                        : launch_main_nt<kGroupMax>(NT, hs.data() + b, e - b, mc, dev_status, claim, stream);
             if (err != cudaSuccess) return err;

@@ -1,89 +1,122 @@
 // Block-scaled verify GEMM on sm_103a tensor cores, included by gemm.cu.
 //
-// tcgen05.mma.kind::mxf8f6f4.block_scale multiplies E2M1 weights by E4M3
-// activations, each 32-k block scaled by one UE8M0 factor per weight row
-// (A) and per activation row (B), and accumulates in fp32 in tensor memory.
-// That is the MX-FP4 product of "Module 11. Speculative Decoding and
-// Quantization" §12 (E2M1 elements, one power-of-two scale per 32-element
-// block) done by the tensor core itself: no weight is ever decoded.
-//   * A = 128 weight rows x 256 k per stage.  The MMA reads E2M1 codes from
-//     a padded shared-memory layout (each 16 codes = 8 bytes, then 8 unused
-//     bytes); TMA writes that layout from the packed bytes in HBM (the
-//     16U4_ALIGN16B type).  Each request of that type covers 64 bytes of a
-//     row, and one 2-D box per 128 k capped a whole GPU near 3 TB/s (measured),
-//     so one 3-D box carries both 128-k chunks of a stage: 5.3 TB/s for the
-//     stream alone.  The A scale factors are the weight's own E8M0 bytes,
-//     unchanged.
-//   * B = X as two E4M3 terms: x = t1 * 2^e1 + t2 * 2^e2 per 32-k block,
-//     e1 set by the block's largest |x| and e2 by the largest residual
-//     (the preparation kernel).  Every bf16 value whose block maximum is
-//     within 2^16 of it is represented exactly, the rest to 16 bits.  The
-//     terms are stacked as B rows (row m = t1 of X row m, row Npad + m = t2),
-//     so one MMA of N = 2 Npad per 32-k block reads A from shared memory
-//     once, and Y[m] = D[m] + D[Npad + m].
-//   * D = 128 x 2 Npad fp32 in tensor memory, double buffered across tiles.
+// tcgen05.mma with .block_scale multiplies E2M1 weights by a low-precision
+// image of X, each 32-k block scaled by one UE8M0 factor per weight row (A)
+// and per X term row (B), and accumulates in fp32 in tensor memory.  That is
+// the MX-FP4 product of "Module 11. Speculative Decoding and Quantization"
+// §12 (E2M1 elements, one power-of-two scale per 32-element block) done by
+// the tensor core itself: no weight is ever decoded.  Two kinds:
+//   * kind::mxf8f6f4 (KIND 0, passes of 33..64 rows): B = X as two E4M3
+//     terms per 32-k block, x = t1 * 2^e1 + t2 * 2^e2, exact for every bf16
+//     element within 2^16 of its block maximum.  The MMA reads E2M1 codes
+//     from a padded shared-memory layout (16 codes = 8 bytes, then 8 unused
+//     bytes), which TMA writes from the packed bytes (the 16U4_ALIGN16B
+//     type): 32 KB of shared memory per 16 KB of weights.
+//   * kind::mxf4 (KIND 1, passes of up to 32 rows): A = the packed E2M1
+//     bytes as they are (16 KB per 16 KB, plain 128-byte-swizzled TMA boxes),
+//     B = X as six E2M1 terms per 32-k block, each with its own UE8M0 scale
+//     (the largest residual maps into (3, 6]).  Six terms carry X to about
+//     1e-7 of its block maximum on normal data; the bound for any block is
+//     the residual after six terms, at most max|x| / 4^6.
+//   The terms are stacked as B rows (row t * Npad + m = term t of X row m),
+//   so one MMA of N = T * Npad reads A from shared memory once, and
+//   Y[m] = sum over t of D[t * Npad + m].  Shared memory per stage is what
+//   bounds the bytes in flight, hence the mxf4 kind where its six terms fit.
 //
-// Scale factors in tensor memory (pinned on this GPU by a one-CTA probe of
-// every placement against a host reference): the MMA reads row m's A factor
-// at lane m, column base + m / 32, byte 0 (factor id 0), and B column n's
-// factor at lane 32 * (m / 32) + n % 32 of the sub-partition computing row m,
-// column base + n / 32.  Each 32-k block gets a group of 4 columns (factor
-// addresses stay 4-column aligned): lane m holds its A factor in all 4, and
-// every lane quadrant holds the same copy of B's factors, column base + c
-// for B columns n = lane + 32 c.  Every tcgen05.st starts at a column that
-// is a multiple of its width.
+// Scale factors (pinned on this GPU by one-CTA probes against a host double
+// reference): one 32-bit tensor-memory cell holds the factors of four
+// consecutive 32-k blocks (byte j = block 4g + j); the MMA's factor id picks
+// the byte (mxf8f6f4: one block per MMA) or the byte pair (mxf4,
+// scale_vec::2X: two blocks per MMA).  A's factor of weight row m is read at
+// lane m, column base + m / 32, and B column n's at lane 32 q + n % 32 of
+// every lane quadrant q, column base + n / 32.  The scale-factor warps write
+// both with tcgen05.st, each into its own lane quadrant: the weight scales
+// from a TMA box that comes with the weights (16 bytes x 128 rows), X's
+// cells from the stage's prepared X (laid out for them by the preparation
+// kernel).
 //
-// Warps: 0 = weight producer (one 3-D TMA box per stage), 1 = MMA issuer
-// (and tensor-memory owner), 2..5 = scale-factor warps (one per lane
-// quadrant: write both operands' factors into tensor memory, flag NaN
-// scales), 6..9 = epilogue warps (tensor memory -> Y, or a split-K partial
-// tile and its reduction), 10 = X producer (bulk copies of the prepared X
-// terms).  A stage slot holds a stage's weights, X terms and (in tensor
-// memory) factors; its full barrier completes when both copies have landed
-// and the factors are written, so the MMA warp waits once and commits once
-// per stage (each wait and commit of that single issuing thread costs the
-// tensor pipe idle time).
+// What bounds a stage (measured with per-stage clocks on this GPU): the one
+// MMA-issuing thread spends ~70-90 cycles per tcgen05 instruction, and a
+// stage of 16 KB of weights must take no more than ~750 cycles to keep pace
+// with HBM, so that thread issues only the stage's MMAs and one commit: the
+// factors reach tensor memory through the scale-factor warps instead of
+// tcgen05.cp, and its loop runs on one lane.  Loading the weight scales
+// with per-thread 8-byte loads cost ~40 % of the stream (as many memory
+// requests as the weights themselves); the TMA box costs ~10 %.
+//
+// Warps: 0 = weight producer (per 256-k stage one TMA box of weights and
+// one of their scales), 1 = MMA issuer (and tensor-memory owner), 2..5 =
+// scale-factor warps (one per lane quadrant: factors into tensor memory,
+// flag NaN scales), 6..9 = epilogue warps (tensor memory -> Y, or a split-K
+// partial tile and its reduction), 10 = X producer (one bulk copy of the
+// stage's prepared X and its factors).  A stage slot's full barrier
+// completes when both copies have landed; its factor barrier when the four
+// scale-factor warps have written the factors (which they do after the full
+// barrier), so the MMA thread waits on the factor barrier alone.
 
 constexpr int kBsRows = 128;                 // weight rows per tile (MMA M)
 constexpr int kBsStageBlocks = 8;            // 32-k blocks per stage (256 k)
-constexpr int kBsAChunk = kBsRows * 128;     // one 128-k chunk of A in the padded layout
-constexpr int kBsAStage = 2 * kBsAChunk;     // padded A of one stage (32 KB)
-constexpr int kBsATx = kBsRows * 128;        // its packed global bytes (the transaction count)
+constexpr int kBsAChunk = kBsRows * 128;     // mxf8f6f4: one 128-k chunk of padded A
+constexpr int kBsATx = kBsRows * 128;        // packed global bytes of a stage's A
 constexpr int kBsMaxNpad = 64;               // X rows per pass at most
+constexpr int kBsF4Terms = 6;                // E2M1 terms of X (mxf4 kind)
 constexpr int kBsFirstEpi = 6;
 constexpr int kBsXWarp = 10;
 constexpr int kBsThreads = 32 * 11;
 constexpr uint32_t kBsTmemCols = 512;
 constexpr int kBsMaxRing = 8;
-constexpr int kBsPfStages = 10;              // L2 prefetch distance of the weights (MXS_GEMM_BS_PF)
+constexpr int kBsScBytes = kBsRows * 16;     // TMA box of weight scales: 16 blocks x 128 rows
+constexpr int kBsCopyBytes = 512;            // one group x 128 columns of X's factor cells
+constexpr int kBsF4MaxRows = 32;             // the mxf4 kind takes passes of at most this many rows
 
-// X rows a pass pads to: 32 or 64 (MMA N = 64 or 128, the widths this
-// kernel's block-scaled MMA has been validated at on this GPU).
-__host__ __device__ constexpr int bs_npad(int m) { return m <= 32 ? 32 : 64; }
-// Prepared X, per 256-k stage: B rows [2 chunks of 128 k][2 Npad rows][128 B]
-// (K-major, 16-byte units swizzled by row % 8; rows 0..Npad-1 = t1, then
-// t2); after all stages, their scale bytes [stage][2 Npad][8 blocks].
-__host__ __device__ constexpr int bs_bstage_bytes(int npad) { return 512 * npad; }
-__host__ __device__ constexpr int bs_sfbstage_bytes(int npad) { return 16 * npad; }
-// One stage slot: padded A, then B.
-__host__ __device__ constexpr int bs_slot_bytes(int npad) { return kBsAStage + bs_bstage_bytes(npad); }
-// Tensor-memory columns: D buffer 0 at column 0 (2 Npad wide), then one
-// factor slot of 64 columns per stage slot (A: 8 blocks x 4, B: 8 blocks x 4),
-// then D buffer 1 at a multiple of 2 Npad (a power of two).
-constexpr int kBsSfCols = 64;
-constexpr int kBsSfbCol = 32;  // B's factors within a slot
-__host__ __device__ constexpr int bs_sf0(int npad) { return 2 * npad; }
-__host__ __device__ constexpr int bs_d1(int npad, int ring) {
-    return (bs_sf0(npad) + ring * kBsSfCols + 2 * npad - 1) / (2 * npad) * (2 * npad);
+// X rows a pass pads to (multiples of 16 keep every term row group's swizzle
+// and tensor-memory columns aligned).
+__host__ __device__ constexpr int bs_npad(int kind, int m) {
+    return kind ? (m <= 16 ? 16 : 32) : (m <= 32 ? 32 : 64);
 }
-__host__ __device__ constexpr int bs_tmem_need(int npad, int ring) { return bs_d1(npad, ring) + 2 * npad; }
+__host__ __device__ constexpr int bs_terms(int kind) { return kind ? kBsF4Terms : 2; }
+// MMA N: the term rows of B
+__host__ __device__ constexpr int bs_ncols(int kind, int npad) { return bs_terms(kind) * npad; }
+// A of one stage in shared memory (padded for mxf8f6f4)
+__host__ __device__ constexpr int bs_a_bytes(int kind) { return kind ? kBsRows * 128 : 2 * kBsRows * 128; }
+// 128-column parts of B's factor cells per group
+__host__ __device__ constexpr int bs_sfb_copies(int kind, int npad) { return (bs_ncols(kind, npad) + 127) / 128; }
+// Prepared X, per 256-k stage: B rows (K-major, 16-byte units swizzled by
+// row % 8; mxf8f6f4: [2 chunks of 128 k][N rows][128 B], mxf4: [N rows][128 B]),
+// then B's factors: [group g][copy h][32 rows][4 cells], cell c of row l =
+// the 4 factor bytes of B column 128 h + 32 c + l for blocks 4 g .. 4 g + 3.
+__host__ __device__ constexpr int bs_brows_bytes(int kind, int npad) { return bs_ncols(kind, npad) * (kind ? 128 : 256); }
+__host__ __device__ constexpr int bs_sfb_bytes(int kind, int npad) { return 2 * bs_sfb_copies(kind, npad) * kBsCopyBytes; }
+__host__ __device__ constexpr int bs_bstage_bytes(int kind, int npad) {
+    return bs_brows_bytes(kind, npad) + bs_sfb_bytes(kind, npad);
+}
+// One stage slot: A, the stage's prepared X (B rows and factors), the weight scales.
+__host__ __device__ constexpr int bs_slot_bytes(int kind, int npad) {
+    return bs_a_bytes(kind) + bs_bstage_bytes(kind, npad) + kBsScBytes;
+}
+// Tensor-memory columns: D buffer 0 at column 0 (N wide), then one factor
+// slot per stage slot (A: 2 groups x 4 columns, then B: 2 groups x 4 columns
+// per copy), then D buffer 1 at the next multiple of 64.
+__host__ __device__ constexpr int bs_sf_cols(int kind, int npad) { return 8 + 8 * bs_sfb_copies(kind, npad); }
+__host__ __device__ constexpr int bs_sf0(int kind, int npad) { return bs_ncols(kind, npad); }
+__host__ __device__ constexpr int bs_d1(int kind, int npad, int ring) {
+    return (bs_sf0(kind, npad) + ring * bs_sf_cols(kind, npad) + 63) / 64 * 64;
+}
+__host__ __device__ constexpr int bs_tmem_need(int kind, int npad, int ring) {
+    return bs_d1(kind, npad, ring) + bs_ncols(kind, npad);
+}
 // shared memory beyond the ring: barriers, NaN flags, TMEM base, abort flag
 constexpr int kBsMiscBytes = 8 * 64 + 2 * kBsRows + 64;
-__host__ __device__ constexpr int bs_smem_bytes(int npad, int ring) {
-    return ring * bs_slot_bytes(npad) + kBsMiscBytes + 1024;
+__host__ __device__ constexpr int bs_smem_bytes(int kind, int npad, int ring) {
+    return ring * bs_slot_bytes(kind, npad) + kBsMiscBytes + 1024;
 }
-// Stage slots (48 or 64 KB each) that fit.
-__host__ __device__ constexpr int bs_ring(int npad) { return npad <= 32 ? 4 : 3; }
+constexpr int kBsSmemAttr = 232448;  // dynamic shared memory the kernel may ask for
+// Stage slots: as many as shared and tensor memory hold (at most kBsMaxRing).
+__host__ __device__ constexpr int bs_ring(int kind, int npad) {
+    int r = kBsMaxRing;
+    while (r > 2 && (bs_smem_bytes(kind, npad, r) > kBsSmemAttr || bs_tmem_need(kind, npad, r) > int(kBsTmemCols))) --r;
+    return r;
+}
 
 struct BsItem {
     int tile, split, kb0, kb1, nst;
@@ -112,7 +145,6 @@ struct BsCursor {
     int64_t sc_pitch;
     int64_t N;
     const uint8_t* xf;      // its prepared X
-    int nst_all;            // stages of its whole K
     bool w8;                // scale rows readable 8 bytes at a time
     __device__ __forceinline__ void load(const ProblemSet<G>& S) {
         if (w < S.items) {
@@ -123,7 +155,6 @@ struct BsCursor {
             sc_pitch = P.sc_pitch;
             N = P.N;
             xf = reinterpret_cast<const uint8_t*>(P.xf);
-            nst_all = (P.nblk + kBsStageBlocks - 1) / kBsStageBlocks;
             w8 = ((sc_pitch | int64_t(reinterpret_cast<uintptr_t>(sc))) & 7) == 0;
         }
     }
@@ -145,104 +176,45 @@ struct BsCursor {
     __device__ __forceinline__ int nb() const { return min(kBsStageBlocks, R.kb1 - kb()); }
 };
 
-// D[128 x N] (+)= A[128 x 32] * B[N x 32]^T with one UE8M0 factor per row of
-// A and of B for the 32-k block (instruction descriptor `idesc`).
-__device__ __forceinline__ void umma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                              uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-        : "memory");
+// D[128 x N] (+)= A[128 x K] * B[N x K]^T, one factor per row and 32-k block
+// (instruction descriptor `idesc`; K = 32 for mxf8f6f4, 64 for mxf4).
+template <int KIND>
+__device__ __forceinline__ void umma_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    if constexpr (KIND == 0)
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+            " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::"r"(
+                d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+            : "memory");
+    else
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+            " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::"r"(
+                d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+            : "memory");
 }
 
-// Instruction descriptor: A E2M1 (5), B E4M3 (0), UE8M0 factors (bit 23),
-// both K-major, M = 128, N = n, factor ids 0.
-__host__ __device__ constexpr uint32_t bs_idesc(int n) {
-    return (5u << 7) | (0u << 10) | (uint32_t(n >> 3) << 17) | (1u << 23) | (uint32_t(kBsRows >> 4) << 24);
+// Instruction descriptor: M = 128, N = n, both K-major, UE8M0 factors (bit
+// 23); mxf8f6f4: A E2M1 (5), B E4M3 (0); mxf4: A and B E2M1 (1).  The factor
+// ids (A: bits 29-30, B: bits 4-5) are or-ed in per MMA by bs_sfid.
+__host__ __device__ constexpr uint32_t bs_idesc(int kind, int n) {
+    return (kind ? ((1u << 7) | (1u << 10)) : (5u << 7)) | (uint32_t(n >> 3) << 17) | (1u << 23) |
+           (uint32_t(kBsRows >> 4) << 24);
 }
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-        "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
-        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]));
-}
-
-// The 8 scale bytes of blocks kb .. kb+7 at `p` (fewer at the end of K;
-// missing ones read as 0), as two little-endian words.
-__device__ __forceinline__ uint2 bs_load8(const uint8_t* p, int nb, bool w8) {
-    if (nb == kBsStageBlocks && w8) return __ldg(reinterpret_cast<const uint2*>(p));
-    uint32_t lo = 0, hi = 0;
-    for (int j = 0; j < nb; ++j) {
-        const uint32_t b = __ldg(p + j);
-        if (j < 4) lo |= b << (8 * j);
-        else hi |= b << (8 * (j - 4));
-    }
-    return make_uint2(lo, hi);
-}
+__device__ __forceinline__ uint32_t bs_sfid(uint32_t j) { return (j << 29) | (j << 4); }
 
 __device__ __forceinline__ bool has_byte_ff(uint32_t w) { return __vcmpeq4(w, 0xFFFFFFFFu) != 0; }
 
-// The factors one stage-warp thread writes for one stage: its weight row's
-// 8 bytes, and those of B rows lane + 32 c (c = 0..3).
-struct BsFactors {
-    uint2 a;
-    uint2 b[4];
-};
-
-template <int G>
-__device__ __forceinline__ BsFactors bs_load_factors(const ProblemSet<G>& S, const BsCursor<G>& c, int r,
-                                                     int lane, int npad) {
-    BsFactors f;
-    f.a = make_uint2(0u, 0u);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) f.b[j] = make_uint2(0u, 0u);
-    if (!c.valid(S)) return f;
-    const int kb = c.kb(), nb = c.nb();
-    const int64_t n = int64_t(c.R.tile) * kBsRows + r;
-    if (n < c.N) f.a = bs_load8(c.sc + n * c.sc_pitch + kb, nb, c.w8);
-    // X-term scales: after the stages' B rows
-    const uint8_t* sfb = c.xf + int64_t(c.nst_all) * bs_bstage_bytes(npad) +
-                         int64_t(kb / kBsStageBlocks) * bs_sfbstage_bytes(npad);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int row = lane + 32 * j;
-        if (row < 2 * npad) f.b[j] = __ldg(reinterpret_cast<const uint2*>(sfb + row * 8));
-    }
-    return f;
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
 }
 
-// One stage's factors into factor slot `sf` (a TMEM address with this warp's
-// lane quadrant, 32-column aligned): block j of A in columns sf + 4j ..
-// sf + 4j + 3 (this thread's row's byte in all four), block j of B in
-// columns sf + 32 + 4j + c (B column lane + 32 c, the same in every quadrant).
-__device__ __forceinline__ void bs_write_factors(uint32_t sf, const BsFactors& f) {
-    {
-        uint32_t v[32];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t b = ((j < 4 ? f.a.x : f.a.y) >> (8 * (j & 3))) & 0xFFu;
-            v[4 * j] = v[4 * j + 1] = v[4 * j + 2] = v[4 * j + 3] = b;
-        }
-        tmem_st32(sf, v);
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {  // blocks 4h .. 4h + 3
-        uint32_t v[16];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) v[4 * jj + c] = ((h ? f.b[c].y : f.b[c].x) >> (8 * jj)) & 0xFFu;
-        tmem_st16(sf + uint32_t(kBsSfbCol + 16 * h), v);
-    }
-}
-
-template <int G>
+template <int G, int KIND>
 __global__ void __launch_bounds__(kBsThreads, 1)
     mxfp4_gemm_bs_kernel(const __grid_constant__ ProblemSet<G> S) {
     extern __shared__ uint8_t smem_raw[];
@@ -251,18 +223,25 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     uint8_t* smem = smem_raw + pad;
     const uint32_t sbase = raw_base + pad;
     const int M = S.M;
-    const int npad = bs_npad(M);
+    const int npad = bs_npad(KIND, M);
+    const int T = bs_terms(KIND);
+    const int N = bs_ncols(KIND, npad);
+    const int copies = bs_sfb_copies(KIND, npad);
     const int R = S.ring;
-    const int bbytes = bs_bstage_bytes(npad);
-    const int slot_bytes = bs_slot_bytes(npad);
-    const uint32_t d1col = uint32_t(bs_d1(npad, R));
+    const int abytes = bs_a_bytes(KIND);
+    const int brows = bs_brows_bytes(KIND, npad);
+    const int bbytes = bs_bstage_bytes(KIND, npad);
+    const int slot_bytes = bs_slot_bytes(KIND, npad);
+    const uint32_t sfcols = uint32_t(bs_sf_cols(KIND, npad));
+    const uint32_t d1col = uint32_t(bs_d1(KIND, npad, R));
     const int misc = R * slot_bytes;
     const uint32_t bars = sbase + misc;
-    // a stage slot is full once both producers' bytes have landed and the four
-    // scale-factor warps have written its factors: the MMA warp waits once
+    // a stage slot is full once both producers' bytes have landed, and its
+    // factors are ready once the four scale-factor warps have written them
     auto full_b = [&](int c) { return bars + 8u * c; };
     auto empty_b = [&](int c) { return bars + 8u * (kBsMaxRing + c); };
-    constexpr int kB2 = 2 * kBsMaxRing;
+    auto sfok_b = [&](int c) { return bars + 8u * (2 * kBsMaxRing + c); };
+    constexpr int kB2 = 3 * kBsMaxRing;
     auto dready_b = [&](int d) { return bars + 8u * (kB2 + d); };
     auto dfree_b = [&](int d) { return bars + 8u * (kB2 + 2 + d); };
     auto flags_b = [&](int d) { return bars + 8u * (kB2 + 4 + d); };
@@ -277,7 +256,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int c = 0; c < R; ++c) {
-            mbar_init(full_b(c), 2 + 4);  // two producers (with their bytes) + four scale-factor warps
+            mbar_init(full_b(c), 2);      // two producers (with their bytes)
+            mbar_init(sfok_b(c), 4);      // four scale-factor warps
             mbar_init(empty_b(c), 1);     // the MMA commit
         }
         for (int d = 0; d < 2; ++d) {
@@ -295,7 +275,6 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     tc_fence_after();
     pdl_trigger();
     const uint32_t tbase = *tbase_ptr;
-    const uint32_t sf0 = tbase + uint32_t(bs_sf0(npad));
 
     // every wait of this kernel sleeps rather than spins: the scale-factor warps
     // share their schedulers with the epilogue and producer warps, which wait
@@ -313,27 +292,12 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             const bool wprod = warp == 0;
             const uint64_t pol = wprod ? policy_evict_first() : policy_evict_last();
             if (!wprod) pdl_wait();  // the prepared X belongs to the preparation kernel until now
-            BsCursor<G> cur, pf;
+            BsCursor<G> cur;
             cur.start(S);
-            pf.start(S);
-            // weights: each stage's boxes prefetched into L2 S.pf_stages stages before
-            // they are loaded, so that the ring waits on L2 rather than HBM latency
-            auto prefetch = [&]() {
-                if (!pf.valid(S)) return;
-                const Problem& pp = S.p[pf.pi];
-                const bool two = pf.nb() > 4;
-                asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                                 reinterpret_cast<uint64_t>(two ? &pp.tm_w : &pp.tm_s)),
-                             "r"(0), "r"(pf.R.tile * kBsRows), "r"(pf.kb() / 4)
-                             : "memory");
-                pf.next(S);
-            };
-            if (wprod)
-                for (int j = 0; j < S.pf_stages; ++j) prefetch();
             int it = 0, last_pi = -1;
+            bool waited_pdl = !wprod;
             for (; cur.valid(S); cur.next(S), ++it) {
                 const int c = it % R;
-                if (wprod && S.pf_stages > 0) prefetch();
                 if (it >= R && !wait(empty_b(c), ((it / R) - 1) & 1)) break;
                 const uint32_t slot = sbase + uint32_t(c * slot_bytes);
                 if (wprod) {
@@ -342,20 +306,30 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                         prefetch_tmap(&pb.tm_w);
                         prefetch_tmap(&pb.tm_s);
                         last_pi = cur.pi;
+                        if (pb.sc_from_prep && !waited_pdl) {
+                            pdl_wait();  // scales realigned by the preparation kernel of this call
+                            waited_pdl = true;
+                        }
                     }
-                    // both 128-k chunks in one request (tm_w), or the last chunk of an
-                    // odd count alone (tm_s)
-                    const bool two = cur.nb() > 4;
-                    mbar_arrive_expect_tx(full_b(c), uint32_t(two ? kBsATx : kBsATx / 2));
-                    asm volatile(
-                        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(slot),
-                        "l"(reinterpret_cast<uint64_t>(two ? &pb.tm_w : &pb.tm_s)), "r"(0),
-                        "r"(cur.R.tile * kBsRows), "r"(cur.kb() / 4), "r"(full_b(c)), "l"(pol)
-                        : "memory");
+                    // the weights' scales: the 16-byte column of 16 blocks holding this stage's 8
+                    mbar_arrive_expect_tx(full_b(c), uint32_t(kBsATx + kBsScBytes));
+                    tma_2d(slot + uint32_t(abytes + bbytes), &pb.tm_s, cur.kb() & ~15, cur.R.tile * kBsRows,
+                           full_b(c), pol);
+                    if constexpr (KIND == 0) {
+                        // both 128-k chunks of the stage (a chunk beyond K reads as zero codes)
+                        asm volatile(
+                            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                            ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(slot),
+                            "l"(reinterpret_cast<uint64_t>(&pb.tm_w)), "r"(0),
+                            "r"(cur.R.tile * kBsRows), "r"(cur.kb() / 4), "r"(full_b(c)), "l"(pol)
+                            : "memory");
+                    } else {
+                        // one 128-byte x 128-row box (bytes beyond K / 2 read as zero codes)
+                        tma_2d(slot, &pb.tm_w, cur.kb() * 16, cur.R.tile * kBsRows, full_b(c), pol);
+                    }
                 } else {
                     mbar_arrive_expect_tx(full_b(c), uint32_t(bbytes));
-                    bulk_g2s(slot + kBsAStage, cur.xf + int64_t(cur.kb() / kBsStageBlocks) * bbytes,
+                    bulk_g2s(slot + uint32_t(abytes), cur.xf + int64_t(cur.kb() / kBsStageBlocks) * bbytes,
                              uint32_t(bbytes), full_b(c), pol);
                 }
             }
@@ -364,111 +338,111 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer
-        const uint32_t idesc = bs_idesc(2 * npad);
-        int it = 0, tc = 0;
-        bool ok = true;
-        for (int w = int(blockIdx.x); ok && w < S.items; w += int(gridDim.x), ++tc) {
-            const Problem& pb = S.p[find_problem(S, w)];
-            const BsItem RI = bs_item(pb, w - pb.item_begin);
-            const int db = tc & 1;
-            if (tc >= 2 && !wait(dfree_b(db), ((tc >> 1) - 1) & 1)) { ok = false; break; }
-            const uint32_t d_t = tbase + (db ? d1col : 0u);
-            for (int i = 0; ok && i < RI.nst; ++i, ++it) {
-                const int c = it % R;
-                const int nb = min(kBsStageBlocks, RI.kb1 - (RI.kb0 + i * kBsStageBlocks));
-                if (!wait(full_b(c), (it / R) & 1)) { ok = false; break; }
-                tc_fence_after();
-                if (lane == 0) {
-                    // descriptors advance by 32 bytes per block within a 128-k chunk
-                    // (2 in their 16-byte address field) and by a chunk after four
+        // one lane: a warp-wide loop costs the tensor pipe a few hundred
+        // cycles of every stage in convergence and slot arithmetic
+        if (lane == 0) {
+            const uint32_t idesc = bs_idesc(KIND, N);
+            const uint32_t sf0c = tbase + uint32_t(bs_sf0(KIND, npad));
+            int tc = 0, c = 0;
+            uint32_t ph = 0;  // parity of slot c's current use
+            bool ok = true;
+            for (int w = int(blockIdx.x); ok && w < S.items; w += int(gridDim.x), ++tc) {
+                const Problem& pb = S.p[find_problem(S, w)];
+                const BsItem RI = bs_item(pb, w - pb.item_begin);
+                const int db = tc & 1;
+                if (tc >= 2 && !wait(dfree_b(db), ((tc >> 1) - 1) & 1)) { ok = false; break; }
+                const uint32_t d_t = tbase + (db ? d1col : 0u);
+                for (int i = 0; i < RI.nst; ++i) {
+                    const int nb = min(kBsStageBlocks, RI.kb1 - (RI.kb0 + i * kBsStageBlocks));
+                    // the factors are written after the stage's bytes landed: their barrier covers both
+                    if (!mbar_try_wait(sfok_b(c), ph) && !wait(sfok_b(c), ph)) { ok = false; break; }
+                    tc_fence_after();
                     const uint32_t slot = sbase + uint32_t(c * slot_bytes);
                     const uint64_t ad0 = umma_desc_sw128(slot);
-                    const uint64_t bd0 = umma_desc_sw128(slot + kBsAStage);
-                    const uint32_t sfa = sf0 + uint32_t(kBsSfCols * c);
+                    const uint64_t bd0 = umma_desc_sw128(slot + uint32_t(abytes));
+                    const uint32_t tsfa = sf0c + sfcols * uint32_t(c);
+                    const uint32_t tsfb = tsfa + 8u;
+                    if constexpr (KIND == 0) {
+                        // descriptors advance by 32 bytes per block within a 128-k chunk
+                        // (2 in their 16-byte address field) and by a chunk after four
 #pragma unroll
-                    for (int kb = 0; kb < kBsStageBlocks; ++kb) {
-                        if (kb < nb)
-                            umma_mxf8f6f4(d_t, ad0 + uint64_t(((kb >> 2) * kBsAChunk + (kb & 3) * 32) >> 4),
-                                          bd0 + uint64_t(((kb >> 2) * (2 * npad * 128) + (kb & 3) * 32) >> 4),
-                                          idesc, sfa + uint32_t(4 * kb), sfa + uint32_t(kBsSfbCol + 4 * kb),
-                                          (i | kb) != 0);
+                        for (int kb = 0; kb < kBsStageBlocks; ++kb)
+                            if (kb < nb)
+                                umma_bs<0>(d_t, ad0 + uint64_t(((kb >> 2) * kBsAChunk + (kb & 3) * 32) >> 4),
+                                           bd0 + uint64_t(((kb >> 2) * (N * 128) + (kb & 3) * 32) >> 4),
+                                           idesc | bs_sfid(uint32_t(kb & 3)), tsfa + uint32_t(4 * (kb >> 2)),
+                                           tsfb + uint32_t(4 * copies * (kb >> 2)), (i | kb) != 0);
+                    } else {
+                        // four MMAs of 64 k (blocks 2j, 2j + 1: factor bytes 2 (j & 1), +1)
+#pragma unroll
+                        for (int j = 0; j < kBsStageBlocks / 2; ++j)
+                            if (2 * j < nb)
+                                umma_bs<1>(d_t, ad0 + uint64_t((j * 32) >> 4), bd0 + uint64_t((j * 32) >> 4),
+                                           idesc | bs_sfid(uint32_t(2 * (j & 1))), tsfa + uint32_t(4 * (j >> 1)),
+                                           tsfb + uint32_t(4 * copies * (j >> 1)), (i | j) != 0);
                     }
                     tc_commit(empty_b(c));
+                    if (++c == R) {
+                        c = 0;
+                        ph ^= 1u;
+                    }
                 }
-                __syncwarp();
+                if (ok) tc_commit(dready_b(db));
             }
-            if (ok && lane == 0) tc_commit(dready_b(db));
-            __syncwarp();
+            // every issued MMA has completed before the allocation is released
+            tc_commit(fin_b);
         }
-        // every issued MMA has completed before the allocation is released
-        if (lane == 0) tc_commit(fin_b);
         __syncwarp();
         mbar_wait_sleep(fin_b, 0, S.status);
     } else if (warp < kBsFirstEpi) {
         // ------------------------------------------------ scale-factor warps
+        // Per stage, once its bytes have landed: this quadrant's weight rows'
+        // scales (from the TMA box) and X's factor cells (from the prepared X)
+        // into the slot's factor columns, for every lane of the quadrant.
         const int q = warp & 3;
         const int r = 32 * q + lane;
         const uint32_t lane_addr = uint32_t(32 * q) << 16;
-        // The factors of a stage are loaded three stages before they are
-        // written: three buffers used in turn (the loop is unrolled by three),
-        // so that no register copy waits for a load.  X's factors are written
-        // by the preparation kernel: read only after it has finished.
-        pdl_wait();
-        BsCursor<G> cur, ld, pf;
+        const uint32_t sf0c = tbase + lane_addr + uint32_t(bs_sf0(KIND, npad));
+        BsCursor<G> cur;
         cur.start(S);
-        ld.start(S);
-        pf.start(S);
-        BsFactors fa = bs_load_factors(S, ld, r, lane, npad);
-        ld.next(S);
-        BsFactors fb = bs_load_factors(S, ld, r, lane, npad);
-        ld.next(S);
-        BsFactors fc = bs_load_factors(S, ld, r, lane, npad);
-        ld.next(S);
-        for (int j = 0; j < 8; ++j) pf.next(S);
-        int it = 0, tc = 0;
+        int it = 0, tc = 0, c = 0;
+        uint32_t ph = 0;
         bool nan = false;
-        // one stage: write its factors into the slot's columns once the MMA is done with them
-        auto stage = [&](const BsFactors& f) -> bool {
-            const int c = it % R;
-            // the weight scales 8 stages ahead into L2, one prefetch per 32-byte sector
-            if (pf.valid(S) && (pf.kb() & 31) == 0) {
-                const int64_t n = int64_t(pf.R.tile) * kBsRows + r;
-                if (n < pf.N) asm volatile("prefetch.global.L2 [%0];" ::"l"(pf.sc + n * pf.sc_pitch + pf.kb()));
-            }
-            pf.next(S);
-            nan |= has_byte_ff(f.a.x) || has_byte_ff(f.a.y);
-            if (it >= R && !wait(empty_b(c), ((it / R) - 1) & 1)) return false;
-            bs_write_factors(sf0 + uint32_t(kBsSfCols * c) + lane_addr, f);
+        for (; cur.valid(S); cur.next(S), ++it) {
+            // the slot's previous stage was consumed before its bytes were requested again
+            if (!wait(full_b(c), ph)) break;
+            const uint8_t* slot = smem + c * slot_bytes;
+            const uint2 f = *reinterpret_cast<const uint2*>(slot + abytes + bbytes + 16 * r + (cur.kb() & 8));
+            nan |= has_byte_ff(f.x) || has_byte_ff(f.y);
+            const uint32_t tsfa = sf0c + sfcols * uint32_t(c);
+            const uint32_t tsfb = tsfa + 8u;
+            tmem_st4(tsfa, f.x, f.x, f.x, f.x);
+            tmem_st4(tsfa + 4u, f.y, f.y, f.y, f.y);
+            const uint8_t* cells = slot + abytes + brows + 16 * lane;
+#pragma unroll
+            for (int gh = 0; gh < 4; ++gh)
+                if (gh < 2 * copies) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(cells + kBsCopyBytes * gh);
+                    tmem_st4(tsfb + uint32_t(4 * gh), v.x, v.y, v.z, v.w);
+                }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(full_b(c));
-            ++it;
+            if (lane == 0) mbar_arrive(sfok_b(c));
+            if (++c == R) {
+                c = 0;
+                ph ^= 1u;
+            }
             if (cur.i == cur.R.nst - 1) {
                 // the tile's NaN-scale flags, once the epilogue is done with the slot's previous tile
                 const int db = tc & 1;
-                if (tc >= 2 && !wait(dfree_b(db), ((tc >> 1) - 1) & 1)) return false;
+                if (tc >= 2 && !wait(dfree_b(db), ((tc >> 1) - 1) & 1)) break;
                 nanflags[db * kBsRows + r] = nan ? 1 : 0;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(flags_b(db));
                 nan = false;
                 ++tc;
             }
-            cur.next(S);
-            return true;
-        };
-        while (cur.valid(S)) {
-            if (!stage(fa)) break;
-            fa = bs_load_factors(S, ld, r, lane, npad);
-            ld.next(S);
-            if (!cur.valid(S)) break;
-            if (!stage(fb)) break;
-            fb = bs_load_factors(S, ld, r, lane, npad);
-            ld.next(S);
-            if (!cur.valid(S)) break;
-            if (!stage(fc)) break;
-            fc = bs_load_factors(S, ld, r, lane, npad);
-            ld.next(S);
         }
     } else {
         // ------------------------------------------------------- epilogue
@@ -480,8 +454,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         for (int w = int(blockIdx.x); w < S.items; w += int(gridDim.x), ++tc) {
             const Problem& pb = S.p[find_problem(S, w)];
             const int wl = w - pb.item_begin;
-            const BsItem R = bs_item(pb, wl);
-            const int64_t n0 = int64_t(R.tile) * kBsRows;
+            const BsItem RI = bs_item(pb, wl);
+            const int64_t n0 = int64_t(RI.tile) * kBsRows;
             const int rows = int(pb.N - n0 < int64_t(kBsRows) ? pb.N - n0 : int64_t(kBsRows));
             const int db = tc & 1;
             if (!wait(dready_b(db), (tc >> 1) & 1)) break;
@@ -493,23 +467,28 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             }
             const bool nan = nanflags[db * kBsRows + r] != 0;
             const float* xun = pb.xun;
-            const int64_t N = pb.N;
+            const int64_t Ny = pb.N;
             float* mine = pb.part + int64_t(wl) * M * kBsRows;
             const uint32_t dcol = tbase + lane_addr + (db ? d1col : 0u);
 #pragma unroll 1
             for (int c0 = 0; c0 < npad; c0 += 16) {
-                uint32_t d1[16], d2[16];
-                tmem_ld16(dcol + uint32_t(c0), d1);
-                tmem_ld16(dcol + uint32_t(npad + c0), d2);
-                tmem_wait_ld();
+                // Y rows c0 .. c0 + 15: the sum of their T term columns, in term order
+                float acc[16];
+#pragma unroll 1
+                for (int t = 0; t < T; ++t) {
+                    uint32_t d[16];
+                    tmem_ld16(dcol + uint32_t(t * npad + c0), d);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) acc[c] = t == 0 ? __uint_as_float(d[c]) : acc[c] + __uint_as_float(d[c]);
+                }
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const int m = c0 + c;
                     if (m < M) {
-                        const float v = nan ? __int_as_float(0x7FC00000)
-                                            : __uint_as_float(d1[c]) + __uint_as_float(d2[c]);
+                        const float v = nan ? __int_as_float(0x7FC00000) : acc[c];
                         if (pb.nsplit == 1) {
-                            if (r < rows) pb.y[int64_t(m) * N + n0 + r] = v * xun[m];
+                            if (r < rows) pb.y[int64_t(m) * Ny + n0 + r] = v * xun[m];
                         } else {
                             __stcg(mine + int64_t(m) * kBsRows + r, v);
                         }
@@ -525,7 +504,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 __threadfence();
                 __syncwarp();
                 int last = 0;
-                if (lane == 0) last = atomicAdd(pb.counters + 4 * R.tile + q, 1) == pb.nsplit - 1;
+                if (lane == 0) last = atomicAdd(pb.counters + 4 * RI.tile + q, 1) == pb.nsplit - 1;
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
                     __threadfence();
@@ -533,11 +512,11 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                         for (int m = 0; m < M; ++m) {
                             float s = 0.f;
                             for (int sp = 0; sp < pb.nsplit; ++sp)
-                                s += __ldcg(pb.part + (int64_t(sp) * pb.ntiles + R.tile) * M * kBsRows +
+                                s += __ldcg(pb.part + (int64_t(sp) * pb.ntiles + RI.tile) * M * kBsRows +
                                             int64_t(m) * kBsRows + r);
-                            pb.y[int64_t(m) * N + n0 + r] = s * xun[m];
+                            pb.y[int64_t(m) * Ny + n0 + r] = s * xun[m];
                         }
-                    if (lane == 0) pb.counters[4 * R.tile + q] = 0;  // ready for the next call
+                    if (lane == 0) pb.counters[4 * RI.tile + q] = 0;  // ready for the next call
                 }
             }
         }

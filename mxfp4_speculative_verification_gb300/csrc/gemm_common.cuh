@@ -42,7 +42,6 @@ struct ProblemSet {
     // and a stage that CTA 0's producer leaves out entirely (-1: none)
     unsigned long long wait_ns;
     int skip_stage;
-    int pf_stages;  // block-scaled kernel: L2 prefetch distance of the weights, in stages
 };
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,

@@ -14,11 +14,13 @@ spec.loader.exec_module(bench)
 
 def test_gemm_passes_split_rows_and_pick_kernels():
     assert bench.gemm_passes(5) == [(5, "mma")]
-    assert bench.gemm_passes(24) == [(24, "mma")]
-    assert bench.gemm_passes(25) == [(25, "bs")]
-    assert bench.gemm_passes(64) == [(64, "bs")]
-    assert bench.gemm_passes(80) == [(64, "bs"), (16, "mma")]
-    assert bench.gemm_passes(320) == [(64, "bs")] * 5
+    assert bench.gemm_passes(24) == [(24, "bs4")]
+    assert bench.gemm_passes(8) == [(8, "mma")]
+    assert bench.gemm_passes(70) == [(64, "bs8"), (6, "mma")]
+    assert bench.gemm_passes(25) == [(25, "bs4")]
+    assert bench.gemm_passes(64) == [(64, "bs8")]
+    assert bench.gemm_passes(80) == [(64, "bs8"), (16, "bs4")]
+    assert bench.gemm_passes(320) == [(64, "bs8")] * 5
     assert sum(r for r, _ in bench.gemm_passes(1000)) == 1000
 
 

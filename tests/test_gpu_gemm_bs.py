@@ -1,8 +1,10 @@
-"""GPU parity of the block-scaled tensor-core verify GEMM (tcgen05 kind::mxf8f6f4).
+"""GPU parity of the block-scaled tensor-core verify GEMM, both kinds:
+kind::mxf8f6f4 (X as two E4M3 terms) and kind::mxf4 (X as six E2M1 terms).
 
-The entry points take this path for passes of 9 or more rows; here it is
-forced (MXS_GEMM_PATH=bs) so that narrow, ragged and pathological shapes
-exercise it too, against the same oracle and bar as every other path.
+The entry points take this path for passes of 9 or more rows (mxf4 up to 32
+rows, mxf8f6f4 beyond); here each kind is forced (MXS_GEMM_PATH=bs8 / bs4)
+so that narrow, ragged and pathological shapes exercise both, against the
+same oracle and bar as every other path.
 """
 import numpy as np
 import pytest
@@ -14,9 +16,9 @@ from helpers import GEMM_REL_TOL, bf16_tensor_from_bits, cuda_or_skip, gemm_row_
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture
-def env(monkeypatch):
-    monkeypatch.setenv("MXS_GEMM_PATH", "bs")
+@pytest.fixture(params=["bs8", "bs4"])
+def env(request, monkeypatch):
+    monkeypatch.setenv("MXS_GEMM_PATH", request.param)
     return cuda_or_skip()
 
 
@@ -42,7 +44,8 @@ def test_bs_rows_m(env, M):
     nib, sc = workloads.mxfp4_weights(300, 1024, 118, 132, seed=M, tensor_id=0)
     x = workloads.bf16_normal(M, 1024, seed=M, tensor_id=1)
     y, ref = _check(env, x, nib, sc)
-    # two E4M3 terms hold bf16 N(0,1) exactly: only fp32 summation error remains
+    # two E4M3 terms hold bf16 N(0,1) exactly, six E2M1 terms to ~1e-7 of
+    # each block maximum: what remains is fp32 summation error
     assert np.all(gemm_row_rel_err(y, ref) < 1e-5)
 
 
