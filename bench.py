@@ -50,12 +50,12 @@ FALLBACK_HBM_GBS = 6800.0
 # is reported as null otherwise (ratio None: not yet captured on the current
 # sources).
 GEMM_TRAFFIC = {
-    # mxfp4_gemm_kernel, passes of <= 24 rows: lm_head 4096 x 128256 at M=5
-    "mma": {"ratio": None, "sha": None},
-    # mxfp4_gemm_bs_kernel, kind::mxf8f6f4 (passes of 33..64 rows)
-    "bs8": {"ratio": None, "sha": None},
-    # mxfp4_gemm_bs_kernel, kind::mxf4 (passes of 9..32 rows)
-    "bs4": {"ratio": None, "sha": None},
+    # mxfp4_gemm_kernel, passes of <= 8 rows: lm_head 4096 x 128256 at M=5
+    "mma": {"ratio": 1.0046, "sha": "9be8dc3ecbe78824"},
+    # mxfp4_gemm_bs_kernel, kind::mxf8f6f4 (passes of 33..64 rows): lm_head at M=64
+    "bs8": {"ratio": 0.9175, "sha": "52c5d9d2a16da9bf"},
+    # mxfp4_gemm_bs_kernel, kind::mxf4 (passes of 9..32 rows): lm_head at M=20
+    "bs4": {"ratio": 0.9853, "sha": "52c5d9d2a16da9bf"},
 }
 BS_MIN_ROWS = 9     # passes of at least this many rows run on the block-scaled kernel
 BS4_MAX_ROWS = 32   # its mxf4 kind takes passes of up to this many rows

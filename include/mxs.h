@@ -102,7 +102,8 @@ mxs_status mxfp4_pack(const void* w, int32_t w_dtype, int64_t N, int64_t K,
  *              workspace first when K % 512 != 0 or not 16-byte aligned)
  *   y          device, [M, N] fp32, 4-byte aligned, written
  *   1 <= M <= 65536, 1 <= N <= 4194240, 32 <= K <= 1048576, K % 32 == 0;
- *              rows are processed 64 at a time, each group one pass over W
+ *              rows are processed in passes of at most 32 or 64 (by the
+ *              kernel, below), each pass one stream over W
  *   workspace  device, >= mxfp4_verify_gemm_workspace_size(M, N, K) bytes,
  *              16-byte aligned; scratch for the converted X, the split-K
  *              counters (zeroed by the call itself) and, when needed, the
@@ -112,18 +113,23 @@ mxs_status mxfp4_pack(const void* w, int32_t w_dtype, int64_t N, int64_t K,
  *              a misaligned `scales` is rejected (MXS_ERR_MISALIGNED) because
  *              the size query assumed the in-place layout.
  *
- * Accuracy: products are exact; sums are fp32.  Each x row is scaled by a
- * power of two so that its largest |x| lies in [2^15, 2^16) before it is
- * rounded to fp16 for the tensor cores: exact for every element within 2^29
- * of that row's largest magnitude.
- *
- * Kernels: a pass of at most 24 rows runs on mma.sync (each 32-k block summed
- * and scaled by its E8M0 factor in fp32, split-K when N is small); a pass of
- * 25..64 rows on 128-row tiles of N >= 8192 runs on the tcgen05 tensor-memory
- * kernel (weights pre-scaled to exact fp16 against each row's largest
- * exponent, whole-tile fp32 accumulation).  The two add in different orders,
- * so their results differ in the last bits, both within the stated accuracy.
- * MXS_GEMM_PATH=mma or =umma in the environment forces one of them.
+ * Kernels and accuracy.  Products are exact and sums are fp32 in every path;
+ * what differs is the image of x the tensor cores multiply:
+ *   - passes of at most 8 rows: mma.sync on fp16 (each x row scaled by a
+ *     power of two that puts its largest |x| in [2^15, 2^16): exact for every
+ *     element within 2^29 of it), each 32-k block summed and scaled by its
+ *     E8M0 factor in fp32, split-K when N is small;
+ *   - passes of 9..32 rows: tcgen05 block-scaled MMA (kind::mxf4) on the E2M1
+ *     weights and x as six E2M1 terms per 32-k block, each with its own
+ *     power-of-two factor: x to within max|x| / 4^6 of each block maximum;
+ *   - passes of 33..64 rows (K % 128 == 0): tcgen05 block-scaled MMA
+ *     (kind::mxf8f6f4) with x as two E4M3 terms per 32-k block: exact for
+ *     every element within 2^16 of its block maximum.
+ * The paths add in different orders, so their results differ in the last
+ * bits, all within the stated 2e-3 per-row bar (measured <= 1e-6 of each
+ * row's largest output).  A row of x holding Inf or NaN gives a row of NaN.
+ * MXS_GEMM_PATH=mma, bs4, bs8 or umma (an earlier tcgen05 kind::f16 kernel)
+ * in the environment forces one kernel wherever it applies.
  * ---------------------------------------------------------------------- */
 size_t mxfp4_verify_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
@@ -149,15 +155,14 @@ mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles,
  *              nibbles [N, K/2] (16-byte aligned), scales [N, K/32]
  *              (16-byte aligned, K % 512 == 0), y [M, N] fp32 written.
  *              No y may overlap any problem's x, nibbles, scales or another y.
- *   1 <= count <= 4096, 1 <= M <= 65536 (rows are processed 64 at a time,
- *   each group of rows one pass over every weight matrix)
+ *   1 <= count <= 4096, 1 <= M <= 65536 (rows are processed in passes of at
+ *   most 32 or 64, each pass one stream over every weight matrix)
  *   workspace  device, >= mxfp4_verify_gemm_grouped_workspace_size(...)
  *              bytes, 16-byte aligned.
  * Results are bit-identical to calling mxfp4_verify_gemm on each problem
  * whenever both take the same kernel and the single call does not split K
- * (splitting changes only the order of fp32 additions).  Passes of at most
- * 24 rows use mma.sync in both; passes of more rows use the tcgen05 kernel
- * here for every problem, but in a single call only for N >= 8192.
+ * (splitting changes only the order of fp32 additions).  Both take the same
+ * kernel for a pass of the same rows (one kind for every problem of a pass).
  * Within each mma.sync launch the problems are ordered by K, largest first,
  * and the CTAs claim work items (a 64- or 128-row tile) from a counter in
  * the workspace, zeroed by the call itself: a longest-first list schedule.

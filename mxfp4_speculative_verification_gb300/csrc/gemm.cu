@@ -32,13 +32,17 @@
 //  * when K is split, each work item writes its partial tile to the
 //    workspace and bumps a per-tile counter; the item that completes the
 //    count sums all partials in split order (deterministic) and writes Y;
-//  * passes of more than 24 rows (and, for a single GEMM, N >= 8192) run
-//    instead on the tcgen05 kernel of gemm_umma.cuh, fed by the same
-//    preparation kernel in its swizzled tile layout (`use_umma`).
+//  * that kernel takes passes of at most 8 rows; passes of 9..64 rows run on
+//    the block-scaled tcgen05 kernel of gemm_bs.cuh (E2M1 weights and their
+//    E8M0 scales straight into the tensor core, X as a sum of narrow terms;
+//    `bs_kind_for`), fed by the same preparation kernel in its own layout.
+//    The earlier tcgen05 kernel of gemm_umma.cuh (weights decoded to fp16 in
+//    tensor memory) stays available behind MXS_GEMM_PATH=umma.
 //
 // Files: gemm_common.cuh (problem table, TMA helpers, work items),
-// gemm_mma.cuh (the mma.sync kernel), gemm_prep.cuh (X preparation),
-// gemm_umma.cuh (the tcgen05 kernel); this file holds the host launchers.
+// gemm_mma.cuh (the mma.sync kernel), gemm_bs.cuh (the block-scaled kernel),
+// gemm_umma.cuh (the fp16 tcgen05 kernel), gemm_prep.cuh (X preparation);
+// this file holds the host launchers.
 #include <cuda.h>  // CUtensorMap and the tensor-map enums (types only)
 
 #include <algorithm>
@@ -524,9 +528,9 @@ static int64_t bs_pass_rows(int kind, int64_t rows_left) {
     return std::min<int64_t>(kind ? kBsF4MaxRows : kBsMaxNpad, rows_left);
 }
 
-// Which kernel a pass of mc rows uses.  mma.sync (legacy tensor path) is
-// faster up to 24 rows; beyond that its m16n8k16 issue rate, not HBM,
-// bounds it and the tcgen05 kernel takes over.  MXS_GEMM_PATH=mma|umma
+// For a pass the block-scaled kernel does not take: whether the fp16
+// tcgen05 kernel runs it instead of mma.sync (more than 24 rows, where the
+// m16n8k16 issue rate rather than HBM bounds mma.sync).  MXS_GEMM_PATH=mma|umma
 // forces one (umma needs more than 8 rows).
 static bool use_umma(int mc, int64_t tiles128, bool grouped) {
     const char* path = std::getenv("MXS_GEMM_PATH");

@@ -1,4 +1,4 @@
-// The mma.sync verify-GEMM kernel (passes of at most 24 rows; the design is
+// The mma.sync verify-GEMM kernel (passes of at most 8 rows by default; the design is
 // described at the top of gemm.cu), included by gemm.cu inside namespace mxs.
 
 // RG groups of 16 weight rows; KW consumer warps share each group, each
