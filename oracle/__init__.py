@@ -20,6 +20,9 @@ What each entry point follows (page title, section):
 * ``spec_accept`` -- Module 11 §4 (left-to-right acceptance, residual
   norm((p-q)+), bonus token) and §5 (strict "draw < acceptance", acceptance 0
   where q = 0).
+* ``sampling_law`` -- Module 11 §4 (the laws acceptance uses are the ones
+  tokens are actually sampled from: temperature, then top-k, then top-p, on
+  the target and the draft alike).
 
 Every function is pinned by ``tests/test_oracle_*.py`` against values the pages
 print, closed forms, invariants and brute force; none is "parity unpinned".
@@ -73,6 +76,8 @@ def _load():
     lib.mxs_oracle_gemm.restype = ctypes.c_int
     lib.mxs_oracle_pack.argtypes = [p, i64, i64, p, p]
     lib.mxs_oracle_pack.restype = ctypes.c_int
+    lib.mxs_oracle_sampling_law.argtypes = [p, i64, i64, ctypes.c_double, i64, ctypes.c_double, p, p, p]
+    lib.mxs_oracle_sampling_law.restype = ctypes.c_int
     for name in ("mxs_oracle_spec_accept", "mxs_oracle_spec_accept_f64"):
         fn = getattr(lib, name)
         fn.argtypes = [p, p, p, p, i64, i64, i64, p, p, p, p, ctypes.c_int]
@@ -187,3 +192,26 @@ def spec_accept(p: np.ndarray, q: np.ndarray, draft: np.ndarray, u: np.ndarray,
     if rc:
         raise ValueError(f"oracle spec_accept failed ({rc})")
     return tokens, n_emitted, flags, edge
+
+
+def sampling_law(logits: np.ndarray, temperature: float = 1.0, top_k: int = 0, top_p: float = 1.0):
+    """Transformed laws of logit rows [..., V] (fp32): temperature, top-k, top-p.
+
+    Returns (probs float64 [..., V], cut_margin float64 [...], kept int64 [...]):
+    cut_margin is the distance of top_p from the cumulative mass at the two
+    positions that decide the top-p cut (inf when top-p keeps everything), kept
+    the number of tokens of positive probability (0: the row has no law).
+    """
+    lg = _c(logits, np.float32)
+    shape = lg.shape
+    V = shape[-1]
+    R = int(np.prod(shape[:-1])) if len(shape) > 1 else 1
+    lg = lg.reshape(R, V)
+    probs = np.empty((R, V), dtype=np.float64)
+    margin = np.empty(R, dtype=np.float64)
+    kept = np.empty(R, dtype=np.int64)
+    rc = _load().mxs_oracle_sampling_law(_ptr(lg), R, V, float(temperature), int(top_k), float(top_p),
+                                         _ptr(probs), _ptr(margin), _ptr(kept))
+    if rc:
+        raise ValueError(f"oracle sampling_law failed ({rc})")
+    return probs.reshape(shape), margin.reshape(shape[:-1]), kept.reshape(shape[:-1])

@@ -444,3 +444,102 @@ int mxs_oracle_spec_accept_f64(const double* p, const double* q,
     J.edge_dist = edge_dist;
     return run_accept(J, nthreads);
 }
+
+/* ------------------------------------------------------------------ */
+/* The law tokens are actually sampled from ([M11] §4)                  */
+/* ------------------------------------------------------------------ */
+/*
+ * [M11] §4 "The exact propose-verify-correct cycle": temperature changes the
+ * sharpness of the logits, top-k keeps the k most probable tokens, top-p keeps
+ * a smallest set of the most probable tokens whose cumulative mass reaches p,
+ * and acceptance must use the transformed laws of both the target and the
+ * draft.  Readings where the page is silent:
+ *   - temperature divides the logits (T > 0);
+ *   - top-k keeps every token whose logit is at least the k-th largest (ties
+ *     at the boundary are kept); k = 0 or k >= V keeps every token;
+ *   - top-p walks the kept tokens from the most probable down and stops at
+ *     the first whose cumulative mass reaches p; every token at least as
+ *     probable as that one is kept (ties kept); p >= 1 keeps every token;
+ *   - the kept masses are renormalised; a logit of -inf (a masked token) has
+ *     probability 0; a row with a NaN or +inf logit, or nothing of positive
+ *     mass, has no law (every probability 0, kept count 0).
+ * cut_margin[r] = distance of p from the cumulative mass at the two positions
+ * that decide the top-p cut (infinity when top-p keeps every token): a kernel
+ * whose masses differ by less than that makes the same cut.
+ */
+static const float* g_sort_row;  /* row being sorted (single-threaded use) */
+
+static int by_logit_desc(const void* a, const void* b) {
+    const int64_t i = *(const int64_t*)a, j = *(const int64_t*)b;
+    const double li = g_sort_row[i], lj = g_sort_row[j];
+    if (li > lj) return -1;
+    if (li < lj) return 1;
+    return (i > j) - (i < j);
+}
+
+int mxs_oracle_sampling_law(const float* logits, int64_t R, int64_t V, double temperature,
+                            int64_t top_k, double top_p, double* probs, double* cut_margin,
+                            int64_t* kept_count) {
+    if (R < 0 || V < 1 || !(temperature > 0.0) || top_k < 0 || !(top_p > 0.0)) return 1;
+    int64_t* order = (int64_t*)malloc((size_t)V * sizeof(int64_t));
+    double* e = (double*)malloc((size_t)V * sizeof(double));
+    if (!order || !e) { free(order); free(e); return 2; }
+    for (int64_t r = 0; r < R; ++r) {
+        const float* l = logits + r * V;
+        double* pr = probs + r * V;
+        cut_margin[r] = INFINITY;
+        kept_count[r] = 0;
+        int bad = 0;
+        for (int64_t t = 0; t < V; ++t) {
+            pr[t] = 0.0;
+            if (isnan(l[t]) || (isinf(l[t]) && l[t] > 0)) bad = 1;
+        }
+        if (bad) continue;
+        /* the tokens from the most probable down (equal logits in index order) */
+        for (int64_t t = 0; t < V; ++t) order[t] = t;
+        g_sort_row = l;
+        qsort(order, (size_t)V, sizeof(int64_t), by_logit_desc);
+        if (isinf(l[order[0]])) continue;  /* every token masked */
+        /* top-k: at least the k-th largest logit */
+        double lk = -INFINITY;
+        if (top_k > 0 && top_k < V) lk = l[order[top_k - 1]];
+        /* temperature, then the softmax over the kept tokens */
+        const double zmax = (double)l[order[0]] / temperature;
+        double S = 0.0;
+        for (int64_t t = 0; t < V; ++t) {
+            e[t] = 0.0;
+            if ((double)l[t] >= lk && !isinf(l[t])) e[t] = exp((double)l[t] / temperature - zmax);
+            S += e[t];
+        }
+        if (!(S > 0.0)) continue;
+        /* top-p: the first position whose cumulative mass reaches p */
+        double lp = lk;
+        if (top_p < 1.0) {
+            double c = 0.0, prev = 0.0;
+            for (int64_t i = 0; i < V; ++i) {
+                const int64_t t = order[i];
+                if (e[t] == 0.0) continue;
+                prev = c;
+                c += e[t] / S;
+                if (c >= top_p) {
+                    lp = l[t];
+                    cut_margin[r] = fmin(fabs(c - top_p), fabs(top_p - prev));
+                    break;
+                }
+            }
+        }
+        /* renormalise over what is kept */
+        double S2 = 0.0;
+        for (int64_t t = 0; t < V; ++t) {
+            if ((double)l[t] < lp) e[t] = 0.0;
+            S2 += e[t];
+        }
+        for (int64_t t = 0; t < V; ++t) {
+            pr[t] = e[t] / S2;
+            if (e[t] > 0.0) ++kept_count[r];
+        }
+    }
+    free(order);
+    free(e);
+    return 0;
+}
