@@ -463,9 +463,10 @@ int mxs_oracle_spec_accept_f64(const double* p, const double* q,
  *   - the kept masses are renormalised; a logit of -inf (a masked token) has
  *     probability 0; a row with a NaN or +inf logit, or nothing of positive
  *     mass, has no law (every probability 0, kept count 0).
- * cut_margin[r] = distance of p from the cumulative mass at the two positions
- * that decide the top-p cut (infinity when top-p keeps every token): a kernel
- * whose masses differ by less than that makes the same cut.
+ * cut_margin[r] = distance of p from the cumulative mass at the positions
+ * that decide the top-p cut -- the one where it stops and the one before it,
+ * if any (infinity when top-p keeps every token): a kernel whose masses
+ * differ by less than that makes the same cut.
  */
 static const float* g_sort_row;  /* row being sorted (single-threaded use) */
 
@@ -515,17 +516,18 @@ int mxs_oracle_sampling_law(const float* logits, int64_t R, int64_t V, double te
         /* top-p: the first position whose cumulative mass reaches p */
         double lp = lk;
         if (top_p < 1.0) {
-            double c = 0.0, prev = 0.0;
+            double c = 0.0, prev = -1.0;  /* prev < 0: no earlier position to stop at */
             for (int64_t i = 0; i < V; ++i) {
                 const int64_t t = order[i];
                 if (e[t] == 0.0) continue;
-                prev = c;
                 c += e[t] / S;
                 if (c >= top_p) {
                     lp = l[t];
-                    cut_margin[r] = fmin(fabs(c - top_p), fabs(top_p - prev));
+                    cut_margin[r] = fabs(c - top_p);
+                    if (prev >= 0.0) cut_margin[r] = fmin(cut_margin[r], fabs(top_p - prev));
                     break;
                 }
+                prev = c;
             }
         }
         /* renormalise over what is kept */
