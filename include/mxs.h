@@ -46,7 +46,7 @@ typedef int32_t mxs_status;
 #define MXS_DEV_BAD_DRAFT 0x1       /* spec_accept: a draft id outside [0,V)          */
 #define MXS_DEV_ZERO_Q 0x2          /* spec_accept: a proposal with q(x) = 0 (reject) */
 #define MXS_DEV_ZERO_RESIDUAL 0x4   /* spec_accept: residual mass 0, sampled p_j      */
-#define MXS_DEV_NO_LAW 0x8          /* spec_accept: the law to sample has no mass     */
+#define MXS_DEV_NO_LAW 0x8          /* spec_accept / laws: a law with no mass         */
 #define MXS_DEV_NEAR_EDGE 0x10      /* spec_accept: u within 1e-5 of a CDF bin edge   */
 #define MXS_DEV_NONFINITE 0x20      /* mxfp4_pack: a block held Inf or NaN            */
 #define MXS_DEV_TIMEOUT 0x40        /* a bounded pipeline wait gave up                */
@@ -252,6 +252,65 @@ mxs_status spec_accept(const float* p, const float* q, const int32_t* draft,
                        const float* u, int64_t B, int64_t K, int64_t V,
                        int32_t* out_tokens, int32_t* n_emitted,
                        int32_t* row_flags, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Sampling laws from logits ("Module 11 ...", §4 "The exact propose-verify-
+ * correct cycle"): acceptance must use the laws tokens are actually sampled
+ * from -- temperature, top-k and top-p applied to the target and the draft
+ * alike; raw probabilities with a filtered law break the proof.
+ *
+ * For one row of logits l[0..V-1]:
+ *   - temperature T > 0 divides the logits;
+ *   - top-k (k >= 1 and k < V; 0 or >= V: off) keeps every token whose logit
+ *     is at least the k-th largest (ties at the boundary kept);
+ *   - top-p (0 < p < 1; 1: off) then keeps, from the most probable down, the
+ *     tokens up to the first whose cumulative mass reaches p, and every token
+ *     as probable as that one (ties kept);
+ *   - the kept tokens get p_t = exp((l_t - max l) / T) / S, the others 0.
+ * A logit of -inf is a masked token (probability 0).  A row with a NaN or
+ * +inf logit, or with every logit -inf, has no law: all probabilities 0 and
+ * MXS_DEV_NO_LAW.  Masses are summed in fixed point (2^-46 units) so that
+ * the top-p cut is a deterministic function of the row; probabilities match
+ * a double-precision evaluation to ~1e-6 relative, and the cut may differ
+ * from it only where p lies within ~1e-6 of a cumulative mass.
+ *
+ *   mxs_sampling   HOST struct: temperature (> 0, finite), top_k (>= 0),
+ *                  top_p (in (0, 1])
+ * ---------------------------------------------------------------------- */
+typedef struct mxs_sampling {
+    float temperature;
+    int32_t top_k;
+    float top_p;
+} mxs_sampling;
+
+/* spec_sampling_law: the transformed laws of R logit rows.
+ *   logits  device, [R, V] fp32, 4-byte aligned
+ *   probs   device, [R, V] fp32, written (may not overlap logits)
+ *   1 <= R <= 2^28, 1 <= V <= 131072 (a row is held by 8 CTAs at most) */
+mxs_status spec_sampling_law(const float* logits, int64_t R, int64_t V,
+                             const mxs_sampling* sampling, float* probs,
+                             int32_t* dev_status, void* stream);
+
+/* spec_accept_logits: spec_accept on the transformed laws of logits, without
+ * writing the laws out: per-row statistics of every logit row (16 bytes each,
+ * in the workspace) are computed first, then the acceptance kernel forms each
+ * probability it needs from a logit and its row's statistics.  Results are
+ * bit-identical to spec_accept on spec_sampling_law's outputs.
+ *   target_logits  device, [B, K+1, V] fp32 (row K: the bonus position)
+ *   draft_logits   device, [B, K, V] fp32
+ *   draft, u, out_tokens, n_emitted, row_flags: as for spec_accept
+ *   workspace      device, >= spec_accept_logits_workspace_size(B, K) bytes,
+ *                  16-byte aligned
+ *   1 <= B, B * (2K + 1) <= 2^28, 0 <= K <= 32, 1 <= V <= 131072 */
+size_t spec_accept_logits_workspace_size(int64_t B, int64_t K);
+
+mxs_status spec_accept_logits(const float* target_logits, const float* draft_logits,
+                              const int32_t* draft, const float* u, int64_t B,
+                              int64_t K, int64_t V, const mxs_sampling* sampling,
+                              void* workspace, size_t workspace_bytes,
+                              int32_t* out_tokens, int32_t* n_emitted,
+                              int32_t* row_flags, int32_t* dev_status,
+                              void* stream);
 
 /* ------------------------------------------------------------------------
  * mxs_hbm_read_probe -- measurement helper (not part of the method):

@@ -24,7 +24,8 @@ from . import _build
 
 __all__ = ["build", "lib", "mxfp4_pack", "mxfp4_verify_gemm", "mxfp4_verify_gemm_workspace_size",
            "mxfp4_verify_gemm_grouped", "mxfp4_verify_gemm_grouped_workspace_size",
-           "mxfp4_verify_gemm_noalloc", "spec_accept", "hbm_read_probe", "hbm_copy_probe", "MxsError",
+           "mxfp4_verify_gemm_noalloc", "spec_accept", "spec_sampling_law", "spec_accept_logits",
+           "spec_accept_logits_workspace_size", "hbm_read_probe", "hbm_copy_probe", "MxsError",
            "DEV_FLAGS",
            "declared_symbols"]
 
@@ -75,6 +76,12 @@ def lib():
     L.mxfp4_verify_gemm_grouped.restype = i32
     L.spec_accept.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, vp, vp, vp]
     L.spec_accept.restype = i32
+    L.spec_sampling_law.argtypes = [vp, i64, i64, vp, vp, vp, vp]
+    L.spec_sampling_law.restype = i32
+    L.spec_accept_logits_workspace_size.argtypes = [i64, i64]
+    L.spec_accept_logits_workspace_size.restype = sz
+    L.spec_accept_logits.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, sz, vp, vp, vp, vp, vp]
+    L.spec_accept_logits.restype = i32
     L.mxs_hbm_read_probe.argtypes = [vp, sz, vp, vp]
     L.mxs_hbm_read_probe.restype = i32
     L.mxs_hbm_copy_probe.argtypes = [vp, vp, sz, vp]
@@ -280,6 +287,86 @@ def spec_accept(p: torch.Tensor, q: torch.Tensor, draft: torch.Tensor, u: torch.
     dev = _need_cuda(p, q, draft, u, out_tokens, n_emitted, row_flags, dev_status)
     _check(lib().spec_accept(_ptr(p), _ptr(q), _ptr(draft), _ptr(u), B, K, V, _ptr(out_tokens),
                              _ptr(n_emitted), _ptr(row_flags), _ptr(dev_status), _stream(dev)))
+    return out_tokens, n_emitted
+
+
+class _Sampling(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
+
+
+def _sampling(temperature: float, top_k: int, top_p: float) -> _Sampling:
+    if not (temperature > 0.0) or top_k < 0 or not (0.0 < top_p <= 1.0):
+        raise MxsError("need temperature > 0, top_k >= 0, 0 < top_p <= 1")
+    return _Sampling(float(temperature), int(min(top_k, 2**31 - 1)), float(top_p))
+
+
+def spec_sampling_law(logits: torch.Tensor, *, temperature: float = 1.0, top_k: int = 0, top_p: float = 1.0,
+                      out: torch.Tensor | None = None, dev_status: torch.Tensor | None = None) -> torch.Tensor:
+    """Transformed laws (temperature, top-k, top-p) of logit rows [..., V] fp32."""
+    if logits.dtype != torch.float32 or logits.dim() < 1:
+        raise MxsError("logits must be a float32 tensor [..., V]")
+    if not logits.is_contiguous():
+        raise MxsError("logits must be contiguous")
+    V = logits.shape[-1]
+    R = logits.numel() // max(V, 1)
+    if out is None:
+        out = torch.empty_like(logits)
+    elif out.dtype != torch.float32 or out.shape != logits.shape or not out.is_contiguous():
+        raise MxsError("out must be a contiguous float32 tensor shaped like logits")
+    _check_status(dev_status)
+    s = _sampling(temperature, top_k, top_p)
+    dev = _need_cuda(logits, out, dev_status)
+    _check(lib().spec_sampling_law(_ptr(logits), R, V, ctypes.addressof(s), _ptr(out), _ptr(dev_status),
+                                   _stream(dev)))
+    return out
+
+
+def spec_accept_logits_workspace_size(B: int, K: int) -> int:
+    return int(lib().spec_accept_logits_workspace_size(B, K))
+
+
+def spec_accept_logits(target_logits: torch.Tensor, draft_logits: torch.Tensor, draft: torch.Tensor,
+                       u: torch.Tensor, *, temperature: float = 1.0, top_k: int = 0, top_p: float = 1.0,
+                       workspace: torch.Tensor | None = None, out_tokens: torch.Tensor | None = None,
+                       n_emitted: torch.Tensor | None = None, row_flags: torch.Tensor | None = None,
+                       dev_status: torch.Tensor | None = None):
+    """Speculative acceptance on the transformed laws of logits.
+
+    target_logits [B, K+1, V] fp32, draft_logits [B, K, V] fp32, draft [B, K] int32,
+    u [B, K+1] fp32.  Returns (out_tokens [B, K+1] int32, n_emitted [B] int32).
+    """
+    if target_logits.dtype != torch.float32 or draft_logits.dtype != torch.float32 or u.dtype != torch.float32:
+        raise MxsError("logits and u must be float32")
+    if draft.dtype != torch.int32:
+        raise MxsError("draft must be int32")
+    if target_logits.dim() != 3:
+        raise MxsError("target_logits must be 3-D [B, K+1, V]")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    if draft_logits.shape != (B, K, V) or draft.shape != (B, K) or u.shape != (B, K + 1):
+        raise MxsError("shape mismatch: target [B,K+1,V], draft logits [B,K,V], draft [B,K], u [B,K+1]")
+    for t in (target_logits, draft_logits, draft, u):
+        if not t.is_contiguous():
+            raise MxsError("inputs must be contiguous")
+    for name, t, shape in (("out_tokens", out_tokens, (B, K + 1)), ("n_emitted", n_emitted, (B,)),
+                           ("row_flags", row_flags, (B,))):
+        if t is not None and (t.dtype != torch.int32 or tuple(t.shape) != shape):
+            raise MxsError(f"{name} must be an int32 tensor of shape {list(shape)}")
+    _check_status(dev_status)
+    s = _sampling(temperature, top_k, top_p)
+    need = spec_accept_logits_workspace_size(B, K)
+    if workspace is None:
+        workspace = _workspace(target_logits.device, need)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=target_logits.device)
+    if n_emitted is None:
+        n_emitted = torch.empty((B,), dtype=torch.int32, device=target_logits.device)
+    dev = _need_cuda(target_logits, draft_logits, draft, u, workspace, out_tokens, n_emitted, row_flags,
+                     dev_status)
+    _check(lib().spec_accept_logits(_ptr(target_logits), _ptr(draft_logits), _ptr(draft), _ptr(u), B, K, V,
+                                    ctypes.addressof(s), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _ptr(out_tokens),
+                                    _ptr(n_emitted), _ptr(row_flags), _ptr(dev_status), _stream(dev)))
     return out_tokens, n_emitted
 
 

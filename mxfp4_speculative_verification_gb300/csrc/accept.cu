@@ -33,6 +33,7 @@
 #include <climits>
 #include <cstdlib>
 
+#include "law.cuh"
 #include "mxs_device.cuh"
 #include "mxs_internal.h"
 
@@ -59,6 +60,11 @@ struct AcceptParams {
     int32_t* n_emitted;
     int32_t* row_flags;
     int32_t* status;
+    // laws given as logits (p and q then point at logit rows): each row's
+    // statistics, and 1 / temperature; p_t = law_value(logit_t, stats, inv_t)
+    const LawStats* pst;  // [B, K+1]
+    const LawStats* qst;  // [B, K]
+    float inv_t;
 };
 
 // What each CTA publishes to the others of its cluster.
@@ -90,6 +96,42 @@ __device__ __forceinline__ void load_law4(const float* __restrict__ prow,
             if (e + i < V) {
                 const float pv = prow[e + i];
                 v = use_res ? fmaxf(pv - qrow[e + i], 0.f) : pv;
+            }
+            r[i] = v;
+        }
+    }
+}
+
+// The same for laws given as logits with their row statistics (LG), or as
+// probabilities (then the same as load_law4).
+template <bool VEC, bool LG>
+__device__ __forceinline__ void load_law4x(const float* __restrict__ prow, const float* __restrict__ qrow,
+                                           bool use_res, int64_t e, int64_t V, float (&r)[4],
+                                           const LawStats& ps, const LawStats& qs, float inv_t) {
+    if constexpr (!LG) {
+        load_law4<VEC>(prow, qrow, use_res, e, V, r);
+    } else {
+        float pl[4], ql[4];
+        if (VEC && e + 3 < V) {
+            const float4 pv = __ldcs(reinterpret_cast<const float4*>(prow + e));
+            pl[0] = pv.x; pl[1] = pv.y; pl[2] = pv.z; pl[3] = pv.w;
+            if (use_res) {
+                const float4 qv = __ldcs(reinterpret_cast<const float4*>(qrow + e));
+                ql[0] = qv.x; ql[1] = qv.y; ql[2] = qv.z; ql[3] = qv.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                pl[i] = e + i < V ? prow[e + i] : -INFINITY;
+                ql[i] = (use_res && e + i < V) ? qrow[e + i] : -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float v = 0.f;
+            if (e + i < V) {
+                const float pv = law_value(pl[i], ps, inv_t);
+                v = use_res ? fmaxf(pv - law_value(ql[i], qs, inv_t), 0.f) : pv;
             }
             r[i] = v;
         }
@@ -171,6 +213,7 @@ __device__ double slice_total(const float* subsum, int n, double* wtot) {
 // gathers p_i(x_i), q_i(x_i) and u_i, tests u*q < p exactly (an fp32 x fp32
 // product is exact in double) and one ballot finds the first rejection j (K if
 // every draft survives).  Lane 0 stores j and the row's flags.
+template <bool LG = false>
 __device__ __forceinline__ void accept_drafts(const AcceptParams& P, int64_t b, int lane, int* sh_j,
                                               int* sh_flags, int* sh_err) {
     const int K = P.K;
@@ -185,8 +228,12 @@ __device__ __forceinline__ void accept_drafts(const AcceptParams& P, int64_t b, 
     } else {
         bool rej = false, zq = false;
         if (active) {
-            const float qx = P.q[(b * K + lane) * V + x];
-            const float px = P.p[(b * (K + 1) + lane) * V + x];
+            float qx = P.q[(b * K + lane) * V + x];
+            float px = P.p[(b * (K + 1) + lane) * V + x];
+            if constexpr (LG) {
+                qx = law_value(qx, P.qst[b * K + lane], P.inv_t);
+                px = law_value(px, P.pst[b * (K + 1) + lane], P.inv_t);
+            }
             const float ui = P.u[b * (K + 1) + lane];
             if (qx > 0.f) {
                 rej = !(double(ui) * double(qx) < double(px));
@@ -516,7 +563,11 @@ constexpr int64_t kRegMaxV = int64_t(kMaxCluster) * kAcceptThreads * 4 * 8;  // 
 // sub-tile from L2 for the rescan: two CTAs share an SM, and with CH = 16
 // (32768-element slices, clusters of 4 at V = 128256) four times as many rows
 // are in flight when a batch would otherwise need several waves.
-template <bool VEC, bool RELOAD, int CH>
+//
+// LG = true: the laws are given as logits with per-row statistics (law.cu),
+// and every probability is formed on the fly from them: the rows of
+// probabilities are never written.
+template <bool VEC, bool RELOAD, int CH, bool LG = false>
 __global__ void __launch_bounds__(kAcceptThreads, RELOAD ? 2 : 1)
     spec_accept_reg_kernel(const AcceptParams P) {
     constexpr int kRegChunks = CH;
@@ -538,7 +589,7 @@ __global__ void __launch_bounds__(kAcceptThreads, RELOAD ? 2 : 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (warp == 0) {
-        accept_drafts(P, b, lane, &sh_j, &sh_flags, &sh_err);
+        accept_drafts<LG>(P, b, lane, &sh_j, &sh_flags, &sh_err);
         if (lane == 0) sh_tstar = INT_MAX;
     }
     __syncthreads();
@@ -563,20 +614,26 @@ __global__ void __launch_bounds__(kAcceptThreads, RELOAD ? 2 : 1)
     const int64_t v0 = int64_t(rank) * kRegSlice;
     const float uK = P.u[b * (K + 1) + K];
     float r[kRegChunks][4];
+    LawStats ps{}, qs{};
+    if constexpr (LG) {
+        ps = P.pst[b * (K + 1) + j];
+        if (use_res) qs = P.qst[b * K + j];
+    }
 
     // Load the slice, form the sub-tile sums and exchange the slice totals.
     // Afterwards sh_S (identical bits in every CTA), sh_slice_prefix,
     // sh_all_lastpos and sh_owner are set.
     auto load_and_exchange = [&]() {
         int lp = -1;
-        // all chunks in flight at once, or (RELOAD) two batches of half as many
-        constexpr int kBatch = RELOAD ? 4 : kRegChunks;
+        // all chunks in flight at once, or (RELOAD) batches of 4 chunks (2 when
+        // each value is formed from a logit: more registers per chunk)
+        constexpr int kBatch = RELOAD ? (LG ? 2 : 4) : kRegChunks;
 #pragma unroll
         for (int i0 = 0; i0 < kRegChunks; i0 += kBatch) {
 #pragma unroll
             for (int i = i0; i < i0 + kBatch; ++i)
-                load_law4<VEC>(prow, qrow, use_res, v0 + 4 * (int64_t(i) * kAcceptThreads + threadIdx.x), V,
-                               r[i]);
+                load_law4x<VEC, LG>(prow, qrow, use_res, v0 + 4 * (int64_t(i) * kAcceptThreads + threadIdx.x), V,
+                                    r[i], ps, qs, P.inv_t);
 #pragma unroll
             for (int i = i0; i < i0 + kBatch; ++i) {
                 const float sm = warp_sum_f((r[i][0] + r[i][1]) + (r[i][2] + r[i][3]));
@@ -705,7 +762,8 @@ __global__ void __launch_bounds__(kAcceptThreads, RELOAD ? 2 : 1)
             float rr[4] = {0.f, 0.f, 0.f, 0.f};
             if constexpr (RELOAD) {
                 // the crossing sub-tile again, from L2 (read moments ago)
-                load_law4<VEC>(prow, qrow, use_res, v0 + 4 * (int64_t(ci) * kAcceptThreads + threadIdx.x), V, rr);
+                load_law4x<VEC, LG>(prow, qrow, use_res, v0 + 4 * (int64_t(ci) * kAcceptThreads + threadIdx.x), V, rr,
+                                    ps, qs, P.inv_t);
             } else {
 #pragma unroll
                 for (int i = 0; i < kRegChunks; ++i)
@@ -764,7 +822,7 @@ __global__ void __launch_bounds__(kAcceptThreads, RELOAD ? 2 : 1)
             pick = sh_all_lastpos;
             float rl[4];
             const int64_t e = int64_t(pick) & ~int64_t(3);
-            load_law4<false>(prow, qrow, use_res, e, V, rl);
+            load_law4x<false, LG>(prow, qrow, use_res, e, V, rl, ps, qs, P.inv_t);
             after = S;
             before = ff_add(S, ff_make(-rl[pick - e]));
         }
@@ -802,6 +860,54 @@ static cudaError_t sm_count(int& sms) {
     return e;
 }
 
+// One cluster of C CTAs per row.
+static cudaError_t launch_cluster(void (*kern)(AcceptParams), const AcceptParams& P, int64_t B, int C,
+                                  size_t smem, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(B * C), 1, 1);
+    cfg.blockDim = dim3(kAcceptThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = unsigned(C);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+// The register-resident kernel (V <= 131072), in one of three forms by how
+// many CTAs the batch needs (C8 = CTAs per row at 16384 elements each):
+//  * B C8 <= SMs / 2: registers kept until the rescan (one CTA per SM);
+//  * B C8 <= 2 SMs: reload form, two CTAs per SM, one wave;
+//  * beyond: reload form with 32768-element slices (clusters of 4 at
+//    V = 128256), so every row is in flight at once.
+// Measured at V = 128256: B <= 4 ~0.4 us faster with registers; B = 16
+// 19.3 -> 11.9 us (reload); B = 64 47.5 -> 25.3 (reload) -> 19.9 us (wide).
+template <bool LG>
+static cudaError_t launch_reg(const AcceptParams& P, int64_t B, int64_t V, bool vec, cudaStream_t stream) {
+    int C = int((V + kAcceptThreads * 32 - 1) / (kAcceptThreads * 32));
+    int sms = 0;
+    cudaError_t e = sm_count(sms);
+    if (e != cudaSuccess) return e;
+    const int64_t ctas = int64_t(B) * C;
+    int form = 2 * ctas <= int64_t(sms) ? 0 : (ctas <= 2 * int64_t(sms) ? 1 : 2);
+    if (const char* f = std::getenv("MXS_ACCEPT_FORM")) form = std::atoi(f) == 1 ? 1 : (std::atoi(f) == 2 ? 2 : 0);
+    if (int64_t(B) * 4 > int64_t(INT32_MAX)) return cudaErrorInvalidConfiguration;  // grid size
+    void (*kern)(AcceptParams);
+    if (form == 2) {
+        C = int((V + kAcceptThreads * 64 - 1) / (kAcceptThreads * 64));
+        kern = vec ? spec_accept_reg_kernel<true, true, 16, LG> : spec_accept_reg_kernel<false, true, 16, LG>;
+    } else if (form == 1) {
+        kern = vec ? spec_accept_reg_kernel<true, true, 8, LG> : spec_accept_reg_kernel<false, true, 8, LG>;
+    } else {
+        kern = vec ? spec_accept_reg_kernel<true, false, 8, LG> : spec_accept_reg_kernel<false, false, 8, LG>;
+    }
+    return launch_cluster(kern, P, B, C, 0, stream);
+}
+
 cudaError_t accept_run(const float* p, const float* q, const int32_t* draft, const float* u,
                        int64_t B, int64_t K, int64_t V, int32_t* out_tokens, int32_t* n_emitted,
                        int32_t* row_flags, int32_t* dev_status, cudaStream_t stream) {
@@ -824,51 +930,37 @@ cudaError_t accept_run(const float* p, const float* q, const int32_t* draft, con
     P.status = dev_status;
     const bool vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
                      (K == 0 || reinterpret_cast<uintptr_t>(q) % 16 == 0);
-    size_t smem = size_t(P.per_cta) * sizeof(float);
+    if (V <= kRegMaxV && std::getenv("MXS_ACCEPT_STREAMING") == nullptr)
+        return launch_reg<false>(P, B, V, vec, stream);
+    const size_t smem = size_t(P.per_cta) * sizeof(float);
     void (*kern)(AcceptParams) = vec ? spec_accept_kernel<true> : spec_accept_kernel<false>;
-    const bool reg = V <= kRegMaxV && std::getenv("MXS_ACCEPT_STREAMING") == nullptr;
-    if (reg) {
-        // one 16384-element slice per CTA, held in registers
-        C = int((V + kAcceptThreads * 32 - 1) / (kAcceptThreads * 32));
-        // Three forms, by how many CTAs the batch needs (C8 = CTAs per row at
-        // 16384 elements each):
-        //  * B C8 <= SMs / 2: registers kept until the rescan (one CTA per SM);
-        //  * B C8 <= 2 SMs: reload form, two CTAs per SM, one wave;
-        //  * beyond: reload form with 32768-element slices (clusters of 4 at
-        //    V = 128256), so every row is in flight at once.
-        // Measured at V = 128256: B <= 4 ~0.4 us faster with registers; B = 16
-        // 19.3 -> 11.9 us (reload); B = 64 47.5 -> 25.3 (reload) -> 19.9 us (wide).
-        int sms = 0;
-        cudaError_t e = sm_count(sms);
-        if (e != cudaSuccess) return e;
-        const int64_t ctas = int64_t(B) * C;
-        int form = 2 * ctas <= int64_t(sms) ? 0 : (ctas <= 2 * int64_t(sms) ? 1 : 2);
-        if (const char* f = std::getenv("MXS_ACCEPT_FORM")) form = std::atoi(f) == 1 ? 1 : (std::atoi(f) == 2 ? 2 : 0);
-        if (form == 2) {
-            C = int((V + kAcceptThreads * 64 - 1) / (kAcceptThreads * 64));
-            kern = vec ? spec_accept_reg_kernel<true, true, 16> : spec_accept_reg_kernel<false, true, 16>;
-        } else if (form == 1) {
-            kern = vec ? spec_accept_reg_kernel<true, true, 8> : spec_accept_reg_kernel<false, true, 8>;
-        } else {
-            kern = vec ? spec_accept_reg_kernel<true, false, 8> : spec_accept_reg_kernel<false, false, 8>;
-        }
-        smem = 0;
-    }
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(unsigned(B * C), 1, 1);
-    cfg.blockDim = dim3(kAcceptThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = unsigned(C);
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, P);
+    return launch_cluster(kern, P, B, C, smem, stream);
+}
+
+cudaError_t accept_logits_run(const float* p_logits, const float* q_logits, const LawStats* pst,
+                              const LawStats* qst, float inv_t, const int32_t* draft, const float* u,
+                              int64_t B, int64_t K, int64_t V, int32_t* out_tokens, int32_t* n_emitted,
+                              int32_t* row_flags, int32_t* dev_status, cudaStream_t stream) {
+    AcceptParams P{};
+    P.p = p_logits;
+    P.q = q_logits;
+    P.draft = draft;
+    P.u = u;
+    P.V = V;
+    P.K = int(K);
+    P.nsub = int((V + kSubTile - 1) / kSubTile);
+    P.out_tokens = out_tokens;
+    P.n_emitted = n_emitted;
+    P.row_flags = row_flags;
+    P.status = dev_status;
+    P.pst = pst;
+    P.qst = qst;
+    P.inv_t = inv_t;
+    const bool vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p_logits) % 16 == 0) &&
+                     (K == 0 || reinterpret_cast<uintptr_t>(q_logits) % 16 == 0);
+    return launch_reg<true>(P, B, V, vec, stream);
 }
 
 }  // namespace mxs

@@ -1,5 +1,6 @@
 // The C ABI of libmxs (declared in include/mxs.h): host-side validation,
 // then the launchers in gemm.cu, accept.cu and pack.cu.
+#include <cmath>
 #include <cstdint>
 #include <vector>
 
@@ -116,6 +117,61 @@ mxs_status spec_accept(const float* p, const float* q, const int32_t* draft, con
         return MXS_ERR_MISALIGNED;
     return cuda_status(mxs::accept_run(p, q, draft, u, B, K, V, out_tokens, n_emitted, row_flags,
                                        dev_status, as_stream(stream)));
+}
+
+static bool sampling_ok(const mxs_sampling* s) {
+    return s && s->temperature > 0.f && std::isfinite(s->temperature) && s->top_k >= 0 && s->top_p > 0.f &&
+           s->top_p <= 1.f;
+}
+
+static mxs::LawSampling law_sampling(const mxs_sampling* s) {
+    mxs::LawSampling l;
+    l.temperature = s->temperature;
+    l.top_k = s->top_k;
+    l.top_p = s->top_p;
+    return l;
+}
+
+mxs_status spec_sampling_law(const float* logits, int64_t R, int64_t V, const mxs_sampling* sampling,
+                             float* probs, int32_t* dev_status, void* stream) {
+    if (R < 1 || V < 1 || !logits || !probs || !sampling_ok(sampling)) return MXS_ERR_INVALID_ARG;
+    if (V > mxs::kLawMaxV || R > INT32_MAX / 8) return MXS_ERR_UNSUPPORTED;
+    if (!aligned(logits, 4) || !aligned(probs, 4) || !aligned(dev_status, 4)) return MXS_ERR_MISALIGNED;
+    return cuda_status(mxs::sampling_law_run(logits, R, V, law_sampling(sampling), probs, dev_status,
+                                             as_stream(stream)));
+}
+
+size_t spec_accept_logits_workspace_size(int64_t B, int64_t K) {
+    if (B < 1 || K < 0 || K > mxs::kAcceptMaxK || B > INT32_MAX) return 0;
+    return size_t(B) * size_t(2 * K + 1) * mxs::kLawStatsBytes;
+}
+
+mxs_status spec_accept_logits(const float* target_logits, const float* draft_logits, const int32_t* draft,
+                              const float* u, int64_t B, int64_t K, int64_t V, const mxs_sampling* sampling,
+                              void* workspace, size_t workspace_bytes, int32_t* out_tokens,
+                              int32_t* n_emitted, int32_t* row_flags, int32_t* dev_status, void* stream) {
+    if (B < 1 || K < 0 || V < 1 || !sampling_ok(sampling)) return MXS_ERR_INVALID_ARG;
+    if (B > INT32_MAX || K > mxs::kAcceptMaxK || V > mxs::kLawMaxV || B * (2 * K + 1) > INT32_MAX / 8)
+        return MXS_ERR_UNSUPPORTED;
+    if (!target_logits || !u || !out_tokens || !n_emitted) return MXS_ERR_INVALID_ARG;
+    if (K > 0 && (!draft_logits || !draft)) return MXS_ERR_INVALID_ARG;
+    if (!aligned(target_logits, 4) || !aligned(draft_logits, 4) || !aligned(draft, 4) || !aligned(u, 4) ||
+        !aligned(out_tokens, 4) || !aligned(n_emitted, 4) || !aligned(row_flags, 4) || !aligned(dev_status, 4))
+        return MXS_ERR_MISALIGNED;
+    const size_t need = spec_accept_logits_workspace_size(B, K);
+    if (!workspace || workspace_bytes < need) return MXS_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return MXS_ERR_MISALIGNED;
+    const cudaStream_t st = as_stream(stream);
+    const mxs::LawSampling ls = law_sampling(sampling);
+    mxs::LawStats* pst = static_cast<mxs::LawStats*>(workspace);
+    mxs::LawStats* qst = reinterpret_cast<mxs::LawStats*>(static_cast<char*>(workspace) +
+                                                          size_t(B) * size_t(K + 1) * mxs::kLawStatsBytes);
+    cudaError_t e = mxs::law_stats_run(target_logits, B * (K + 1), V, ls, pst, dev_status, st);
+    if (e == cudaSuccess && K > 0) e = mxs::law_stats_run(draft_logits, B * K, V, ls, qst, dev_status, st);
+    if (e == cudaSuccess)
+        e = mxs::accept_logits_run(target_logits, draft_logits, pst, qst, 1.0f / sampling->temperature, draft,
+                                   u, B, K, V, out_tokens, n_emitted, row_flags, dev_status, st);
+    return cuda_status(e);
 }
 
 mxs_status mxs_hbm_read_probe(const void* src, size_t bytes, uint64_t* sink, void* stream) {

@@ -53,6 +53,31 @@ cudaError_t accept_run(const float* p, const float* q, const int32_t* draft, con
                        int32_t* n_emitted, int32_t* row_flags, int32_t* dev_status,
                        cudaStream_t stream);
 
+// ---------------------------------------------------- sampling laws
+struct LawStats;
+constexpr int64_t kLawMaxV = int64_t(1) << 17;  // 131072: a row per cluster of 8 CTAs, in registers
+
+struct LawSampling {
+    float temperature;  // > 0
+    int64_t top_k;      // 0 (or >= V): off
+    float top_p;        // (0, 1]; 1: off
+};
+
+// The transformed laws of R logit rows, written out ([R, V] fp32).
+cudaError_t sampling_law_run(const float* logits, int64_t R, int64_t V, const LawSampling& s, float* probs,
+                             int32_t* dev_status, cudaStream_t stream);
+// Their per-row statistics only (`stats` holds R entries of 16 bytes).
+cudaError_t law_stats_run(const float* logits, int64_t R, int64_t V, const LawSampling& s, LawStats* stats,
+                          int32_t* dev_status, cudaStream_t stream);
+constexpr size_t kLawStatsBytes = 16;
+
+// Acceptance on laws given as logits + per-row statistics (the kernels of
+// accept.cu evaluate each probability on the fly).
+cudaError_t accept_logits_run(const float* p_logits, const float* q_logits, const LawStats* pst,
+                              const LawStats* qst, float inv_t, const int32_t* draft, const float* u,
+                              int64_t B, int64_t K, int64_t V, int32_t* out_tokens, int32_t* n_emitted,
+                              int32_t* row_flags, int32_t* dev_status, cudaStream_t stream);
+
 // ---------------------------------------------------------------- pack
 cudaError_t pack_run(const void* w, int w_dtype, int64_t N, int64_t K, uint8_t* nibbles,
                      uint8_t* scales, int32_t* dev_status, cudaStream_t stream);

@@ -122,3 +122,27 @@ def test_hbm_probes_reject_bad_arguments_on_host(L):
     assert copy(FAKE, FAKE + 2048, 4096, None) == 1            # overlapping buffers
     assert read(FAKE, 0, FAKE, None) == 1
     assert read(FAKE + 4, 4096, FAKE, None) == 2
+
+
+def test_law_calls_reject_bad_arguments_on_host(L):
+    # fake, never-dereferenced device pointers: every case fails validation first
+    p = ctypes.c_void_p(4096)
+    s = mxs._Sampling(1.0, 0, 1.0)
+    ok = ctypes.addressof(s)
+    assert L.spec_sampling_law(p, 4, 1000, ok, None, None, None) == 1  # no output
+    for bad in (mxs._Sampling(0.0, 0, 1.0), mxs._Sampling(1.0, -1, 1.0), mxs._Sampling(1.0, 0, 0.0),
+                mxs._Sampling(1.0, 0, 1.5), mxs._Sampling(float("inf"), 0, 1.0)):
+        assert L.spec_sampling_law(p, 4, 1000, ctypes.addressof(bad), p, None, None) == 1
+    assert L.spec_sampling_law(p, 4, 131073, ok, p, None, None) == 3  # beyond one cluster per row
+    assert L.spec_sampling_law(ctypes.c_void_p(4098), 4, 1000, ok, p, None, None) == 2
+    assert L.spec_accept_logits_workspace_size(2, 4) == 2 * 9 * 16
+    assert L.spec_accept_logits_workspace_size(0, 4) == 0
+    ws = L.spec_accept_logits_workspace_size(2, 4)
+    args = lambda **k: [k.get("tl", p), k.get("dl", p), k.get("d", p), k.get("u", p), k.get("B", 2), k.get("K", 4),
+                        k.get("V", 1000), k.get("s", ok), k.get("ws", p), k.get("wsb", ws), p, p, None, None, None]
+    assert L.spec_accept_logits(*args(wsb=ws - 1)) == 5
+    assert L.spec_accept_logits(*args(ws=None)) == 5
+    assert L.spec_accept_logits(*args(K=33)) == 3
+    assert L.spec_accept_logits(*args(V=200000)) == 3
+    assert L.spec_accept_logits(*args(dl=None)) == 1
+    assert L.spec_accept_logits(*args(ws=ctypes.c_void_p(4104))) == 2
