@@ -20,6 +20,8 @@ What each entry point follows (page title, section):
 * ``spec_accept`` -- Module 11 §4 (left-to-right acceptance, residual
   norm((p-q)+), bonus token) and §5 (strict "draw < acceptance", acceptance 0
   where q = 0).
+* ``e4m3_value`` / ``nvfp4_dequant`` / ``nvfp4_gemm`` -- Module 11 §12 (NVFP4:
+  16 E2M1 values per E4M3 scale, one FP32 scale per tensor).
 * ``sampling_law`` -- Module 11 §4 (the laws acceptance uses are the ones
   tokens are actually sampled from: temperature, then top-k, then top-p, on
   the target and the draft alike).
@@ -76,6 +78,12 @@ def _load():
     lib.mxs_oracle_gemm.restype = ctypes.c_int
     lib.mxs_oracle_pack.argtypes = [p, i64, i64, p, p]
     lib.mxs_oracle_pack.restype = ctypes.c_int
+    lib.mxs_oracle_e4m3_value.argtypes = [ctypes.c_int]
+    lib.mxs_oracle_e4m3_value.restype = ctypes.c_double
+    lib.mxs_oracle_nvfp4_dequant.argtypes = [p, p, ctypes.c_double, i64, i64, p]
+    lib.mxs_oracle_nvfp4_dequant.restype = ctypes.c_int
+    lib.mxs_oracle_nvfp4_gemm.argtypes = [p, p, p, ctypes.c_double, i64, i64, i64, p]
+    lib.mxs_oracle_nvfp4_gemm.restype = ctypes.c_int
     lib.mxs_oracle_sampling_law.argtypes = [p, i64, i64, ctypes.c_double, i64, ctypes.c_double, p, p, p]
     lib.mxs_oracle_sampling_law.restype = ctypes.c_int
     for name in ("mxs_oracle_spec_accept", "mxs_oracle_spec_accept_f64"):
@@ -215,3 +223,34 @@ def sampling_law(logits: np.ndarray, temperature: float = 1.0, top_k: int = 0, t
     if rc:
         raise ValueError(f"oracle sampling_law failed ({rc})")
     return probs.reshape(shape), margin.reshape(shape[:-1]), kept.reshape(shape[:-1])
+
+
+def e4m3_value(code: int) -> float:
+    return _load().mxs_oracle_e4m3_value(int(code))
+
+
+def nvfp4_dequant(nibbles: np.ndarray, scales: np.ndarray, global_scale: float) -> np.ndarray:
+    """NVFP4 [N, K/2] nibbles + [N, K/16] E4M3 scales + FP32 tensor scale -> float64 [N, K]."""
+    nib = _c(nibbles, np.uint8)
+    sc = _c(scales, np.uint8)
+    N, half = nib.shape
+    K = 2 * half
+    assert sc.shape == (N, K // 16)
+    w = np.empty((N, K), dtype=np.float64)
+    if _load().mxs_oracle_nvfp4_dequant(_ptr(nib), _ptr(sc), float(global_scale), N, K, _ptr(w)):
+        raise ValueError("oracle nvfp4_dequant failed")
+    return w
+
+
+def nvfp4_gemm(x_bf16_bits: np.ndarray, nibbles: np.ndarray, scales: np.ndarray, global_scale: float) -> np.ndarray:
+    """Y[M, N] (float64) = X (bf16 bits [M, K]) . nvfp4_dequant(W)^T."""
+    x = _c(x_bf16_bits, np.uint16)
+    nib = _c(nibbles, np.uint8)
+    sc = _c(scales, np.uint8)
+    M, K = x.shape
+    N = nib.shape[0]
+    assert nib.shape == (N, K // 2) and sc.shape == (N, K // 16)
+    y = np.empty((M, N), dtype=np.float64)
+    if _load().mxs_oracle_nvfp4_gemm(_ptr(x), _ptr(nib), _ptr(sc), float(global_scale), M, N, K, _ptr(y)):
+        raise ValueError("oracle nvfp4_gemm failed")
+    return y

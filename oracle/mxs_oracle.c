@@ -545,3 +545,57 @@ int mxs_oracle_sampling_law(const float* logits, int64_t R, int64_t V, double te
     free(e);
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* NVFP4 ([M11] §12)                                                    */
+/* ------------------------------------------------------------------ */
+/*
+ * [M11] §12: NVFP4 holds E2M1 values in blocks of 16 that share an E4M3
+ * scale, with one FP32 scale for the whole tensor (4.5 bits per value
+ * counting the local scale).  E4M3: one sign bit, four exponent bits (bias
+ * 7), three fraction bits, exponent field 0 subnormal.  Reading where the page
+ * is silent: the two codes with every exponent and fraction bit set (0x7F,
+ * 0xFF) are NaN and there is no infinity (the usual E4M3 convention); a scale
+ * may carry a sign; the layout is nibbles [N, K/2] as for MXFP4 and scales
+ * [N, K/16], one byte per 16 consecutive k of a row.
+ */
+double mxs_oracle_e4m3_value(int code) {
+    code &= 0xFF;
+    const int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+int mxs_oracle_nvfp4_dequant(const uint8_t* nibbles, const uint8_t* scales, double global_scale,
+                             int64_t N, int64_t K, double* w) {
+    if (N < 0 || K < 0 || K % 16) return 1;
+    for (int64_t n = 0; n < N; ++n) {
+        const uint8_t* row = nibbles + n * (K / 2);
+        for (int64_t k = 0; k < K; ++k) {
+            const double s = mxs_oracle_e4m3_value(scales[n * (K / 16) + k / 16]);
+            w[n * K + k] = mxs_oracle_e2m1_value(nibble_of(row, k)) * s * global_scale;
+        }
+    }
+    return 0;
+}
+
+/* Y[m, n] = sum_k x[m, k] * w[n, k] with w the NVFP4 dequantisation, in
+ * double, k in order (single-threaded: the shapes tested are small). */
+int mxs_oracle_nvfp4_gemm(const uint16_t* x_bf16, const uint8_t* nibbles, const uint8_t* scales,
+                          double global_scale, int64_t M, int64_t N, int64_t K, double* y) {
+    if (M < 0 || N < 0 || K < 0 || K % 16) return 1;
+    for (int64_t n = 0; n < N; ++n) {
+        const uint8_t* row = nibbles + n * (K / 2);
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double s = mxs_oracle_e4m3_value(scales[n * (K / 16) + k / 16]);
+                const double w = mxs_oracle_e2m1_value(nibble_of(row, k)) * s * global_scale;
+                acc += bf16_to_double(x_bf16[m * K + k]) * w;
+            }
+            y[m * N + n] = acc;
+        }
+    }
+    return 0;
+}
