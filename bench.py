@@ -51,11 +51,11 @@ FALLBACK_HBM_GBS = 6800.0
 # sources).
 GEMM_TRAFFIC = {
     # mxfp4_gemm_kernel, passes of <= 8 rows: lm_head 4096 x 128256 at M=5
-    "mma": {"ratio": 1.0046, "sha": "9be8dc3ecbe78824"},
+    "mma": {"ratio": 1.0049, "sha": "ed7d8461370ecdec"},
     # mxfp4_gemm_bs_kernel, kind::mxf8f6f4 (passes of 33..64 rows): lm_head at M=64
-    "bs8": {"ratio": 0.9175, "sha": "52c5d9d2a16da9bf"},
+    "bs8": {"ratio": 0.9171, "sha": "ccc56ef6a2c1e0c7"},
     # mxfp4_gemm_bs_kernel, kind::mxf4 (passes of 9..32 rows): lm_head at M=20
-    "bs4": {"ratio": 0.9853, "sha": "52c5d9d2a16da9bf"},
+    "bs4": {"ratio": 0.9853, "sha": "ccc56ef6a2c1e0c7"},
 }
 BS_MIN_ROWS = 9     # passes of at least this many rows run on the block-scaled kernel
 BS4_MAX_ROWS = 32   # its mxf4 kind takes passes of up to this many rows
@@ -534,7 +534,7 @@ def run_mxs(args, world, rank, local):
 
     # the other configurations, each timed the same way (weights of the same
     # stack reused; the 70B stack generated once on the device)
-    sweep, acc_sweep = [], None
+    sweep, acc_sweep, logits_acc, nv = [], None, None, None
     if not args.no_sweep and rank == 0 and world == 1:
         wcache = {model: weights}
         clocks2 = ClockSampler(local)
@@ -553,6 +553,8 @@ def run_mxs(args, world, rank, local):
         del wcache
         torch.cuda.empty_cache()
         acc_sweep = accept_sweep_rows(mxs, torch, dev, peak)
+        logits_acc = logits_accept_rows(mxs, torch, dev, peak)
+        nv = nvfp4_rows(mxs, torch, dev, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -602,6 +604,8 @@ def run_mxs(args, world, rank, local):
         "peaks_in_process": inproc,
         "sweep": sweep,
         "accept_sweep": acc_sweep,
+        "accept_logits": logits_acc,
+        "nvfp4_lm_head": nv,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -728,11 +732,24 @@ def profile_target(args):
     M = args.profile_m or B * (K_spec + 1)
     if args.profile_gemm:
         K, N = (int(v) for v in args.profile_gemm.split(","))
-        nib, sc = workloads.device_mxfp4_weights(N, K, *workloads.LLAMA_EXP_RANGE, seed=0, device=dev)
         x = workloads.device_bf16_normal(M, K, seed=1, device=dev)
         y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        if args.profile_nvfp4:
+            nib, sc = workloads.device_nvfp4_weights(N, K, seed=0, device=dev)
+            for _ in range(4):
+                mxs.nvfp4_verify_gemm(x, nib, sc, 0.0731, out=y)
+        else:
+            nib, sc = workloads.device_mxfp4_weights(N, K, *workloads.LLAMA_EXP_RANGE, seed=0, device=dev)
+            for _ in range(4):
+                mxs.mxfp4_verify_gemm(x, nib, sc, out=y)
+    elif args.profile_law:
+        # the sampling law of the workload's B (K + 1) target rows, T = 0.8, top-p 0.9
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(0)
+        logits = torch.randn((B * (K_spec + 1), workloads.VOCAB_LLAMA), generator=gen, device=dev) * 3.0
+        out = torch.empty_like(logits)
         for _ in range(4):
-            mxs.mxfp4_verify_gemm(x, nib, sc, out=y)
+            mxs.spec_sampling_law(logits, out=out, **LOGITS_SAMPLING)
     else:
         V = workloads.VOCAB_LLAMA
         p, q, d, u = (torch.from_numpy(a).to(dev) for a in workloads.spec_inputs(
@@ -806,6 +823,95 @@ def accept_sweep_rows(mxs, torch, dev, peak, max_rounds=1500):
             "rows": rows}
 
 
+LOGITS_SAMPLING = {"temperature": 0.8, "top_k": 0, "top_p": 0.9}
+
+
+def logits_accept_rows(mxs, torch, dev, peak, reps=20):
+    """Acceptance from logits (laws formed on the device, temperature 0.8 and
+    top-p 0.9 on the target and the draft alike), B = 1 / 16 / 64, K = 4,
+    V = 128256.  Target logits N(0, 3), draft logits = target + N(0, 0.4),
+    drafts sampled from the draft's transformed law.  Algorithmic bytes: every
+    logit row read once (the statistics pass) plus the rows the acceptance
+    reads again (the rejected position's pair, or the bonus row), ids,
+    uniforms and outputs."""
+    V, K = workloads.VOCAB_LLAMA, 4
+    rows = []
+    for B in (1, 16, 64):
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(300 + B)
+        tl = torch.randn((B, K + 1, V), generator=gen, device=dev) * 3.0
+        dl = tl[:, :K] + torch.randn((B, K, V), generator=gen, device=dev) * 0.4
+        q = mxs.spec_sampling_law(dl.contiguous(), **LOGITS_SAMPLING)
+        d = torch.multinomial(q.view(B * K, V), 1, generator=gen).view(B, K).to(torch.int32)
+        u = torch.rand((B, K + 1), generator=gen, device=dev)
+        dlc = dl.contiguous()
+        ws = torch.empty(mxs.spec_accept_logits_workspace_size(B, K), dtype=torch.uint8, device=dev)
+        out_tok = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+        n_emit = torch.empty((B,), dtype=torch.int32, device=dev)
+        call = lambda: mxs.spec_accept_logits(tl, dlc, d, u, workspace=ws, out_tokens=out_tok, n_emitted=n_emit,
+                                              **LOGITS_SAMPLING)
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        n = n_emit.cpu().numpy()
+        nb = 4 * B * (2 * K + 1) * V + accept_bytes(B, K, V, n)
+        rows.append({"B": B, "K": K, "us_per_call": us, "rows_per_s": B / (us * 1e-6),
+                     "mean_emitted": float(n.mean()), "bytes_per_call": nb,
+                     "hbm_gbs": nb / (us * 1e-6) / 1e9, "pct_of_peak": nb / (us * 1e-6) / 1e9 / peak})
+        del tl, dl, dlc, q, d, u, ws
+    return {"metric": "spec_accept_logits: laws from logits (statistics pass + acceptance), us per call",
+            "V": V, "sampling": LOGITS_SAMPLING, "rows": rows}
+
+
+def nvfp4_rows(mxs, torch, dev, peak, reps=20):
+    """The lm_head of the 8B stack (K = 4096, N = 128256) on NVFP4 weights
+    (E4M3 scale per 16 elements, one FP32 tensor scale) at M = 5 / 20 / 64,
+    beside the same shape on MXFP4.  Weights and scales (296 MB NVFP4) exceed
+    L2, so back-to-back calls stream them from HBM.  Algorithmic bytes:
+    nibbles + scale bytes + X (bf16) + Y (fp32)."""
+    N, K = workloads.VOCAB_LLAMA, 4096
+    nib, sc = workloads.device_nvfp4_weights(N, K, seed=71, device=dev)
+    mnib, msc = workloads.device_mxfp4_weights(N, K, *workloads.LLAMA_EXP_RANGE, seed=71, device=dev)
+    rows = []
+    for M in (5, 20, 64):
+        x = workloads.device_bf16_normal(M, K, seed=72 + M, device=dev)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        for fmt in ("nvfp4", "mxfp4"):
+            if fmt == "nvfp4":
+                ws = torch.empty(mxs.nvfp4_verify_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+                call = lambda: mxs.nvfp4_verify_gemm(x, nib, sc, 0.0731, out=y, workspace=ws)
+                nb = N * K // 2 + N * K // 16 + M * K * 2 + M * N * 4
+            else:
+                ws = torch.empty(mxs.mxfp4_verify_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+                call = lambda: mxs.mxfp4_verify_gemm(x, mnib, msc, out=y, workspace=ws)
+                nb = gemm_bytes(M, N, K)
+            for _ in range(5):
+                call()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                call()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            rows.append({"format": fmt, "M": M, "us_per_call": us, "bytes_per_call": nb,
+                         "hbm_gbs": nb / (us * 1e-6) / 1e9, "pct_of_peak": nb / (us * 1e-6) / 1e9 / peak})
+            del ws
+        del x, y
+    del nib, sc, mnib, msc
+    torch.cuda.empty_cache()
+    return {"metric": "lm_head GEMM (K=4096, N=128256), one call incl. X preparation, us per call",
+            "rows": rows}
+
+
 def accept_sweep(args):
     """The acceptance-heavy sweep alone, as its own JSON line."""
     import torch
@@ -837,6 +943,10 @@ def main():
                          "and exit; a small target for ncu captures")
     ap.add_argument("--profile-m", type=int, default=0,
                     help="rows of the --profile-gemm call (default: the workload's M)")
+    ap.add_argument("--profile-nvfp4", action="store_true",
+                    help="with --profile-gemm: NVFP4 weights (nvfp4_verify_gemm) instead of MXFP4")
+    ap.add_argument("--profile-law", action="store_true",
+                    help="only run spec_sampling_law on the workload's target rows 4 times and exit (ncu target)")
     ap.add_argument("--profile-accept", action="store_true",
                     help="only run spec_accept of the workload 4 times and exit (ncu target)")
     ap.add_argument("--accept-sweep", action="store_true",
@@ -846,7 +956,7 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup(args)
-    if args.profile_gemm or args.profile_accept:
+    if args.profile_gemm or args.profile_accept or args.profile_law:
         profile_target(args)
         return
     if args.accept_sweep:

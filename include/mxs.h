@@ -6,8 +6,12 @@
  *
  *   mxfp4_pack         real weights -> E2M1 nibbles + E8M0 block scales
  *   mxfp4_verify_gemm  Y[M,N] = X[M,K] . dequant(W)^T, bf16 X, fp32 Y
+ *                      (also grouped, without workspace, and on NVFP4
+ *                      weights: nvfp4_verify_gemm)
  *   spec_accept        left-to-right acceptance, residual / bonus sampling,
- *                      emission of 1..K+1 tokens per sequence
+ *                      emission of 1..K+1 tokens per sequence (also from
+ *                      logits under temperature / top-k / top-p:
+ *                      spec_accept_logits, spec_sampling_law)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -138,6 +142,45 @@ mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles,
                              int64_t N, int64_t K, void* workspace,
                              size_t workspace_bytes, int32_t* dev_status,
                              void* stream);
+
+/* ------------------------------------------------------------------------
+ * nvfp4_verify_gemm -- the verify GEMM on NVFP4 weights
+ *
+ * Format ("Module 11. Speculative Decoding and Quantization", §12, NVFP4):
+ * E2M1 codes as for MXFP4 (element k of row n in byte k/2 of [N, K/2], even k
+ * in the low nibble), but each run of 16 consecutive elements along K shares
+ * one E4M3 scale byte (sign | 4 exponent bits, bias 7 | 3 fraction bits;
+ * subnormals at exponent field 0; 0x7F and 0xFF are NaN; largest finite 448),
+ * and the whole tensor one FP32 scale g:
+ *   Y[m, n] = g * sum_k x[m, k] * e2m1(W[n, k]) * e4m3(S[n, k/16]).
+ *
+ *   x            device, [M, K] bf16 (raw bits as uint16), 2-byte aligned
+ *   nibbles      device, [N, K/2] uint8, 16-byte aligned
+ *   scales       device, [N, K/16] uint8 E4M3 (any alignment; copied to the
+ *                workspace first when K % 256 != 0 or not 16-byte aligned;
+ *                with K % 256 == 0 a misaligned `scales` is rejected,
+ *                MXS_ERR_MISALIGNED)
+ *   global_scale the tensor's FP32 scale g, applied to every output
+ *   y            device, [M, N] fp32, 4-byte aligned, written
+ *   sizes        as for mxfp4_verify_gemm (K % 32 == 0)
+ *   workspace    device, >= nvfp4_verify_gemm_workspace_size(M, N, K) bytes,
+ *                16-byte aligned; not shared by two calls in flight
+ *
+ * Kernel and accuracy: passes of at most 64 rows on the mma.sync kernel; each
+ * decoded E2M1 code is multiplied by its block's E4M3 scale in fp16 (exact:
+ * the product has at most 6 significant bits and lies in [2^-10, 2688]),
+ * x as for mxfp4_verify_gemm's mma.sync path (exact for every element within
+ * 2^29 of its row maximum), fp32 sums over all of K, then one rounding for g.
+ * A NaN scale gives NaN in its row n; a row of x holding Inf or NaN a row of
+ * NaN.
+ * ---------------------------------------------------------------------- */
+size_t nvfp4_verify_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+mxs_status nvfp4_verify_gemm(const void* x, const uint8_t* nibbles,
+                             const uint8_t* scales, float global_scale,
+                             float* y, int64_t M, int64_t N, int64_t K,
+                             void* workspace, size_t workspace_bytes,
+                             int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
  * mxfp4_verify_gemm_grouped -- many independent verify GEMMs in one go

@@ -1,10 +1,13 @@
 """Python binding of libmxs: MXFP4 speculative verification on GB300 (sm_103a).
 
-The three calls of the C ABI (``include/mxs.h``) under the same names:
+The calls of the C ABI (``include/mxs.h``) under the same names:
 
 * :func:`mxfp4_pack` -- real weights -> E2M1 nibbles + E8M0 scales;
-* :func:`mxfp4_verify_gemm` -- Y = X . dequant(W)^T, bf16 X, fp32 Y;
-* :func:`spec_accept` -- acceptance, residual / bonus sampling, emission.
+* :func:`mxfp4_verify_gemm` -- Y = X . dequant(W)^T, bf16 X, fp32 Y (also
+  grouped, without workspace, and :func:`nvfp4_verify_gemm` on NVFP4 weights);
+* :func:`spec_accept` -- acceptance, residual / bonus sampling, emission
+  (also :func:`spec_accept_logits` from logits under temperature / top-k /
+  top-p, and :func:`spec_sampling_law` for the law itself).
 
 This module only marshals arguments: it checks dtypes, shapes and devices,
 allocates the output tensors with torch, and passes raw device pointers and
@@ -24,7 +27,8 @@ from . import _build
 
 __all__ = ["build", "lib", "mxfp4_pack", "mxfp4_verify_gemm", "mxfp4_verify_gemm_workspace_size",
            "mxfp4_verify_gemm_grouped", "mxfp4_verify_gemm_grouped_workspace_size",
-           "mxfp4_verify_gemm_noalloc", "spec_accept", "spec_sampling_law", "spec_accept_logits",
+           "mxfp4_verify_gemm_noalloc", "nvfp4_verify_gemm", "nvfp4_verify_gemm_workspace_size",
+           "spec_accept", "spec_sampling_law", "spec_accept_logits",
            "spec_accept_logits_workspace_size", "hbm_read_probe", "hbm_copy_probe", "MxsError",
            "DEV_FLAGS",
            "declared_symbols"]
@@ -70,6 +74,10 @@ def lib():
     L.mxfp4_verify_gemm_workspace_size.restype = sz
     L.mxfp4_verify_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, sz, vp, vp]
     L.mxfp4_verify_gemm.restype = i32
+    L.nvfp4_verify_gemm_workspace_size.argtypes = [i64, i64, i64]
+    L.nvfp4_verify_gemm_workspace_size.restype = sz
+    L.nvfp4_verify_gemm.argtypes = [vp, vp, vp, ctypes.c_float, vp, i64, i64, i64, vp, sz, vp, vp]
+    L.nvfp4_verify_gemm.restype = i32
     L.mxfp4_verify_gemm_grouped_workspace_size.argtypes = [vp, i32, i64]
     L.mxfp4_verify_gemm_grouped_workspace_size.restype = sz
     L.mxfp4_verify_gemm_grouped.argtypes = [vp, i32, i64, vp, sz, vp, vp]
@@ -166,16 +174,17 @@ def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
 
 
 def _gemm_shapes(x: torch.Tensor, nibbles: torch.Tensor, scales: torch.Tensor,
-                 out: torch.Tensor | None, dev_status: torch.Tensor | None):
-    """Check the GEMM operands (the C side cannot see buffer extents); returns (M, N, K)."""
+                 out: torch.Tensor | None, dev_status: torch.Tensor | None, block: int = 32):
+    """Check the GEMM operands (the C side cannot see buffer extents); returns
+    (M, N, K).  block: elements per scale byte (32 MXFP4, 16 NVFP4)."""
     if x.dtype != torch.bfloat16 or x.dim() != 2:
         raise MxsError("x must be a 2-D bfloat16 tensor [M, K]")
     if nibbles.dtype != torch.uint8 or scales.dtype != torch.uint8 or nibbles.dim() != 2:
         raise MxsError("nibbles and scales must be 2-D uint8 tensors")
     M, K = x.shape
     N = nibbles.shape[0]
-    if K % 32 != 0 or nibbles.shape != (N, K // 2) or scales.shape != (N, K // 32):
-        raise MxsError("W shapes must be [N, K/2] and [N, K/32] with K % 32 == 0")
+    if K % 32 != 0 or nibbles.shape != (N, K // 2) or scales.shape != (N, K // block):
+        raise MxsError(f"W shapes must be [N, K/2] and [N, K/{block}] with K % 32 == 0")
     if out is not None and (out.dtype != torch.float32 or tuple(out.shape) != (M, N)):
         raise MxsError("out must be a float32 tensor [M, N]")
     _check_status(dev_status)
@@ -203,6 +212,32 @@ def mxfp4_verify_gemm(x: torch.Tensor, nibbles: torch.Tensor, scales: torch.Tens
     if workspace is None:
         workspace = _workspace(dev, need)
     _check(lib().mxfp4_verify_gemm(_ptr(x), _ptr(nibbles), _ptr(scales), _ptr(out), M, N, K,
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _ptr(dev_status), _stream(dev)))
+    return out
+
+
+def nvfp4_verify_gemm_workspace_size(M: int, N: int, K: int) -> int:
+    return int(lib().nvfp4_verify_gemm_workspace_size(M, N, K))
+
+
+def nvfp4_verify_gemm(x: torch.Tensor, nibbles: torch.Tensor, scales: torch.Tensor, global_scale: float = 1.0,
+                      *, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                      dev_status: torch.Tensor | None = None) -> torch.Tensor:
+    """Y[M, N] (fp32) = global_scale * X[M, K] (bf16) . dequant(W)^T for NVFP4 W
+    ([N, K/2] E2M1 nibbles + [N, K/16] E4M3 scale bytes)."""
+    M, N, K = _gemm_shapes(x, nibbles, scales, out, dev_status, block=16)
+    if workspace is not None and workspace.dtype != torch.uint8:
+        raise MxsError("workspace must be a uint8 tensor")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    dev = _need_cuda(x, nibbles, scales, out, workspace, dev_status)
+    need = nvfp4_verify_gemm_workspace_size(M, N, K)
+    if need == 0:
+        raise MxsError("unsupported GEMM shape")
+    if workspace is None:
+        workspace = _workspace(dev, need)
+    _check(lib().nvfp4_verify_gemm(_ptr(x), _ptr(nibbles), _ptr(scales), float(global_scale), _ptr(out), M, N, K,
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _ptr(dev_status), _stream(dev)))
     return out

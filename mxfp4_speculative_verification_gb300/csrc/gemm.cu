@@ -114,17 +114,18 @@ static size_t bs_x_bytes(int64_t mc, int64_t K) {
     return size_t((K + 255) / 256) * size_t(per_stage);
 }
 
-GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales_aligned) {
+GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales_aligned, int sdiv) {
     GemmWorkspace w{};
-    const int64_t nblk = K / 32;
+    const bool nv = sdiv == 16;  // NVFP4: scale bytes per 16 k, mma.sync passes only
+    const int64_t nblk = K / sdiv;
     const int64_t mc = std::min<int64_t>(M, kGemmMaxRowsPerPass);
     const int64_t mcb = std::min<int64_t>(M, kBsMaxNpad);
-    w.repack_scales = !(K % 512 == 0 && scales_aligned);
+    w.repack_scales = !(K % (16 * sdiv) == 0 && scales_aligned);
     w.sc_pitch = w.repack_scales ? int(align_up(size_t(nblk), 16)) : int(nblk);
     size_t off = 0;
     w.xf_off = off;
     off = align_up(off + std::max(size_t(kGemmMaxRowsPerPass) * align_up(size_t(K), 512) * 2,
-                                  bs_may_run(M, K) ? bs_x_bytes(mcb, K) : size_t(0)),
+                                  !nv && bs_may_run(M, K) ? bs_x_bytes(mcb, K) : size_t(0)),
                    256);
     w.xun_off = off;
     off = align_up(off + kBsMaxNpad * sizeof(float), 256);
@@ -138,7 +139,7 @@ GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales
             part = std::max<int64_t>(part, cap * mc * bn);
         }
     }
-    if (bs_may_run(M, K)) {
+    if (!nv && bs_may_run(M, K)) {
         const int64_t cap = bs_split_items_cap(N, K);
         if (cap > 0) {
             ncnt = std::max<int64_t>(ncnt, 4 * ((N + kBsRows - 1) / kBsRows));
@@ -261,6 +262,8 @@ struct HostGemm {
     int* counters;
     int64_t N, K;
     int64_t items_cap;   // 0: never split K
+    int sdiv = 32;       // k per scale byte: 32 (MXFP4, E8M0) or 16 (NVFP4, E4M3)
+    float gscale = 1.f;  // NVFP4 tensor scale
 };
 
 // Fill the launch's problem table for tiles of BN rows.
@@ -295,6 +298,7 @@ static cudaError_t build_problems(ProblemSet<G>& S, const HostGemm* gs, int coun
         p.sc_from_prep = h.sc_from_prep ? 1 : 0;
         p.sc = h.sc;
         p.sc_pitch = h.sc_pitch;
+        p.gscale = h.gscale;
         const int sblk = bs ? kBsStageBlocks : kStageBlocks;
         const int stages_total = (p.nblk + sblk - 1) / sblk;
         p.nsplit = 1;
@@ -328,7 +332,8 @@ static cudaError_t build_problems(ProblemSet<G>& S, const HostGemm* gs, int coun
         }
         if (!make_map(&p.tm_w, h.nib, h.N, h.K / 2, h.K / 2, kBoxBytes, uint32_t(BN), true))
             return cudaErrorInvalidValue;
-        if (!make_map(&p.tm_s, h.sc, h.N, p.nblk, h.sc_pitch, 16, uint32_t(BN), false))
+        // one 16-byte (MXFP4) or 32-byte (NVFP4) column of scales per 512-k stage
+        if (!make_map(&p.tm_s, h.sc, h.N, h.K / h.sdiv, h.sc_pitch, h.sdiv == 16 ? 32 : 16, uint32_t(BN), false))
             return cudaErrorInvalidValue;
     }
     S.items = int(items);
@@ -375,11 +380,11 @@ static cudaError_t launch_persistent(Kern kern, const Set& S, int threads, int s
     return cudaLaunchKernelEx(&cfg, kern, S);
 }
 
-template <int NT, int RG, int KW, int STAGES, int G>
+template <int NT, int RG, int KW, int STAGES, int G, bool NV = false>
 static cudaError_t launch_main(const HostGemm* gs, int count, int M, int32_t* status,
                                int* sched, cudaStream_t stream) {
-    using C = GemmCfg<NT, RG, KW, STAGES>;
-    auto kern = mxfp4_gemm_kernel<NT, RG, KW, STAGES, G>;
+    using C = GemmCfg<NT, RG, KW, STAGES, NV>;
+    auto kern = mxfp4_gemm_kernel<NT, RG, KW, STAGES, G, NV>;
     static LaunchFacts facts;
     int sms = 0, occ = 0;
     cudaError_t err = launch_facts(facts, kern, C::kThreads, C::kSmemBytes, sms, occ);
@@ -404,15 +409,15 @@ static cudaError_t launch_main(const HostGemm* gs, int count, int M, int32_t* st
 }
 
 // Kernel shape for a pass of M <= 64 rows: NT fragment tiles of 8 rows.
-template <int G>
+template <int G, bool NV = false>
 static cudaError_t launch_main_nt(int NT, const HostGemm* gs, int count, int M, int32_t* status,
                                   int* sched, cudaStream_t stream) {
     switch (NT) {
-        case 1: return launch_main<1, 4, 2, 4, G>(gs, count, M, status, sched, stream);
-        case 2: return launch_main<2, 4, 2, 3, G>(gs, count, M, status, sched, stream);
-        case 3: return launch_main<3, 8, 2, 3, G>(gs, count, M, status, sched, stream);
-        case 4: return launch_main<4, 8, 2, 2, G>(gs, count, M, status, sched, stream);
-        default: return launch_main<8, 4, 2, 2, G>(gs, count, M, status, sched, stream);
+        case 1: return launch_main<1, 4, 2, 4, G, NV>(gs, count, M, status, sched, stream);
+        case 2: return launch_main<2, 4, 2, 3, G, NV>(gs, count, M, status, sched, stream);
+        case 3: return launch_main<3, 8, 2, 3, G, NV>(gs, count, M, status, sched, stream);
+        case 4: return launch_main<4, 8, 2, 2, G, NV>(gs, count, M, status, sched, stream);
+        default: return launch_main<8, 4, 2, 2, G, NV>(gs, count, M, status, sched, stream);
     }
 }
 
@@ -671,6 +676,70 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
         h.items_cap = items_cap;
         err = umma ? launch_umma_np<1>(umma_npad(int(mc)), &h, 1, int(mc), dev_status, stream)
                    : launch_main_nt<1>(NT, &h, 1, int(mc), dev_status, nullptr, stream);
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+// NVFP4 weights ("Module 11 ...", §12: E2M1 in blocks of 16 sharing an E4M3
+// scale, one FP32 scale per tensor): passes of up to 64 rows on the mma.sync
+// kernel, each block's scale folded into the decoded fp16 weights.
+cudaError_t gemm_run_nv(const uint16_t* x, const uint8_t* nibbles, const uint8_t* scales, float global_scale,
+                        float* y, int64_t M, int64_t N, int64_t K, void* workspace, const GemmWorkspace& ws,
+                        int32_t* dev_status, cudaStream_t stream) {
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    uint16_t* xf = reinterpret_cast<uint16_t*>(wsb + ws.xf_off);
+    float* xun = reinterpret_cast<float*>(wsb + ws.xun_off);
+    int* counters = reinterpret_cast<int*>(wsb + ws.cnt_off);
+    float* part = reinterpret_cast<float*>(wsb + ws.part_off);
+    uint8_t* sc_aligned = ws.repack_scales ? wsb + ws.sc_off : nullptr;
+    const int nsb = int(K / 16);  // scale bytes per row
+    const int64_t mc0 = std::min<int64_t>(M, kGemmMaxRowsPerPass);
+    bool scales_realigned = false;
+    for (int64_t m0 = 0, mc = 0; m0 < M; m0 += mc) {
+        mc = std::min<int64_t>(kGemmMaxRowsPerPass, M - m0);
+        const int NT = tiles_nt(int(mc));
+        const int bn = bn_for_nt(NT);
+        int64_t items_cap = split_items_cap(N, K, bn);
+        if (ws.n_counters < (N + bn - 1) / bn || mc > mc0) items_cap = 0;
+        const bool repack = ws.repack_scales && !scales_realigned;
+        scales_realigned = true;
+        PrepSet Q{};
+        Q.job[0].x = x + m0 * K;
+        Q.job[0].xf = xf;
+        Q.job[0].xun = xun;
+        Q.job[0].K = int(K);
+        Q.njobs = 1;
+        Q.M = int(mc);
+        Q.NT = NT;
+        Q.counters = counters;
+        Q.ncounters = ws.n_counters;
+        if (repack) {
+            Q.sc_in = scales;
+            Q.N = N;
+            Q.nblk = nsb;
+            Q.sc_pitch = ws.sc_pitch;
+            Q.sc_out = sc_aligned;
+            Q.repack_ctas = int(std::min<int64_t>((N * ws.sc_pitch + kPrepThreads - 1) / kPrepThreads, 1024));
+        }
+        cudaError_t err = launch_prep(Q, stream);
+        if (err != cudaSuccess) return err;
+        HostGemm h{};
+        h.nib = nibbles;
+        h.sc = ws.repack_scales ? sc_aligned : scales;
+        h.sc_pitch = ws.sc_pitch;
+        h.sc_from_prep = ws.repack_scales;
+        h.xf = xf;
+        h.xun = xun;
+        h.y = y + m0 * N;
+        h.part = part;
+        h.counters = counters;
+        h.N = N;
+        h.K = K;
+        h.items_cap = items_cap;
+        h.sdiv = 16;
+        h.gscale = global_scale;
+        err = launch_main_nt<1, true>(NT, &h, 1, int(mc), dev_status, nullptr, stream);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;

@@ -24,6 +24,7 @@ struct Problem {
     int sc_from_prep;      // scales were realigned by the preparation kernel
     const uint8_t* sc;     // the scale rows that tm_s streams (row pitch sc_pitch bytes)
     int64_t sc_pitch;
+    float gscale;          // NVFP4: the tensor's FP32 scale (unused for MXFP4)
 };
 
 // The GEMMs of one launch (a kernel parameter, read in place).  They share

@@ -3,7 +3,9 @@
 
 // RG groups of 16 weight rows; KW consumer warps share each group, each
 // taking 16/KW of a stage's blocks (KW = 2: one nibble box per warp).
-template <int NT, int RG, int KW, int STAGES>
+// NV: NVFP4 weights (one E4M3 scale per 16 k, 32 scale bytes per row per
+// 512-k stage) instead of MXFP4 (one E8M0 scale per 32 k, 16 bytes).
+template <int NT, int RG, int KW, int STAGES, bool NV = false>
 struct GemmCfg {
     static constexpr int BN = 16 * RG;
     static constexpr int NWC = RG * KW;
@@ -11,7 +13,8 @@ struct GemmCfg {
     static constexpr int kThreads = kConsumers + 32;
     static constexpr int kBoxW = BN * kBoxBytes;            // one nibble box
     static constexpr int kWBytes = 2 * kBoxW;
-    static constexpr int kSBytes = BN * 16;
+    static constexpr int kSBytes = BN * (NV ? 32 : 16);
+    static constexpr int kScaleWords = NV ? 8 : 4;          // 32-bit scale words per row per stage
     static constexpr int kXBytes = kStageBlocks * NT * kFragBytesPerBlockTile;
     static constexpr int kStageBytes = kWBytes + kSBytes + kXBytes;
     static constexpr int kPartPitch = 8 * NT + 1;            // floats per row of the partial tile
@@ -45,6 +48,20 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
           "f"(c[3]));
 }
 
+__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// An E4M3 byte as an f16x2 pair {s, s} (exact: every E4M3 value is an fp16 value).
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_pair(uint32_t byte) {
+    uint32_t out;
+    const uint32_t two = byte | (byte << 8);
+    asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n" : "=r"(out) : "r"(two));
+    return out;
+}
+
 __device__ __forceinline__ void consumer_bar(int nthreads) {
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
@@ -70,11 +87,17 @@ __device__ __forceinline__ bool consumer_any(int nthreads, bool v) {
 // offset of the lane's 16-byte chunk for block pair j; sgw/sg8w: the scale
 // bytes of the warp's blocks for rows g and g+8; xs: the X fragments of the
 // warp's first block.
-template <int NT, int BOXW, int KW, bool FULL>
+//
+// NV: each lane's 8 decoded codes of a 32-k block lie in one 16-element NVFP4
+// block (codes 8t .. 8t + 7 for t = lane % 4), so they are multiplied by that
+// block's E4M3 scale in fp16 before the MMA (E2M1 x E4M3 has at most 6
+// significant bits and lies in [2^-10, 2688]: exact), and the MMAs accumulate
+// straight into acc.
+template <int NT, int BOXW, int KW, bool FULL, bool NV = false>
 __device__ __forceinline__ void consume_stage(float (&acc)[NT][4], uint32_t w_row,
                                               const uint32_t (&lm)[4],
-                                              const uint32_t (&sgw)[4 / KW],
-                                              const uint32_t (&sg8w)[4 / KW],
+                                              const uint32_t (&sgw)[(NV ? 8 : 4) / KW],
+                                              const uint32_t (&sg8w)[(NV ? 8 : 4) / KW],
                                               const uint4* __restrict__ xs, int lane, int nbl) {
     const float zero[4] = {0.f, 0.f, 0.f, 0.f};
     constexpr int kPairs = kStageBlocks / 2 / KW;  // block pairs per k-warp
@@ -91,6 +114,24 @@ __device__ __forceinline__ void consume_stage(float (&acc)[NT][4], uint32_t w_ro
             uint32_t ag[4], ag8[4];
             e2m1x8_to_f16x2x4(h ? r2 : r0, ag[0], ag[1], ag[2], ag[3]);
             e2m1x8_to_f16x2x4(h ? r3 : r1, ag8[0], ag8[1], ag8[2], ag8[3]);
+            if constexpr (NV) {
+                const int bi = 2 * blk + ((lane & 3) >> 1);  // this lane's NVFP4 block in the warp's share
+                const uint32_t sh = 8u * uint32_t(bi & 3);
+                const uint32_t s2 = e4m3_to_f16x2_pair((sgw[bi >> 2] >> sh) & 0xFFu);
+                const uint32_t s28 = e4m3_to_f16x2_pair((sg8w[bi >> 2] >> sh) & 0xFFu);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    ag[i] = hmul2_f16(ag[i], s2);
+                    ag8[i] = hmul2_f16(ag8[i], s28);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint4 xv = xs[(blk * NT + nt) * 32 + lane];
+                    mma_16816(acc[nt], ag[0], ag8[0], ag[1], ag8[1], xv.x, xv.y, acc[nt]);
+                    mma_16816(acc[nt], ag[2], ag8[2], ag[3], ag8[3], xv.z, xv.w, acc[nt]);
+                }
+                continue;
+            }
             const uint32_t sel = (blk & 3) | ((4 + (blk & 3)) << 4);
             float s_g, s_g8;
             e8m0x2_to_f32x2(__byte_perm(sgw[blk >> 2], sg8w[blk >> 2], sel), s_g, s_g8);
@@ -113,11 +154,11 @@ __device__ __forceinline__ void consume_stage(float (&acc)[NT][4], uint32_t w_ro
 // items run fastest with the budget set for the CTAs per SM that fit (no
 // spills in the per-item path); the grouped launches' long items with the
 // compiler's own budget.
-template <int NT, int RG, int KW, int STAGES, int G>
-__global__ void __launch_bounds__(GemmCfg<NT, RG, KW, STAGES>::kThreads,
-                                  G == 1 ? GemmCfg<NT, RG, KW, STAGES>::kMinBlocks : 0)
+template <int NT, int RG, int KW, int STAGES, int G, bool NV = false>
+__global__ void __launch_bounds__(GemmCfg<NT, RG, KW, STAGES, NV>::kThreads,
+                                  G == 1 ? GemmCfg<NT, RG, KW, STAGES, NV>::kMinBlocks : 0)
     mxfp4_gemm_kernel(const __grid_constant__ ProblemSet<G> S) {
-    using C = GemmCfg<NT, RG, KW, STAGES>;
+    using C = GemmCfg<NT, RG, KW, STAGES, NV>;
     constexpr int NWC = C::NWC;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte-swizzled TMA destinations need 1 KB alignment
@@ -160,7 +201,7 @@ __global__ void __launch_bounds__(GemmCfg<NT, RG, KW, STAGES>::kThreads,
             const Problem& pb = S.p[pi];
             const uint32_t stage = smem_base + slot * C::kStageBytes;
             const uint32_t bar = full_bar + 8 * slot;
-            if (pb.sc_from_prep) tma_2d(stage + C::kWBytes, &pb.tm_s, kb, n0, bar, pol_w);
+            if (pb.sc_from_prep) tma_2d(stage + C::kWBytes, &pb.tm_s, NV ? 2 * kb : kb, n0, bar, pol_w);
             bulk_g2s(stage + C::kWBytes + C::kSBytes,
                      pb.xf + int64_t(kb) * NT * (kFragBytesPerBlockTile / 2),
                      uint32_t(nb) * NT * kFragBytesPerBlockTile, bar, pol_x);
@@ -208,7 +249,7 @@ __global__ void __launch_bounds__(GemmCfg<NT, RG, KW, STAGES>::kThreads,
                                                uint32_t(nb) * NT * kFragBytesPerBlockTile);
                 tma_2d(stage, &pb.tm_w, kb * 16, n0, bar, pol_w);
                 tma_2d(stage + C::kBoxW, &pb.tm_w, kb * 16 + kBoxBytes, n0, bar, pol_w);
-                if (!pb.sc_from_prep) tma_2d(stage + C::kWBytes, &pb.tm_s, kb, n0, bar, pol_w);
+                if (!pb.sc_from_prep) tma_2d(stage + C::kWBytes, &pb.tm_s, NV ? 2 * kb : kb, n0, bar, pol_w);
                 if (waited) {
                     issue_dep(slot, kb, nb, n0, pi);
                 } else {
@@ -306,13 +347,13 @@ __global__ void __launch_bounds__(GemmCfg<NT, RG, KW, STAGES>::kThreads,
             }
             const int nb = min(kStageBlocks, R.kb1 - (R.kb0 + i * kStageBlocks));
             const uint8_t* stage = smem + slot * C::kStageBytes;
-            constexpr int kWords = 4 / KW;  // scale words (4 blocks each) per k-warp
+            constexpr int kWords = C::kScaleWords / KW;  // scale words (4 scales each) per k-warp
             const uint32_t* s_row = reinterpret_cast<const uint32_t*>(stage + C::kWBytes);
             uint32_t sgw[kWords], sg8w[kWords];
 #pragma unroll
             for (int q = 0; q < kWords; ++q) {
-                sgw[q] = s_row[(rbase + g) * 4 + kw * kWords + q];
-                sg8w[q] = s_row[(rbase + g + 8) * 4 + kw * kWords + q];
+                sgw[q] = s_row[(rbase + g) * C::kScaleWords + kw * kWords + q];
+                sg8w[q] = s_row[(rbase + g + 8) * C::kScaleWords + kw * kWords + q];
             }
             constexpr int kBlocksPerWarp = kStageBlocks / KW;
             const uint4* xs = reinterpret_cast<const uint4*>(stage + C::kWBytes + C::kSBytes) +
@@ -322,9 +363,9 @@ __global__ void __launch_bounds__(GemmCfg<NT, RG, KW, STAGES>::kThreads,
                                    uint32_t((kw * kBlocksPerWarp) / 8) * C::kBoxW;
             const int nbl = nb - kw * kBlocksPerWarp;
             if (nb == kStageBlocks)
-                consume_stage<NT, C::kBoxW, KW, true>(acc, w_row, lm, sgw, sg8w, xs, lane, nbl);
+                consume_stage<NT, C::kBoxW, KW, true, NV>(acc, w_row, lm, sgw, sg8w, xs, lane, nbl);
             else
-                consume_stage<NT, C::kBoxW, KW, false>(acc, w_row, lm, sgw, sg8w, xs, lane, nbl);
+                consume_stage<NT, C::kBoxW, KW, false, NV>(acc, w_row, lm, sgw, sg8w, xs, lane, nbl);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar + 8 * slot);
         }
@@ -358,7 +399,8 @@ __global__ void __launch_bounds__(GemmCfg<NT, RG, KW, STAGES>::kThreads,
         if (P.nsplit == 1) {
             for (int o = threadIdx.x; o < C::BN * M; o += C::kConsumers) {
                 const int r = o % C::BN, m = o / C::BN;
-                if (r < rows) P.y[int64_t(m) * P.N + n0 + r] = tile_val(r, m) * P.xun[m];
+                if (r < rows) P.y[int64_t(m) * P.N + n0 + r] = NV ? (tile_val(r, m) * P.xun[m]) * P.gscale
+                                                                  : tile_val(r, m) * P.xun[m];
             }
         } else {
             float* mine = P.part + int64_t(wl) * M * C::BN;
@@ -379,7 +421,7 @@ __global__ void __launch_bounds__(GemmCfg<NT, RG, KW, STAGES>::kThreads,
                         for (int q = 0; q < P.nsplit; ++q)
                             s += __ldcg(P.part + (int64_t(q) * P.ntiles + R.tile) * M * C::BN +
                                         int64_t(m) * C::BN + r);
-                        P.y[int64_t(m) * P.N + n0 + r] = s * P.xun[m];
+                        P.y[int64_t(m) * P.N + n0 + r] = NV ? (s * P.xun[m]) * P.gscale : s * P.xun[m];
                     }
                 }
                 if (threadIdx.x == 0) P.counters[R.tile] = 0;  // ready for the next call

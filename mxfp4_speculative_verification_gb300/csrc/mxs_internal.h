@@ -24,11 +24,17 @@ struct GemmWorkspace {
     bool repack_scales;  // scales must be copied to the workspace first
 };
 
-GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales_aligned);
+// sdiv: k per scale byte, 32 (MXFP4) or 16 (NVFP4)
+GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales_aligned, int sdiv = 32);
 
 cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* scales, float* y,
                      int64_t M, int64_t N, int64_t K, void* workspace,
                      const GemmWorkspace& ws, int32_t* dev_status, cudaStream_t stream);
+
+// The same GEMM on NVFP4 weights: scales [N, K/16] E4M3, one FP32 tensor scale.
+cudaError_t gemm_run_nv(const uint16_t* x, const uint8_t* nibbles, const uint8_t* scales, float global_scale,
+                        float* y, int64_t M, int64_t N, int64_t K, void* workspace, const GemmWorkspace& ws,
+                        int32_t* dev_status, cudaStream_t stream);
 
 // One GEMM of a grouped call (independent GEMMs sharing M <= 64).
 struct GroupedGemm {

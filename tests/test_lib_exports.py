@@ -57,6 +57,23 @@ def test_gemm_rejects_bad_arguments_on_host(L):
     assert f(FAKE, FAKE, FAKE, FAKE, 5, 64, 512, FAKE, 16, None, None) == 5
 
 
+def test_nvfp4_gemm_rules_on_host(L):
+    assert L.nvfp4_verify_gemm_workspace_size(5, 4096, 4096) > 0
+    assert L.nvfp4_verify_gemm_workspace_size(5, 4096, 4100) == 0  # K % 32
+    # scale rows are realigned unless K % 256 == 0 (K/16 bytes a multiple of 16)
+    a = L.nvfp4_verify_gemm_workspace_size(5, 1000, 288)
+    b = L.nvfp4_verify_gemm_workspace_size(5, 1000, 256)
+    assert a >= b + 1000 * 32
+    ws = 1 << 30
+    f = L.nvfp4_verify_gemm
+    assert f(None, FAKE, FAKE, 1.0, FAKE, 5, 64, 512, FAKE, ws, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, 1.0, FAKE, 5, 64, 496, FAKE, ws, None, None) == 1   # K % 32
+    assert f(FAKE, FAKE, FAKE, 1.0, FAKE, 1 << 20, 64, 512, FAKE, ws, None, None) == 3
+    assert f(FAKE, FAKE + 8, FAKE, 1.0, FAKE, 5, 64, 512, FAKE, ws, None, None) == 2
+    assert f(FAKE, FAKE, FAKE + 4, 1.0, FAKE, 5, 64, 256, FAKE, ws, None, None) == 2   # scales, K%256==0
+    assert f(FAKE, FAKE, FAKE, 1.0, FAKE, 5, 64, 512, FAKE, 16, None, None) == 5
+
+
 def test_accept_rejects_bad_arguments_on_host(L):
     f = L.spec_accept
     assert f(FAKE, FAKE, FAKE, FAKE, 0, 3, 8, FAKE, FAKE, None, None, None) == 1

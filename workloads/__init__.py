@@ -77,6 +77,19 @@ def mxfp4_weights(N: int, K: int, exp_lo: int, exp_hi: int, seed: int,
     return nib, sc
 
 
+def nvfp4_weights(N: int, K: int, seed: int, tensor_id: int = 0, exp_lo: int = 4,
+                  exp_hi: int = 10) -> tuple[np.ndarray, np.ndarray]:
+    """Random packed NVFP4 weights: (nibbles uint8 [N, K/2], E4M3 scale bytes
+    uint8 [N, K/16]); positive scales with exponent field in [exp_lo, exp_hi]
+    (<= 14: no NaN) and a random 3-bit fraction."""
+    assert K % 16 == 0 and 0 <= exp_lo <= exp_hi <= 14
+    g = host_rng(seed, tensor_id)
+    nib = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    e = g.integers(exp_lo, exp_hi + 1, size=(N, K // 16), dtype=np.uint8)
+    f = g.integers(0, 8, size=(N, K // 16), dtype=np.uint8)
+    return nib, ((e << 3) | f).astype(np.uint8)
+
+
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
     """Round finite fp32 values to bf16 (nearest, ties to even); return uint16 bits."""
     u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
@@ -110,6 +123,17 @@ def device_mxfp4_weights(N: int, K: int, exp_lo: int, exp_hi: int, seed: int, de
     sc = torch.randint(exp_lo, exp_hi + 1, (N, K // 32), generator=gen, device=device,
                        dtype=torch.int32).to(torch.uint8)
     return nib, sc
+
+
+def device_nvfp4_weights(N: int, K: int, seed: int, device, exp_lo: int = 4, exp_hi: int = 10):
+    """nvfp4_weights' distribution, generated in device memory (torch RNG)."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    nib = torch.randint(0, 256, (N, K // 2), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+    e = torch.randint(exp_lo, exp_hi + 1, (N, K // 16), generator=gen, device=device, dtype=torch.int32)
+    f = torch.randint(0, 8, (N, K // 16), generator=gen, device=device, dtype=torch.int32)
+    return nib, ((e << 3) | f).to(torch.uint8)
 
 
 def device_bf16_normal(M: int, K: int, seed: int, device, std: float = 1.0):
