@@ -3,23 +3,33 @@
 // temperature, then top-k, then top-p, applied to the target and the draft
 // alike; raw probabilities with a filtered law break the proof).
 //
-// One thread-block cluster of C CTAs x 1024 threads per logit row, the row
-// held in registers (16 logits per thread, V <= 131072).  Steps:
+// One thread-block cluster of C CTAs x 512 threads per logit row, each CTA
+// holding a 16384-logit slice in shared memory (V <= 131072); two CTAs share
+// an SM, so one row's barriers overlap another row's work.  Steps:
 //  * the row's largest finite logit m, and whether it holds NaN or +inf (then
 //    it has no law);
 //  * top-k: the key (monotone uint32 image of the logit) of the k-th largest
-//    logit, by a radix select of 4 rounds of 8 bits over token counts;
-//    every token with key >= it is kept (ties kept);
-//  * top-p: over the kept tokens' masses exp((l - m) / T), the key where the
-//    cumulative mass from the top first reaches p, by the same radix select
-//    over masses; masses are fixed point (floor(e * 2^46), exact in uint64
-//    for any order of addition), so the cut is a deterministic function of
-//    the row; ties at the cut are kept;
+//    logit; every token with key >= it is kept (ties kept);
+//  * top-p: over the kept tokens' masses exp((l - m) / T) in fixed point
+//    (floor(e * 2^46), exact in uint64 for any order of addition, so the cut
+//    is a deterministic function of the row), the key where the cumulative
+//    mass from the top first reaches ceil(p * total); ties at the cut kept;
 //  * the kept mass S, and p_t = exp((l_t - m) / T) * 2^46 / S.
-// Each round every CTA builds a 256-bin histogram of its slice in shared
-// memory; after one cluster barrier every CTA sums the C histograms through
-// distributed shared memory and takes the same decision.  Histograms
-// alternate between two buffers, so one barrier per round suffices.
+//
+// Each cut (by token count for top-k, by mass for top-p) is found in three
+// narrowing steps over tokens ordered by their log-mass a = (l - m) / T,
+// which is monotone in the key:
+//  1. one pass over the slice sums the weight of four classes, a in (-2, 0],
+//     (-4, -2], (-8, -4] and below, in registers; one cluster exchange gives
+//     the class where the cumulative weight reaches the target;
+//  2. the tokens of that class fill a 256-bin histogram of finer log-mass
+//     steps; one exchange gives the bin;
+//  3. the tokens of that bin (typically a handful) are gathered from every
+//     CTA, and each CTA ranks them by key exactly.
+// If the bin holds too many tokens to gather, a radix select over its keys
+// (4 rounds of 8 bits, one exchange each) finishes instead.  Every step is a
+// function of the row alone, so all CTAs of a cluster take the same
+// decisions, and the result is the same as one radix select over the row.
 #include <cooperative_groups.h>
 
 #include <climits>
@@ -33,10 +43,15 @@ namespace cg = cooperative_groups;
 
 namespace mxs {
 
-constexpr int kLawThreads = 1024;
-constexpr int kLawChunks = 16;  // logits per thread
+constexpr int kLawThreads = 512;
+constexpr int kLawWarps = kLawThreads / 32;
+constexpr int kLawChunks = 32;  // logits per thread
 constexpr int kLawMaxCluster = 8;
 constexpr int64_t kLawSlice = int64_t(kLawThreads) * kLawChunks;
+constexpr int kLawBins = 256;
+constexpr int kGatherCap = 128;    // tokens one CTA may contribute to a gather
+constexpr int kGatherTotal = 256;  // tokens a cluster may gather
+constexpr int kLawVals = 4;        // values one step publishes to the cluster
 static_assert(kLawMaxV == kLawMaxCluster * kLawSlice, "vocabulary limit");
 
 struct LawArgs {
@@ -50,21 +65,67 @@ struct LawArgs {
     int32_t* status;
 };
 
-struct LawPub {  // what each CTA publishes to its cluster once
-    float m;
-    int bad;
-    unsigned long long w;
+struct GatherEntry {
+    uint32_t key;
+    float x;
 };
 
-__global__ void __launch_bounds__(kLawThreads, 1) sampling_law_kernel(const LawArgs A) {
-    __shared__ unsigned long long hist[2][256];
-    __shared__ unsigned long long scan_w[8];
-    __shared__ float red_m[32];
-    __shared__ int red_b[32];
-    __shared__ unsigned long long red_w[32];
-    __shared__ LawPub pub;
-    __shared__ int sel_first, sel_last;
-    __shared__ unsigned long long sel_above, sel_bin, sel_total;
+// Shared memory of one CTA (dynamic, about 70 KB).
+struct LawSmem {
+    float xs[kLawChunks * kLawThreads];  // element v0 + i * 512 + t at [i * 512 + t]
+    GatherEntry glist[kGatherCap];       // this CTA's tokens of the gathered bin
+    GatherEntry gall[kGatherTotal];      // the cluster's, in CTA order
+    unsigned long long gw[kGatherTotal]; // and their weights
+    unsigned long long red[kLawWarps][kLawVals];
+    unsigned long long tot[kLawVals];    // cluster sums
+    unsigned long long scan_w[8];
+    unsigned long long sel_above, sel_at, sel_total;
+    int gcount;                          // tokens found for the gather (may exceed the cap)
+    int goff[kLawMaxCluster + 1];
+    int sel_first, sel_last;
+    uint32_t sel_key, sel_min;
+    int sel_any, sel_idx;
+    float pub_m;
+    int pub_bad;
+    float m;
+    int bad;
+};
+constexpr int kLawSmem = int(sizeof(LawSmem));
+
+// Log-mass class of a token, a = (l - m) / T <= 0: 0 for a > -2, 1 for
+// (-4, -2], 2 for (-8, -4], 3 below.
+__device__ __forceinline__ int law_class(float a) {
+    return int(a <= -2.f) + int(a <= -4.f) + int(a <= -8.f);
+}
+
+// Fine bin of a token within its class (0 holds the largest logits): steps
+// of 1/128 nat in classes 0 and 1, 1/64 in class 2, 1/8 in class 3 (bin 255
+// also takes every token 40 or more below the maximum).  Monotone in a.
+__device__ __forceinline__ int law_fine(float a, int c) {
+    const float lo = c == 0 ? 0.f : c == 1 ? 2.f : c == 2 ? 4.f : 8.f;
+    const float sc = c <= 1 ? 128.f : c == 2 ? 64.f : 8.f;
+    const float f = (-a - lo) * sc;
+    return f >= 255.f ? 255 : int(f);
+}
+
+// Sum of a 64-bit value over a warp (two 32-bit shuffles per step).
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+struct LawCut {
+    uint32_t key;              // the cut: tokens with key >= it are kept
+    unsigned long long above;  // weight of the tokens with larger keys
+    unsigned long long at;     // weight of the tokens with this key
+};
+
+__global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawArgs A) {
+    extern __shared__ __align__(16) uint8_t law_smem_raw[];
+    LawSmem& S = *reinterpret_cast<LawSmem*>(law_smem_raw);
+    __shared__ uint32_t hist_cnt[2][kLawBins], hist_lo[2][kLawBins], hist_hi[2][kLawBins];
+    __shared__ unsigned long long pubv[2][kLawVals];
 
     cg::cluster_group cluster = cg::this_cluster();
     const int C = int(cluster.num_blocks());
@@ -72,175 +133,399 @@ __global__ void __launch_bounds__(kLawThreads, 1) sampling_law_kernel(const LawA
     const int64_t r = blockIdx.x / C;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t V = A.V;
-    const float* row = A.logits + r * V;
     const int64_t v0 = int64_t(rank) * kLawSlice;
+    const int nv = int(V - v0 < kLawSlice ? V - v0 : kLawSlice);  // tokens in this slice, >= 1
 
-    // ---- the slice into registers (element v0 + i * 1024 + tid)
-    float x[kLawChunks];
-    float mx = -INFINITY;
-    int bad = 0;
+    // ---- the slice into shared memory; its largest finite logit, and NaN / +inf
+    {
+        const float* row = A.logits + r * V + v0;
+        float mx = -INFINITY;
+        int bad = 0;
 #pragma unroll
-    for (int i = 0; i < kLawChunks; ++i) {
-        const int64_t idx = v0 + int64_t(i) * kLawThreads + tid;
-        x[i] = idx < V ? __ldg(row + idx) : -INFINITY;
-        if (idx < V) {
-            if (isnan(x[i]) || x[i] == INFINITY) bad = 1;
-            else mx = fmaxf(mx, x[i]);
+        for (int i = 0; i < kLawChunks; ++i) {
+            const int j = i * kLawThreads + tid;
+            float v = -INFINITY;
+            if (j < nv) {
+                v = __ldg(row + j);
+                if (isnan(v) || v == INFINITY) bad = 1;
+                else mx = fmaxf(mx, v);
+            }
+            S.xs[j] = v;
         }
-    }
-    auto valid = [&](int i) { return v0 + int64_t(i) * kLawThreads + tid < V; };
-
-    // ---- m and the row's validity across the cluster
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        bad |= __shfl_xor_sync(0xffffffffu, bad, o);
-    }
-    if (lane == 0) {
-        red_m[warp] = mx;
-        red_b[warp] = bad;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        float a = -INFINITY;
-        int b = 0;
-        for (int w = 0; w < kLawThreads / 32; ++w) {
-            a = fmaxf(a, red_m[w]);
-            b |= red_b[w];
+        for (int o = 16; o > 0; o >>= 1) {
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            bad |= __shfl_xor_sync(0xffffffffu, bad, o);
         }
-        pub.m = a;
-        pub.bad = b;
+        if (lane == 0) {
+            S.red[warp][0] = __float_as_uint(mx);
+            S.red[warp][1] = unsigned(bad);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float a = -INFINITY;
+            int b = 0;
+            for (int w = 0; w < kLawWarps; ++w) {
+                a = fmaxf(a, __uint_as_float(uint32_t(S.red[w][0])));
+                b |= int(S.red[w][1]);
+            }
+            S.pub_m = a;
+            S.pub_bad = b;
+        }
+        cluster.sync();
+        if (warp == 0) {
+            float a = -INFINITY;
+            int b = 0;
+            if (lane < C) {
+                const LawSmem* o = cluster.map_shared_rank(&S, lane);
+                a = o->pub_m;
+                b = o->pub_bad;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+                b |= __shfl_xor_sync(0xffffffffu, b, o);
+            }
+            if (lane == 0) {
+                S.m = a;
+                S.bad = b;
+            }
+        }
+        __syncthreads();
     }
-    cluster.sync();
-    float m = -INFINITY;
-    bad = 0;
-    for (int c = 0; c < C; ++c) {
-        const LawPub* o = cluster.map_shared_rank(&pub, c);
-        m = fmaxf(m, o->m);
-        bad |= o->bad;
-    }
+    const float m = S.m;
+    const float inv_t = A.inv_t;
     LawStats st;
     st.m = m;
     st.cut = 0;
     st.inv_s = 0.f;
-    st.ok = !bad && m > -INFINITY;
-    const float inv_t = A.inv_t;
+    st.ok = !S.bad && m > -INFINITY;
 
-    int round = 0;  // alternates the histogram buffers
-    // One radix-select pass over the keys >= lo: the largest key K with
-    // weight(key >= K) >= target (the weights of valid tokens being 1, or
-    // their fixed-point masses).  Returns K; *above gets weight(key > K), and
-    // *at weight(key == K).  A target of 0 means "the full weight" (mass
-    // pass: the target is taken from the first round's total as ceil(p * W)).
-    auto select = [&](bool by_mass, uint32_t lo, unsigned long long target, unsigned long long* above,
-                      unsigned long long* at) -> uint32_t {
-        uint32_t prefix = 0;
-        unsigned long long acc_above = 0;
-        for (int rr = 0; rr < 4; ++rr, ++round) {
-            const int shift = 24 - 8 * rr;
-            unsigned long long* h = hist[round & 1];
-            if (tid < 256) h[tid] = 0;
-            __syncthreads();
+    int pb = 0;  // alternates the published-sum buffers
+    int hb = 0;  // alternates the histogram buffers
+    // Sums of kLawVals values over the cluster, into S.tot (all threads).
+    auto cluster_sum = [&](unsigned long long (&v)[kLawVals]) {
 #pragma unroll
-            for (int i = 0; i < kLawChunks; ++i) {
-                if (!valid(i)) continue;
-                const uint32_t k = law_key(x[i]);
-                if (k < lo || (rr > 0 && (k >> (shift + 8)) != prefix)) continue;
-                const unsigned long long w = by_mass ? law_mass(law_exp(x[i], m, inv_t)) : 1ull;
-                if (w) atomicAdd(h + ((k >> shift) & 255u), w);
-            }
-            __syncthreads();
-            cluster.sync();
-            // thread t < 256 takes bin 255 - t: an inclusive scan from the top bin down
-            unsigned long long tot = 0, incl = 0;
-            if (tid < 256) {
-                for (int c = 0; c < C; ++c) tot += cluster.map_shared_rank(h, c)[255 - tid];
-                incl = tot;
+        for (int j = 0; j < kLawVals; ++j) v[j] = warp_sum_u64(v[j]);
+        if (lane == 0)
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned long long n = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += n;
+            for (int j = 0; j < kLawVals; ++j) S.red[warp][j] = v[j];
+        __syncthreads();
+        unsigned long long* pub = pubv[pb];
+        pb ^= 1;
+        if (tid < kLawVals) {
+            unsigned long long t = 0;
+            for (int w = 0; w < kLawWarps; ++w) t += S.red[w][tid];
+            pub[tid] = t;
+        }
+        cluster.sync();
+        if (tid < kLawVals) {
+            unsigned long long t = 0;
+            for (int c = 0; c < C; ++c) t += cluster.map_shared_rank(pub, c)[tid];
+            S.tot[tid] = t;
+        }
+        __syncthreads();
+    };
+    // A fresh CTA histogram; returns its buffer index.
+    auto hist_begin = [&]() -> int {
+        const int b = hb;
+        hb ^= 1;
+        if (tid < kLawBins) {
+            hist_cnt[b][tid] = 0;
+            hist_lo[b][tid] = 0;
+            hist_hi[b][tid] = 0;
+        }
+        __syncthreads();
+        return b;
+    };
+    auto hist_put = [&](int b, int bin, bool by_mass, unsigned long long w) {
+        if (!by_mass) {
+            atomicAdd(&hist_cnt[b][bin], 1u);
+            return;
+        }
+        const uint32_t lo = uint32_t(w);
+        uint32_t hi = uint32_t(w >> 32);
+        const uint32_t old = atomicAdd(&hist_lo[b][bin], lo);
+        if (old + lo < old) ++hi;
+        if (hi) atomicAdd(&hist_hi[b][bin], hi);
+    };
+    // After every CTA filled buffer b: the cluster's weight at bin tid (tid < 256).
+    auto hist_end = [&](int b, bool by_mass) -> unsigned long long {
+        __syncthreads();
+        cluster.sync();
+        unsigned long long t = 0;
+        if (tid < kLawBins)
+            for (int c = 0; c < C; ++c) {
+                if (by_mass) {
+                    const uint32_t lo = *cluster.map_shared_rank(&hist_lo[b][tid], c);
+                    const uint32_t hi = *cluster.map_shared_rank(&hist_hi[b][tid], c);
+                    t += (static_cast<unsigned long long>(hi) << 32) + lo;
+                } else {
+                    t += *cluster.map_shared_rank(&hist_cnt[b][tid], c);
                 }
-                if (lane == 31) scan_w[warp] = incl;
+            }
+        return t;
+    };
+    // From the weights at positions 0..255 (tid < 256; position 0 first): the
+    // first position where the cumulative weight reaches target or, if that
+    // is out of reach, the last position holding any weight.  *above: weight
+    // before it; *at: its weight.
+    auto pick = [&](unsigned long long tot, unsigned long long target, unsigned long long* above,
+                    unsigned long long* at) -> int {
+        unsigned long long incl = 0;
+        if (tid < kLawBins) {
+            incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            if (lane == 31) S.scan_w[warp] = incl;
+        }
+        if (tid == 0) {
+            S.sel_first = INT_MAX;
+            S.sel_last = -1;
+        }
+        __syncthreads();
+        if (tid < kLawBins) {
+            for (int w = 0; w < warp; ++w) incl += S.scan_w[w];
+            if (tot > 0) {
+                if (incl >= target) atomicMin(&S.sel_first, tid);
+                atomicMax(&S.sel_last, tid);
+            }
+        }
+        __syncthreads();
+        const int s = S.sel_first != INT_MAX ? S.sel_first : (S.sel_last > 0 ? S.sel_last : 0);
+        if (tid == s) {
+            S.sel_above = incl - tot;
+            S.sel_at = tot;
+        }
+        __syncthreads();
+        *above = S.sel_above;
+        *at = S.sel_at;
+        return s;
+    };
+    auto weight_of = [&](float x, bool by_mass) -> unsigned long long {
+        return by_mass ? law_mass(law_exp(x, m, inv_t)) : 1ull;
+    };
+
+    // The cut by count (top-k, target k) or by mass (top-p, target ceil(p *
+    // total)) among the tokens with key >= lo: the largest key K whose tokens
+    // with key >= K weigh at least the target.
+    auto find_cut = [&](bool by_mass, uint32_t lo, unsigned long long target) -> LawCut {
+        // 1. class weights; masks of this thread's tokens in each class
+        uint32_t cm0 = 0u, cm1 = 0u, cm2 = 0u, cm3 = 0u;  // this thread's tokens of each class
+        {
+            unsigned long long v[kLawVals] = {0ull, 0ull, 0ull, 0ull};
+            // branch-free, so that unrolled iterations overlap (padding slots
+            // hold -inf: no mass; the count weight checks the slot)
+#pragma unroll 8
+            for (int i = 0; i < kLawChunks; ++i) {
+                const int j = i * kLawThreads + tid;
+                const float x = S.xs[j];
+                const bool in = j < nv && law_key(x) >= lo;
+                const unsigned long long w = in ? weight_of(x, by_mass) : 0ull;
+                const float a = (x - m) * inv_t;
+                v[0] += w;
+                v[1] += a > -2.f ? w : 0ull;
+                v[2] += a > -4.f ? w : 0ull;
+                v[3] += a > -8.f ? w : 0ull;
+                const int cl = law_class(a);
+                const uint32_t bit = w ? 1u << i : 0u;
+                cm0 |= cl == 0 ? bit : 0u;
+                cm1 |= cl == 1 ? bit : 0u;
+                cm2 |= cl == 2 ? bit : 0u;
+                cm3 |= cl == 3 ? bit : 0u;
+            }
+            cluster_sum(v);
+        }
+        if (by_mass) {
+            target = (unsigned long long)ceil(double(A.top_p) * double(S.tot[0]));
+            if (target == 0) target = 1;
+        }
+        int c = 3;
+        unsigned long long base = S.tot[3];
+        if (S.tot[1] >= target) {
+            c = 0;
+            base = 0;
+        } else if (S.tot[2] >= target) {
+            c = 1;
+            base = S.tot[1];
+        } else if (S.tot[3] >= target) {
+            c = 2;
+            base = S.tot[2];
+        }
+        const uint32_t mine = c == 0 ? cm0 : c == 1 ? cm1 : c == 2 ? cm2 : cm3;
+
+        // 2. fine histogram of class c
+        uint32_t fmask = 0;
+        int f;
+        {
+            const int b = hist_begin();
+            for (uint32_t bits = mine; bits; bits &= bits - 1) {
+                const int i = __ffs(bits) - 1;
+                const float x = S.xs[i * kLawThreads + tid];
+                hist_put(b, law_fine((x - m) * inv_t, c), by_mass, weight_of(x, by_mass));
+            }
+            unsigned long long above = 0, at = 0;
+            f = pick(hist_end(b, by_mass), target - base, &above, &at);
+            base += above;
+        }
+        for (uint32_t bits = mine; bits; bits &= bits - 1) {
+            const int i = __ffs(bits) - 1;
+            if (law_fine((S.xs[i * kLawThreads + tid] - m) * inv_t, c) == f) fmask |= 1u << i;
+        }
+        const unsigned long long need = target - base;  // weight to take from bin f
+
+        // 3. gather bin f's tokens from the cluster
+        if (tid == 0) S.gcount = 0;
+        __syncthreads();
+        {
+            const int n_mine = __popc(fmask);
+            int incl = n_mine;  // warp-inclusive count
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            int base_w = 0;
+            if (lane == 31 && incl) base_w = atomicAdd(&S.gcount, incl);
+            base_w = __shfl_sync(0xffffffffu, base_w, 31);
+            int pos = base_w + incl - n_mine;
+            for (uint32_t bits = fmask; bits; bits &= bits - 1, ++pos) {
+                const int i = __ffs(bits) - 1;
+                if (pos < kGatherCap) {
+                    const float x = S.xs[i * kLawThreads + tid];
+                    S.glist[pos] = GatherEntry{law_key(x), x};
+                }
+            }
+        }
+        __syncthreads();
+        cluster.sync();
+        if (warp == 0) {
+            const int cnt = lane < C ? cluster.map_shared_rank(&S, lane)->gcount : 0;
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            const bool over = __any_sync(0xffffffffu, cnt > kGatherCap);
+            const int total = __shfl_sync(0xffffffffu, incl, 31);  // lanes >= C add nothing
+            if (lane < C) S.goff[lane] = incl - cnt;
+            if (lane == 0) S.goff[kLawMaxCluster] = over ? INT_MAX : total;
+        }
+        __syncthreads();
+        const int n = S.goff[kLawMaxCluster];
+        LawCut cut;
+        if (n <= kGatherTotal) {
+            // every CTA ranks the n gathered tokens by key
+            if (tid < n) {
+                int cc = 0;
+                while (cc + 1 < C && S.goff[cc + 1] <= tid) ++cc;
+                const GatherEntry e = cluster.map_shared_rank(&S, cc)->glist[tid - S.goff[cc]];
+                S.gall[tid] = e;
+                S.gw[tid] = weight_of(e.x, by_mass);
             }
             if (tid == 0) {
-                sel_first = INT_MAX;
-                sel_last = -1;
+                S.sel_key = 0u;
+                S.sel_min = 0xFFFFFFFFu;
+                S.sel_any = 0;
+                S.sel_idx = INT_MAX;
             }
             __syncthreads();
-            if (tid < 256) {
-                for (int w = 0; w < warp; ++w) incl += scan_w[w];
-                if (tid == 255 && rr == 0 && by_mass && target == 0) sel_total = incl;
+            unsigned long long ge = 0, eq = 0;  // weight of the gathered tokens with key >= / == this one
+            uint32_t kt = 0;
+            if (tid < n) {
+                kt = S.gall[tid].key;
+                for (int u = 0; u < n; ++u) {
+                    const uint32_t ku = S.gall[u].key;
+                    const unsigned long long wu = S.gw[u];
+                    ge += ku >= kt ? wu : 0ull;
+                    eq += ku == kt ? wu : 0ull;
+                }
+                if (ge >= need) {
+                    atomicMax(&S.sel_key, kt);
+                    S.sel_any = 1;
+                }
+                atomicMin(&S.sel_min, kt);
             }
             __syncthreads();
-            if (by_mass && target == 0 && rr == 0) {
-                // the top-p target from the total kept mass
-                target = (unsigned long long)ceil(double(A.top_p) * double(sel_total));
-                if (target == 0) target = 1;
-            }
-            // the first bin (from the top) where the cumulative weight reaches the
-            // target; if rounding leaves the target out of reach, the last bin
-            // holding any weight (everything under the prefix is kept)
-            if (tid < 256 && tot > 0) {
-                if (incl >= target) atomicMin(&sel_first, tid);
-                atomicMax(&sel_last, tid);
+            // out of reach (rounding only): everything in the bin is kept
+            const uint32_t K = S.sel_any ? S.sel_key : S.sel_min;
+            if (tid < n && kt == K) atomicMin(&S.sel_idx, tid);
+            __syncthreads();
+            if (tid == S.sel_idx) {
+                S.sel_above = ge - eq;
+                S.sel_at = eq;
             }
             __syncthreads();
-            int s = sel_first != INT_MAX ? sel_first : sel_last;
-            if (s < 0) s = 0;
-            if (tid == s) {
-                sel_above = incl - tot;
-                sel_bin = tot;
+            cut.key = n > 0 ? K : lo;
+            cut.above = base + (n > 0 ? S.sel_above : 0ull);
+            cut.at = n > 0 ? S.sel_at : 0ull;
+        } else {
+            // too many to gather: radix select over the keys of bin f
+            uint32_t prefix = 0;
+            unsigned long long acc = 0, at = 0, tgt = need;
+            for (int rr = 0; rr < 4; ++rr) {
+                const int shift = 24 - 8 * rr;
+                const int b = hist_begin();
+                for (uint32_t bits = fmask; bits; bits &= bits - 1) {
+                    const int i = __ffs(bits) - 1;
+                    const float x = S.xs[i * kLawThreads + tid];
+                    const uint32_t k = law_key(x);
+                    if (rr > 0 && (k >> (shift + 8)) != prefix) continue;
+                    hist_put(b, 255 - int((k >> shift) & 255u), by_mass, weight_of(x, by_mass));
+                }
+                unsigned long long a = 0;
+                const int s = pick(hist_end(b, by_mass), tgt, &a, &at);
+                prefix = (prefix << 8) | uint32_t(255 - s);
+                acc += a;
+                tgt -= a;
             }
-            __syncthreads();
-            prefix = (prefix << 8) | uint32_t(255 - s);
-            acc_above += sel_above;
-            target -= sel_above;
-            if (rr == 3) *at = sel_bin;
-            __syncthreads();
+            cut.key = prefix;
+            cut.above = base + acc;
+            cut.at = at;
         }
-        *above = acc_above;
-        return prefix;
+        return cut;
     };
 
     if (st.ok) {
         uint32_t cut = 0;
-        unsigned long long above = 0, at = 0, S = 0;
+        unsigned long long kept = 0;
         const bool topk = A.top_k > 0 && A.top_k < V;
         const bool topp = A.top_p < 1.f;
-        if (topk) cut = select(false, 0u, (unsigned long long)A.top_k, &above, &at);
+        if (topk) cut = find_cut(false, 0u, (unsigned long long)A.top_k).key;
         if (topp) {
-            cut = select(true, cut, 0ull, &above, &at);
-            S = above + at;
+            const LawCut c = find_cut(true, cut, 0ull);
+            cut = c.key;
+            kept = c.above + c.at;
         } else {
             // the kept mass, one cluster reduction
-            unsigned long long w = 0;
-#pragma unroll
-            for (int i = 0; i < kLawChunks; ++i)
-                if (valid(i) && law_key(x[i]) >= cut) w += law_mass(law_exp(x[i], m, inv_t));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-            if (lane == 0) red_w[warp] = w;
-            __syncthreads();
-            if (tid == 0) {
-                unsigned long long t = 0;
-                for (int q = 0; q < kLawThreads / 32; ++q) t += red_w[q];
-                pub.w = t;
+            unsigned long long v[kLawVals] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll 8
+            for (int i = 0; i < kLawChunks; ++i) {
+                const float x = S.xs[i * kLawThreads + tid];  // padding: -inf, no mass
+                const unsigned long long w = law_mass(law_exp(x, m, inv_t));
+                v[0] += law_key(x) >= cut ? w : 0ull;
             }
-            cluster.sync();
-            for (int c = 0; c < C; ++c) S += cluster.map_shared_rank(&pub, c)->w;
+            cluster_sum(v);
+            kept = S.tot[0];
         }
         st.cut = cut;
-        st.inv_s = S > 0 ? float(70368744177664.0 / double(S)) : 0.f;
-        if (S == 0) st.ok = 0;
+        st.inv_s = kept > 0 ? float(70368744177664.0 / double(kept)) : 0.f;
+        if (kept == 0) st.ok = 0;
     }
     if (!st.ok && rank == 0 && tid == 0) report(A.status, MXS_DEV_NO_LAW);
     if (A.stats && rank == 0 && tid == 0) A.stats[r] = st;
     if (A.probs) {
-        float* out = A.probs + r * V;
-#pragma unroll
-        for (int i = 0; i < kLawChunks; ++i)
-            if (valid(i)) out[v0 + int64_t(i) * kLawThreads + tid] = law_value(x[i], st, inv_t);
+        float* out = A.probs + r * V + v0;
+#pragma unroll 8
+        for (int i = 0; i < kLawChunks; ++i) {
+            const int j = i * kLawThreads + tid;
+            const float v = law_value(S.xs[j], st, inv_t);
+            if (j < nv) out[j] = v;
+        }
     }
     cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
@@ -249,10 +534,13 @@ __global__ void __launch_bounds__(kLawThreads, 1) sampling_law_kernel(const LawA
 static cudaError_t launch_law(const LawArgs& A, cudaStream_t stream) {
     const int C = int((A.V + kLawSlice - 1) / kLawSlice);
     if (A.R < 1) return cudaSuccess;
+    static const cudaError_t attr_err =
+        cudaFuncSetAttribute(sampling_law_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLawSmem);
+    if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(A.R * C), 1, 1);
     cfg.blockDim = dim3(kLawThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = kLawSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;

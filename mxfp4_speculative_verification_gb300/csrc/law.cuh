@@ -35,10 +35,18 @@ __device__ __forceinline__ float law_value(float l, const LawStats& s, float inv
     return law_exp(l, s.m, inv_t) * s.inv_s;
 }
 
-// Fixed-point mass of one token (scale 2^46): sums of these are exact in any
-// order, so the top-p cut does not depend on which thread added what.
+// Fixed-point mass of one token, floor(e * 2^46) for e in [0, 1]: sums of
+// these are exact in any order, so the top-p cut does not depend on which
+// thread added what.  Taken from the bits: a normal e is M * 2^(E - 150) with
+// M its 24-bit significand and E its biased exponent, so e * 2^46 is
+// M * 2^(E - 104); zero and subnormal e (< 2^-126) give 0.
 __device__ __forceinline__ unsigned long long law_mass(float e) {
-    return __float2ull_rz(e * 70368744177664.0f);
+    const uint32_t b = __float_as_uint(e);
+    const int E = int(b >> 23);
+    const unsigned long long M = (b & 0x7FFFFFu) | 0x800000u;
+    const int sh = E - 104;
+    if (E == 0 || sh <= -24) return 0ull;
+    return sh >= 0 ? M << sh : M >> -sh;
 }
 
 }  // namespace mxs

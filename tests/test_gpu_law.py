@@ -90,6 +90,18 @@ def test_law_filters(env, temperature, top_k, top_p):
     _check_law(got, l, temperature, top_k, top_p)
 
 
+@pytest.mark.parametrize("std,kw", [(0.01, {"top_p": 0.5}), (0.01, {"top_k": 1000}), (30.0, {"top_p": 0.99}),
+                                    (3.0, {"top_k": 60000, "top_p": 0.999999}), (0.3, {"temperature": 0.05, "top_p": 0.9}),
+                                    (3.0, {"temperature": 20.0, "top_k": 5000, "top_p": 0.7})])
+def test_law_extreme_spreads(env, std, kw):
+    # flat rows (one fine bin holds thousands of tokens: the radix finish),
+    # very peaked rows, and cuts deep in the tail
+    l = _logits(8, 128256, seed=int(std * 100) + len(kw), std=std)
+    got, st = _law_gpu(env, l, **kw)
+    assert st == 0
+    _check_law(got, l, kw.get("temperature", 1.0), kw.get("top_k", 0), kw.get("top_p", 1.0))
+
+
 def test_law_ties_masked_and_rows_without_law(env):
     V = 4096
     l = _logits(5, V, seed=3)
