@@ -58,6 +58,22 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Sum of the n <= 32 split-K partials p[0], p[stride], ... added in index
+// order (the order fixes the result's bits); the loads go out 8 at a time so
+// their L2 round trips overlap.
+__device__ __forceinline__ float sum_partials(const float* p, int64_t stride, int n) {
+    float s = 0.f;
+    for (int q0 = 0; q0 < n; q0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = q0 + j < n ? __ldcg(p + int64_t(q0 + j) * stride) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (q0 + j < n) s += v[j];
+    }
+    return s;
+}
+
 struct ItemRange {
     int tile, split, kb0, kb1, nst;
 };

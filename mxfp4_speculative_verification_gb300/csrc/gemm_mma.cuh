@@ -417,10 +417,8 @@ __global__ void __launch_bounds__(GemmCfg<NT, RG, KW, STAGES, NV>::kThreads,
                 for (int o = threadIdx.x; o < C::BN * M; o += C::kConsumers) {
                     const int r = o % C::BN, m = o / C::BN;
                     if (r < rows) {
-                        float s = 0.f;
-                        for (int q = 0; q < P.nsplit; ++q)
-                            s += __ldcg(P.part + (int64_t(q) * P.ntiles + R.tile) * M * C::BN +
-                                        int64_t(m) * C::BN + r);
+                        const float s = sum_partials(P.part + int64_t(R.tile) * M * C::BN + int64_t(m) * C::BN + r,
+                                                     int64_t(P.ntiles) * M * C::BN, P.nsplit);
                         P.y[int64_t(m) * P.N + n0 + r] = NV ? (s * P.xun[m]) * P.gscale : s * P.xun[m];
                     }
                 }
