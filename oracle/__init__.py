@@ -25,6 +25,10 @@ What each entry point follows (page title, section):
 * ``sampling_law`` -- Module 11 §4 (the laws acceptance uses are the ones
   tokens are actually sampled from: temperature, then top-k, then top-p, on
   the target and the draft alike).
+* ``kv_append`` / ``kv_commit`` / ``kv_dequant`` -- the MX-FP4 KV cache of
+  "Next-Gen Speculative Decoding and FP4 Quantization ..." (pipeline diagram,
+  "Benchmarks and Real-World Impact" item 2) and Module 11 §4 (the unaccepted
+  suffix and its cache entries are discarded).
 
 Every function is pinned by ``tests/test_oracle_*.py`` against values the pages
 print, closed forms, invariants and brute force; none is "parity unpinned".
@@ -86,6 +90,12 @@ def _load():
     lib.mxs_oracle_nvfp4_gemm.restype = ctypes.c_int
     lib.mxs_oracle_sampling_law.argtypes = [p, i64, i64, ctypes.c_double, i64, ctypes.c_double, p, p, p]
     lib.mxs_oracle_sampling_law.restype = ctypes.c_int
+    lib.mxs_oracle_kv_append.argtypes = [p, i64, i64, i64, p, p, i64, p, p]
+    lib.mxs_oracle_kv_append.restype = ctypes.c_int
+    lib.mxs_oracle_kv_commit.argtypes = [p, p, i64, i64]
+    lib.mxs_oracle_kv_commit.restype = ctypes.c_int
+    lib.mxs_oracle_kv_dequant.argtypes = [p, p, i64, i64, i64, p, p]
+    lib.mxs_oracle_kv_dequant.restype = ctypes.c_int
     for name in ("mxs_oracle_spec_accept", "mxs_oracle_spec_accept_f64"):
         fn = getattr(lib, name)
         fn.argtypes = [p, p, p, p, i64, i64, i64, p, p, p, p, ctypes.c_int]
@@ -254,3 +264,53 @@ def nvfp4_gemm(x_bf16_bits: np.ndarray, nibbles: np.ndarray, scales: np.ndarray,
     if _load().mxs_oracle_nvfp4_gemm(_ptr(x), _ptr(nib), _ptr(sc), float(global_scale), M, N, K, _ptr(y)):
         raise ValueError("oracle nvfp4_gemm failed")
     return y
+
+
+def kv_append(kv: np.ndarray, nibbles: np.ndarray, scales: np.ndarray, lens: np.ndarray, *,
+              dtype: str = "f32") -> int:
+    """Quantise rows kv [B, T, W] into the cache (nibbles [B, L, W/2], scales
+    [B, L, W/32], updated in place) at positions lens[b] + t.  Returns the
+    number of rows that fell at or beyond L and were not written."""
+    if dtype == "f32":
+        kd = np.ascontiguousarray(kv, dtype=np.float32).astype(np.float64)
+    elif dtype == "bf16":
+        kd = bf16_bits_to_f64(kv)
+    else:
+        raise ValueError(dtype)
+    kd = np.ascontiguousarray(kd)
+    B, T, W = kd.shape
+    L = nibbles.shape[1]
+    assert nibbles.shape == (B, L, W // 2) and scales.shape == (B, L, W // 32)
+    assert nibbles.flags.c_contiguous and scales.flags.c_contiguous
+    assert nibbles.dtype == np.uint8 and scales.dtype == np.uint8
+    ln = np.ascontiguousarray(lens, dtype=np.int32)
+    full = np.zeros(1, dtype=np.int64)
+    rc = _load().mxs_oracle_kv_append(_ptr(kd), B, T, W, _ptr(nibbles), _ptr(scales), L, _ptr(ln), _ptr(full))
+    if rc not in (0, 4):
+        raise ValueError(f"oracle kv_append failed ({rc})")
+    return int(full[0])
+
+
+def kv_commit(lens: np.ndarray, n_emitted: np.ndarray, L: int) -> np.ndarray:
+    """New committed lengths: min(lens + max(n_emitted, 0), L)."""
+    ln = np.array(lens, dtype=np.int32, copy=True)
+    ne = np.ascontiguousarray(n_emitted, dtype=np.int32)
+    rc = _load().mxs_oracle_kv_commit(_ptr(ln), _ptr(ne), ln.size, int(L))
+    if rc:
+        raise ValueError(f"oracle kv_commit failed ({rc})")
+    return ln
+
+
+def kv_dequant(nibbles: np.ndarray, scales: np.ndarray, lens: np.ndarray) -> np.ndarray:
+    """Decoded cache [B, L, W] (float64), zero past each sequence's length."""
+    nib = _c(nibbles, np.uint8)
+    sc = _c(scales, np.uint8)
+    B, L, half = nib.shape
+    W = 2 * half
+    assert sc.shape == (B, L, W // 32)
+    ln = np.ascontiguousarray(lens, dtype=np.int32)
+    out = np.empty((B, L, W), dtype=np.float64)
+    rc = _load().mxs_oracle_kv_dequant(_ptr(nib), _ptr(sc), B, L, W, _ptr(ln), _ptr(out))
+    if rc:
+        raise ValueError(f"oracle kv_dequant failed ({rc})")
+    return out

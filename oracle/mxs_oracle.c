@@ -599,3 +599,84 @@ int mxs_oracle_nvfp4_gemm(const uint16_t* x_bf16, const uint8_t* nibbles, const 
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* MX-FP4 KV cache of the verification block                           */
+/* ------------------------------------------------------------------ */
+/*
+ * "Next-Gen Speculative Decoding and FP4 Quantization ...": keys and values
+ * are stored as MX-FP4 (the "KV Cache Memory Pool (FP4)" of its pipeline
+ * diagram; "Benchmarks and Real-World Impact", item 2).  [M11] §4: after
+ * acceptance the unaccepted suffix and its cache entries are discarded and
+ * decoding continues from the corrected prefix.
+ *
+ * Cache of one layer's keys (or values) for B sequences: nibbles
+ * [B, L_max, W/2] and E8M0 scales [B, L_max, W/32], one row of W values
+ * (all heads of one position) per position, blocks of 32 along the row.
+ * lens[b] is the number of committed positions of sequence b.
+ *
+ * kv_append: the verification pass feeds T = K + 1 positions per sequence
+ * (the last committed token and the K drafts); row t of kv [B, T, W] is
+ * quantised by mxs_oracle_pack's rule into position lens[b] + t.  A position
+ * at or beyond L_max is not written; *n_full counts them.
+ */
+int mxs_oracle_kv_append(const double* kv, int64_t B, int64_t T, int64_t W, uint8_t* nibbles,
+                         uint8_t* scales, int64_t L_max, const int32_t* lens, int64_t* n_full) {
+    if (B < 0 || T < 0 || W < 0 || W % 32 || L_max < 0) return 1;
+    int64_t full = 0;
+    int rc = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t t = 0; t < T; ++t) {
+            const int64_t pos = (int64_t)lens[b] + t;
+            if (pos < 0 || pos >= L_max) {
+                ++full;
+                continue;
+            }
+            const int r = mxs_oracle_pack(kv + (b * T + t) * W, 1, W, nibbles + (b * L_max + pos) * (W / 2),
+                                          scales + (b * L_max + pos) * (W / 32));
+            if (r == 4) rc = 4;
+            else if (r) return r;
+        }
+    }
+    if (n_full) *n_full = full;
+    return rc;
+}
+
+/*
+ * kv_commit: the verification block of sequence b emitted n_emitted[b]
+ * tokens (the accepted drafts and one replacement or bonus token; 0 for a
+ * row acceptance refused).  Its cache entries for the last committed token
+ * and the accepted drafts stay, n_emitted[b] positions in all; the entries
+ * of the rejected drafts are the discarded suffix.  So
+ * lens[b] <- min(lens[b] + n_emitted[b], L_max), and the emitted
+ * replacement or bonus token is fed, and cached, by the next pass.
+ */
+int mxs_oracle_kv_commit(int32_t* lens, const int32_t* n_emitted, int64_t B, int64_t L_max) {
+    if (B < 0 || L_max < 0) return 1;
+    for (int64_t b = 0; b < B; ++b) {
+        int64_t n = n_emitted[b] > 0 ? n_emitted[b] : 0;
+        int64_t l = (int64_t)lens[b] + n;
+        lens[b] = (int32_t)(l < L_max ? l : L_max);
+    }
+    return 0;
+}
+
+/* kv_dequant: out[b, l, :] = the decoded row at position l for l < lens[b],
+ * and 0 for the positions past the committed length. */
+int mxs_oracle_kv_dequant(const uint8_t* nibbles, const uint8_t* scales, int64_t B, int64_t L_max,
+                          int64_t W, const int32_t* lens, double* out) {
+    if (B < 0 || L_max < 0 || W < 0 || W % 32) return 1;
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t l = 0; l < L_max; ++l) {
+            double* o = out + (b * L_max + l) * W;
+            if (l < lens[b]) {
+                const int r = mxs_oracle_dequant(nibbles + (b * L_max + l) * (W / 2),
+                                                 scales + (b * L_max + l) * (W / 32), 1, W, o);
+                if (r) return r;
+            } else {
+                for (int64_t k = 0; k < W; ++k) o[k] = 0.0;
+            }
+        }
+    }
+    return 0;
+}
