@@ -534,7 +534,7 @@ def run_mxs(args, world, rank, local):
 
     # the other configurations, each timed the same way (weights of the same
     # stack reused; the 70B stack generated once on the device)
-    sweep, acc_sweep, logits_acc, nv = [], None, None, None
+    sweep, acc_sweep, logits_acc, nv, kvc = [], None, None, None, None
     if not args.no_sweep and rank == 0 and world == 1:
         wcache = {model: weights}
         clocks2 = ClockSampler(local)
@@ -555,6 +555,7 @@ def run_mxs(args, world, rank, local):
         acc_sweep = accept_sweep_rows(mxs, torch, dev, peak)
         logits_acc = logits_accept_rows(mxs, torch, dev, peak)
         nv = nvfp4_rows(mxs, torch, dev, peak)
+        kvc = kv_cache_rows(mxs, torch, dev, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -606,6 +607,7 @@ def run_mxs(args, world, rank, local):
         "accept_sweep": acc_sweep,
         "accept_logits": logits_acc,
         "nvfp4_lm_head": nv,
+        "kv_cache": kvc,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -910,6 +912,54 @@ def nvfp4_rows(mxs, torch, dev, peak, reps=20):
     torch.cuda.empty_cache()
     return {"metric": "lm_head GEMM (K=4096, N=128256), one call incl. X preparation, us per call",
             "rows": rows}
+
+
+def kv_cache_rows(mxs, torch, dev, peak, reps=20):
+    """The MX-FP4 KV cache of the 8B stack's verification block: every layer's
+    keys and values of one position (32 layers x 2 x 8 heads x 128 = 65536
+    values) as one cache row, T = K + 1 = 5 positions appended from bf16 and
+    committed, at B = 1 / 16 / 64; and the read side (the whole cache decoded
+    to fp32) at L = 1024.  Algorithmic bytes: append = bf16 rows read + nibbles
+    and scales written; dequant = the cache read + fp32 rows written."""
+    W, T, L = 65536, 5, 1024
+    rows = []
+    for B in (1, 16, 64):
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(400 + B)
+        kv = torch.randn((B, T, W), generator=gen, device=dev).to(torch.bfloat16)
+        nib = torch.zeros((B, L, W // 2), dtype=torch.uint8, device=dev)
+        sc = torch.zeros((B, L, W // 32), dtype=torch.uint8, device=dev)
+        lens = torch.full((B,), 100, dtype=torch.int32, device=dev)
+        n_emit = torch.zeros((B,), dtype=torch.int32, device=dev)  # commit 0: the lengths stay put
+        out = torch.empty((B, L, W), dtype=torch.float32, device=dev) if B == 1 else None
+
+        def step():
+            mxs.mxfp4_kv_append(kv, nib, sc, lens)
+            mxs.spec_kv_commit(lens, n_emit, L)
+
+        res = {"B": B}
+        for name, fn, nb in (("append_commit", step, B * T * W * (2 + 17 / 32)),
+                             ("dequant", (lambda: mxs.mxfp4_kv_dequant(nib, sc, lens, out=out)) if out is not None
+                              else None, B * L * W * (17 / 32 + 4))):
+            if fn is None:
+                continue
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            res[name] = {"us_per_call": us, "bytes_per_call": nb, "hbm_gbs": nb / (us * 1e-6) / 1e9,
+                         "pct_of_peak": nb / (us * 1e-6) / 1e9 / peak}
+        rows.append(res)
+        del kv, nib, sc, lens, n_emit, out
+    torch.cuda.empty_cache()
+    return {"metric": "MX-FP4 KV cache, 8B stack's keys and values (65536 values per position)",
+            "T": T, "L": L, "rows": rows}
 
 
 def accept_sweep(args):

@@ -12,6 +12,9 @@
  *                      emission of 1..K+1 tokens per sequence (also from
  *                      logits under temperature / top-k / top-p:
  *                      spec_accept_logits, spec_sampling_law)
+ *   mxfp4_kv_append,   the MX-FP4 KV cache of the verification block:
+ *   spec_kv_commit,    append, keep what acceptance kept, read back
+ *   mxfp4_kv_dequant
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -54,6 +57,7 @@ typedef int32_t mxs_status;
 #define MXS_DEV_NEAR_EDGE 0x10      /* spec_accept: u within 1e-5 of a CDF bin edge   */
 #define MXS_DEV_NONFINITE 0x20      /* mxfp4_pack: a block held Inf or NaN            */
 #define MXS_DEV_TIMEOUT 0x40        /* a bounded pipeline wait gave up                */
+#define MXS_DEV_KV_FULL 0x80        /* mxfp4_kv_append: a row fell past the cache     */
 
 /* Input element types for mxfp4_pack. */
 #define MXS_F32 0
@@ -181,6 +185,49 @@ mxs_status nvfp4_verify_gemm(const void* x, const uint8_t* nibbles,
                              float* y, int64_t M, int64_t N, int64_t K,
                              void* workspace, size_t workspace_bytes,
                              int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * MX-FP4 KV cache of the verification block
+ *
+ * Keys and values stored as MX-FP4 ("Next-Gen Speculative Decoding and FP4
+ * Quantization ...": the "KV Cache Memory Pool (FP4)" of its pipeline
+ * diagram, "Benchmarks and Real-World Impact" item 2), and the unaccepted
+ * suffix's entries discarded after acceptance ("Module 11 ...", §4).
+ *
+ * One cache holds one layer's keys (or values) for B sequences: nibbles
+ * [B, L, W/2] and E8M0 scales [B, L, W/32] uint8, one row of W values (all
+ * heads of one position, W % 32 == 0) per position, in the mxfp4_pack format;
+ * lens [B] int32 (device) holds each sequence's committed length.
+ *
+ * mxfp4_kv_append: the verification pass feeds T = K + 1 positions per
+ * sequence (the last committed token, then the K drafts).  Row t of
+ * kv [B, T, W] (fp32 or bf16 by kv_dtype, 16-byte aligned) is packed by the
+ * mxfp4_pack rule into position lens[b] + t.  Positions outside [0, L) are
+ * not written and set MXS_DEV_KV_FULL; a non-finite block sets
+ * MXS_DEV_NONFINITE.  lens is read, not changed.
+ *
+ * spec_kv_commit: lens[b] <- min(lens[b] + max(n_emitted[b], 0), L), with
+ * n_emitted as spec_accept writes it.  The entries of the last committed
+ * token and of the accepted drafts stay; the rejected drafts' entries are
+ * the discarded suffix (overwritten by the next append); the replacement or
+ * bonus token is fed, and cached, by the next pass.  A refused row (0
+ * tokens) commits nothing.
+ *
+ * mxfp4_kv_dequant: out [B, L, W] fp32 (16-byte aligned) = the decoded
+ * cache, exact, and 0 at every position l >= lens[b].
+ *
+ * Sizes: B, T >= 0, L >= 1, W >= 32, W % 32 == 0, B * L * W < 2^40.
+ * ---------------------------------------------------------------------- */
+mxs_status mxfp4_kv_append(const void* kv, int32_t kv_dtype, int64_t B, int64_t T,
+                           int64_t W, uint8_t* nibbles, uint8_t* scales, int64_t L,
+                           const int32_t* lens, int32_t* dev_status, void* stream);
+
+mxs_status spec_kv_commit(int32_t* lens, const int32_t* n_emitted, int64_t B,
+                          int64_t L, void* stream);
+
+mxs_status mxfp4_kv_dequant(const uint8_t* nibbles, const uint8_t* scales,
+                            int64_t B, int64_t L, int64_t W,
+                            const int32_t* lens, float* out, void* stream);
 
 /* ------------------------------------------------------------------------
  * mxfp4_verify_gemm_grouped -- many independent verify GEMMs in one go

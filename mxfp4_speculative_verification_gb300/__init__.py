@@ -7,7 +7,9 @@ The calls of the C ABI (``include/mxs.h``) under the same names:
   grouped, without workspace, and :func:`nvfp4_verify_gemm` on NVFP4 weights);
 * :func:`spec_accept` -- acceptance, residual / bonus sampling, emission
   (also :func:`spec_accept_logits` from logits under temperature / top-k /
-  top-p, and :func:`spec_sampling_law` for the law itself).
+  top-p, and :func:`spec_sampling_law` for the law itself);
+* :func:`mxfp4_kv_append`, :func:`spec_kv_commit`, :func:`mxfp4_kv_dequant` --
+  the MX-FP4 KV cache of the verification block.
 
 This module only marshals arguments: it checks dtypes, shapes and devices,
 allocates the output tensors with torch, and passes raw device pointers and
@@ -28,7 +30,7 @@ from . import _build
 __all__ = ["build", "lib", "mxfp4_pack", "mxfp4_verify_gemm", "mxfp4_verify_gemm_workspace_size",
            "mxfp4_verify_gemm_grouped", "mxfp4_verify_gemm_grouped_workspace_size",
            "mxfp4_verify_gemm_noalloc", "nvfp4_verify_gemm", "nvfp4_verify_gemm_workspace_size",
-           "spec_accept", "spec_sampling_law", "spec_accept_logits",
+           "spec_accept", "mxfp4_kv_append", "spec_kv_commit", "mxfp4_kv_dequant", "spec_sampling_law", "spec_accept_logits",
            "spec_accept_logits_workspace_size", "hbm_read_probe", "hbm_copy_probe", "MxsError",
            "DEV_FLAGS",
            "declared_symbols"]
@@ -36,7 +38,7 @@ __all__ = ["build", "lib", "mxfp4_pack", "mxfp4_verify_gemm", "mxfp4_verify_gemm
 MXS_F32, MXS_BF16 = 0, 1
 DEV_FLAGS = {
     "BAD_DRAFT": 0x1, "ZERO_Q": 0x2, "ZERO_RESIDUAL": 0x4, "NO_LAW": 0x8,
-    "NEAR_EDGE": 0x10, "NONFINITE": 0x20, "TIMEOUT": 0x40,
+    "NEAR_EDGE": 0x10, "NONFINITE": 0x20, "TIMEOUT": 0x40, "KV_FULL": 0x80,
 }
 
 _lib = None
@@ -78,6 +80,12 @@ def lib():
     L.nvfp4_verify_gemm_workspace_size.restype = sz
     L.nvfp4_verify_gemm.argtypes = [vp, vp, vp, ctypes.c_float, vp, i64, i64, i64, vp, sz, vp, vp]
     L.nvfp4_verify_gemm.restype = i32
+    L.mxfp4_kv_append.argtypes = [vp, i32, i64, i64, i64, vp, vp, i64, vp, vp, vp]
+    L.mxfp4_kv_append.restype = i32
+    L.spec_kv_commit.argtypes = [vp, vp, i64, i64, vp]
+    L.spec_kv_commit.restype = i32
+    L.mxfp4_kv_dequant.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp]
+    L.mxfp4_kv_dequant.restype = i32
     L.mxfp4_verify_gemm_grouped_workspace_size.argtypes = [vp, i32, i64]
     L.mxfp4_verify_gemm_grouped_workspace_size.restype = sz
     L.mxfp4_verify_gemm_grouped.argtypes = [vp, i32, i64, vp, sz, vp, vp]
@@ -240,6 +248,59 @@ def nvfp4_verify_gemm(x: torch.Tensor, nibbles: torch.Tensor, scales: torch.Tens
     _check(lib().nvfp4_verify_gemm(_ptr(x), _ptr(nibbles), _ptr(scales), float(global_scale), _ptr(out), M, N, K,
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _ptr(dev_status), _stream(dev)))
+    return out
+
+
+def _kv_cache_shapes(nibbles: torch.Tensor, scales: torch.Tensor, lens: torch.Tensor):
+    """(B, L, W) of an MX-FP4 KV cache, checked."""
+    if nibbles.dtype != torch.uint8 or scales.dtype != torch.uint8 or nibbles.dim() != 3:
+        raise MxsError("cache nibbles and scales must be 3-D uint8 tensors [B, L, W/2] and [B, L, W/32]")
+    B, L, half = nibbles.shape
+    W = 2 * half
+    if W % 32 != 0 or W < 32 or tuple(scales.shape) != (B, L, W // 32):
+        raise MxsError("cache shapes must be [B, L, W/2] and [B, L, W/32] with W % 32 == 0")
+    if lens.dtype != torch.int32 or tuple(lens.shape) != (B,):
+        raise MxsError("lens must be an int32 tensor [B]")
+    return B, L, W
+
+
+def mxfp4_kv_append(kv: torch.Tensor, nibbles: torch.Tensor, scales: torch.Tensor, lens: torch.Tensor, *,
+                    dev_status: torch.Tensor | None = None) -> None:
+    """Pack kv [B, T, W] (fp32 or bf16) into the cache at positions lens[b] + t."""
+    B, L, W = _kv_cache_shapes(nibbles, scales, lens)
+    if kv.dim() != 3 or kv.shape[0] != B or kv.shape[2] != W:
+        raise MxsError("kv must be [B, T, W] matching the cache")
+    if kv.dtype == torch.float32:
+        dt = MXS_F32
+    elif kv.dtype == torch.bfloat16:
+        dt = MXS_BF16
+    else:
+        raise MxsError("kv must be float32 or bfloat16")
+    _check_status(dev_status)
+    dev = _need_cuda(kv, nibbles, scales, lens, dev_status)
+    _check(lib().mxfp4_kv_append(_ptr(kv), dt, B, kv.shape[1], W, _ptr(nibbles), _ptr(scales), L, _ptr(lens),
+                                 _ptr(dev_status), _stream(dev)))
+
+
+def spec_kv_commit(lens: torch.Tensor, n_emitted: torch.Tensor, L: int) -> None:
+    """lens[b] <- min(lens[b] + n_emitted[b], L) in place (the rejected suffix is discarded)."""
+    if lens.dtype != torch.int32 or n_emitted.dtype != torch.int32 or lens.dim() != 1 \
+            or tuple(n_emitted.shape) != tuple(lens.shape):
+        raise MxsError("lens and n_emitted must be int32 tensors [B]")
+    dev = _need_cuda(lens, n_emitted)
+    _check(lib().spec_kv_commit(_ptr(lens), _ptr(n_emitted), lens.shape[0], int(L), _stream(dev)))
+
+
+def mxfp4_kv_dequant(nibbles: torch.Tensor, scales: torch.Tensor, lens: torch.Tensor, *,
+                     out: torch.Tensor | None = None) -> torch.Tensor:
+    """The decoded cache [B, L, W] (fp32), zero past each sequence's length."""
+    B, L, W = _kv_cache_shapes(nibbles, scales, lens)
+    if out is None:
+        out = torch.empty((B, L, W), dtype=torch.float32, device=nibbles.device)
+    elif out.dtype != torch.float32 or tuple(out.shape) != (B, L, W):
+        raise MxsError("out must be a float32 tensor [B, L, W]")
+    dev = _need_cuda(nibbles, scales, lens, out)
+    _check(lib().mxfp4_kv_dequant(_ptr(nibbles), _ptr(scales), B, L, W, _ptr(lens), _ptr(out), _stream(dev)))
     return out
 
 

@@ -1,5 +1,6 @@
 // The C ABI of libmxs (declared in include/mxs.h): host-side validation,
 // then the launchers in gemm.cu, accept.cu and pack.cu.
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <vector>
@@ -104,6 +105,40 @@ mxs_status nvfp4_verify_gemm(const void* x, const uint8_t* nibbles, const uint8_
     if (!aligned(workspace, 16)) return MXS_ERR_MISALIGNED;
     return cuda_status(mxs::gemm_run_nv(static_cast<const uint16_t*>(x), nibbles, scales, global_scale, y,
                                         M, N, K, workspace, ws, dev_status, as_stream(stream)));
+}
+
+static bool kv_sizes_ok(int64_t B, int64_t L, int64_t W) {
+    return B >= 0 && L >= 1 && W >= 32 && W % 32 == 0 && B <= (int64_t(1) << 31) &&
+           (B == 0 || L <= ((int64_t(1) << 40) / W) / B) && L <= INT32_MAX;
+}
+
+mxs_status mxfp4_kv_append(const void* kv, int32_t kv_dtype, int64_t B, int64_t T, int64_t W, uint8_t* nibbles,
+                           uint8_t* scales, int64_t L, const int32_t* lens, int32_t* dev_status, void* stream) {
+    if (kv_dtype != MXS_F32 && kv_dtype != MXS_BF16) return MXS_ERR_INVALID_ARG;
+    if (T < 0 || !kv_sizes_ok(B, L, W)) return MXS_ERR_INVALID_ARG;
+    if (T > (int64_t(1) << 20)) return MXS_ERR_UNSUPPORTED;
+    if (B == 0 || T == 0) return MXS_OK;
+    if (!kv || !nibbles || !scales || !lens) return MXS_ERR_INVALID_ARG;
+    if (!aligned(kv, 16) || !aligned(lens, 4) || !aligned(dev_status, 4)) return MXS_ERR_MISALIGNED;
+    return cuda_status(mxs::kv_append_run(kv, kv_dtype, B, T, W, nibbles, scales, L, lens, dev_status,
+                                          as_stream(stream)));
+}
+
+mxs_status spec_kv_commit(int32_t* lens, const int32_t* n_emitted, int64_t B, int64_t L, void* stream) {
+    if (B < 0 || L < 1 || L > INT32_MAX) return MXS_ERR_INVALID_ARG;
+    if (B == 0) return MXS_OK;
+    if (!lens || !n_emitted) return MXS_ERR_INVALID_ARG;
+    if (!aligned(lens, 4) || !aligned(n_emitted, 4)) return MXS_ERR_MISALIGNED;
+    return cuda_status(mxs::kv_commit_run(lens, n_emitted, B, L, as_stream(stream)));
+}
+
+mxs_status mxfp4_kv_dequant(const uint8_t* nibbles, const uint8_t* scales, int64_t B, int64_t L, int64_t W,
+                            const int32_t* lens, float* out, void* stream) {
+    if (!kv_sizes_ok(B, L, W)) return MXS_ERR_INVALID_ARG;
+    if (B == 0) return MXS_OK;
+    if (!nibbles || !scales || !lens || !out) return MXS_ERR_INVALID_ARG;
+    if (!aligned(nibbles, 16) || !aligned(lens, 4) || !aligned(out, 16)) return MXS_ERR_MISALIGNED;
+    return cuda_status(mxs::kv_dequant_run(nibbles, scales, B, L, W, lens, out, as_stream(stream)));
 }
 
 size_t mxfp4_verify_gemm_grouped_workspace_size(const mxs_gemm_problem* problems, int32_t count,

@@ -36,6 +36,13 @@ cudaError_t gemm_run_nv(const uint16_t* x, const uint8_t* nibbles, const uint8_t
                         float* y, int64_t M, int64_t N, int64_t K, void* workspace, const GemmWorkspace& ws,
                         int32_t* dev_status, cudaStream_t stream);
 
+// MX-FP4 KV cache of the verification block (kv.cu).
+cudaError_t kv_append_run(const void* kv, int kv_dtype, int64_t B, int64_t T, int64_t W, uint8_t* nibbles,
+                          uint8_t* scales, int64_t L, const int32_t* lens, int32_t* dev_status, cudaStream_t stream);
+cudaError_t kv_commit_run(int32_t* lens, const int32_t* n_emitted, int64_t B, int64_t L, cudaStream_t stream);
+cudaError_t kv_dequant_run(const uint8_t* nibbles, const uint8_t* scales, int64_t B, int64_t L, int64_t W,
+                           const int32_t* lens, float* out, cudaStream_t stream);
+
 // One GEMM of a grouped call (independent GEMMs sharing M <= 64).
 struct GroupedGemm {
     const uint16_t* x;

@@ -9,6 +9,7 @@
 //
 // One thread per 32-element block; element-wise and bandwidth-bound, off the
 // verification path.
+#include "mx_block.cuh"
 #include "mxs_device.cuh"
 #include "mxs_internal.h"
 
@@ -23,19 +24,6 @@ __device__ __forceinline__ float load_elem<uint16_t>(const uint16_t* w, int64_t 
     return __uint_as_float(uint32_t(w[i]) << 16);
 }
 
-__device__ __forceinline__ float exact_pow2(int e) {  // e in [-149, 127]
-    if (e >= -126) return __uint_as_float(uint32_t(e + 127) << 23);
-    return __uint_as_float(1u << (e + 149));
-}
-
-// Grid code (0..7) of a in [0, 6]: count of decision boundaries passed.
-// Midpoints 0.25, 1.25, 2.5, 5 tie to the lower (even) code, midpoints
-// 0.75, 1.75, 3.5 tie to the upper (even) code.
-__device__ __forceinline__ uint32_t e2m1_magnitude_code(float a) {
-    return uint32_t(a > 0.25f) + uint32_t(a >= 0.75f) + uint32_t(a > 1.25f) +
-           uint32_t(a >= 1.75f) + uint32_t(a > 2.5f) + uint32_t(a >= 3.5f) + uint32_t(a > 5.0f);
-}
-
 template <typename T>
 __global__ void __launch_bounds__(256)
     mxfp4_pack_kernel(const T* __restrict__ w, int64_t N, int64_t K, uint8_t* __restrict__ nib,
@@ -47,41 +35,9 @@ __global__ void __launch_bounds__(256)
         const int64_t n = i / nblk, blk = i - n * nblk;
         const int64_t base = n * K + blk * 32;
         float v[32];
-        float amax = 0.f;
-        bool finite = true;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            v[k] = load_elem<T>(w, base + k);
-            const float a = fabsf(v[k]);
-            if (!(a <= 3.402823466e38f)) finite = false;  // Inf or NaN
-            else amax = fmaxf(amax, a);
-        }
-        uint8_t* out = nib + n * (K / 2) + blk * 16;
-        if (!finite) {
-            sc[i] = 255;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) out[k] = 0;
-            report(status, MXS_DEV_NONFINITE);
-            continue;
-        }
-        int e = 0;
-        if (amax > 0.f) {
-            const uint32_t bits = __float_as_uint(amax);
-            const int ex = int(bits >> 23);
-            const uint32_t man = bits & 0x7FFFFFu;
-            e = (ex == 0) ? -127 : ex - 129 + (man > 0x400000u ? 1 : 0);
-            e = max(-127, min(127, e));
-        }
-        sc[i] = uint8_t(e + 127);
-        const float inv = exact_pow2(-e);
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-            const uint32_t c0 = e2m1_magnitude_code(fabsf(v[k]) * inv) |
-                                ((__float_as_uint(v[k]) >> 31) << 3);
-            const uint32_t c1 = e2m1_magnitude_code(fabsf(v[k + 1]) * inv) |
-                                ((__float_as_uint(v[k + 1]) >> 31) << 3);
-            out[k / 2] = uint8_t(c0 | (c1 << 4));
-        }
+        for (int k = 0; k < 32; ++k) v[k] = load_elem<T>(w, base + k);
+        if (!pack_block32(v, nib + n * (K / 2) + blk * 16, sc + i)) report(status, MXS_DEV_NONFINITE);
     }
 }
 

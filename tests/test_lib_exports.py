@@ -74,6 +74,26 @@ def test_nvfp4_gemm_rules_on_host(L):
     assert f(FAKE, FAKE, FAKE, 1.0, FAKE, 5, 64, 512, FAKE, 16, None, None) == 5
 
 
+def test_kv_cache_calls_reject_bad_arguments_on_host(L):
+    f = L.mxfp4_kv_append
+    assert f(FAKE, 2, 2, 5, 1024, FAKE, FAKE, 64, FAKE, None, None) == 1           # dtype
+    assert f(FAKE, 0, 2, 5, 1000, FAKE, FAKE, 64, FAKE, None, None) == 1           # W % 32
+    assert f(FAKE, 0, 2, 5, 1024, FAKE, FAKE, 0, FAKE, None, None) == 1            # L
+    assert f(FAKE, 0, -1, 5, 1024, FAKE, FAKE, 64, FAKE, None, None) == 1
+    assert f(FAKE, 0, 2, 0, 1024, None, None, 64, None, None, None) == 0           # nothing to append
+    assert f(None, 0, 2, 5, 1024, FAKE, FAKE, 64, FAKE, None, None) == 1
+    assert f(FAKE + 4, 0, 2, 5, 1024, FAKE, FAKE, 64, FAKE, None, None) == 2       # kv 16 B
+    assert f(FAKE, 0, 2, 5, 1024, FAKE, FAKE, 64, FAKE + 2, None, None) == 2       # lens 4 B
+    g = L.spec_kv_commit
+    assert g(FAKE, FAKE, 4, 0, None) == 1 and g(None, FAKE, 4, 64, None) == 1 and g(FAKE + 1, FAKE, 4, 64, None) == 2
+    assert g(None, None, 0, 64, None) == 0
+    h = L.mxfp4_kv_dequant
+    assert h(FAKE, FAKE, 2, 64, 100, FAKE, FAKE, None) == 1                        # W % 32
+    assert h(FAKE, FAKE, 2, 64, 1024, FAKE, None, None) == 1
+    assert h(FAKE, FAKE, 2, 64, 1024, FAKE, FAKE + 4, None) == 2                   # out 16 B
+    assert h(FAKE, FAKE, 1 << 20, 1 << 20, 1024, FAKE, FAKE, None) == 1            # size limit
+
+
 def test_accept_rejects_bad_arguments_on_host(L):
     f = L.spec_accept
     assert f(FAKE, FAKE, FAKE, FAKE, 0, 3, 8, FAKE, FAKE, None, None, None) == 1
