@@ -510,9 +510,14 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                     __threadfence();
                     if (r < rows)
                         for (int m = 0; m < M; ++m) {
-                            const float s =
-                                sum_partials(pb.part + int64_t(RI.tile) * M * kBsRows + int64_t(m) * kBsRows + r,
-                                             int64_t(pb.ntiles) * M * kBsRows, pb.nsplit);
+                            const float* pp = pb.part + int64_t(RI.tile) * M * kBsRows + int64_t(m) * kBsRows + r;
+                            const int64_t stride = int64_t(pb.ntiles) * M * kBsRows;
+                            float s = 0.f;
+                            if constexpr (G == 1) {
+                                s = sum_partials(pp, stride, pb.nsplit);
+                            } else {
+                                for (int sp = 0; sp < pb.nsplit; ++sp) s += __ldcg(pp + int64_t(sp) * stride);
+                            }
                             pb.y[int64_t(m) * Ny + n0 + r] = s * xun[m];
                         }
                     if (lane == 0) pb.counters[4 * RI.tile + q] = 0;  // ready for the next call
