@@ -51,11 +51,11 @@ FALLBACK_HBM_GBS = 6800.0
 # sources).
 GEMM_TRAFFIC = {
     # mxfp4_gemm_kernel, passes of <= 8 rows: lm_head 4096 x 128256 at M=5
-    "mma": {"ratio": 1.0049, "sha": "ed7d8461370ecdec"},
+    "mma": {"ratio": 1.0064, "sha": "9ae7e066d3872169"},
     # mxfp4_gemm_bs_kernel, kind::mxf8f6f4 (passes of 33..64 rows): lm_head at M=64
-    "bs8": {"ratio": 0.9171, "sha": "ccc56ef6a2c1e0c7"},
+    "bs8": {"ratio": 0.9172, "sha": "0155ba7702062541"},
     # mxfp4_gemm_bs_kernel, kind::mxf4 (passes of 9..32 rows): lm_head at M=20
-    "bs4": {"ratio": 0.9853, "sha": "ccc56ef6a2c1e0c7"},
+    "bs4": {"ratio": 0.9848, "sha": "0155ba7702062541"},
 }
 BS_MIN_ROWS = 9     # passes of at least this many rows run on the block-scaled kernel
 BS4_MAX_ROWS = 32   # its mxf4 kind takes passes of up to this many rows

@@ -510,13 +510,14 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                     __threadfence();
                     if (r < rows)
                         for (int m = 0; m < M; ++m) {
-                            const float* pp = pb.part + int64_t(RI.tile) * M * kBsRows + int64_t(m) * kBsRows + r;
-                            const int64_t stride = int64_t(pb.ntiles) * M * kBsRows;
                             float s = 0.f;
                             if constexpr (G == 1) {
-                                s = sum_partials(pp, stride, pb.nsplit);
+                                s = sum_partials(pb.part + int64_t(RI.tile) * M * kBsRows + int64_t(m) * kBsRows + r,
+                                                 int64_t(pb.ntiles) * M * kBsRows, pb.nsplit);
                             } else {
-                                for (int sp = 0; sp < pb.nsplit; ++sp) s += __ldcg(pp + int64_t(sp) * stride);
+                                for (int sp = 0; sp < pb.nsplit; ++sp)
+                                    s += __ldcg(pb.part + (int64_t(sp) * pb.ntiles + RI.tile) * M * kBsRows +
+                                                int64_t(m) * kBsRows + r);
                             }
                             pb.y[int64_t(m) * Ny + n0 + r] = s * xun[m];
                         }

@@ -417,16 +417,17 @@ __global__ void __launch_bounds__(GemmCfg<NT, RG, KW, STAGES, NV>::kThreads,
                 for (int o = threadIdx.x; o < C::BN * M; o += C::kConsumers) {
                     const int r = o % C::BN, m = o / C::BN;
                     if (r < rows) {
-                        const float* pp = P.part + int64_t(R.tile) * M * C::BN + int64_t(m) * C::BN + r;
-                        const int64_t stride = int64_t(P.ntiles) * M * C::BN;
                         float s = 0.f;
                         // a single GEMM's tail waits on this sum; the grouped
-                        // kernel's register allocation runs its main loop
-                        // faster with the plain loop (same-box A/B)
+                        // kernel's main loop is faster as compiled with the
+                        // plain loop (same-box A/B)
                         if constexpr (G == 1) {
-                            s = sum_partials(pp, stride, P.nsplit);
+                            s = sum_partials(P.part + int64_t(R.tile) * M * C::BN + int64_t(m) * C::BN + r,
+                                             int64_t(P.ntiles) * M * C::BN, P.nsplit);
                         } else {
-                            for (int q = 0; q < P.nsplit; ++q) s += __ldcg(pp + int64_t(q) * stride);
+                            for (int q = 0; q < P.nsplit; ++q)
+                                s += __ldcg(P.part + (int64_t(q) * P.ntiles + R.tile) * M * C::BN +
+                                            int64_t(m) * C::BN + r);
                         }
                         P.y[int64_t(m) * P.N + n0 + r] = NV ? (s * P.xun[m]) * P.gscale : s * P.xun[m];
                     }
