@@ -567,8 +567,10 @@ constexpr int64_t kRegMaxV = int64_t(kMaxCluster) * kAcceptThreads * 4 * 8;  // 
 // LG = true: the laws are given as logits with per-row statistics (law.cu),
 // and every probability is formed on the fly from them: the rows of
 // probabilities are never written.
+// Reload forms ask for two CTAs per SM, except when each value is formed from
+// a logit: the law's temporaries then spilled at that budget.
 template <bool VEC, bool RELOAD, int CH, bool LG = false>
-__global__ void __launch_bounds__(kAcceptThreads, RELOAD ? 2 : 1)
+__global__ void __launch_bounds__(kAcceptThreads, RELOAD && !LG ? 2 : 1)
     spec_accept_reg_kernel(const AcceptParams P) {
     constexpr int kRegChunks = CH;
     constexpr int kRegSlice = kAcceptThreads * 4 * kRegChunks;  // elements per CTA
@@ -894,6 +896,7 @@ static cudaError_t launch_reg(const AcceptParams& P, int64_t B, int64_t V, bool 
     if (e != cudaSuccess) return e;
     const int64_t ctas = int64_t(B) * C;
     int form = 2 * ctas <= int64_t(sms) ? 0 : (ctas <= 2 * int64_t(sms) ? 1 : 2);
+    if (LG && form == 2) form = 1;  // one CTA per SM either way; the wide slice would spill
     if (const char* f = std::getenv("MXS_ACCEPT_FORM")) form = std::atoi(f) == 1 ? 1 : (std::atoi(f) == 2 ? 2 : 0);
     if (int64_t(B) * 4 > int64_t(INT32_MAX)) return cudaErrorInvalidConfiguration;  // grid size
     void (*kern)(AcceptParams);

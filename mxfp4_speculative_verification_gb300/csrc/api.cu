@@ -225,8 +225,8 @@ mxs_status spec_accept_logits(const float* target_logits, const float* draft_log
     mxs::LawStats* pst = static_cast<mxs::LawStats*>(workspace);
     mxs::LawStats* qst = reinterpret_cast<mxs::LawStats*>(static_cast<char*>(workspace) +
                                                           size_t(B) * size_t(K + 1) * mxs::kLawStatsBytes);
-    cudaError_t e = mxs::law_stats_run(target_logits, B * (K + 1), V, ls, pst, dev_status, st);
-    if (e == cudaSuccess && K > 0) e = mxs::law_stats_run(draft_logits, B * K, V, ls, qst, dev_status, st);
+    // the target's and the draft's rows in one launch (qst follows pst)
+    cudaError_t e = mxs::law_stats_run2(target_logits, B * (K + 1), draft_logits, B * K, V, ls, pst, dev_status, st);
     if (e == cudaSuccess)
         e = mxs::accept_logits_run(target_logits, draft_logits, pst, qst, 1.0f / sampling->temperature, draft,
                                    u, B, K, V, out_tokens, n_emitted, row_flags, dev_status, st);

@@ -19,13 +19,13 @@
 // Each cut (by token count for top-k, by mass for top-p) is found in three
 // narrowing steps over tokens ordered by their log-mass a = (l - m) / T,
 // which is monotone in the key:
-//  1. one pass over the slice sums the weight of four classes, a in (-2, 0],
-//     (-4, -2], (-8, -4] and below, in registers; one cluster exchange gives
+//  1. one pass over the slice sums the weight of four classes, a in (-4, 0],
+//     (-8, -4], (-16, -8] and below, in registers; one cluster exchange gives
 //     the class where the cumulative weight reaches the target;
-//  2. the tokens of that class fill a 256-bin histogram of finer log-mass
-//     steps; one exchange gives the bin;
-//  3. the tokens of that bin (typically a handful) are gathered from every
-//     CTA, and each CTA ranks them by key exactly.
+//  2. the tokens of that class fill a 512-bin histogram of finer log-mass
+//     steps (1/128 nat in the top classes); one exchange gives the bin;
+//  3. the tokens of that bin (typically tens) are gathered from every CTA,
+//     and each CTA ranks them by key exactly.
 // If the bin holds too many tokens to gather, a radix select over its keys
 // (4 rounds of 8 bits, one exchange each) finishes instead.  Every step is a
 // function of the row alone, so all CTAs of a cluster take the same
@@ -48,14 +48,16 @@ constexpr int kLawWarps = kLawThreads / 32;
 constexpr int kLawChunks = 32;  // logits per thread
 constexpr int kLawMaxCluster = 8;
 constexpr int64_t kLawSlice = int64_t(kLawThreads) * kLawChunks;
-constexpr int kLawBins = 256;
+constexpr int kLawBins = 512;  // one fine-histogram bin per thread
 constexpr int kGatherCap = 128;    // tokens one CTA may contribute to a gather
 constexpr int kGatherTotal = 256;  // tokens a cluster may gather
 constexpr int kLawVals = 4;        // values one step publishes to the cluster
 static_assert(kLawMaxV == kLawMaxCluster * kLawSlice, "vocabulary limit");
 
 struct LawArgs {
-    const float* logits;  // [R, V]
+    const float* logits;   // rows 0 .. R1-1: [R1, V]
+    const float* logits2;  // rows R1 .. R-1: [R - R1, V] (a second tensor, one launch for both)
+    int64_t R1;
     int64_t R, V;
     float inv_t;
     int64_t top_k;        // 0 or >= V: no top-k
@@ -78,7 +80,7 @@ struct LawSmem {
     unsigned long long gw[kGatherTotal]; // and their weights
     unsigned long long red[kLawWarps][kLawVals];
     unsigned long long tot[kLawVals];    // cluster sums
-    unsigned long long scan_w[8];
+    unsigned long long scan_w[kLawWarps];
     unsigned long long sel_above, sel_at, sel_total;
     int gcount;                          // tokens found for the gather (may exceed the cap)
     int goff[kLawMaxCluster + 1];
@@ -92,20 +94,21 @@ struct LawSmem {
 };
 constexpr int kLawSmem = int(sizeof(LawSmem));
 
-// Log-mass class of a token, a = (l - m) / T <= 0: 0 for a > -2, 1 for
-// (-4, -2], 2 for (-8, -4], 3 below.
+// Log-mass class of a token, a = (l - m) / T <= 0: 0 for a > -4, 1 for
+// (-8, -4], 2 for (-16, -8], 3 below.  (On logits like N(0, 3) at T = 0.8 the
+// top-p 0.9 cut lies 7 to 9 nats below the maximum.)
 __device__ __forceinline__ int law_class(float a) {
-    return int(a <= -2.f) + int(a <= -4.f) + int(a <= -8.f);
+    return int(a <= -4.f) + int(a <= -8.f) + int(a <= -16.f);
 }
 
 // Fine bin of a token within its class (0 holds the largest logits): steps
-// of 1/128 nat in classes 0 and 1, 1/64 in class 2, 1/8 in class 3 (bin 255
-// also takes every token 40 or more below the maximum).  Monotone in a.
+// of 1/128 nat in classes 0 and 1, 1/64 in class 2, 1/16 in class 3 (bin 511
+// also takes every token 48 or more below the maximum).  Monotone in a.
 __device__ __forceinline__ int law_fine(float a, int c) {
-    const float lo = c == 0 ? 0.f : c == 1 ? 2.f : c == 2 ? 4.f : 8.f;
-    const float sc = c <= 1 ? 128.f : c == 2 ? 64.f : 8.f;
+    const float lo = c == 0 ? 0.f : c == 1 ? 4.f : c == 2 ? 8.f : 16.f;
+    const float sc = c <= 1 ? 128.f : c == 2 ? 64.f : 16.f;
     const float f = (-a - lo) * sc;
-    return f >= 255.f ? 255 : int(f);
+    return f >= float(kLawBins - 1) ? kLawBins - 1 : int(f);
 }
 
 // Sum of a 64-bit value over a warp (two 32-bit shuffles per step).
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
 
     // ---- the slice into shared memory; its largest finite logit, and NaN / +inf
     {
-        const float* row = A.logits + r * V + v0;
+        const float* row = (r < A.R1 ? A.logits + r * V : A.logits2 + (r - A.R1) * V) + v0;
         float mx = -INFINITY;
         int bad = 0;
 #pragma unroll
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
         if (old + lo < old) ++hi;
         if (hi) atomicAdd(&hist_hi[b][bin], hi);
     };
-    // After every CTA filled buffer b: the cluster's weight at bin tid (tid < 256).
+    // After every CTA filled buffer b: the cluster's weight at bin tid.
     auto hist_end = [&](int b, bool by_mass) -> unsigned long long {
         __syncthreads();
         cluster.sync();
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
             }
         return t;
     };
-    // From the weights at positions 0..255 (tid < 256; position 0 first): the
+    // From the weights at positions 0..511 (one per thread; position 0 first): the
     // first position where the cumulative weight reaches target or, if that
     // is out of reach, the last position holding any weight.  *above: weight
     // before it; *at: its weight.
@@ -327,9 +330,9 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
                 const unsigned long long w = in ? weight_of(x, by_mass) : 0ull;
                 const float a = (x - m) * inv_t;
                 v[0] += w;
-                v[1] += a > -2.f ? w : 0ull;
-                v[2] += a > -4.f ? w : 0ull;
-                v[3] += a > -8.f ? w : 0ull;
+                v[1] += a > -4.f ? w : 0ull;
+                v[2] += a > -8.f ? w : 0ull;
+                v[3] += a > -16.f ? w : 0ull;
                 const int cl = law_class(a);
                 const uint32_t bit = w ? 1u << i : 0u;
                 cm0 |= cl == 0 ? bit : 0u;
@@ -555,6 +558,8 @@ static cudaError_t launch_law(const LawArgs& A, cudaStream_t stream) {
 static LawArgs law_args(const float* logits, int64_t R, int64_t V, const LawSampling& s, int32_t* status) {
     LawArgs A{};
     A.logits = logits;
+    A.logits2 = nullptr;
+    A.R1 = R;
     A.R = R;
     A.V = V;
     A.inv_t = 1.0f / s.temperature;
@@ -574,6 +579,15 @@ cudaError_t sampling_law_run(const float* logits, int64_t R, int64_t V, const La
 cudaError_t law_stats_run(const float* logits, int64_t R, int64_t V, const LawSampling& s, LawStats* stats,
                           int32_t* dev_status, cudaStream_t stream) {
     LawArgs A = law_args(logits, R, V, s, dev_status);
+    A.stats = stats;
+    return launch_law(A, stream);
+}
+
+cudaError_t law_stats_run2(const float* logits_a, int64_t Ra, const float* logits_b, int64_t Rb, int64_t V,
+                           const LawSampling& s, LawStats* stats, int32_t* dev_status, cudaStream_t stream) {
+    LawArgs A = law_args(logits_a, Ra + Rb, V, s, dev_status);
+    A.logits2 = logits_b;
+    A.R1 = Ra;
     A.stats = stats;
     return launch_law(A, stream);
 }

@@ -82,6 +82,9 @@ cudaError_t sampling_law_run(const float* logits, int64_t R, int64_t V, const La
 // Their per-row statistics only (`stats` holds R entries of 16 bytes).
 cudaError_t law_stats_run(const float* logits, int64_t R, int64_t V, const LawSampling& s, LawStats* stats,
                           int32_t* dev_status, cudaStream_t stream);
+// Both tensors' rows in one launch: stats[0 .. Ra) from logits_a, then stats[Ra .. Ra+Rb) from logits_b.
+cudaError_t law_stats_run2(const float* logits_a, int64_t Ra, const float* logits_b, int64_t Rb, int64_t V,
+                           const LawSampling& s, LawStats* stats, int32_t* dev_status, cudaStream_t stream);
 constexpr size_t kLawStatsBytes = 16;
 
 // Acceptance on laws given as logits + per-row statistics (the kernels of
