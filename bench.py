@@ -852,16 +852,7 @@ def logits_accept_rows(mxs, torch, dev, peak, reps=20):
         n_emit = torch.empty((B,), dtype=torch.int32, device=dev)
         call = lambda: mxs.spec_accept_logits(tl, dlc, d, u, workspace=ws, out_tokens=out_tok, n_emitted=n_emit,
                                               **LOGITS_SAMPLING)
-        for _ in range(5):
-            call()
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            call()
-        e1.record()
-        torch.cuda.synchronize(dev)
-        us = e0.elapsed_time(e1) * 1e3 / reps
+        us = graph_us(torch, dev, call, reps)
         n = n_emit.cpu().numpy()
         nb = 4 * B * (2 * K + 1) * V + accept_bytes(B, K, V, n)
         rows.append({"B": B, "K": K, "us_per_call": us, "rows_per_s": B / (us * 1e-6),
@@ -870,6 +861,29 @@ def logits_accept_rows(mxs, torch, dev, peak, reps=20):
         del tl, dl, dlc, q, d, u, ws
     return {"metric": "spec_accept_logits: laws from logits (statistics pass + acceptance), us per call",
             "V": V, "sampling": LOGITS_SAMPLING, "rows": rows}
+
+
+def graph_us(torch, dev, fn, reps=20, warm=3):
+    """Device time of fn (its launches captured in a CUDA graph, so host
+    launch overhead is left out), averaged over reps replays."""
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        for _ in range(warm):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) * 1e3 / reps
 
 
 def nvfp4_rows(mxs, torch, dev, peak, reps=20):
@@ -943,16 +957,7 @@ def kv_cache_rows(mxs, torch, dev, peak, reps=20):
                               else None, B * L * W * (17 / 32 + 4))):
             if fn is None:
                 continue
-            for _ in range(5):
-                fn()
-            torch.cuda.synchronize(dev)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(reps):
-                fn()
-            e1.record()
-            torch.cuda.synchronize(dev)
-            us = e0.elapsed_time(e1) * 1e3 / reps
+            us = graph_us(torch, dev, fn, reps)
             res[name] = {"us_per_call": us, "bytes_per_call": nb, "hbm_gbs": nb / (us * 1e-6) / 1e9,
                          "pct_of_peak": nb / (us * 1e-6) / 1e9 / peak}
         rows.append(res)
