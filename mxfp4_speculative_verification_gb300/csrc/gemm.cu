@@ -100,23 +100,26 @@ static int64_t bs_split_items_cap(int64_t N, int64_t K) {
 }
 
 static int bs_kind_for(int64_t rows_left, int64_t K, const void* nib);
+static bool bs_nv_for(int64_t rows_left, int64_t K, const void* nib);
 
 // Whether a call of M rows may run a block-scaled pass (sizes its workspace;
 // the nibbles' alignment is not known yet, so assume the best).
 static bool bs_may_run(int64_t M, int64_t K) { return bs_kind_for(M, K, nullptr) >= 0; }
+static bool bs_nv_may_run(int64_t M, int64_t K) { return bs_nv_for(M, K, nullptr); }
 
 // Bytes of X prepared for the block-scaled kernel (passes of at most mc
 // rows, either kind).
-static size_t bs_x_bytes(int64_t mc, int64_t K) {
+static size_t bs_x_bytes(int64_t mc, int64_t K, bool nv = false) {
     const int m = int(std::min<int64_t>(mc, kBsMaxNpad));
-    const int per_stage = std::max(bs_bstage_bytes(0, bs_npad(0, m)),
-                                   bs_bstage_bytes(1, bs_npad(1, std::min(m, kBsF4MaxRows))));
+    const int per_stage = nv ? bs_bstage_bytes(2, bs_npad(2, std::min(m, kBsF4MaxRows)))
+                             : std::max(bs_bstage_bytes(0, bs_npad(0, m)),
+                                        bs_bstage_bytes(1, bs_npad(1, std::min(m, kBsF4MaxRows))));
     return size_t((K + 255) / 256) * size_t(per_stage);
 }
 
 GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales_aligned, int sdiv) {
     GemmWorkspace w{};
-    const bool nv = sdiv == 16;  // NVFP4: scale bytes per 16 k, mma.sync passes only
+    const bool nv = sdiv == 16;  // NVFP4: scale bytes per 16 k
     const int64_t nblk = K / sdiv;
     const int64_t mc = std::min<int64_t>(M, kGemmMaxRowsPerPass);
     const int64_t mcb = std::min<int64_t>(M, kBsMaxNpad);
@@ -125,7 +128,7 @@ GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales
     size_t off = 0;
     w.xf_off = off;
     off = align_up(off + std::max(size_t(kGemmMaxRowsPerPass) * align_up(size_t(K), 512) * 2,
-                                  !nv && bs_may_run(M, K) ? bs_x_bytes(mcb, K) : size_t(0)),
+                                  (nv ? bs_nv_may_run(M, K) : bs_may_run(M, K)) ? bs_x_bytes(mcb, K, nv) : size_t(0)),
                    256);
     w.xun_off = off;
     off = align_up(off + kBsMaxNpad * sizeof(float), 256);
@@ -139,7 +142,7 @@ GemmWorkspace gemm_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales
             part = std::max<int64_t>(part, cap * mc * bn);
         }
     }
-    if (!nv && bs_may_run(M, K)) {
+    if (nv ? bs_nv_may_run(M, K) : bs_may_run(M, K)) {
         const int64_t cap = bs_split_items_cap(N, K);
         if (cap > 0) {
             ncnt = std::max<int64_t>(ncnt, 4 * ((N + kBsRows - 1) / kBsRows));
@@ -326,7 +329,7 @@ static cudaError_t build_problems(ProblemSet<G>& S, const HostGemm* gs, int coun
             // K % 512 == 0 in place, else realigned in the workspace)
             const bool wmap = bs == 1 ? make_map_e2m1_spread(&p.tm_w, h.nib, h.N, h.K, 2)
                                       : make_map(&p.tm_w, h.nib, h.N, h.K / 2, h.K / 2, kBoxBytes, uint32_t(kBsRows), true);
-            if (!wmap || !make_map(&p.tm_s, h.sc, h.N, p.nblk, h.sc_pitch, 16, uint32_t(kBsRows), false))
+            if (!wmap || !make_map(&p.tm_s, h.sc, h.N, h.K / h.sdiv, h.sc_pitch, 16, uint32_t(kBsRows), false))
                 return cudaErrorInvalidValue;
             continue;
         }
@@ -479,7 +482,7 @@ static cudaError_t launch_bs(const HostGemm* gs, int count, int M, int32_t* stat
     if (err != cudaSuccess) return err;
     static thread_local ProblemSet<G>* S_buf = nullptr;
     if (!S_buf) S_buf = new ProblemSet<G>;
-    err = build_problems(*S_buf, gs, count, M, status, kBsRows, int64_t(sms), nullptr, KIND == 0 ? 1 : 2);
+    err = build_problems(*S_buf, gs, count, M, status, kBsRows, int64_t(sms), nullptr, KIND == 0 ? 1 : KIND + 1);
     if (err != cudaSuccess) return err;
     const int npad = bs_npad(KIND, M);
     S_buf->ring = bs_ring_for(KIND, npad);
@@ -490,12 +493,15 @@ static cudaError_t launch_bs(const HostGemm* gs, int count, int M, int32_t* stat
 template <int G>
 static cudaError_t launch_bs_kind(int kind, const HostGemm* gs, int count, int M, int32_t* status,
                                   cudaStream_t stream) {
+    if constexpr (G == 1) {
+        if (kind == 2) return launch_bs<1, 2>(gs, count, M, status, stream);  // NVFP4: single calls only
+    }
     return kind ? launch_bs<G, 1>(gs, count, M, status, stream) : launch_bs<G, 0>(gs, count, M, status, stream);
 }
 
 // Every pass size the block-scaled kernel takes fits its shared and tensor memory.
 static constexpr bool bs_shapes_fit() {
-    for (int kind = 0; kind < 2; ++kind)
+    for (int kind = 0; kind < 3; ++kind)
         for (int m = 1; m <= (kind ? kBsF4MaxRows : kBsMaxNpad); ++m) {
             const int npad = bs_npad(kind, m);
             const int rc = bs_ring(kind, npad);
@@ -531,6 +537,18 @@ static int bs_kind_for(int64_t rows_left, int64_t K, const void* nib) {
 // Rows of a block-scaled pass of the given kind.
 static int64_t bs_pass_rows(int kind, int64_t rows_left) {
     return std::min<int64_t>(kind ? kBsF4MaxRows : kBsMaxNpad, rows_left);
+}
+
+// Whether the next NVFP4 pass (rows_left rows) takes the block-scaled kernel
+// (kind::mxf4nvf4, passes of at most 32 rows): 16-byte aligned nibbles, and
+// passes of at least MXS_GEMM_NV_BS_MIN rows (default 1); MXS_GEMM_PATH=mma
+// keeps every pass on the mma.sync kernel, =bs sends every pass it can.
+static bool bs_nv_for(int64_t rows_left, int64_t K, const void* nib) {
+    const bool ok = K % 32 == 0 && (reinterpret_cast<uintptr_t>(nib) & 15) == 0;
+    const char* path = std::getenv("MXS_GEMM_PATH");
+    if (path && std::strcmp(path, "mma") == 0) return false;
+    if (path && (std::strcmp(path, "bs") == 0 || std::strcmp(path, "bs4") == 0)) return ok;
+    return ok && rows_left >= env_int("MXS_GEMM_NV_BS_MIN", 1);
 }
 
 // For a pass the block-scaled kernel does not take: whether the fp16
@@ -697,6 +715,53 @@ cudaError_t gemm_run_nv(const uint16_t* x, const uint8_t* nibbles, const uint8_t
     const int64_t mc0 = std::min<int64_t>(M, kGemmMaxRowsPerPass);
     bool scales_realigned = false;
     for (int64_t m0 = 0, mc = 0; m0 < M; m0 += mc) {
+        if (bs_nv_for(M - m0, K, nibbles)) {
+            // block-scaled pass (kind::mxf4nvf4): its own X layout
+            mc = bs_pass_rows(2, M - m0);
+            const bool repack = ws.repack_scales && !scales_realigned;
+            scales_realigned = true;
+            PrepSet Q{};
+            Q.job[0].x = x + m0 * K;
+            Q.job[0].xf = xf;
+            Q.job[0].xun = xun;
+            Q.job[0].K = int(K);
+            Q.njobs = 1;
+            Q.M = int(mc);
+            Q.NT = 1;
+            Q.bs_npad = bs_npad(2, int(mc));
+            Q.bs_kind = 2;
+            Q.counters = counters;
+            Q.ncounters = ws.n_counters;
+            if (repack) {
+                Q.sc_in = scales;
+                Q.N = N;
+                Q.nblk = nsb;
+                Q.sc_pitch = ws.sc_pitch;
+                Q.sc_out = sc_aligned;
+                Q.repack_ctas = int(std::min<int64_t>((N * ws.sc_pitch + kPrepThreadsBs - 1) / kPrepThreadsBs, 1024));
+            }
+            cudaError_t err = launch_prep(Q, stream);
+            if (err != cudaSuccess) return err;
+            HostGemm h{};
+            h.nib = nibbles;
+            h.sc = ws.repack_scales ? sc_aligned : scales;
+            h.sc_pitch = ws.sc_pitch;
+            h.sc_from_prep = ws.repack_scales;
+            h.xf = xf;
+            h.xun = xun;
+            h.y = y + m0 * N;
+            h.part = part;
+            h.counters = counters;
+            h.N = N;
+            h.K = K;
+            h.sdiv = 16;
+            h.gscale = global_scale;
+            const int64_t cap = bs_split_items_cap(N, K);
+            h.items_cap = (cap > 0 && ws.n_counters >= 4 * ((N + kBsRows - 1) / kBsRows)) ? cap : 0;
+            err = launch_bs_kind<1>(2, &h, 1, int(mc), dev_status, stream);
+            if (err != cudaSuccess) return err;
+            continue;
+        }
         mc = std::min<int64_t>(kGemmMaxRowsPerPass, M - m0);
         const int NT = tiles_nt(int(mc));
         const int bn = bn_for_nt(NT);

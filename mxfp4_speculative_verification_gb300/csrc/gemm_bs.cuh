@@ -18,6 +18,16 @@
 //     (the largest residual maps into (3, 6]).  Six terms carry X to about
 //     1e-7 of its block maximum on normal data; the bound for any block is
 //     the residual after six terms, at most max|x| / 4^6.
+//   * kind::mxf4nvf4 (KIND 2, NVFP4 weights, passes of up to 32 rows): A =
+//     the packed E2M1 bytes, each 16-k block scaled by its E4M3 byte read as
+//     UE4M3 (scale_vec::4X: one 32-bit factor cell per MMA of 64 k); B = X
+//     as four E2M1 terms per 16-k block, each with its own UE4M3 factor (the
+//     smallest at or above the residual's maximum / 6).  A negative weight
+//     scale is folded into its block's codes (sign bits flipped in shared
+//     memory before the MMA reads them); the tensor's FP32 scale multiplies
+//     Y in the epilogue.  Four terms carry a bf16 row to ~1e-5 of its
+//     maximum (rows are first scaled by a power of two into [2^10, 2^11),
+//     inside the UE4M3 range).
 //   The terms are stacked as B rows (row t * Npad + m = term t of X row m),
 //   so one MMA of N = T * Npad reads A from shared memory once, and
 //   Y[m] = sum over t of D[t * Npad + m].  Shared memory per stage is what
@@ -60,6 +70,7 @@ constexpr int kBsAChunk = kBsRows * 128;     // mxf8f6f4: one 128-k chunk of pad
 constexpr int kBsATx = kBsRows * 128;        // packed global bytes of a stage's A
 constexpr int kBsMaxNpad = 64;               // X rows per pass at most
 constexpr int kBsF4Terms = 6;                // E2M1 terms of X (mxf4 kind)
+constexpr int kBsNvTerms = 4;                // E2M1 terms of X (mxf4nvf4 kind)
 constexpr int kBsFirstEpi = 6;
 constexpr int kBsXWarp = 10;
 constexpr int kBsThreads = 32 * 11;
@@ -74,7 +85,9 @@ constexpr int kBsF4MaxRows = 32;             // the mxf4 kind takes passes of at
 __host__ __device__ constexpr int bs_npad(int kind, int m) {
     return kind ? (m <= 16 ? 16 : 32) : (m <= 32 ? 32 : 64);
 }
-__host__ __device__ constexpr int bs_terms(int kind) { return kind ? kBsF4Terms : 2; }
+__host__ __device__ constexpr int bs_terms(int kind) { return kind == 2 ? kBsNvTerms : (kind ? kBsF4Terms : 2); }
+// factor groups per 256-k stage: one per MMA of 64 k (NVFP4), else per 4 blocks of 32 k
+__host__ __device__ constexpr int bs_groups(int kind) { return kind == 2 ? 4 : 2; }
 // MMA N: the term rows of B
 __host__ __device__ constexpr int bs_ncols(int kind, int npad) { return bs_terms(kind) * npad; }
 // A of one stage in shared memory (padded for mxf8f6f4)
@@ -84,9 +97,12 @@ __host__ __device__ constexpr int bs_sfb_copies(int kind, int npad) { return (bs
 // Prepared X, per 256-k stage: B rows (K-major, 16-byte units swizzled by
 // row % 8; mxf8f6f4: [2 chunks of 128 k][N rows][128 B], mxf4: [N rows][128 B]),
 // then B's factors: [group g][copy h][32 rows][4 cells], cell c of row l =
-// the 4 factor bytes of B column 128 h + 32 c + l for blocks 4 g .. 4 g + 3.
+// the 4 factor bytes of B column 128 h + 32 c + l for blocks 4 g .. 4 g + 3
+// (32-k blocks; 16-k blocks for NVFP4, one group per MMA).
 __host__ __device__ constexpr int bs_brows_bytes(int kind, int npad) { return bs_ncols(kind, npad) * (kind ? 128 : 256); }
-__host__ __device__ constexpr int bs_sfb_bytes(int kind, int npad) { return 2 * bs_sfb_copies(kind, npad) * kBsCopyBytes; }
+__host__ __device__ constexpr int bs_sfb_bytes(int kind, int npad) {
+    return bs_groups(kind) * bs_sfb_copies(kind, npad) * kBsCopyBytes;
+}
 __host__ __device__ constexpr int bs_bstage_bytes(int kind, int npad) {
     return bs_brows_bytes(kind, npad) + bs_sfb_bytes(kind, npad);
 }
@@ -95,9 +111,12 @@ __host__ __device__ constexpr int bs_slot_bytes(int kind, int npad) {
     return bs_a_bytes(kind) + bs_bstage_bytes(kind, npad) + kBsScBytes;
 }
 // Tensor-memory columns: D buffer 0 at column 0 (N wide), then one factor
-// slot per stage slot (A: 2 groups x 4 columns, then B: 2 groups x 4 columns
-// per copy), then D buffer 1 at the next multiple of 64.
-__host__ __device__ constexpr int bs_sf_cols(int kind, int npad) { return 8 + 8 * bs_sfb_copies(kind, npad); }
+// slot per stage slot (A: groups x 4 columns, then B: groups x 4 columns per
+// copy; every factor address a multiple of 4 columns), then D buffer 1 at the
+// next multiple of 64.
+__host__ __device__ constexpr int bs_sf_cols(int kind, int npad) {
+    return 4 * bs_groups(kind) * (1 + bs_sfb_copies(kind, npad));
+}
 __host__ __device__ constexpr int bs_sf0(int kind, int npad) { return bs_ncols(kind, npad); }
 __host__ __device__ constexpr int bs_d1(int kind, int npad, int ring) {
     return (bs_sf0(kind, npad) + ring * bs_sf_cols(kind, npad) + 63) / 64 * 64;
@@ -181,7 +200,14 @@ struct BsCursor {
 template <int KIND>
 __device__ __forceinline__ void umma_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-    if constexpr (KIND == 0)
+    if constexpr (KIND == 2)
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+            " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::"r"(
+                d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+            : "memory");
+    else if constexpr (KIND == 0)
         asm volatile(
             "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
             " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::"r"(
@@ -197,11 +223,12 @@ __device__ __forceinline__ void umma_bs(uint32_t d_tmem, uint64_t a_desc, uint64
             : "memory");
 }
 
-// Instruction descriptor: M = 128, N = n, both K-major, UE8M0 factors (bit
-// 23); mxf8f6f4: A E2M1 (5), B E4M3 (0); mxf4: A and B E2M1 (1).  The factor
-// ids (A: bits 29-30, B: bits 4-5) are or-ed in per MMA by bs_sfid.
+// Instruction descriptor: M = 128, N = n, both K-major; mxf8f6f4: A E2M1
+// (5), B E4M3 (0); mxf4 and mxf4nvf4: A and B E2M1 (1).  Factors UE8M0 (bit
+// 23 set), or UE4M3 for mxf4nvf4 (clear).  The factor ids (A: bits 29-30, B:
+// bits 4-5) are or-ed in per MMA by bs_sfid (always 0 for mxf4nvf4).
 __host__ __device__ constexpr uint32_t bs_idesc(int kind, int n) {
-    return (kind ? ((1u << 7) | (1u << 10)) : (5u << 7)) | (uint32_t(n >> 3) << 17) | (1u << 23) |
+    return (kind ? ((1u << 7) | (1u << 10)) : (5u << 7)) | (uint32_t(n >> 3) << 17) | (kind == 2 ? 0u : (1u << 23)) |
            (uint32_t(kBsRows >> 4) << 24);
 }
 __device__ __forceinline__ uint32_t bs_sfid(uint32_t j) { return (j << 29) | (j << 4); }
@@ -312,9 +339,10 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                         }
                     }
                     // the weights' scales: the 16-byte column of 16 blocks holding this stage's 8
+                    // (NVFP4: the stage's own 16 bytes, one per 16 k)
                     mbar_arrive_expect_tx(full_b(c), uint32_t(kBsATx + kBsScBytes));
-                    tma_2d(slot + uint32_t(abytes + bbytes), &pb.tm_s, cur.kb() & ~15, cur.R.tile * kBsRows,
-                           full_b(c), pol);
+                    tma_2d(slot + uint32_t(abytes + bbytes), &pb.tm_s, KIND == 2 ? 2 * cur.kb() : cur.kb() & ~15,
+                           cur.R.tile * kBsRows, full_b(c), pol);
                     if constexpr (KIND == 0) {
                         // both 128-k chunks of the stage (a chunk beyond K reads as zero codes)
                         asm volatile(
@@ -361,8 +389,15 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                     const uint64_t ad0 = umma_desc_sw128(slot);
                     const uint64_t bd0 = umma_desc_sw128(slot + uint32_t(abytes));
                     const uint32_t tsfa = sf0c + sfcols * uint32_t(c);
-                    const uint32_t tsfb = tsfa + 8u;
-                    if constexpr (KIND == 0) {
+                    const uint32_t tsfb = tsfa + uint32_t(4 * bs_groups(KIND));
+                    if constexpr (KIND == 2) {
+                        // four MMAs of 64 k, each with its own factor cells (4 x 16 k)
+#pragma unroll
+                        for (int j = 0; j < kBsStageBlocks / 2; ++j)
+                            if (2 * j < nb)
+                                umma_bs<2>(d_t, ad0 + uint64_t((j * 32) >> 4), bd0 + uint64_t((j * 32) >> 4), idesc,
+                                           tsfa + uint32_t(4 * j), tsfb + uint32_t(4 * copies * j), (i | j) != 0);
+                    } else if constexpr (KIND == 0) {
                         // descriptors advance by 32 bytes per block within a 128-k chunk
                         // (2 in their 16-byte address field) and by a chunk after four
 #pragma unroll
@@ -411,17 +446,48 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         for (; cur.valid(S); cur.next(S), ++it) {
             // the slot's previous stage was consumed before its bytes were requested again
             if (!wait(full_b(c), ph)) break;
-            const uint8_t* slot = smem + c * slot_bytes;
-            const uint2 f = *reinterpret_cast<const uint2*>(slot + abytes + bbytes + 16 * r + (cur.kb() & 8));
-            nan |= has_byte_ff(f.x) || has_byte_ff(f.y);
+            uint8_t* slot = smem + c * slot_bytes;
             const uint32_t tsfa = sf0c + sfcols * uint32_t(c);
-            const uint32_t tsfb = tsfa + 8u;
-            tmem_st4(tsfa, f.x, f.x, f.x, f.x);
-            tmem_st4(tsfa + 4u, f.y, f.y, f.y, f.y);
+            const uint32_t tsfb = tsfa + uint32_t(4 * bs_groups(KIND));
+            if constexpr (KIND == 2) {
+                // the stage's 16 E4M3 scales of row r: NaN flags the row; a
+                // negative scale is folded into its 16 codes (sign bits flipped
+                // in the slot's A tile, 128-byte swizzled) and used as |scale|
+                const uint4 f = *reinterpret_cast<const uint4*>(slot + abytes + bbytes + 16 * r);
+                const uint32_t w[4] = {f.x, f.y, f.z, f.w};
+                uint32_t neg = 0u;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t mag = w[j] & 0x7F7F7F7Fu;
+                    nan |= __vcmpeq4(mag, 0x7F7F7F7Fu) != 0u;
+                    neg |= w[j] & 0x80808080u;
+                    tmem_st4(tsfa + uint32_t(4 * j), mag, mag, mag, mag);
+                }
+                bool flipped = false;
+                if (neg) {
+                    // rare: fold each negative scale into its block's codes
+#pragma unroll 1
+                    for (int blk = 0; blk < 16; ++blk) {
+                        const uint32_t b = (w[blk >> 2] >> (8 * (blk & 3))) & 0xFFu;
+                        if ((b & 0x80u) && (b & 0x7Fu) != 0x7Fu) {
+                            uint64_t* codes = reinterpret_cast<uint64_t*>(
+                                slot + r * 128 + ((((blk >> 1) ^ (r & 7))) << 4) + 8 * (blk & 1));
+                            *codes ^= 0x8888888888888888ull;
+                            flipped = true;
+                        }
+                    }
+                }
+                if (flipped) fence_proxy_async_smem();
+            } else {
+                const uint2 f = *reinterpret_cast<const uint2*>(slot + abytes + bbytes + 16 * r + (cur.kb() & 8));
+                nan |= has_byte_ff(f.x) || has_byte_ff(f.y);
+                tmem_st4(tsfa, f.x, f.x, f.x, f.x);
+                tmem_st4(tsfa + 4u, f.y, f.y, f.y, f.y);
+            }
             const uint8_t* cells = slot + abytes + brows + 16 * lane;
 #pragma unroll
             for (int gh = 0; gh < 4; ++gh)
-                if (gh < 2 * copies) {
+                if (gh < bs_groups(KIND) * copies) {
                     const uint4 v = *reinterpret_cast<const uint4*>(cells + kBsCopyBytes * gh);
                     tmem_st4(tsfb + uint32_t(4 * gh), v.x, v.y, v.z, v.w);
                 }
@@ -488,7 +554,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                     if (m < M) {
                         const float v = nan ? __int_as_float(0x7FC00000) : acc[c];
                         if (pb.nsplit == 1) {
-                            if (r < rows) pb.y[int64_t(m) * Ny + n0 + r] = v * xun[m];
+                            if (r < rows)
+                                pb.y[int64_t(m) * Ny + n0 + r] = KIND == 2 ? (v * xun[m]) * pb.gscale : v * xun[m];
                         } else {
                             __stcg(mine + int64_t(m) * kBsRows + r, v);
                         }
@@ -519,7 +586,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                                     s += __ldcg(pb.part + (int64_t(sp) * pb.ntiles + RI.tile) * M * kBsRows +
                                                 int64_t(m) * kBsRows + r);
                             }
-                            pb.y[int64_t(m) * Ny + n0 + r] = s * xun[m];
+                            pb.y[int64_t(m) * Ny + n0 + r] = KIND == 2 ? (s * xun[m]) * pb.gscale : s * xun[m];
                         }
                     if (lane == 0) pb.counters[4 * RI.tile + q] = 0;  // ready for the next call
                 }

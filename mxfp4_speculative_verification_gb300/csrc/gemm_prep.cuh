@@ -117,6 +117,20 @@ __device__ __forceinline__ void e2m1x8_decode(uint32_t w, float (&v)[8]) {
     }
 }
 
+// The smallest E4M3 value >= v for 0 <= v <= 448, and its byte (a UE4M3
+// factor: positive E4M3 bytes are ordered like their values).
+__device__ __forceinline__ uint32_t ue4m3_ceil(float v, float& value) {
+    uint32_t b = e4m3x2_rn(v, 0.f) & 0xFFu;
+    float lo, hi;
+    e4m3x2_decode(b, lo, hi);
+    if (lo < v && b < 0x7Eu) {
+        ++b;
+        e4m3x2_decode(b, lo, hi);
+    }
+    value = lo;
+    return b;
+}
+
 // Byte of B column n's factor for block j of group g in a stage's factor area.
 __device__ __forceinline__ int bs_sfb_offset(int n, int g, int j, int copies) {
     return (g * copies + (n >> 7)) * kBsCopyBytes + 16 * (n & 31) + 4 * ((n & 127) >> 5) + j;
@@ -137,20 +151,25 @@ __device__ void prep_bs_row(const uint16_t* __restrict__ x, uint8_t* __restrict_
     const uint16_t* row = x + int64_t(m) * K;
     const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
     const int nchunks = K / 8;
-    float rsc = 1.f, run = 1.f;  // row scale 2^sh and its inverse (mxf4)
-    if (KIND == 1 && m < M) {
+    float rsc = 1.f, run = 1.f;  // row scale 2^sh and its inverse (mxf4, mxf4nvf4)
+    if (KIND >= 1 && m < M) {
         uint32_t mx = 0;  // largest |x| of the row, as bf16 bits (NaN and Inf above every finite)
         for (int k = threadIdx.x; k < K; k += blockDim.x) mx = max(mx, uint32_t(row[k] & 0x7FFFu));
         for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if ((threadIdx.x & 31) == 0) atomicMax(&s_max, mx);
         __syncthreads();
         const int ef = int(s_max >> 7);  // biased exponent of the row's largest |x|
+        // the largest |x| into [1, 2) (mxf4), or into [2^10, 2^11) (mxf4nvf4:
+        // the first term's UE4M3 factor, max / 6, stays below 448 and the
+        // fourth's well above its smallest value)
         if (ef >= 1 && ef <= 254) {
-            rsc = pow2f_exact(127 - ef);
-            run = pow2f_exact(ef - 127);
+            const int sh = min(KIND == 2 ? 137 - ef : 127 - ef, 127);
+            rsc = pow2f_exact(sh);
+            run = pow2f_exact(-sh);
         } else if (ef == 0 && s_max != 0) {  // a row of subnormals (below 2^-126): into the normal range
-            rsc = pow2f_exact(64);
-            run = pow2f_exact(-64);
+            const int sh = KIND == 2 ? 127 : 64;
+            rsc = pow2f_exact(sh);
+            run = pow2f_exact(-sh);
         }
     }
     const int nst = (K + 255) / 256;
@@ -179,7 +198,7 @@ __device__ void prep_bs_row(const uint16_t* __restrict__ x, uint8_t* __restrict_
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             bad |= !isfinite(f[j]);
-            if (KIND == 1) f[j] *= rsc;  // exact: a power of two, no overflow below the row's maximum
+            if (KIND >= 1) f[j] *= rsc;  // exact: a power of two, no overflow below the row's maximum
         }
         const int k0 = 8 * c;
         const int st = k0 >> 8;
@@ -217,6 +236,30 @@ __device__ void prep_bs_row(const uint16_t* __restrict__ x, uint8_t* __restrict_
             if (lead) {
                 sfb[bs_sfb_offset(m, g, j, copies)] = act ? uint8_t(e1 + 127) : uint8_t(127);
                 sfb[bs_sfb_offset(npad + m, g, j, copies)] = act ? uint8_t(e2 + 127) : uint8_t(127);
+            }
+        } else if constexpr (KIND == 2) {
+            // 8 codes = 4 bytes of the stage's 128-byte row segment; a 16-k block is
+            // this lane and its neighbour (c ^ 1), one factor per block and term
+            const int b = (k0 & 255) >> 1;
+            const int unit = (((b >> 4) ^ (m & 7)) << 4) + (b & 15);
+            const int blk = (k0 & 255) >> 4;  // 16-k block of the stage: group blk / 4 (one MMA), byte blk % 4
+            const bool lead16 = (c & 1) == 0;
+#pragma unroll 1
+            for (int t = 0; t < kBsNvTerms; ++t) {
+                float amax = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                float s = 0.f;
+                const uint32_t sbyte = ue4m3_ceil(amax * (1.f / 6.f), s);
+                const uint32_t codes = act && s > 0.f ? e2m1x8(f, 1.f / s) : 0u;
+                float d[8];
+                e2m1x8_decode(codes, d);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) f[q] = __fsub_rn(f[q], d[q] * s);
+                const int n = t * npad + m;  // B row (npad % 16 == 0: the same swizzle as row m)
+                *reinterpret_cast<uint32_t*>(stage + n * 128 + unit) = codes;
+                if (lead16) sfb[bs_sfb_offset(n, blk >> 2, blk & 3, copies)] = act ? uint8_t(sbyte) : uint8_t(0x38);
             }
         } else {
             // 8 codes = 4 bytes of the stage's 128-byte row segment
@@ -264,7 +307,8 @@ struct PrepSet {
     int NT;
     int umma_npad;        // 0: mma.sync fragments; else swizzled tcgen05 tiles of this many rows
     int bs_npad;          // > 0: X terms + block scales for the block-scaled kernel, this many rows
-    int bs_kind;          // its kind: 0 = two E4M3 terms (mxf8f6f4), 1 = six E2M1 terms (mxf4)
+    int bs_kind;          // its kind: 0 = two E4M3 terms (mxf8f6f4), 1 = six E2M1 terms (mxf4),
+                          // 2 = four E2M1 terms with UE4M3 factors per 16 k (mxf4nvf4)
     int* counters;        // split-K counters to zero (may be null)
     int ncounters;
     const uint8_t* sc_in;  // scale realignment (single GEMM only; null otherwise)
@@ -284,7 +328,9 @@ __global__ void __launch_bounds__(kPrepThreads) mxfp4_gemm_prep_kernel(const __g
     const int nrow_ctas = Q.njobs * mpad;
     if (int(blockIdx.x) < nrow_ctas && Q.bs_npad > 0) {
         const PrepJob& J = Q.job[blockIdx.x / mpad];
-        if (Q.bs_kind)
+        if (Q.bs_kind == 2)
+            prep_bs_row<2>(J.x, reinterpret_cast<uint8_t*>(J.xf), J.xun, J.K, blockIdx.x % mpad, M, Q.bs_npad);
+        else if (Q.bs_kind)
             prep_bs_row<1>(J.x, reinterpret_cast<uint8_t*>(J.xf), J.xun, J.K, blockIdx.x % mpad, M, Q.bs_npad);
         else
             prep_bs_row<0>(J.x, reinterpret_cast<uint8_t*>(J.xf), J.xun, J.K, blockIdx.x % mpad, M, Q.bs_npad);

@@ -24,6 +24,12 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
+// Writes of this thread to shared memory, made visible to the async proxy
+// (tensor-core and TMA reads that follow).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void report(int32_t* status, int32_t bits) {
     if (status) atomicOr(status, bits);
 }
