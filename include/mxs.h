@@ -170,13 +170,19 @@ mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles,
  *   workspace    device, >= nvfp4_verify_gemm_workspace_size(M, N, K) bytes,
  *                16-byte aligned; not shared by two calls in flight
  *
- * Kernel and accuracy: passes of at most 64 rows on the mma.sync kernel; each
- * decoded E2M1 code is multiplied by its block's E4M3 scale in fp16 (exact:
- * the product has at most 6 significant bits and lies in [2^-10, 2688]),
- * x as for mxfp4_verify_gemm's mma.sync path (exact for every element within
- * 2^29 of its row maximum), fp32 sums over all of K, then one rounding for g.
- * A NaN scale gives NaN in its row n; a row of x holding Inf or NaN a row of
- * NaN.
+ * Kernels and accuracy (products exact, sums fp32 in both):
+ *   - passes of up to 32 rows: tcgen05 block-scaled MMA
+ *     (kind::mxf4nvf4, scale_vec::4X) on the E2M1 codes with each scale
+ *     read as UE4M3 (a negative scale is folded into its block's codes, a
+ *     NaN scale gives NaN in its row n), and x as four E2M1 terms per 16-k
+ *     block with UE4M3 factors: within ~1e-4 of each row's largest output
+ *     on the parity cases, inside the 2e-3 bar;
+ *   - MXS_GEMM_PATH=mma: passes of up to 64 rows on the mma.sync kernel,
+ *     each decoded E2M1 code multiplied by its block's E4M3 scale in fp16
+ *     (exact: at most 6 significant bits, in [2^-10, 2688]), x exact within
+ *     2^29 of its row maximum.
+ * Both apply g once, to the fp32 sum.  A row of x holding Inf or NaN gives a
+ * row of NaN.
  * ---------------------------------------------------------------------- */
 size_t nvfp4_verify_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
