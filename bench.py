@@ -50,8 +50,10 @@ FALLBACK_HBM_GBS = 6800.0
 # is reported as null otherwise (ratio None: not yet captured on the current
 # sources).
 GEMM_TRAFFIC = {
-    # mxfp4_gemm_kernel, passes of <= 8 rows: lm_head 4096 x 128256 at M=5
-    "mma": {"ratio": 1.0064, "sha": "9ae7e066d3872169"},
+    # mxfp4_gemm_kernel, passes of <= 8 rows, as the step launches it: the grouped
+    # instance over the 8B stack's first 8 layers (32 GEMMs, 936 MB) at M=5
+    # (a single lm_head call at M=5 measured 1.0064)
+    "mma": {"ratio": 1.0000, "sha": "9ae7e066d3872169"},
     # mxfp4_gemm_bs_kernel, kind::mxf8f6f4 (passes of 33..64 rows): lm_head at M=64
     "bs8": {"ratio": 0.9172, "sha": "0155ba7702062541"},
     # mxfp4_gemm_bs_kernel, kind::mxf4 (passes of 9..32 rows): lm_head at M=20
@@ -732,7 +734,21 @@ def profile_target(args):
     dev = torch.device("cuda:0")
     model, B, K_spec = WORKLOADS[args.workload]
     M = args.profile_m or B * (K_spec + 1)
-    if args.profile_gemm:
+    if args.profile_grouped:
+        # the first LAYERS layers of the stack (4 GEMMs each) in one grouped
+        # launch: the kernel instance of the step's grouped launches, small
+        # enough for a counter capture
+        shapes = workloads.stack_shapes(model)[: 4 * args.profile_grouped]
+        lo, hi = workloads.LLAMA_EXP_RANGE
+        xs = {K: workloads.device_bf16_normal(M, K, seed=K, device=dev) for K in sorted({K for _, K, _ in shapes})}
+        problems = []
+        for i, (_, K, N) in enumerate(shapes):
+            nib, sc = workloads.device_mxfp4_weights(N, K, lo, hi, seed=i, device=dev)
+            problems.append((xs[K], nib, sc, torch.empty((M, N), dtype=torch.float32, device=dev)))
+        ws = torch.empty(mxs.mxfp4_verify_gemm_grouped_workspace_size(problems), dtype=torch.uint8, device=dev)
+        for _ in range(4):
+            mxs.mxfp4_verify_gemm_grouped(problems, workspace=ws)
+    elif args.profile_gemm:
         K, N = (int(v) for v in args.profile_gemm.split(","))
         x = workloads.device_bf16_normal(M, K, seed=1, device=dev)
         y = torch.empty((M, N), dtype=torch.float32, device=dev)
@@ -998,6 +1014,8 @@ def main():
                          "and exit; a small target for ncu captures")
     ap.add_argument("--profile-m", type=int, default=0,
                     help="rows of the --profile-gemm call (default: the workload's M)")
+    ap.add_argument("--profile-grouped", type=int, default=0, metavar="LAYERS",
+                    help="only run one grouped verify GEMM over the stack's first LAYERS layers 4 times (ncu target)")
     ap.add_argument("--profile-nvfp4", action="store_true",
                     help="with --profile-gemm: NVFP4 weights (nvfp4_verify_gemm) instead of MXFP4")
     ap.add_argument("--profile-law", action="store_true",
@@ -1011,7 +1029,7 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup(args)
-    if args.profile_gemm or args.profile_accept or args.profile_law:
+    if args.profile_gemm or args.profile_accept or args.profile_law or args.profile_grouped:
         profile_target(args)
         return
     if args.accept_sweep:
