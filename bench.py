@@ -53,11 +53,11 @@ GEMM_TRAFFIC = {
     # mxfp4_gemm_kernel, passes of <= 8 rows, as the step launches it: the grouped
     # instance over the 8B stack's first 8 layers (32 GEMMs, 936 MB) at M=5
     # (a single lm_head call at M=5 measured 1.0064)
-    "mma": {"ratio": 1.0000, "sha": "9ae7e066d3872169"},
+    "mma": {"ratio": 1.0000, "sha": "bf0b691ec7beb45b"},
     # mxfp4_gemm_bs_kernel, kind::mxf8f6f4 (passes of 33..64 rows): lm_head at M=64
-    "bs8": {"ratio": 0.9172, "sha": "0155ba7702062541"},
+    "bs8": {"ratio": 0.9170, "sha": "86e783d7a9debe52"},
     # mxfp4_gemm_bs_kernel, kind::mxf4 (passes of 9..32 rows): lm_head at M=20
-    "bs4": {"ratio": 0.9848, "sha": "0155ba7702062541"},
+    "bs4": {"ratio": 0.9851, "sha": "86e783d7a9debe52"},
 }
 BS_MIN_ROWS = 9     # passes of at least this many rows run on the block-scaled kernel
 BS4_MAX_ROWS = 32   # its mxf4 kind takes passes of up to this many rows
