@@ -59,6 +59,25 @@ GEMM_TRAFFIC = {
     # mxfp4_gemm_bs_kernel, kind::mxf4 (passes of 9..32 rows): lm_head at M=20
     "bs4": {"ratio": 0.9851, "sha": "86e783d7a9debe52"},
 }
+# sm__pipe_tensor_cycles_active (% of peak, elapsed) of each kernel, from the
+# same captures as GEMM_TRAFFIC (keyed alike: None once the kernel changed)
+GEMM_TENSOR_PCT = {
+    "mma": 27.89,   # grouped instance, 8 layers at M=5
+    "bs8": 34.70,   # lm_head at M=64
+    "bs4": 34.64,   # lm_head at M=20
+}
+
+
+def tensor_pct(passes):
+    """Captured tensor-pipe activity of each pass's kernel, or None per kernel
+    whose capture predates its current sources."""
+    out = {}
+    for rows, kind in passes:
+        t = GEMM_TRAFFIC[kind]
+        out[f"{rows} rows: {kind}"] = GEMM_TENSOR_PCT[kind] if t["sha"] == src_sha(kind) else None
+    return out
+
+
 BS_MIN_ROWS = 9     # passes of at least this many rows run on the block-scaled kernel
 BS4_MAX_ROWS = 32   # its mxf4 kind takes passes of up to this many rows
 GROUP_MAX = 84      # GEMMs per grouped launch at most (the problem table is a kernel parameter)
@@ -585,7 +604,8 @@ def run_mxs(args, world, rank, local):
                      "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": gemm_b / n_main, "launches_per_step": n_main,
-                     "avg_launch_us": ms_gemm * 1e3 / n_main, "traffic": traffic},
+                     "avg_launch_us": ms_gemm * 1e3 / n_main, "traffic": traffic,
+                     "tensor_pipe_pct_captured": tensor_pct(passes)},
         "per_call": {"value": job_tbps(world, step_b, ms_step_pc * 1e-3), "unit": "TB/s",
                      "ms_per_step": ms_step_pc,
                      "gemm_gbs": gemm_b / (ms_gemm_pc * 1e-3) / 1e9,
@@ -689,7 +709,8 @@ def sweep_point(mxs, torch, dev, stream, wl, weights, args, peak):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "bytes_per_launch": gemm_b / n_main, "launches_per_step": n_main,
                      "avg_launch_us": ms_gemm * 1e3 / n_main, "traffic": traffic,
-                     "useful_tflops": flops / (ms_gemm * 1e-3) / 1e12},
+                     "useful_tflops": flops / (ms_gemm * 1e-3) / 1e12,
+                     "tensor_pipe_pct_captured": tensor_pct(passes)},
         "spec_accept": {"B": B, "us_per_call": ms_acc * 1e3, "rows_per_s": B / (ms_acc * 1e-3),
                         "mean_emitted": float(np.mean(n_emitted)), "mean_overlap": alpha,
                         "closed_form_emitted": (1.0 - alpha ** (K_spec + 1)) / (1.0 - alpha),

@@ -56,3 +56,10 @@ def test_recorded_traffic_keys_name_the_current_kernels():
     for kind, rec in bench.GEMM_TRAFFIC.items():
         if rec["ratio"] is not None:
             assert rec["sha"] == bench.src_sha(kind), kind
+
+
+def test_tensor_pipe_table_covers_every_kernel():
+    assert set(bench.GEMM_TENSOR_PCT) == set(bench.GEMM_TRAFFIC)
+    for M in (5, 20, 64, 80, 320):
+        pct = bench.tensor_pct(bench.gemm_passes(M))
+        assert all(v is None or 0.0 < v < 100.0 for v in pct.values())
