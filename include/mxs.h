@@ -171,7 +171,7 @@ mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles,
  *                16-byte aligned; not shared by two calls in flight
  *
  * Kernels and accuracy (products exact, sums fp32 in both):
- *   - passes of up to 32 rows: tcgen05 block-scaled MMA
+ *   - passes of up to 64 rows: tcgen05 block-scaled MMA
  *     (kind::mxf4nvf4, scale_vec::4X) on the E2M1 codes with each scale
  *     read as UE4M3 (a negative scale is folded into its block's codes, a
  *     NaN scale gives NaN in its row n), and x as four E2M1 terms per 16-k

@@ -111,7 +111,7 @@ static bool bs_nv_may_run(int64_t M, int64_t K) { return bs_nv_for(M, K, nullptr
 // rows, either kind).
 static size_t bs_x_bytes(int64_t mc, int64_t K, bool nv = false) {
     const int m = int(std::min<int64_t>(mc, kBsMaxNpad));
-    const int per_stage = nv ? bs_bstage_bytes(2, bs_npad(2, std::min(m, kBsF4MaxRows)))
+    const int per_stage = nv ? bs_bstage_bytes(2, bs_npad(2, std::min(m, bs_max_rows(2))))
                              : std::max(bs_bstage_bytes(0, bs_npad(0, m)),
                                         bs_bstage_bytes(1, bs_npad(1, std::min(m, kBsF4MaxRows))));
     return size_t((K + 255) / 256) * size_t(per_stage);
@@ -502,7 +502,7 @@ static cudaError_t launch_bs_kind(int kind, const HostGemm* gs, int count, int M
 // Every pass size the block-scaled kernel takes fits its shared and tensor memory.
 static constexpr bool bs_shapes_fit() {
     for (int kind = 0; kind < 3; ++kind)
-        for (int m = 1; m <= (kind ? kBsF4MaxRows : kBsMaxNpad); ++m) {
+        for (int m = 1; m <= bs_max_rows(kind); ++m) {
             const int npad = bs_npad(kind, m);
             const int rc = bs_ring(kind, npad);
             if (bs_smem_bytes(kind, npad, rc) > kBsSmemAttr || bs_tmem_need(kind, npad, rc) > int(kBsTmemCols) ||
@@ -536,11 +536,11 @@ static int bs_kind_for(int64_t rows_left, int64_t K, const void* nib) {
 }
 // Rows of a block-scaled pass of the given kind.
 static int64_t bs_pass_rows(int kind, int64_t rows_left) {
-    return std::min<int64_t>(kind ? kBsF4MaxRows : kBsMaxNpad, rows_left);
+    return std::min<int64_t>(bs_max_rows(kind), rows_left);
 }
 
 // Whether the next NVFP4 pass (rows_left rows) takes the block-scaled kernel
-// (kind::mxf4nvf4, passes of at most 32 rows): 16-byte aligned nibbles, and
+// (kind::mxf4nvf4, passes of at most 64 rows): 16-byte aligned nibbles, and
 // passes of at least MXS_GEMM_NV_BS_MIN rows (default 1); MXS_GEMM_PATH=mma
 // keeps every pass on the mma.sync kernel, =bs sends every pass it can.
 static bool bs_nv_for(int64_t rows_left, int64_t K, const void* nib) {

@@ -18,7 +18,7 @@
 //     (the largest residual maps into (3, 6]).  Six terms carry X to about
 //     1e-7 of its block maximum on normal data; the bound for any block is
 //     the residual after six terms, at most max|x| / 4^6.
-//   * kind::mxf4nvf4 (KIND 2, NVFP4 weights, passes of up to 32 rows): A =
+//   * kind::mxf4nvf4 (KIND 2, NVFP4 weights, passes of up to 64 rows): A =
 //     the packed E2M1 bytes, each 16-k block scaled by its E4M3 byte read as
 //     UE4M3 (scale_vec::4X: one 32-bit factor cell per MMA of 64 k); B = X
 //     as four E2M1 terms per 16-k block, each with its own UE4M3 factor (the
@@ -83,8 +83,14 @@ constexpr int kBsF4MaxRows = 32;             // the mxf4 kind takes passes of at
 // X rows a pass pads to (multiples of 16 keep every term row group's swizzle
 // and tensor-memory columns aligned).
 __host__ __device__ constexpr int bs_npad(int kind, int m) {
-    return kind ? (m <= 16 ? 16 : 32) : (m <= 32 ? 32 : 64);
+    return kind == 2 ? (m <= 16 ? 16 : (m <= 32 ? 32 : 64)) : (kind ? (m <= 16 ? 16 : 32) : (m <= 32 ? 32 : 64));
 }
+// X rows a pass of this kind takes at most
+__host__ __device__ constexpr int bs_max_rows(int kind) { return kind == 1 ? 32 : 64; }
+// One D buffer in tensor memory instead of two (the next tile's MMAs wait for
+// the epilogue): NVFP4 passes of 33..64 rows, whose N = 4 x 64 = 256 columns
+// leave no room for a second buffer beside the factor slots.
+__host__ __device__ constexpr bool bs_single_d(int kind, int npad) { return kind == 2 && npad == 64; }
 __host__ __device__ constexpr int bs_terms(int kind) { return kind == 2 ? kBsNvTerms : (kind ? kBsF4Terms : 2); }
 // factor groups per 256-k stage: one per MMA of 64 k (NVFP4), else per 4 blocks of 32 k
 __host__ __device__ constexpr int bs_groups(int kind) { return kind == 2 ? 4 : 2; }
@@ -119,10 +125,11 @@ __host__ __device__ constexpr int bs_sf_cols(int kind, int npad) {
 }
 __host__ __device__ constexpr int bs_sf0(int kind, int npad) { return bs_ncols(kind, npad); }
 __host__ __device__ constexpr int bs_d1(int kind, int npad, int ring) {
-    return (bs_sf0(kind, npad) + ring * bs_sf_cols(kind, npad) + 63) / 64 * 64;
+    return bs_single_d(kind, npad) ? 0 : (bs_sf0(kind, npad) + ring * bs_sf_cols(kind, npad) + 63) / 64 * 64;
 }
 __host__ __device__ constexpr int bs_tmem_need(int kind, int npad, int ring) {
-    return bs_d1(kind, npad, ring) + bs_ncols(kind, npad);
+    return bs_single_d(kind, npad) ? bs_sf0(kind, npad) + ring * bs_sf_cols(kind, npad)
+                                   : bs_d1(kind, npad, ring) + bs_ncols(kind, npad);
 }
 // shared memory beyond the ring: barriers, NaN flags, TMEM base, abort flag
 constexpr int kBsMiscBytes = 8 * 64 + 2 * kBsRows + 64;
@@ -378,7 +385,13 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 const Problem& pb = S.p[find_problem(S, w)];
                 const BsItem RI = bs_item(pb, w - pb.item_begin);
                 const int db = tc & 1;
-                if (tc >= 2 && !wait(dfree_b(db), ((tc >> 1) - 1) & 1)) { ok = false; break; }
+                // D of tile tc - 2 (two buffers) or tc - 1 (one) has been read out
+                if (bs_single_d(KIND, npad)) {
+                    if (tc >= 1 && !wait(dfree_b((tc - 1) & 1), ((tc - 1) >> 1) & 1)) { ok = false; break; }
+                } else if (tc >= 2 && !wait(dfree_b(db), ((tc >> 1) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t d_t = tbase + (db ? d1col : 0u);
                 for (int i = 0; i < RI.nst; ++i) {
                     const int nb = min(kBsStageBlocks, RI.kb1 - (RI.kb0 + i * kBsStageBlocks));
@@ -486,7 +499,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             }
             const uint8_t* cells = slot + abytes + brows + 16 * lane;
 #pragma unroll
-            for (int gh = 0; gh < 4; ++gh)
+            for (int gh = 0; gh < 8; ++gh)
                 if (gh < bs_groups(KIND) * copies) {
                     const uint4 v = *reinterpret_cast<const uint4*>(cells + kBsCopyBytes * gh);
                     tmem_st4(tsfb + uint32_t(4 * gh), v.x, v.y, v.z, v.w);
