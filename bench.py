@@ -55,16 +55,16 @@ GEMM_TRAFFIC = {
     # (a single lm_head call at M=5 measured 1.0064)
     "mma": {"ratio": 1.0000, "sha": "bf0b691ec7beb45b"},
     # mxfp4_gemm_bs_kernel, kind::mxf8f6f4 (passes of 33..64 rows): lm_head at M=64
-    "bs8": {"ratio": 0.9170, "sha": "86e783d7a9debe52"},
+    "bs8": {"ratio": 0.9170, "sha": "6eb5555238bdf2e9"},
     # mxfp4_gemm_bs_kernel, kind::mxf4 (passes of 9..32 rows): lm_head at M=20
-    "bs4": {"ratio": 0.9851, "sha": "86e783d7a9debe52"},
+    "bs4": {"ratio": 0.9841, "sha": "6eb5555238bdf2e9"},
 }
 # sm__pipe_tensor_cycles_active (% of peak, elapsed) of each kernel, from the
 # same captures as GEMM_TRAFFIC (keyed alike: None once the kernel changed)
 GEMM_TENSOR_PCT = {
     "mma": 27.89,   # grouped instance, 8 layers at M=5
-    "bs8": 34.70,   # lm_head at M=64
-    "bs4": 34.64,   # lm_head at M=20
+    "bs8": 34.34,   # lm_head at M=64
+    "bs4": 34.58,   # lm_head at M=20
 }
 
 
