@@ -470,6 +470,7 @@ def run_mxs(args, world, rank, local):
         accept()
 
     stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))  # inputs were made on the current stream
     ACC_REPS = 20
     graphs = {}
     with torch.cuda.stream(stream):
@@ -904,6 +905,7 @@ def graph_us(torch, dev, fn, reps=20, warm=3):
     """Device time of fn (its launches captured in a CUDA graph, so host
     launch overhead is left out), averaged over reps replays."""
     stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))  # fn's inputs come from the current stream
     with torch.cuda.stream(stream):
         for _ in range(warm):
             fn()

@@ -34,6 +34,8 @@
 
 #include <climits>
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 
 #include "law.cuh"
 #include "mxs_device.cuh"
@@ -533,8 +535,405 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
     cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
-// Clusters of C CTAs, C = ceil(V / 16384) (1..8), one per row.
+// ---------------------------------------------------------------------------
+// Row form, for batches of many rows: one CTA of 1024 threads per row and no
+// cluster.  No row is held on chip: every pass streams the row again (the
+// first pass from HBM, the later ones from L2, which holds the rows of all
+// CTAs in flight), so about one row per SM is in flight against 36 for the
+// cluster form, whose slices fill shared memory, and the steps need block
+// barriers only.  The steps and every decision are the cluster form's (the
+// same classes, fine bins, gather and radix fallback on the same keys and
+// fixed-point weights), so both forms give the same statistics bit for bit.
+// ---------------------------------------------------------------------------
+constexpr int kRowThreads = 1024;
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kRowUnroll = 4;  // 16-byte loads in flight per thread in a pass
+
+template <bool B>
+struct LawTag {
+    static constexpr bool value = B;
+};
+
+// The 16-byte-aligned body of a row (rows are 4-byte aligned): logits
+// [head, head + 4 n4) as float4, the rest (at most 3 at each end) scalar.
+struct RowSpan {
+    int64_t head, n4, tail0;
+    __device__ RowSpan(const float* row, int64_t V) {
+        head = ((16 - (reinterpret_cast<uintptr_t>(row) & 15)) & 15) >> 2;
+        if (head > V) head = V;
+        n4 = (V - head) >> 2;
+        tail0 = head + (n4 << 2);
+    }
+};
+
+// f(x) for every logit of the row, each thread a strided share.
+template <class F>
+__device__ __forceinline__ void row_visit(const float* __restrict__ row, int64_t V, F&& f) {
+    const int tid = threadIdx.x;
+    const RowSpan s(row, V);
+    if (tid < s.head) f(__ldg(row + tid));
+    if (tid < V - s.tail0) f(__ldg(row + s.tail0 + tid));
+    const float4* body = reinterpret_cast<const float4*>(row + s.head);
+    int64_t i = tid;
+    for (; i + (kRowUnroll - 1) * kRowThreads < s.n4; i += kRowUnroll * kRowThreads) {
+        float4 v[kRowUnroll];
+#pragma unroll
+        for (int u = 0; u < kRowUnroll; ++u) v[u] = __ldg(body + i + u * kRowThreads);
+#pragma unroll
+        for (int u = 0; u < kRowUnroll; ++u) {
+            f(v[u].x);
+            f(v[u].y);
+            f(v[u].z);
+            f(v[u].w);
+        }
+    }
+    for (; i < s.n4; i += kRowThreads) {
+        const float4 v = __ldg(body + i);
+        f(v.x);
+        f(v.y);
+        f(v.z);
+        f(v.w);
+    }
+}
+
+// out[t] = f(row[t]) for every logit of the row (16-byte stores where out
+// has the row's alignment phase).
+template <class F>
+__device__ __forceinline__ void row_map(const float* __restrict__ row, float* __restrict__ out, int64_t V, F&& f) {
+    const int tid = threadIdx.x;
+    const RowSpan s(row, V);
+    if (tid < s.head) out[tid] = f(__ldg(row + tid));
+    if (tid < V - s.tail0) out[s.tail0 + tid] = f(__ldg(row + s.tail0 + tid));
+    const bool vec = ((reinterpret_cast<uintptr_t>(out) ^ reinterpret_cast<uintptr_t>(row)) & 15) == 0;
+    const float4* body = reinterpret_cast<const float4*>(row + s.head);
+    float* ob = out + s.head;
+    for (int64_t i = tid; i < s.n4; i += kRowThreads) {
+        const float4 v = __ldg(body + i);
+        const float4 o = make_float4(f(v.x), f(v.y), f(v.z), f(v.w));
+        if (vec) {
+            *reinterpret_cast<float4*>(ob + 4 * i) = o;
+        } else {
+            ob[4 * i] = o.x;
+            ob[4 * i + 1] = o.y;
+            ob[4 * i + 2] = o.z;
+            ob[4 * i + 3] = o.w;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kRowThreads, 1) sampling_law_row_kernel(const LawArgs A) {
+    __shared__ uint32_t hist_cnt[kLawBins], hist_lo[kLawBins], hist_hi[kLawBins];
+    __shared__ GatherEntry gall[kGatherTotal];
+    __shared__ unsigned long long gw[kGatherTotal];
+    __shared__ unsigned long long red[kRowWarps][kLawVals];
+    __shared__ unsigned long long tot[kLawVals];
+    __shared__ unsigned long long scan_w[kLawBins / 32];
+    __shared__ unsigned long long sel_above, sel_at;
+    __shared__ int gcount, sel_first, sel_last, sel_any, sel_idx;
+    __shared__ uint32_t sel_key, sel_min;
+    __shared__ float sh_m;
+    __shared__ int sh_bad;
+
+    const int64_t r = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t V = A.V;
+    const float* row = r < A.R1 ? A.logits + r * V : A.logits2 + (r - A.R1) * V;
+
+    // ---- the largest finite logit m, and NaN / +inf
+    {
+        float mx = -INFINITY;
+        int bad = 0;
+        row_visit(row, V, [&](float v) {
+            if (isnan(v) || v == INFINITY) bad = 1;
+            else mx = fmaxf(mx, v);
+        });
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+        }
+        if (lane == 0) {
+            red[warp][0] = __float_as_uint(mx);
+            red[warp][1] = unsigned(bad);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float a = -INFINITY;
+            int b = 0;
+            for (int w = 0; w < kRowWarps; ++w) {
+                a = fmaxf(a, __uint_as_float(uint32_t(red[w][0])));
+                b |= int(red[w][1]);
+            }
+            sh_m = a;
+            sh_bad = b;
+        }
+        __syncthreads();
+    }
+    const float m = sh_m;
+    const float inv_t = A.inv_t;
+    LawStats st;
+    st.m = m;
+    st.cut = 0;
+    st.inv_s = 0.f;
+    st.ok = !sh_bad && m > -INFINITY;
+
+    // Sums of kLawVals values over the CTA, into tot (all threads).
+    auto block_sum = [&](unsigned long long (&v)[kLawVals]) {
+#pragma unroll
+        for (int j = 0; j < kLawVals; ++j) v[j] = warp_sum_u64(v[j]);
+        if (lane == 0)
+#pragma unroll
+            for (int j = 0; j < kLawVals; ++j) red[warp][j] = v[j];
+        __syncthreads();
+        if (tid < kLawVals) {
+            unsigned long long t = 0;
+            for (int w = 0; w < kRowWarps; ++w) t += red[w][tid];
+            tot[tid] = t;
+        }
+        __syncthreads();
+    };
+    auto hist_begin = [&]() {
+        if (tid < kLawBins) {
+            hist_cnt[tid] = 0;
+            hist_lo[tid] = 0;
+            hist_hi[tid] = 0;
+        }
+        __syncthreads();
+    };
+    auto hist_put = [&](int bin, bool by_mass, unsigned long long w) {
+        if (!by_mass) {
+            atomicAdd(&hist_cnt[bin], 1u);
+            return;
+        }
+        const uint32_t lo = uint32_t(w);
+        uint32_t hi = uint32_t(w >> 32);
+        const uint32_t old = atomicAdd(&hist_lo[bin], lo);
+        if (old + lo < old) ++hi;
+        if (hi) atomicAdd(&hist_hi[bin], hi);
+    };
+    // After the pass: the weight at bin tid (threads below kLawBins).
+    auto hist_end = [&](bool by_mass) -> unsigned long long {
+        __syncthreads();
+        if (tid >= kLawBins) return 0ull;
+        return by_mass ? (static_cast<unsigned long long>(hist_hi[tid]) << 32) + hist_lo[tid]
+                       : static_cast<unsigned long long>(hist_cnt[tid]);
+    };
+    // As the cluster form's pick: the first of 512 positions where the
+    // cumulative weight reaches target, else the last one holding weight.
+    auto pick = [&](unsigned long long w, unsigned long long target, unsigned long long* above,
+                    unsigned long long* at) -> int {
+        unsigned long long incl = 0;
+        if (tid < kLawBins) {
+            incl = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            if (lane == 31) scan_w[warp] = incl;
+        }
+        if (tid == 0) {
+            sel_first = INT_MAX;
+            sel_last = -1;
+        }
+        __syncthreads();
+        if (tid < kLawBins) {
+            for (int q = 0; q < warp; ++q) incl += scan_w[q];
+            if (w > 0) {
+                if (incl >= target) atomicMin(&sel_first, tid);
+                atomicMax(&sel_last, tid);
+            }
+        }
+        __syncthreads();
+        const int s = sel_first != INT_MAX ? sel_first : (sel_last > 0 ? sel_last : 0);
+        if (tid == s) {
+            sel_above = incl - w;
+            sel_at = w;
+        }
+        __syncthreads();
+        *above = sel_above;
+        *at = sel_at;
+        return s;
+    };
+
+    // The cut by count or by mass among the tokens with key >= lo (the
+    // cluster form's find_cut, streaming the row for each step).
+    auto find_cut = [&](auto tag, uint32_t lo, unsigned long long target) -> LawCut {
+        constexpr bool by_mass = decltype(tag)::value;
+        auto weight_of = [&](float x) -> unsigned long long {
+            if constexpr (by_mass) return law_mass(law_exp(x, m, inv_t));
+            else return 1ull;
+        };
+        // 1. class weights
+        {
+            unsigned long long v[kLawVals] = {0ull, 0ull, 0ull, 0ull};
+            row_visit(row, V, [&](float x) {
+                const unsigned long long w = law_key(x) >= lo ? weight_of(x) : 0ull;
+                const float a = (x - m) * inv_t;
+                v[0] += w;
+                v[1] += a > -4.f ? w : 0ull;
+                v[2] += a > -8.f ? w : 0ull;
+                v[3] += a > -16.f ? w : 0ull;
+            });
+            block_sum(v);
+        }
+        if (by_mass) {
+            target = (unsigned long long)ceil(double(A.top_p) * double(tot[0]));
+            if (target == 0) target = 1;
+        }
+        int c = 3;
+        unsigned long long base = tot[3];
+        if (tot[1] >= target) {
+            c = 0;
+            base = 0;
+        } else if (tot[2] >= target) {
+            c = 1;
+            base = tot[1];
+        } else if (tot[3] >= target) {
+            c = 2;
+            base = tot[2];
+        }
+        __syncthreads();  // tot is read by all before the next block_sum
+
+        // 2. fine histogram of class c
+        int f;
+        {
+            hist_begin();
+            row_visit(row, V, [&](float x) {
+                const float a = (x - m) * inv_t;
+                if (law_class(a) == c && law_key(x) >= lo) hist_put(law_fine(a, c), by_mass, weight_of(x));
+            });
+            unsigned long long above = 0, at = 0;
+            f = pick(hist_end(by_mass), target - base, &above, &at);
+            base += above;
+        }
+        const unsigned long long need = target - base;
+
+        // 3. gather bin f's tokens
+        if (tid == 0) gcount = 0;
+        __syncthreads();
+        row_visit(row, V, [&](float x) {
+            const float a = (x - m) * inv_t;
+            if (law_class(a) == c && law_key(x) >= lo && law_fine(a, c) == f) {
+                const int pos = atomicAdd(&gcount, 1);
+                if (pos < kGatherTotal) gall[pos] = GatherEntry{law_key(x), x};
+            }
+        });
+        __syncthreads();
+        const int n = gcount;
+        LawCut cut;
+        if (n <= kGatherTotal) {
+            if (tid < n) gw[tid] = weight_of(gall[tid].x);
+            if (tid == 0) {
+                sel_key = 0u;
+                sel_min = 0xFFFFFFFFu;
+                sel_any = 0;
+                sel_idx = INT_MAX;
+            }
+            __syncthreads();
+            unsigned long long ge = 0, eq = 0;
+            uint32_t kt = 0;
+            if (tid < n) {
+                kt = gall[tid].key;
+                for (int u = 0; u < n; ++u) {
+                    const uint32_t ku = gall[u].key;
+                    const unsigned long long wu = gw[u];
+                    ge += ku >= kt ? wu : 0ull;
+                    eq += ku == kt ? wu : 0ull;
+                }
+                if (ge >= need) {
+                    atomicMax(&sel_key, kt);
+                    sel_any = 1;
+                }
+                atomicMin(&sel_min, kt);
+            }
+            __syncthreads();
+            const uint32_t K = sel_any ? sel_key : sel_min;
+            if (tid < n && kt == K) atomicMin(&sel_idx, tid);
+            __syncthreads();
+            if (tid == sel_idx) {
+                sel_above = ge - eq;
+                sel_at = eq;
+            }
+            __syncthreads();
+            cut.key = n > 0 ? K : lo;
+            cut.above = base + (n > 0 ? sel_above : 0ull);
+            cut.at = n > 0 ? sel_at : 0ull;
+            __syncthreads();  // sel_* are reused by the next step
+        } else {
+            // too many to gather: radix select over the keys of bin f
+            uint32_t prefix = 0;
+            unsigned long long acc = 0, at = 0, tgt = need;
+            for (int rr = 0; rr < 4; ++rr) {
+                const int shift = 24 - 8 * rr;
+                hist_begin();
+                row_visit(row, V, [&](float x) {
+                    const float a = (x - m) * inv_t;
+                    const uint32_t k = law_key(x);
+                    if (law_class(a) != c || k < lo || law_fine(a, c) != f) return;
+                    if (rr > 0 && (k >> (shift + 8)) != prefix) return;
+                    hist_put(255 - int((k >> shift) & 255u), by_mass, weight_of(x));
+                });
+                unsigned long long a = 0;
+                const int s = pick(hist_end(by_mass), tgt, &a, &at);
+                prefix = (prefix << 8) | uint32_t(255 - s);
+                acc += a;
+                tgt -= a;
+            }
+            cut.key = prefix;
+            cut.above = base + acc;
+            cut.at = at;
+        }
+        return cut;
+    };
+
+    if (st.ok) {
+        uint32_t cut = 0;
+        unsigned long long kept = 0;
+        const bool topk = A.top_k > 0 && A.top_k < V;
+        const bool topp = A.top_p < 1.f;
+        if (topk) cut = find_cut(LawTag<false>{}, 0u, (unsigned long long)A.top_k).key;
+        if (topp) {
+            const LawCut c = find_cut(LawTag<true>{}, cut, 0ull);
+            cut = c.key;
+            kept = c.above + c.at;
+        } else {
+            unsigned long long v[kLawVals] = {0ull, 0ull, 0ull, 0ull};
+            row_visit(row, V, [&](float x) {
+                const unsigned long long w = law_mass(law_exp(x, m, inv_t));
+                v[0] += law_key(x) >= cut ? w : 0ull;
+            });
+            block_sum(v);
+            kept = tot[0];
+        }
+        st.cut = cut;
+        st.inv_s = kept > 0 ? float(70368744177664.0 / double(kept)) : 0.f;
+        if (kept == 0) st.ok = 0;
+    }
+    if (!st.ok && tid == 0) report(A.status, MXS_DEV_NO_LAW);
+    if (A.stats && tid == 0) A.stats[r] = st;
+    if (A.probs) row_map(row, A.probs + r * V, V, [&](float x) { return law_value(x, st, inv_t); });
+}
+
+// The form for R rows (MXS_LAW_FORM=cluster / row overrides).  Measured at
+// V = 128256, top-p: 80 rows 82 us (cluster) / 117 us (row); 144 rows 146 /
+// 128 us; 576 rows 514 / 465 us.  Below ~100 rows the cluster form spreads
+// each row over 4 SMs; above, the row form keeps more rows in flight.
+constexpr int64_t kLawRowMinRows = 128;
+static bool law_row_form(int64_t R) {
+    if (const char* f = std::getenv("MXS_LAW_FORM")) {
+        if (std::strcmp(f, "row") == 0) return true;
+        if (std::strcmp(f, "cluster") == 0) return false;
+    }
+    return R >= kLawRowMinRows;
+}
+
+// Clusters of C CTAs, C = ceil(V / 16384) (1..8), one per row; or the row form.
 static cudaError_t launch_law(const LawArgs& A, cudaStream_t stream) {
+    if (A.R >= 1 && law_row_form(A.R)) {
+        sampling_law_row_kernel<<<unsigned(A.R), kRowThreads, 0, stream>>>(A);
+        return cudaGetLastError();
+    }
     const int C = int((A.V + kLawSlice - 1) / kLawSlice);
     if (A.R < 1) return cudaSuccess;
     static const cudaError_t attr_err =

@@ -34,6 +34,14 @@ def env():
     return cuda_or_skip()
 
 
+@pytest.fixture(params=["cluster", "row"])
+def form(request, monkeypatch):
+    """Both kernel forms of the laws: one cluster per row, or one CTA per row
+    streaming the row for each pass (the library picks by row count)."""
+    monkeypatch.setenv("MXS_LAW_FORM", request.param)
+    return request.param
+
+
 def _law_gpu(env, l, **kw):
     torch, mxs = env
     dev = torch.device("cuda:0")
@@ -72,7 +80,7 @@ def _check_law(got, l, temperature=1.0, top_k=0, top_p=1.0):
 
 
 @pytest.mark.parametrize("V", [1, 7, 1000, 16384, 16385, 50257, 128256, 131072])
-def test_law_plain_softmax(env, V):
+def test_law_plain_softmax(env, form, V):
     l = _logits(6, V, seed=V)
     got, st = _law_gpu(env, l)
     assert st == 0
@@ -82,7 +90,7 @@ def test_law_plain_softmax(env, V):
 @pytest.mark.parametrize("temperature,top_k,top_p", [
     (1.0, 50, 1.0), (0.7, 0, 0.9), (1.5, 40, 0.8), (0.3, 1, 1.0), (1.0, 0, 1e-6), (1.0, 128255, 0.999),
     (2.0, 1000, 0.5), (1.0, 3, 0.999999)])
-def test_law_filters(env, temperature, top_k, top_p):
+def test_law_filters(env, form, temperature, top_k, top_p):
     V = 128256
     l = _logits(24, V, seed=int(temperature * 10) + top_k)
     got, st = _law_gpu(env, l, temperature=temperature, top_k=top_k, top_p=top_p)
@@ -93,7 +101,7 @@ def test_law_filters(env, temperature, top_k, top_p):
 @pytest.mark.parametrize("std,kw", [(0.01, {"top_p": 0.5}), (0.01, {"top_k": 1000}), (30.0, {"top_p": 0.99}),
                                     (3.0, {"top_k": 60000, "top_p": 0.999999}), (0.3, {"temperature": 0.05, "top_p": 0.9}),
                                     (3.0, {"temperature": 20.0, "top_k": 5000, "top_p": 0.7})])
-def test_law_extreme_spreads(env, std, kw):
+def test_law_extreme_spreads(env, form, std, kw):
     # flat rows (one fine bin holds thousands of tokens: the radix finish),
     # very peaked rows, and cuts deep in the tail
     l = _logits(8, 128256, seed=int(std * 100) + len(kw), std=std)
@@ -102,7 +110,7 @@ def test_law_extreme_spreads(env, std, kw):
     _check_law(got, l, kw.get("temperature", 1.0), kw.get("top_k", 0), kw.get("top_p", 1.0))
 
 
-def test_law_ties_masked_and_rows_without_law(env):
+def test_law_ties_masked_and_rows_without_law(env, form):
     V = 4096
     l = _logits(5, V, seed=3)
     l[0, ::3] = -np.inf                     # masked tokens
@@ -119,11 +127,43 @@ def test_law_ties_masked_and_rows_without_law(env):
     _check_law(got[:2], l[:2], 1.0, 10, 0.95)
 
 
-def test_law_deterministic(env):
+def test_law_deterministic(env, form):
     l = _logits(16, 128256, seed=9)
     a, _ = _law_gpu(env, l, temperature=0.8, top_k=500, top_p=0.9)
     b, _ = _law_gpu(env, l, temperature=0.8, top_k=500, top_p=0.9)
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("V,kw", [
+    (1, {}), (7, {"top_k": 3}), (1001, {"top_p": 0.9}), (16385, {"temperature": 0.7, "top_k": 50, "top_p": 0.9}),
+    (50257, {"top_p": 0.95}), (128256, {"temperature": 0.8, "top_p": 0.9}), (131071, {"top_k": 1000}),
+    (128255, {"top_k": 60000, "top_p": 0.999999}), (4099, {"temperature": 0.05, "top_p": 0.5})])
+def test_law_forms_bit_identical(env, monkeypatch, V, kw):
+    """The two kernel forms take the same decisions on the same fixed-point
+    weights: every probability is the same bits.  Odd V puts the rows at
+    every 4-byte phase, and the second input starts 4 bytes past a 16-byte
+    boundary (unaligned heads and tails; probabilities then written with
+    another phase than their logits)."""
+    torch, mxs = env
+    dev = torch.device("cuda:0")
+    R = 9
+    l = _logits(R, V, seed=V + 5)
+    if V > 8:
+        l[3] *= np.float32(0.001)   # flat row: thousands of tokens in one fine bin
+        l[5, V // 2] = np.nan       # no law
+        l[6, : V // 3] = -np.inf    # masked tokens
+        l[7, :5] = l[7].max() + 1   # ties at the top
+    flat = torch.from_numpy(np.concatenate([np.zeros(1, np.float32), l.ravel()])).to(dev)
+    outs = []
+    for f in ("cluster", "row"):
+        monkeypatch.setenv("MXS_LAW_FORM", f)
+        for t in (torch.from_numpy(l).to(dev), flat[1:].view(R, V)):
+            outs.append(mxs.spec_sampling_law(t, **kw).cpu().numpy().view(np.uint32))
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert np.array_equal(outs[0], o)
+    if V > 8:
+        assert not outs[0][5].any() and outs[0][0].any()
 
 
 def _spec_logits(B, K, V, seed):
@@ -149,7 +189,7 @@ def _drafts(dl_laws, rng):
 @pytest.mark.parametrize("B,K,kw", [(1, 4, {}), (4, 4, {"temperature": 0.7, "top_p": 0.9}),
                                     (16, 4, {"top_k": 50, "top_p": 0.95}), (64, 4, {"temperature": 1.3}),
                                     (64, 7, {"top_k": 200}), (64, 1, {"top_p": 0.8}), (3, 0, {"top_p": 0.9})])
-def test_accept_logits_equals_accept_on_written_laws(env, B, K, kw):
+def test_accept_logits_equals_accept_on_written_laws(env, form, B, K, kw):
     torch, mxs = env
     dev = torch.device("cuda:0")
     V = 128256
@@ -174,7 +214,7 @@ def test_accept_logits_equals_accept_on_written_laws(env, B, K, kw):
 
 @pytest.mark.parametrize("B,K,kw", [(8, 4, {}), (8, 4, {"temperature": 0.8, "top_k": 100, "top_p": 0.9}),
                                     (6, 7, {"top_p": 0.5})])
-def test_accept_logits_matches_oracle(env, B, K, kw):
+def test_accept_logits_matches_oracle(env, form, B, K, kw):
     torch, mxs = env
     dev = torch.device("cuda:0")
     V = 128256
