@@ -96,12 +96,9 @@ struct LawSmem {
 };
 constexpr int kLawSmem = int(sizeof(LawSmem));
 
-// Log-mass class of a token, a = (l - m) / T <= 0: 0 for a > -4, 1 for
-// (-8, -4], 2 for (-16, -8], 3 below.  (On logits like N(0, 3) at T = 0.8 the
-// top-p 0.9 cut lies 7 to 9 nats below the maximum.)
-__device__ __forceinline__ int law_class(float a) {
-    return int(a <= -4.f) + int(a <= -8.f) + int(a <= -16.f);
-}
+// Log-mass classes of the tokens, by a = (l - m) / T <= 0: 0 for a > -4, 1
+// for (-8, -4], 2 for (-16, -8], 3 below.  (On logits like N(0, 3) at T =
+// 0.8 the top-p 0.9 cut lies 7 to 9 nats below the maximum.)
 
 // Fine bin of a token within its class (0 holds the largest logits): steps
 // of 1/128 nat in classes 0 and 1, 1/64 in class 2, 1/16 in class 3 (bin 511
@@ -125,6 +122,70 @@ struct LawCut {
     unsigned long long above;  // weight of the tokens with larger keys
     unsigned long long at;     // weight of the tokens with this key
 };
+
+template <bool B>
+struct LawTag {
+    static constexpr bool value = B;
+};
+
+// One token of the class pass: its weight (1, or its fixed-point mass as two
+// 23-bit digits; 0 below the key lo, or for a slot without a token) added to
+// the cumulative class sums -- sum 0 over every token, sums 1..3 over the
+// tokens with a > -4, -8, -16 -- each digit kept in 32 bits (a digit is at
+// most 2^23 and a thread adds at most 128 tokens: at most 2^30).  Returns the
+// three comparisons.
+template <bool BY_MASS, bool HAS_LO>
+__device__ __forceinline__ void class_add(float x, float m, float inv_t, uint32_t lo, bool valid,
+                                          uint32_t (&h)[kLawVals], uint32_t (&l)[kLawVals], bool& p4, bool& p8,
+                                          bool& p16) {
+    const float a = (x - m) * inv_t;
+    p4 = a > -4.f;
+    p8 = a > -8.f;
+    p16 = a > -16.f;
+    const bool in = valid && (!HAS_LO || law_key(x) >= lo);
+    if constexpr (BY_MASS) {
+        uint32_t hb, lb;
+        law_mass_digits(in ? law_exp(x, m, inv_t) : 0.f, hb, lb);
+        hb -= kMassBias;
+        lb -= kMassBias;
+        h[0] += hb;
+        l[0] += lb;
+        if (p4) {
+            h[1] += hb;
+            l[1] += lb;
+        }
+        if (p8) {
+            h[2] += hb;
+            l[2] += lb;
+        }
+        if (p16) {
+            h[3] += hb;
+            l[3] += lb;
+        }
+    } else {
+        const uint32_t w = in ? 1u : 0u;
+        l[0] += w;
+        l[1] += p4 ? w : 0u;
+        l[2] += p8 ? w : 0u;
+        l[3] += p16 ? w : 0u;
+    }
+}
+
+// The class sums of one thread as 64-bit weights.
+template <bool BY_MASS>
+__device__ __forceinline__ void class_sums(const uint32_t (&h)[kLawVals], const uint32_t (&l)[kLawVals],
+                                           unsigned long long (&v)[kLawVals]) {
+#pragma unroll
+    for (int j = 0; j < kLawVals; ++j)
+        v[j] = BY_MASS ? (static_cast<unsigned long long>(h[j]) << 23) + l[j] : static_cast<unsigned long long>(l[j]);
+}
+
+// Whether a token of log-mass a lies in class c.
+__device__ __forceinline__ bool in_class(float a, int c) {
+    const float hi = c == 0 ? INFINITY : c == 1 ? -4.f : c == 2 ? -8.f : -16.f;
+    const float lo = c == 0 ? -4.f : c == 1 ? -8.f : -16.f;
+    return a <= hi && (c == 3 || a > lo);
+}
 
 __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawArgs A) {
     extern __shared__ __align__(16) uint8_t law_smem_raw[];
@@ -152,8 +213,8 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
             float v = -INFINITY;
             if (j < nv) {
                 v = __ldg(row + j);
-                if (isnan(v) || v == INFINITY) bad = 1;
-                else mx = fmaxf(mx, v);
+                bad |= int(v != v);
+                mx = fmaxf(mx, v);  // NaN ignored; +inf makes the row bad below
             }
             S.xs[j] = v;
         }
@@ -204,7 +265,7 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
     st.m = m;
     st.cut = 0;
     st.inv_s = 0.f;
-    st.ok = !S.bad && m > -INFINITY;
+    st.ok = !S.bad && m > -INFINITY && m < INFINITY;
 
     int pb = 0;  // alternates the published-sum buffers
     int hb = 0;  // alternates the histogram buffers
@@ -310,38 +371,42 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
         *at = S.sel_at;
         return s;
     };
-    auto weight_of = [&](float x, bool by_mass) -> unsigned long long {
-        return by_mass ? law_mass(law_exp(x, m, inv_t)) : 1ull;
-    };
-
     // The cut by count (top-k, target k) or by mass (top-p, target ceil(p *
     // total)) among the tokens with key >= lo: the largest key K whose tokens
     // with key >= K weigh at least the target.
-    auto find_cut = [&](bool by_mass, uint32_t lo, unsigned long long target) -> LawCut {
-        // 1. class weights; masks of this thread's tokens in each class
-        uint32_t cm0 = 0u, cm1 = 0u, cm2 = 0u, cm3 = 0u;  // this thread's tokens of each class
+    auto find_cut = [&](auto tag, uint32_t lo, unsigned long long target) -> LawCut {
+        constexpr bool by_mass = decltype(tag)::value;
+        auto weight_of = [&](float x) -> unsigned long long {
+            if constexpr (by_mass) return law_mass(law_exp(x, m, inv_t));
+            else return 1ull;
+        };
+        // 1. class weights; bits of this thread's tokens above each class edge
+        uint32_t b4 = 0u, b8 = 0u, b16 = 0u, kin = 0u;
         {
-            unsigned long long v[kLawVals] = {0ull, 0ull, 0ull, 0ull};
-            // branch-free, so that unrolled iterations overlap (padding slots
-            // hold -inf: no mass; the count weight checks the slot)
+            uint32_t h[kLawVals] = {0u, 0u, 0u, 0u}, l[kLawVals] = {0u, 0u, 0u, 0u};
+            auto pass = [&](auto has_lo) {
+                constexpr bool kHasLo = decltype(has_lo)::value;
 #pragma unroll 8
-            for (int i = 0; i < kLawChunks; ++i) {
-                const int j = i * kLawThreads + tid;
-                const float x = S.xs[j];
-                const bool in = j < nv && law_key(x) >= lo;
-                const unsigned long long w = in ? weight_of(x, by_mass) : 0ull;
-                const float a = (x - m) * inv_t;
-                v[0] += w;
-                v[1] += a > -4.f ? w : 0ull;
-                v[2] += a > -8.f ? w : 0ull;
-                v[3] += a > -16.f ? w : 0ull;
-                const int cl = law_class(a);
-                const uint32_t bit = w ? 1u << i : 0u;
-                cm0 |= cl == 0 ? bit : 0u;
-                cm1 |= cl == 1 ? bit : 0u;
-                cm2 |= cl == 2 ? bit : 0u;
-                cm3 |= cl == 3 ? bit : 0u;
+                for (int i = 0; i < kLawChunks; ++i) {
+                    const int j = i * kLawThreads + tid;
+                    const float x = S.xs[j];  // padding: -inf
+                    bool p4, p8, p16;
+                    class_add<by_mass, kHasLo>(x, m, inv_t, lo, j < nv, h, l, p4, p8, p16);
+                    const uint32_t bit = 1u << i;
+                    b4 |= p4 ? bit : 0u;
+                    b8 |= p8 ? bit : 0u;
+                    b16 |= p16 ? bit : 0u;
+                    if (kHasLo) kin |= law_key(x) >= lo ? bit : 0u;
+                }
+            };
+            if (lo) {
+                pass(LawTag<true>{});
+            } else {
+                pass(LawTag<false>{});
+                kin = 0xFFFFFFFFu;
             }
+            unsigned long long v[kLawVals];
+            class_sums<by_mass>(h, l, v);
             cluster_sum(v);
         }
         if (by_mass) {
@@ -360,7 +425,14 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
             c = 2;
             base = S.tot[2];
         }
-        const uint32_t mine = c == 0 ? cm0 : c == 1 ? cm1 : c == 2 ? cm2 : cm3;
+        // this thread's tokens of class c (slots holding a token, key >= lo)
+        uint32_t valid = 0xFFFFFFFFu;
+        if (nv < kLawSlice) {
+            valid = 0u;
+#pragma unroll
+            for (int i = 0; i < kLawChunks; ++i) valid |= i * kLawThreads + tid < nv ? 1u << i : 0u;
+        }
+        const uint32_t mine = kin & valid & (c == 0 ? b4 : c == 1 ? (b8 & ~b4) : c == 2 ? (b16 & ~b8) : ~b16);
 
         // 2. fine histogram of class c
         uint32_t fmask = 0;
@@ -370,7 +442,7 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
             for (uint32_t bits = mine; bits; bits &= bits - 1) {
                 const int i = __ffs(bits) - 1;
                 const float x = S.xs[i * kLawThreads + tid];
-                hist_put(b, law_fine((x - m) * inv_t, c), by_mass, weight_of(x, by_mass));
+                hist_put(b, law_fine((x - m) * inv_t, c), by_mass, weight_of(x));
             }
             unsigned long long above = 0, at = 0;
             f = pick(hist_end(b, by_mass), target - base, &above, &at);
@@ -430,7 +502,7 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
                 while (cc + 1 < C && S.goff[cc + 1] <= tid) ++cc;
                 const GatherEntry e = cluster.map_shared_rank(&S, cc)->glist[tid - S.goff[cc]];
                 S.gall[tid] = e;
-                S.gw[tid] = weight_of(e.x, by_mass);
+                S.gw[tid] = weight_of(e.x);
             }
             if (tid == 0) {
                 S.sel_key = 0u;
@@ -480,7 +552,7 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
                     const float x = S.xs[i * kLawThreads + tid];
                     const uint32_t k = law_key(x);
                     if (rr > 0 && (k >> (shift + 8)) != prefix) continue;
-                    hist_put(b, 255 - int((k >> shift) & 255u), by_mass, weight_of(x, by_mass));
+                    hist_put(b, 255 - int((k >> shift) & 255u), by_mass, weight_of(x));
                 }
                 unsigned long long a = 0;
                 const int s = pick(hist_end(b, by_mass), tgt, &a, &at);
@@ -500,20 +572,23 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
         unsigned long long kept = 0;
         const bool topk = A.top_k > 0 && A.top_k < V;
         const bool topp = A.top_p < 1.f;
-        if (topk) cut = find_cut(false, 0u, (unsigned long long)A.top_k).key;
+        if (topk) cut = find_cut(LawTag<false>{}, 0u, (unsigned long long)A.top_k).key;
         if (topp) {
-            const LawCut c = find_cut(true, cut, 0ull);
+            const LawCut c = find_cut(LawTag<true>{}, cut, 0ull);
             cut = c.key;
             kept = c.above + c.at;
         } else {
             // the kept mass, one cluster reduction
-            unsigned long long v[kLawVals] = {0ull, 0ull, 0ull, 0ull};
+            uint32_t hs = 0u, ls = 0u;
 #pragma unroll 8
             for (int i = 0; i < kLawChunks; ++i) {
                 const float x = S.xs[i * kLawThreads + tid];  // padding: -inf, no mass
-                const unsigned long long w = law_mass(law_exp(x, m, inv_t));
-                v[0] += law_key(x) >= cut ? w : 0ull;
+                uint32_t hb, lb;
+                law_mass_digits(law_key(x) >= cut ? law_exp(x, m, inv_t) : 0.f, hb, lb);
+                hs += hb - kMassBias;
+                ls += lb - kMassBias;
             }
+            unsigned long long v[kLawVals] = {(static_cast<unsigned long long>(hs) << 23) + ls, 0ull, 0ull, 0ull};
             cluster_sum(v);
             kept = S.tot[0];
         }
@@ -539,20 +614,20 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
 // Row form, for batches of many rows: one CTA of 1024 threads per row and no
 // cluster.  No row is held on chip: every pass streams the row again (the
 // first pass from HBM, the later ones from L2, which holds the rows of all
-// CTAs in flight), so about one row per SM is in flight against 36 for the
-// cluster form, whose slices fill shared memory, and the steps need block
-// barriers only.  The steps and every decision are the cluster form's (the
-// same classes, fine bins, gather and radix fallback on the same keys and
-// fixed-point weights), so both forms give the same statistics bit for bit.
+// CTAs in flight), so about one row per SM is in flight against 36 rows for
+// the cluster form, whose slices fill shared memory, and the steps need
+// block barriers only.  The steps and every decision are the cluster form's
+// (the same classes, fine bins, gather and radix fallback on the same keys
+// and fixed-point weights), so both forms give the same statistics bit for
+// bit.  (Measured alternatives, 576 rows, top-p: two CTAs of 512 threads per
+// SM, 432 us; the row streamed through a shared-memory ring of 1-D bulk
+// copies, 489 us; this form, 400 us.  Each pass is bound by instruction issue
+// on its SM, not by the bytes in flight.)
 // ---------------------------------------------------------------------------
 constexpr int kRowThreads = 1024;
 constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kRowUnroll = 4;  // 16-byte loads in flight per thread in a pass
-
-template <bool B>
-struct LawTag {
-    static constexpr bool value = B;
-};
+static_assert(kRowThreads >= kLawBins, "one fine-histogram bin per thread in pick");
 
 // The 16-byte-aligned body of a row (rows are 4-byte aligned): logits
 // [head, head + 4 n4) as float4, the rest (at most 3 at each end) scalar.
@@ -644,8 +719,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) sampling_law_row_kernel(const 
         float mx = -INFINITY;
         int bad = 0;
         row_visit(row, V, [&](float v) {
-            if (isnan(v) || v == INFINITY) bad = 1;
-            else mx = fmaxf(mx, v);
+            bad |= int(v != v);
+            mx = fmaxf(mx, v);  // NaN ignored; +inf makes the row bad below
         });
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -675,7 +750,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) sampling_law_row_kernel(const 
     st.m = m;
     st.cut = 0;
     st.inv_s = 0.f;
-    st.ok = !sh_bad && m > -INFINITY;
+    st.ok = !sh_bad && m > -INFINITY && m < INFINITY;
 
     // Sums of kLawVals values over the CTA, into tot (all threads).
     auto block_sum = [&](unsigned long long (&v)[kLawVals]) {
@@ -766,15 +841,17 @@ __global__ void __launch_bounds__(kRowThreads, 1) sampling_law_row_kernel(const 
         };
         // 1. class weights
         {
-            unsigned long long v[kLawVals] = {0ull, 0ull, 0ull, 0ull};
-            row_visit(row, V, [&](float x) {
-                const unsigned long long w = law_key(x) >= lo ? weight_of(x) : 0ull;
-                const float a = (x - m) * inv_t;
-                v[0] += w;
-                v[1] += a > -4.f ? w : 0ull;
-                v[2] += a > -8.f ? w : 0ull;
-                v[3] += a > -16.f ? w : 0ull;
-            });
+            uint32_t h[kLawVals] = {0u, 0u, 0u, 0u}, l[kLawVals] = {0u, 0u, 0u, 0u};
+            auto pass = [&](auto has_lo) {
+                row_visit(row, V, [&](float x) {
+                    bool p4, p8, p16;
+                    class_add<by_mass, decltype(has_lo)::value>(x, m, inv_t, lo, true, h, l, p4, p8, p16);
+                });
+            };
+            if (lo) pass(LawTag<true>{});
+            else pass(LawTag<false>{});
+            unsigned long long v[kLawVals];
+            class_sums<by_mass>(h, l, v);
             block_sum(v);
         }
         if (by_mass) {
@@ -801,7 +878,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) sampling_law_row_kernel(const 
             hist_begin();
             row_visit(row, V, [&](float x) {
                 const float a = (x - m) * inv_t;
-                if (law_class(a) == c && law_key(x) >= lo) hist_put(law_fine(a, c), by_mass, weight_of(x));
+                if (in_class(a, c) && law_key(x) >= lo) hist_put(law_fine(a, c), by_mass, weight_of(x));
             });
             unsigned long long above = 0, at = 0;
             f = pick(hist_end(by_mass), target - base, &above, &at);
@@ -814,7 +891,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) sampling_law_row_kernel(const 
         __syncthreads();
         row_visit(row, V, [&](float x) {
             const float a = (x - m) * inv_t;
-            if (law_class(a) == c && law_key(x) >= lo && law_fine(a, c) == f) {
+            if (in_class(a, c) && law_key(x) >= lo && law_fine(a, c) == f) {
                 const int pos = atomicAdd(&gcount, 1);
                 if (pos < kGatherTotal) gall[pos] = GatherEntry{law_key(x), x};
             }
@@ -870,7 +947,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) sampling_law_row_kernel(const 
                 row_visit(row, V, [&](float x) {
                     const float a = (x - m) * inv_t;
                     const uint32_t k = law_key(x);
-                    if (law_class(a) != c || k < lo || law_fine(a, c) != f) return;
+                    if (!in_class(a, c) || k < lo || law_fine(a, c) != f) return;
                     if (rr > 0 && (k >> (shift + 8)) != prefix) return;
                     hist_put(255 - int((k >> shift) & 255u), by_mass, weight_of(x));
                 });
@@ -898,11 +975,14 @@ __global__ void __launch_bounds__(kRowThreads, 1) sampling_law_row_kernel(const 
             cut = c.key;
             kept = c.above + c.at;
         } else {
-            unsigned long long v[kLawVals] = {0ull, 0ull, 0ull, 0ull};
+            uint32_t hs = 0u, ls = 0u;
             row_visit(row, V, [&](float x) {
-                const unsigned long long w = law_mass(law_exp(x, m, inv_t));
-                v[0] += law_key(x) >= cut ? w : 0ull;
+                uint32_t hb, lb;
+                law_mass_digits(law_key(x) >= cut ? law_exp(x, m, inv_t) : 0.f, hb, lb);
+                hs += hb - kMassBias;
+                ls += lb - kMassBias;
             });
+            unsigned long long v[kLawVals] = {(static_cast<unsigned long long>(hs) << 23) + ls, 0ull, 0ull, 0ull};
             block_sum(v);
             kept = tot[0];
         }
@@ -916,8 +996,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) sampling_law_row_kernel(const 
 }
 
 // The form for R rows (MXS_LAW_FORM=cluster / row overrides).  Measured at
-// V = 128256, top-p: 80 rows 82 us (cluster) / 117 us (row); 144 rows 146 /
-// 128 us; 576 rows 514 / 465 us.  Below ~100 rows the cluster form spreads
+// V = 128256, top-p: 80 rows 71 us (cluster) / 99 us (row); 144 rows 124 /
+// 112 us; 576 rows 433 / 400 us.  Below ~100 rows the cluster form spreads
 // each row over 4 SMs; above, the row form keeps more rows in flight.
 constexpr int64_t kLawRowMinRows = 128;
 static bool law_row_form(int64_t R) {

@@ -39,17 +39,29 @@ __device__ __forceinline__ float law_value(float l, const LawStats& s, float inv
 
 // Fixed-point mass of one token, floor(e * 2^46) for e in [0, 1]: sums of
 // these are exact in any order, so the top-p cut does not depend on which
-// thread added what.  Taken from the bits (a normal e is M * 2^(E - 150), M
-// its 24-bit significand, E its biased exponent, so e * 2^46 = M * 2^(E - 104);
-// zero and subnormal e give 0), which measured faster here than the 64-bit
-// float-to-integer conversion.
+// thread added what.  Formed as two 23-bit digits by exact fp32 operations
+// (cheaper than 64-bit integer shifts): y = e 2^23 (exact), the add y + 2^23
+// rounded toward zero holds 2^23 + floor(y), whose bit pattern is
+// kMassBias + floor(y); the fraction y - floor(y) is exact, and the same add
+// on it times 2^23 gives the low digit.  floor(e 2^46) = hi 2^23 + lo, equal
+// to the integer definition for every float in [0, 1].
+constexpr uint32_t kMassBias = 0x4B000000u;  // the bit pattern of 2^23
+
+// The two digits, each still carrying kMassBias (callers subtract it, often
+// inside an accumulation).
+__device__ __forceinline__ void law_mass_digits(float e, uint32_t& hb, uint32_t& lb) {
+    const float two23 = 8388608.f;
+    const float y = __fmul_rn(e, two23);
+    const float t = __fadd_rz(y, two23);
+    const float z = __fmul_rn(__fsub_rn(y, __fsub_rn(t, two23)), two23);
+    hb = __float_as_uint(t);
+    lb = __float_as_uint(__fadd_rz(z, two23));
+}
+
 __device__ __forceinline__ unsigned long long law_mass(float e) {
-    const uint32_t b = __float_as_uint(e);
-    const int E = int(b >> 23);
-    const unsigned long long M = (b & 0x7FFFFFu) | 0x800000u;
-    const int sh = E - 104;
-    if (E == 0 || sh <= -24) return 0ull;
-    return sh >= 0 ? M << sh : M >> -sh;
+    uint32_t hb, lb;
+    law_mass_digits(e, hb, lb);
+    return (static_cast<unsigned long long>(hb - kMassBias) << 23) + (lb - kMassBias);
 }
 
 }  // namespace mxs
