@@ -25,6 +25,18 @@ __device__ __forceinline__ uint32_t e2m1_magnitude_code(float a) {
            uint32_t(a >= 1.75f) + uint32_t(a > 2.5f) + uint32_t(a >= 3.5f) + uint32_t(a > 5.0f);
 }
 
+// The block exponent of a finite block with largest magnitude amax: the
+// smallest integer e with amax <= 6 * 2^e, clamped to [-127, 127]; 0 for an
+// all-zero block.
+__device__ __forceinline__ int mx_block_exp(float amax) {
+    if (!(amax > 0.f)) return 0;
+    const uint32_t bits = __float_as_uint(amax);
+    const int ex = int(bits >> 23);
+    const uint32_t man = bits & 0x7FFFFFu;
+    const int e = (ex == 0) ? -127 : ex - 129 + (man > 0x400000u ? 1 : 0);
+    return max(-127, min(127, e));
+}
+
 // Packs v[0..31] into 16 nibble bytes (element k in byte k/2, even k in the
 // low nibble) and one E8M0 byte.  Returns false for a non-finite block.
 __device__ __forceinline__ bool pack_block32(const float (&v)[32], uint8_t* __restrict__ out16,
@@ -43,14 +55,7 @@ __device__ __forceinline__ bool pack_block32(const float (&v)[32], uint8_t* __re
         for (int k = 0; k < 16; ++k) out16[k] = 0;
         return false;
     }
-    int e = 0;
-    if (amax > 0.f) {
-        const uint32_t bits = __float_as_uint(amax);
-        const int ex = int(bits >> 23);
-        const uint32_t man = bits & 0x7FFFFFu;
-        e = (ex == 0) ? -127 : ex - 129 + (man > 0x400000u ? 1 : 0);
-        e = max(-127, min(127, e));
-    }
+    const int e = mx_block_exp(amax);
     *scale = uint8_t(e + 127);
     const float inv = exact_pow2(-e);
 #pragma unroll
