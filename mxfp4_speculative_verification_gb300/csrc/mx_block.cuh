@@ -17,14 +17,6 @@ __device__ __forceinline__ float exact_pow2(int e) {  // e in [-149, 127]
     return __uint_as_float(1u << (e + 149));
 }
 
-// Grid code (0..7) of a in [0, 6]: count of decision boundaries passed.
-// Midpoints 0.25, 1.25, 2.5, 5 tie to the lower (even) code, midpoints
-// 0.75, 1.75, 3.5 tie to the upper (even) code.
-__device__ __forceinline__ uint32_t e2m1_magnitude_code(float a) {
-    return uint32_t(a > 0.25f) + uint32_t(a >= 0.75f) + uint32_t(a > 1.25f) +
-           uint32_t(a >= 1.75f) + uint32_t(a > 2.5f) + uint32_t(a >= 3.5f) + uint32_t(a > 5.0f);
-}
-
 // The block exponent of a finite block with largest magnitude amax: the
 // smallest integer e with amax <= 6 * 2^e, clamped to [-127, 127]; 0 for an
 // all-zero block.
@@ -35,6 +27,36 @@ __device__ __forceinline__ int mx_block_exp(float amax) {
     const uint32_t man = bits & 0x7FFFFFu;
     const int e = (ex == 0) ? -127 : ex - 129 + (man > 0x400000u ? 1 : 0);
     return max(-127, min(127, e));
+}
+
+// The 16 nibble bytes of a block, as four little-endian words, into out16:
+// one 16-byte store where out16 is 16-byte aligned, else byte stores.
+__device__ __forceinline__ void store_block16(uint8_t* __restrict__ out16, const uint32_t (&w)[4]) {
+    if ((reinterpret_cast<uintptr_t>(out16) & 15) == 0) {
+        *reinterpret_cast<uint4*>(out16) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) out16[j] = uint8_t(w[j >> 2] >> (8 * (j & 3)));
+    }
+}
+
+// Elements v[k0 .. k0+7] times inv (an exact power of two) as eight E2M1
+// codes, element k0 in the low nibble of byte 0: the hardware conversion
+// rounds to the nearest grid value with ties to the even code and keeps the
+// sign (also of a value that rounds to zero), which is the pack rule; the
+// scaled values never exceed 6, so saturation never acts.
+__device__ __forceinline__ uint32_t e2m1x8_rn(const float (&v)[32], int k0, float inv) {
+    uint32_t o;
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+        " mov.b32 %0, {b0, b1, b2, b3};\n}\n"
+        : "=r"(o)
+        : "f"(v[k0] * inv), "f"(v[k0 + 1] * inv), "f"(v[k0 + 2] * inv), "f"(v[k0 + 3] * inv),
+          "f"(v[k0 + 4] * inv), "f"(v[k0 + 5] * inv), "f"(v[k0 + 6] * inv), "f"(v[k0 + 7] * inv));
+    return o;
 }
 
 // Packs v[0..31] into 16 nibble bytes (element k in byte k/2, even k in the
@@ -49,21 +71,18 @@ __device__ __forceinline__ bool pack_block32(const float (&v)[32], uint8_t* __re
         if (!(a <= 3.402823466e38f)) finite = false;  // Inf or NaN
         else amax = fmaxf(amax, a);
     }
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
     if (!finite) {
         *scale = 255;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) out16[k] = 0;
+        store_block16(out16, w);
         return false;
     }
     const int e = mx_block_exp(amax);
     *scale = uint8_t(e + 127);
     const float inv = exact_pow2(-e);
 #pragma unroll
-    for (int k = 0; k < 32; k += 2) {
-        const uint32_t c0 = e2m1_magnitude_code(fabsf(v[k]) * inv) | ((__float_as_uint(v[k]) >> 31) << 3);
-        const uint32_t c1 = e2m1_magnitude_code(fabsf(v[k + 1]) * inv) | ((__float_as_uint(v[k + 1]) >> 31) << 3);
-        out16[k / 2] = uint8_t(c0 | (c1 << 4));
-    }
+    for (int j = 0; j < 4; ++j) w[j] = e2m1x8_rn(v, 8 * j, inv);
+    store_block16(out16, w);
     return true;
 }
 
