@@ -65,3 +65,16 @@ def test_pack_rejects_wrong_outputs():
         mxs.mxfp4_pack(w, scales=torch.zeros((4, 2), dtype=torch.int8))
     with pytest.raises(mxs.MxsError):
         mxs.mxfp4_pack(torch.zeros((4, 48), dtype=torch.float32))
+
+
+def test_grouped_plan_checks_its_problems_once_at_construction():
+    x, nib, sc = _gemm_operands()
+    y = torch.zeros((5, 64), dtype=torch.float32)
+    with pytest.raises(mxs.MxsError):
+        mxs.GroupedGemm([])
+    with pytest.raises(mxs.MxsError):
+        mxs.GroupedGemm([(x, nib, sc[:, :3], y)])                            # scales too short
+    with pytest.raises(mxs.MxsError):
+        mxs.GroupedGemm([(x, nib, sc, torch.zeros((5, 63), dtype=torch.float32))])  # y too small
+    with pytest.raises(mxs.MxsError):
+        mxs.GroupedGemm([(x, nib, sc, y)])                                   # CPU tensors: no device launch

@@ -126,3 +126,28 @@ def test_grouped_claim_order_does_not_change_results(env, monkeypatch, M):
     torch.cuda.synchronize()
     for a, (*_, b) in zip(dyn, probs):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("M", [5, 20])
+def test_grouped_plan_equals_the_call(env, M):
+    """GroupedGemm (checked once, one C call per step) writes the same bits as
+    mxfp4_verify_gemm_grouped, call after call, and sees in-place updates of x."""
+    torch, mxs = env
+    shapes = [(4096, 640), (1024, 64), (2048, 257), (4096, 1000)]
+    probs, _ = _problems(env, M, shapes)
+    mxs.mxfp4_verify_gemm_grouped(probs)
+    torch.cuda.synchronize()
+    ref = [p[3].clone() for p in probs]
+    plan = mxs.GroupedGemm(probs)
+    for _ in range(3):
+        for p in probs:
+            p[3].fill_(float("nan"))
+        plan()
+        torch.cuda.synchronize()
+        for p, r in zip(probs, ref):
+            assert torch.equal(p[3].view(torch.int32), r.view(torch.int32))
+    x0 = probs[0][0]
+    x0.mul_(2.0)  # exact: a power of two
+    plan()
+    torch.cuda.synchronize()
+    assert torch.equal(probs[0][3], 2.0 * ref[0])
