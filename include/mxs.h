@@ -382,7 +382,8 @@ typedef struct mxs_sampling {
 /* spec_sampling_law: the transformed laws of R logit rows.
  *   logits  device, [R, V] fp32, 4-byte aligned
  *   probs   device, [R, V] fp32, written (may not overlap logits)
- *   1 <= R <= 2^28, 1 <= V <= 131072 (a row is held by 8 CTAs at most) */
+ *   1 <= R <= 2^28, 1 <= V <= 131072 (below 128 rows a cluster of up to 8 CTAs
+ *   holds each row; from 128 rows one CTA streams each row) */
 mxs_status spec_sampling_law(const float* logits, int64_t R, int64_t V,
                              const mxs_sampling* sampling, float* probs,
                              int32_t* dev_status, void* stream);
