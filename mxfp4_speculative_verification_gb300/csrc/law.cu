@@ -3,9 +3,12 @@
 // temperature, then top-k, then top-p, applied to the target and the draft
 // alike; raw probabilities with a filtered law break the proof).
 //
-// One thread-block cluster of C CTAs x 512 threads per logit row, each CTA
+// Two forms compute the same statistics bit for bit.  Below 128 rows: one
+// thread-block cluster of C CTAs x 512 threads per logit row, each CTA
 // holding a 16384-logit slice in shared memory (V <= 131072); two CTAs share
-// an SM, so one row's barriers overlap another row's work.  Steps:
+// an SM, so one row's barriers overlap another row's work.  From 128 rows:
+// one 1024-thread CTA per row that streams the row again for each pass (the
+// row form, further down), with about one row per SM in flight.  Steps:
 //  * the row's largest finite logit m, and whether it holds NaN or +inf (then
 //    it has no law);
 //  * top-k: the key (monotone uint32 image of the logit) of the k-th largest
@@ -30,6 +33,10 @@
 // (4 rounds of 8 bits, one exchange each) finishes instead.  Every step is a
 // function of the row alone, so all CTAs of a cluster take the same
 // decisions, and the result is the same as one radix select over the row.
+// Tokens of zero weight (below the top-k cut, or of zero fixed-point mass)
+// may enter the fine histogram and the gather: they add nothing to any sum,
+// and the cut, the largest key whose tokens at or above it reach the target,
+// never falls on them (the bin holding the cut has weight).
 #include <cooperative_groups.h>
 
 #include <climits>
