@@ -33,10 +33,10 @@
 // (4 rounds of 8 bits, one exchange each) finishes instead.  Every step is a
 // function of the row alone, so all CTAs of a cluster take the same
 // decisions, and the result is the same as one radix select over the row.
-// Tokens of zero weight (below the top-k cut, or of zero fixed-point mass)
-// may enter the fine histogram and the gather: they add nothing to any sum,
-// and the cut, the largest key whose tokens at or above it reach the target,
-// never falls on them (the bin holding the cut has weight).
+// Tokens of zero fixed-point mass (e < 2^-46) may enter the fine histogram
+// and the gather of a top-p cut (tokens below the top-k cut never do): they
+// add nothing to any sum, and the cut, the largest key whose tokens at or
+// above it reach the target, never falls on them.
 #include <cooperative_groups.h>
 
 #include <climits>
