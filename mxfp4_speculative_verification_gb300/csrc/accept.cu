@@ -578,7 +578,10 @@ __global__ void __launch_bounds__(kAcceptThreads, RELOAD && !LG ? 2 : 1)
     static_assert(kRegSub <= kAcceptThreads, "one sub-tile per thread in the scan");
     __shared__ float subsum[kRegSub];
     __shared__ ff wsum[kRegSub / 32];
-    __shared__ SliceSummaryFF sh_mine;
+    // every CTA's slice summary, written into every CTA of the cluster before
+    // one cluster barrier (one buffer per exchange: a second exchange follows
+    // when the residual has no mass)
+    __shared__ SliceSummaryFF sh_sums[2][kMaxCluster];
     __shared__ ff sh_S, sh_slice_prefix, sh_prefix;
     __shared__ int sh_j, sh_flags, sh_err, sh_lastpos, sh_all_lastpos, sh_owner, sh_tstar;
 
@@ -625,6 +628,7 @@ __global__ void __launch_bounds__(kAcceptThreads, RELOAD && !LG ? 2 : 1)
     // Load the slice, form the sub-tile sums and exchange the slice totals.
     // Afterwards sh_S (identical bits in every CTA), sh_slice_prefix,
     // sh_all_lastpos and sh_owner are set.
+    int xr = 0;  // exchanges done
     auto load_and_exchange = [&]() {
         int lp = -1;
         // all chunks in flight at once, or (RELOAD) batches of 4 chunks (2 when
@@ -663,15 +667,15 @@ __global__ void __launch_bounds__(kAcceptThreads, RELOAD && !LG ? 2 : 1)
             ff tot = wsum[0];
 #pragma unroll
             for (int w = 1; w < kRegSub / 32; ++w) tot = ff_add(tot, wsum[w]);
-            sh_mine.total = tot;
-            sh_mine.lastpos = sh_lastpos;
+            const SliceSummaryFF mine{tot, sh_lastpos};
+            for (int c = 0; c < C; ++c) cluster.map_shared_rank(&sh_sums[xr][0], c)[rank] = mine;
         }
-        cluster.sync();
+        cluster.sync();  // every summary has landed in every CTA; none is read remotely afterwards
         if (threadIdx.x == 0) {
             SliceSummaryFF o[kMaxCluster];
 #pragma unroll
             for (int c = 0; c < kMaxCluster; ++c)
-                if (c < C) o[c] = *cluster.map_shared_rank(&sh_mine, c);
+                if (c < C) o[c] = sh_sums[xr][c];
             ff S{0.f, 0.f}, prefix{0.f, 0.f};
             int last = -1;
 #pragma unroll
@@ -699,7 +703,8 @@ __global__ void __launch_bounds__(kAcceptThreads, RELOAD && !LG ? 2 : 1)
             sh_all_lastpos = last;
             sh_owner = owner;
         }
-        cluster.sync();  // every CTA has read every summary
+        __syncthreads();
+        ++xr;
     };
     load_and_exchange();
     if (!(sh_S.hi > 0.f)) {
