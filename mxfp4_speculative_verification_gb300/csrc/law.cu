@@ -54,14 +54,17 @@ namespace mxs {
 
 constexpr int kLawThreads = 512;
 constexpr int kLawWarps = kLawThreads / 32;
-constexpr int kLawChunks = 32;  // logits per thread
-constexpr int kLawMaxCluster = 8;
-constexpr int64_t kLawSlice = int64_t(kLawThreads) * kLawChunks;
+constexpr int kLawChunksWide = 32;  // logits per thread: 16384-logit slices, clusters of up to 8
+constexpr int kLawChunksNarrow = 16;  // 8192-logit slices, clusters of up to 16 (few rows)
+constexpr int kLawMaxClusterAll = 16;
+template <int CH>
+constexpr int law_max_cluster() { return int(kLawMaxV / (int64_t(kLawThreads) * CH)); }
 constexpr int kLawBins = 512;  // one fine-histogram bin per thread
 constexpr int kGatherCap = 128;    // tokens one CTA may contribute to a gather
 constexpr int kGatherTotal = 256;  // tokens a cluster may gather
 constexpr int kLawVals = 4;        // values one step publishes to the cluster
-static_assert(kLawMaxV == kLawMaxCluster * kLawSlice, "vocabulary limit");
+static_assert(law_max_cluster<kLawChunksWide>() == 8 && law_max_cluster<kLawChunksNarrow>() == kLawMaxClusterAll,
+              "vocabulary limit");
 
 struct LawArgs {
     const float* logits;   // rows 0 .. R1-1: [R1, V]
@@ -81,9 +84,10 @@ struct GatherEntry {
     float x;
 };
 
-// Shared memory of one CTA (dynamic, about 70 KB).
+// Shared memory of one CTA (dynamic, about 70 KB with 16384-logit slices).
+template <int CH>
 struct LawSmem {
-    float xs[kLawChunks * kLawThreads];  // element v0 + i * 512 + t at [i * 512 + t]
+    float xs[CH * kLawThreads];          // element v0 + i * 512 + t at [i * 512 + t]
     GatherEntry glist[kGatherCap];       // this CTA's tokens of the gathered bin
     GatherEntry gall[kGatherTotal];      // the cluster's, in CTA order
     unsigned long long gw[kGatherTotal]; // and their weights
@@ -92,7 +96,7 @@ struct LawSmem {
     unsigned long long scan_w[kLawWarps];
     unsigned long long sel_above, sel_at, sel_total;
     int gcount;                          // tokens found for the gather (may exceed the cap)
-    int goff[kLawMaxCluster + 1];
+    int goff[kLawMaxClusterAll + 1];
     int sel_first, sel_last;
     uint32_t sel_key, sel_min;
     int sel_any, sel_idx;
@@ -101,7 +105,6 @@ struct LawSmem {
     float m;
     int bad;
 };
-constexpr int kLawSmem = int(sizeof(LawSmem));
 
 // Log-mass classes of the tokens, by a = (l - m) / T <= 0: 0 for a > -4, 1
 // for (-8, -4], 2 for (-16, -8], 3 below.  (On logits like N(0, 3) at T =
@@ -194,9 +197,13 @@ __device__ __forceinline__ bool in_class(float a, int c) {
     return a <= hi && (c == 3 || a > lo);
 }
 
+template <int CH>
 __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawArgs A) {
+    constexpr int kLawChunks = CH;
+    constexpr int64_t kLawSlice = int64_t(kLawThreads) * CH;
+    constexpr int kLawMaxCluster = law_max_cluster<CH>();
     extern __shared__ __align__(16) uint8_t law_smem_raw[];
-    LawSmem& S = *reinterpret_cast<LawSmem*>(law_smem_raw);
+    LawSmem<CH>& S = *reinterpret_cast<LawSmem<CH>*>(law_smem_raw);
     __shared__ uint32_t hist_cnt[2][kLawBins], hist_lo[2][kLawBins], hist_hi[2][kLawBins];
     __shared__ unsigned long long pubv[2][kLawVals];
 
@@ -250,7 +257,7 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
             float a = -INFINITY;
             int b = 0;
             if (lane < C) {
-                const LawSmem* o = cluster.map_shared_rank(&S, lane);
+                const LawSmem<CH>* o = cluster.map_shared_rank(&S, lane);
                 a = o->pub_m;
                 b = o->pub_bad;
             }
@@ -433,7 +440,9 @@ __global__ void __launch_bounds__(kLawThreads, 2) sampling_law_kernel(const LawA
             base = S.tot[2];
         }
         // this thread's tokens of class c (slots holding a token, key >= lo)
-        uint32_t valid = 0xFFFFFFFFu;
+        // the slots of this thread (CH of the mask's bits; class 3 is taken
+        // as the complement of the class edges, so the mask must stop there)
+        uint32_t valid = CH >= 32 ? 0xFFFFFFFFu : (1u << CH) - 1u;
         if (nv < kLawSlice) {
             valid = 0u;
 #pragma unroll
@@ -1002,34 +1011,44 @@ __global__ void __launch_bounds__(kRowThreads, 1) sampling_law_row_kernel(const 
     if (A.probs) row_map(row, A.probs + r * V, V, [&](float x) { return law_value(x, st, inv_t); });
 }
 
-// The form for R rows (MXS_LAW_FORM=cluster / row overrides).  Measured at
-// V = 128256, top-p: 80 rows 71 us (cluster) / 99 us (row); 144 rows 124 /
-// 112 us; 576 rows 433 / 400 us.  Below ~100 rows the cluster form spreads
-// each row over 4 SMs; above, the row form keeps more rows in flight.
+// The form for R rows (MXS_LAW_FORM=cluster16 / cluster / row overrides).
+// Measured at V = 128256, top-p: 80 rows 71 us (clusters of 8) / 99 us (row);
+// 144 rows 124 / 112 us; 576 rows 433 / 400 us.  Below ~100 rows the cluster
+// form spreads each row over 4 SMs; above, the row form keeps more rows in
+// flight.  When clusters of 8 would leave most SMs idle (R * C <= 76), the
+// narrow slices (8192 logits, clusters of up to 16) spread each row over
+// twice the SMs: 1 row 18.7 / 10.5 us (top-p / plain) against 20.7 / 14.4;
+// 4 rows 20.6 / 10.4 against 20.6 / 14.4; even at 9 rows; slower from 16.
 constexpr int64_t kLawRowMinRows = 128;
-static bool law_row_form(int64_t R) {
+enum class LawForm { kNarrow, kWide, kRow };
+static LawForm law_form(int64_t R, int64_t V) {
     if (const char* f = std::getenv("MXS_LAW_FORM")) {
-        if (std::strcmp(f, "row") == 0) return true;
-        if (std::strcmp(f, "cluster") == 0) return false;
+        if (std::strcmp(f, "row") == 0) return LawForm::kRow;
+        if (std::strcmp(f, "cluster") == 0) return LawForm::kWide;
+        if (std::strcmp(f, "cluster16") == 0) return LawForm::kNarrow;
     }
-    return R >= kLawRowMinRows;
+    if (R >= kLawRowMinRows) return LawForm::kRow;
+    const int64_t c8 = (V + int64_t(kLawThreads) * kLawChunksWide - 1) / (int64_t(kLawThreads) * kLawChunksWide);
+    return R * c8 <= 76 ? LawForm::kNarrow : LawForm::kWide;
 }
 
-// Clusters of C CTAs, C = ceil(V / 16384) (1..8), one per row; or the row form.
-static cudaError_t launch_law(const LawArgs& A, cudaStream_t stream) {
-    if (A.R >= 1 && law_row_form(A.R)) {
-        sampling_law_row_kernel<<<unsigned(A.R), kRowThreads, 0, stream>>>(A);
-        return cudaGetLastError();
-    }
-    const int C = int((A.V + kLawSlice - 1) / kLawSlice);
-    if (A.R < 1) return cudaSuccess;
-    static const cudaError_t attr_err =
-        cudaFuncSetAttribute(sampling_law_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLawSmem);
+// One cluster of C = ceil(V / (512 CH)) CTAs per row.
+template <int CH>
+static cudaError_t launch_law_cluster(const LawArgs& A, cudaStream_t stream) {
+    constexpr int64_t kSlice = int64_t(kLawThreads) * CH;
+    constexpr int kSmem = int(sizeof(LawSmem<CH>));
+    const int C = int((A.V + kSlice - 1) / kSlice);
+    static const cudaError_t attr_err = [] {
+        cudaError_t e = cudaFuncSetAttribute(sampling_law_kernel<CH>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e == cudaSuccess && law_max_cluster<CH>() > 8)  // clusters beyond the portable 8
+            e = cudaFuncSetAttribute(sampling_law_kernel<CH>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        return e;
+    }();
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(A.R * C), 1, 1);
     cfg.blockDim = dim3(kLawThreads, 1, 1);
-    cfg.dynamicSmemBytes = kLawSmem;
+    cfg.dynamicSmemBytes = kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -1038,7 +1057,20 @@ static cudaError_t launch_law(const LawArgs& A, cudaStream_t stream) {
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, sampling_law_kernel, A);
+    return cudaLaunchKernelEx(&cfg, sampling_law_kernel<CH>, A);
+}
+
+static cudaError_t launch_law(const LawArgs& A, cudaStream_t stream) {
+    if (A.R < 1) return cudaSuccess;
+    switch (law_form(A.R, A.V)) {
+        case LawForm::kRow:
+            sampling_law_row_kernel<<<unsigned(A.R), kRowThreads, 0, stream>>>(A);
+            return cudaGetLastError();
+        case LawForm::kNarrow:
+            return launch_law_cluster<kLawChunksNarrow>(A, stream);
+        default:
+            return launch_law_cluster<kLawChunksWide>(A, stream);
+    }
 }
 
 static LawArgs law_args(const float* logits, int64_t R, int64_t V, const LawSampling& s, int32_t* status) {

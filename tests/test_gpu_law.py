@@ -34,9 +34,10 @@ def env():
     return cuda_or_skip()
 
 
-@pytest.fixture(params=["cluster", "row"])
+@pytest.fixture(params=["cluster16", "cluster", "row"])
 def form(request, monkeypatch):
-    """Both kernel forms of the laws: one cluster per row, or one CTA per row
+    """Every kernel form of the laws: one cluster per row of 8192-logit slices
+    (up to 16 CTAs) or of 16384-logit slices (up to 8), or one CTA per row
     streaming the row for each pass (the library picks by row count)."""
     monkeypatch.setenv("MXS_LAW_FORM", request.param)
     return request.param
@@ -139,7 +140,7 @@ def test_law_deterministic(env, form):
     (50257, {"top_p": 0.95}), (128256, {"temperature": 0.8, "top_p": 0.9}), (131071, {"top_k": 1000}),
     (128255, {"top_k": 60000, "top_p": 0.999999}), (4099, {"temperature": 0.05, "top_p": 0.5})])
 def test_law_forms_bit_identical(env, monkeypatch, V, kw):
-    """The two kernel forms take the same decisions on the same fixed-point
+    """The kernel forms take the same decisions on the same fixed-point
     weights: every probability is the same bits.  Odd V puts the rows at
     every 4-byte phase, and the second input starts 4 bytes past a 16-byte
     boundary (unaligned heads and tails; probabilities then written with
@@ -155,7 +156,7 @@ def test_law_forms_bit_identical(env, monkeypatch, V, kw):
         l[7, :5] = l[7].max() + 1   # ties at the top
     flat = torch.from_numpy(np.concatenate([np.zeros(1, np.float32), l.ravel()])).to(dev)
     outs = []
-    for f in ("cluster", "row"):
+    for f in ("cluster16", "cluster", "row"):
         monkeypatch.setenv("MXS_LAW_FORM", f)
         for t in (torch.from_numpy(l).to(dev), flat[1:].view(R, V)):
             outs.append(mxs.spec_sampling_law(t, **kw).cpu().numpy().view(np.uint32))
