@@ -190,6 +190,24 @@ __device__ __forceinline__ void class_sums(const uint32_t (&h)[kLawVals], const 
         v[j] = BY_MASS ? (static_cast<unsigned long long>(h[j]) << 23) + l[j] : static_cast<unsigned long long>(l[j]);
 }
 
+// The tokens of fine bin f of class c are those whose t = -a lies in [*tlo,
+// *thi]: law_fine is non-decreasing in t, so both ends are found by bisection
+// over the bit patterns of non-negative floats, with law_fine itself (the
+// same float operations as the per-token test they replace).
+__device__ inline void fine_bin_range(int c, int f, float* tlo, float* thi) {
+    auto first_at_least = [&](int g) {  // smallest t >= 0 with law_fine(-t, c) >= g
+        uint32_t lo = 0u, hi = 0x7F800000u;  // +inf lands in bin 511
+        while (lo < hi) {
+            const uint32_t mid = lo + ((hi - lo) >> 1);
+            if (law_fine(-__uint_as_float(mid), c) >= g) hi = mid;
+            else lo = mid + 1u;
+        }
+        return lo;
+    };
+    *tlo = __uint_as_float(first_at_least(f));
+    *thi = f >= kLawBins - 1 ? INFINITY : __uint_as_float(first_at_least(f + 1) - 1u);
+}
+
 // Whether a token of log-mass a lies in class c.
 __device__ __forceinline__ bool in_class(float a, int c) {
     const float hi = c == 0 ? INFINITY : c == 1 ? -4.f : c == 2 ? -8.f : -16.f;
@@ -722,7 +740,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) sampling_law_row_kernel(const 
     __shared__ unsigned long long sel_above, sel_at;
     __shared__ int gcount, sel_first, sel_last, sel_any, sel_idx;
     __shared__ uint32_t sel_key, sel_min;
-    __shared__ float sh_m;
+    __shared__ float sh_m, sh_tlo, sh_thi;
     __shared__ int sh_bad;
 
     const int64_t r = blockIdx.x;
@@ -892,26 +910,42 @@ __global__ void __launch_bounds__(kRowThreads, 1) sampling_law_row_kernel(const 
         int f;
         {
             hist_begin();
-            row_visit(row, V, [&](float x) {
-                const float a = (x - m) * inv_t;
-                if (in_class(a, c) && law_key(x) >= lo) hist_put(law_fine(a, c), by_mass, weight_of(x));
-            });
+            auto fine_pass = [&](auto has_lo) {
+                row_visit(row, V, [&](float x) {
+                    const float a = (x - m) * inv_t;
+                    if (in_class(a, c) && (!decltype(has_lo)::value || law_key(x) >= lo))
+                        hist_put(law_fine(a, c), by_mass, weight_of(x));
+                });
+            };
+            if (lo) fine_pass(LawTag<true>{});
+            else fine_pass(LawTag<false>{});
             unsigned long long above = 0, at = 0;
             f = pick(hist_end(by_mass), target - base, &above, &at);
             base += above;
         }
         const unsigned long long need = target - base;
 
-        // 3. gather bin f's tokens
-        if (tid == 0) gcount = 0;
+        // 3. gather bin f's tokens (bin f as an interval of t = -a)
+        if (tid == 0) {
+            gcount = 0;
+            fine_bin_range(c, f, &sh_tlo, &sh_thi);
+        }
         __syncthreads();
-        row_visit(row, V, [&](float x) {
-            const float a = (x - m) * inv_t;
-            if (in_class(a, c) && law_key(x) >= lo && law_fine(a, c) == f) {
-                const int pos = atomicAdd(&gcount, 1);
-                if (pos < kGatherTotal) gall[pos] = GatherEntry{law_key(x), x};
-            }
-        });
+        {
+            const float tlo = sh_tlo, thi = sh_thi;
+            auto gather_pass = [&](auto has_lo) {
+                row_visit(row, V, [&](float x) {
+                    const float a = (x - m) * inv_t;
+                    if (in_class(a, c) && -a >= tlo && -a <= thi &&
+                        (!decltype(has_lo)::value || law_key(x) >= lo)) {
+                        const int pos = atomicAdd(&gcount, 1);
+                        if (pos < kGatherTotal) gall[pos] = GatherEntry{law_key(x), x};
+                    }
+                });
+            };
+            if (lo) gather_pass(LawTag<true>{});
+            else gather_pass(LawTag<false>{});
+        }
         __syncthreads();
         const int n = gcount;
         LawCut cut;
