@@ -55,16 +55,19 @@ GEMM_TRAFFIC = {
     # (a single lm_head call at M=5 measured 1.0064)
     "mma": {"ratio": 1.0000, "sha": "bf0b691ec7beb45b"},
     # mxfp4_gemm_bs_kernel, kind::mxf8f6f4 (passes of 33..64 rows): lm_head at M=64
-    "bs8": {"ratio": 0.9170, "sha": "6eb5555238bdf2e9"},
+    "bs8": {"ratio": 0.9171, "sha": "4dfbefb90e4d63a5"},
     # mxfp4_gemm_bs_kernel, kind::mxf4 (passes of 9..32 rows): lm_head at M=20
-    "bs4": {"ratio": 0.9841, "sha": "6eb5555238bdf2e9"},
+    "bs4": {"ratio": 0.9849, "sha": "4dfbefb90e4d63a5"},
+    # mxfp4_gemm_bs_kernel, W4A4 (X quantised in the call, passes of <= 256 rows): lm_head at M=256
+    "w4a4": {"ratio": 0.8917, "sha": "4dfbefb90e4d63a5"},
 }
 # sm__pipe_tensor_cycles_active (% of peak, elapsed) of each kernel, from the
 # same captures as GEMM_TRAFFIC (keyed alike: None once the kernel changed)
 GEMM_TENSOR_PCT = {
     "mma": 27.89,   # grouped instance, 8 layers at M=5
     "bs8": 34.34,   # lm_head at M=64
-    "bs4": 34.58,   # lm_head at M=20
+    "bs4": 34.47,   # lm_head at M=20
+    "w4a4": 13.67,  # lm_head at M=256
 }
 
 
@@ -240,6 +243,7 @@ KERNEL_SOURCES = {
     "mma": ("mxs_device.cuh", "gemm_common.cuh", "gemm_mma.cuh"),
     "bs8": ("mxs_device.cuh", "gemm_common.cuh", "gemm_bs.cuh"),
     "bs4": ("mxs_device.cuh", "gemm_common.cuh", "gemm_bs.cuh"),
+    "w4a4": ("mxs_device.cuh", "gemm_common.cuh", "gemm_bs.cuh"),
 }
 
 
@@ -578,7 +582,7 @@ def run_mxs(args, world, rank, local):
 
     # the other configurations, each timed the same way (weights of the same
     # stack reused; the 70B stack generated once on the device)
-    sweep, acc_sweep, logits_acc, nv, kvc = [], None, None, None, None
+    sweep, acc_sweep, logits_acc, nv, kvc, w4 = [], None, None, None, None, None
     if not args.no_sweep and rank == 0 and world == 1:
         wcache = {model: weights}
         clocks2 = ClockSampler(local)
@@ -600,6 +604,7 @@ def run_mxs(args, world, rank, local):
         logits_acc = logits_accept_rows(mxs, torch, dev, peak)
         nv = nvfp4_rows(mxs, torch, dev, peak)
         kvc = kv_cache_rows(mxs, torch, dev, peak)
+        w4 = w4a4_rows(mxs, torch, dev, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -657,6 +662,7 @@ def run_mxs(args, world, rank, local):
         "accept_logits": logits_acc,
         "nvfp4_lm_head": nv,
         "kv_cache": kvc,
+        "w4a4": w4,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -804,6 +810,10 @@ def profile_target(args):
             nib, sc = workloads.device_nvfp4_weights(N, K, seed=0, device=dev)
             for _ in range(4):
                 mxs.nvfp4_verify_gemm(x, nib, sc, 0.0731, out=y)
+        elif args.profile_w4a4:
+            nib, sc = workloads.device_mxfp4_weights(N, K, *workloads.LLAMA_EXP_RANGE, seed=0, device=dev)
+            for _ in range(4):
+                mxs.mxfp4_verify_gemm_w4a4(x, nib, sc, out=y)
         else:
             nib, sc = workloads.device_mxfp4_weights(N, K, *workloads.LLAMA_EXP_RANGE, seed=0, device=dev)
             for _ in range(4):
@@ -1008,6 +1018,78 @@ def nvfp4_rows(mxs, torch, dev, peak, reps=20):
             "timing": "back-to-back calls; the weights (279 / 296 MB) exceed L2", "rows": rows}
 
 
+def w4a4_rows(mxs, torch, dev, peak, reps=20):
+    """W4A4 (X quantised to MX-FP4 by the pack rule inside the call, block-
+    scaled kind::mxf4 product, passes of up to 256 rows) beside the W4A16
+    entry point on the same MXFP4 weights: the 8B lm_head (K = 4096,
+    N = 128256, 279 MB, beyond L2) at M = 80 / 160 / 256 / 320, back-to-back
+    calls; and the whole 8B stack (32 layers x 4 GEMMs + lm_head, 4.3 GB) at
+    M = 80 and 256, one call per GEMM, in a CUDA graph.  Algorithmic bytes as
+    for the verify GEMM: nibbles + scales + bf16 X + fp32 Y."""
+    N, K = workloads.VOCAB_LLAMA, 4096
+    lo, hi = workloads.LLAMA_EXP_RANGE
+    nib, sc = workloads.device_mxfp4_weights(N, K, lo, hi, seed=81, device=dev)
+    rows = []
+    for M in (80, 160, 256, 320):
+        x = workloads.device_bf16_normal(M, K, seed=82 + M, device=dev)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        for mode in ("w4a4", "w4a16"):
+            if mode == "w4a4":
+                ws = torch.empty(mxs.mxfp4_verify_gemm_w4a4_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+                call = lambda: mxs.mxfp4_verify_gemm_w4a4(x, nib, sc, out=y, workspace=ws)
+                w_passes = (M + 255) // 256
+            else:
+                ws = torch.empty(mxs.mxfp4_verify_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+                call = lambda: mxs.mxfp4_verify_gemm(x, nib, sc, out=y, workspace=ws)
+                w_passes = len(gemm_passes(M))
+            for _ in range(5):
+                call()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                call()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            nb = gemm_bytes(M, N, K)
+            rows.append({"mode": mode, "M": M, "passes_over_W": w_passes, "us_per_call": us, "bytes_per_call": nb,
+                         "hbm_gbs": nb / (us * 1e-6) / 1e9, "pct_of_peak": nb / (us * 1e-6) / 1e9 / peak,
+                         "tflops": 2.0 * M * N * K / (us * 1e-6) / 1e12})
+            del ws
+        del x, y
+    del nib, sc
+    torch.cuda.empty_cache()
+    stack = []
+    shapes = workloads.stack_shapes("llama8b")
+    weights = [workloads.device_mxfp4_weights(N_, K_, lo, hi, seed=900 + i, device=dev)
+               for i, (_, K_, N_) in enumerate(shapes)]
+    for M in (80, 256):
+        xs = {K_: workloads.device_bf16_normal(M, K_, seed=K_ + M, device=dev) for K_ in sorted({k for _, k, _ in shapes})}
+        ys = [torch.empty((M, N_), dtype=torch.float32, device=dev) for _, _, N_ in shapes]
+        nb = sum(gemm_bytes(M, N_, K_) for _, K_, N_ in shapes)
+        for mode in ("w4a4", "w4a16"):
+            size = mxs.mxfp4_verify_gemm_w4a4_workspace_size if mode == "w4a4" else mxs.mxfp4_verify_gemm_workspace_size
+            fn = mxs.mxfp4_verify_gemm_w4a4 if mode == "w4a4" else mxs.mxfp4_verify_gemm
+            ws = torch.empty(max(size(M, N_, K_) for _, K_, N_ in shapes), dtype=torch.uint8, device=dev)
+
+            def stack_call():
+                for (_, K_, N_), (wn, wsc), y_ in zip(shapes, weights, ys):
+                    fn(xs[K_], wn, wsc, out=y_, workspace=ws)
+
+            us = graph_us(torch, dev, stack_call, reps=5)
+            stack.append({"mode": mode, "M": M, "gemms": len(shapes), "us_per_stack": us, "bytes": nb,
+                          "hbm_gbs": nb / (us * 1e-6) / 1e9, "pct_of_peak": nb / (us * 1e-6) / 1e9 / peak})
+            del ws
+        del xs, ys
+    del weights
+    torch.cuda.empty_cache()
+    return {"metric": "W4A4 verify GEMM (X quantised to MX-FP4 in the call) vs W4A16, us per call",
+            "timing": "lm_head: back-to-back calls, weights 279 MB beyond L2; stack: one call per GEMM "
+                      "(quantisation + product each) in a CUDA graph, 4.3 GB of weights",
+            "lm_head": rows, "stack_llama8b": stack}
+
+
 def kv_cache_rows(mxs, torch, dev, peak, reps=20):
     """The MX-FP4 KV cache of the 8B stack's verification block: every layer's
     keys and values of one position (32 layers x 2 x 8 heads x 128 = 65536
@@ -1086,6 +1168,8 @@ def main():
                     help="only run one grouped verify GEMM over the stack's first LAYERS layers 4 times (ncu target)")
     ap.add_argument("--profile-nvfp4", action="store_true",
                     help="with --profile-gemm: NVFP4 weights (nvfp4_verify_gemm) instead of MXFP4")
+    ap.add_argument("--profile-w4a4", action="store_true",
+                    help="with --profile-gemm: the W4A4 entry point (mxfp4_verify_gemm_w4a4)")
     ap.add_argument("--profile-law", action="store_true",
                     help="only run spec_sampling_law on the workload's target rows 4 times and exit (ncu target)")
     ap.add_argument("--profile-accept", action="store_true",

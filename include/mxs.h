@@ -6,8 +6,9 @@
  *
  *   mxfp4_pack         real weights -> E2M1 nibbles + E8M0 block scales
  *   mxfp4_verify_gemm  Y[M,N] = X[M,K] . dequant(W)^T, bf16 X, fp32 Y
- *                      (also grouped, without workspace, and on NVFP4
- *                      weights: nvfp4_verify_gemm)
+ *                      (also grouped, without workspace, on NVFP4
+ *                      weights: nvfp4_verify_gemm, and W4A4 with X
+ *                      quantised to MX-FP4: mxfp4_verify_gemm_w4a4)
  *   spec_accept        left-to-right acceptance, residual / bonus sampling,
  *                      emission of 1..K+1 tokens per sequence (also from
  *                      logits under temperature / top-k / top-p:
@@ -146,6 +147,33 @@ mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles,
                              int64_t N, int64_t K, void* workspace,
                              size_t workspace_bytes, int32_t* dev_status,
                              void* stream);
+
+/* ------------------------------------------------------------------------
+ * mxfp4_verify_gemm_w4a4 -- the verify GEMM with MX-FP4 activations (W4A4)
+ *
+ * "Module 11. Speculative Decoding and Quantization", §12 ("Microscaled FP4,
+ * W4A4, and the role of hardware"): weights and activations both MX-FP4.
+ * Each 32-element block of each row of X is quantised by mxfp4_pack's rule
+ * (e the smallest integer with max|x| <= 6 * 2^e, clamped to [-127, 127],
+ * 0 for an all-zero block; each element the nearest E2M1 value of x / 2^e,
+ * ties to the even code, the sign kept), and
+ *   Y[m, n] = sum_k q(X)[m, k] * dequant(W)[n, k]     (fp32 accumulation).
+ * This is a different product from mxfp4_verify_gemm's (X is rounded to 4
+ * bits); the block-scaled tensor core takes both operands as stored, and a
+ * pass covers up to 256 rows of X, so W is read once for M <= 256.
+ *
+ *   x, nibbles, scales, y, M, N, K: as for mxfp4_verify_gemm
+ *   workspace  device, >= mxfp4_verify_gemm_w4a4_workspace_size(M, N, K)
+ *              bytes, 16-byte aligned; not shared by two calls in flight
+ * A row of X holding Inf or NaN gives NaN in every output of that row.
+ * ---------------------------------------------------------------------- */
+size_t mxfp4_verify_gemm_w4a4_workspace_size(int64_t M, int64_t N, int64_t K);
+
+mxs_status mxfp4_verify_gemm_w4a4(const void* x, const uint8_t* nibbles,
+                                  const uint8_t* scales, float* y, int64_t M,
+                                  int64_t N, int64_t K, void* workspace,
+                                  size_t workspace_bytes, int32_t* dev_status,
+                                  void* stream);
 
 /* ------------------------------------------------------------------------
  * nvfp4_verify_gemm -- the verify GEMM on NVFP4 weights

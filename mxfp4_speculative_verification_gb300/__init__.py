@@ -29,7 +29,8 @@ from . import _build
 
 __all__ = ["build", "lib", "mxfp4_pack", "mxfp4_verify_gemm", "mxfp4_verify_gemm_workspace_size",
            "mxfp4_verify_gemm_grouped", "mxfp4_verify_gemm_grouped_workspace_size", "GroupedGemm",
-           "mxfp4_verify_gemm_noalloc", "nvfp4_verify_gemm", "nvfp4_verify_gemm_workspace_size",
+           "mxfp4_verify_gemm_noalloc", "mxfp4_verify_gemm_w4a4", "mxfp4_verify_gemm_w4a4_workspace_size",
+           "nvfp4_verify_gemm", "nvfp4_verify_gemm_workspace_size",
            "spec_accept", "mxfp4_kv_append", "spec_kv_commit", "mxfp4_kv_dequant", "spec_sampling_law", "spec_accept_logits",
            "spec_accept_logits_workspace_size", "hbm_read_probe", "hbm_copy_probe", "MxsError",
            "DEV_FLAGS",
@@ -76,6 +77,10 @@ def lib():
     L.mxfp4_verify_gemm_workspace_size.restype = sz
     L.mxfp4_verify_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, sz, vp, vp]
     L.mxfp4_verify_gemm.restype = i32
+    L.mxfp4_verify_gemm_w4a4_workspace_size.argtypes = [i64, i64, i64]
+    L.mxfp4_verify_gemm_w4a4_workspace_size.restype = sz
+    L.mxfp4_verify_gemm_w4a4.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, sz, vp, vp]
+    L.mxfp4_verify_gemm_w4a4.restype = i32
     L.nvfp4_verify_gemm_workspace_size.argtypes = [i64, i64, i64]
     L.nvfp4_verify_gemm_workspace_size.restype = sz
     L.nvfp4_verify_gemm.argtypes = [vp, vp, vp, ctypes.c_float, vp, i64, i64, i64, vp, sz, vp, vp]
@@ -222,6 +227,31 @@ def mxfp4_verify_gemm(x: torch.Tensor, nibbles: torch.Tensor, scales: torch.Tens
     _check(lib().mxfp4_verify_gemm(_ptr(x), _ptr(nibbles), _ptr(scales), _ptr(out), M, N, K,
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _ptr(dev_status), _stream(dev)))
+    return out
+
+
+def mxfp4_verify_gemm_w4a4_workspace_size(M: int, N: int, K: int) -> int:
+    return int(lib().mxfp4_verify_gemm_w4a4_workspace_size(M, N, K))
+
+
+def mxfp4_verify_gemm_w4a4(x: torch.Tensor, nibbles: torch.Tensor, scales: torch.Tensor, *,
+                           out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                           dev_status: torch.Tensor | None = None) -> torch.Tensor:
+    """W4A4: Y[M, N] (fp32) = q(X) . dequant(W)^T, q = X quantised to MX-FP4 by the pack rule."""
+    M, N, K = _gemm_shapes(x, nibbles, scales, out, dev_status)
+    if workspace is not None and workspace.dtype != torch.uint8:
+        raise MxsError("workspace must be a uint8 tensor")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    dev = _need_cuda(x, nibbles, scales, out, workspace, dev_status)
+    need = mxfp4_verify_gemm_w4a4_workspace_size(M, N, K)
+    if need == 0:
+        raise MxsError("unsupported GEMM shape")
+    if workspace is None:
+        workspace = _workspace(dev, need)
+    _check(lib().mxfp4_verify_gemm_w4a4(_ptr(x), _ptr(nibbles), _ptr(scales), _ptr(out), M, N, K,
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _ptr(dev_status), _stream(dev)))
     return out
 
 

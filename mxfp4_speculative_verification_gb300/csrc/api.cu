@@ -83,6 +83,29 @@ mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles, const uint8_
                                      workspace, ws, dev_status, as_stream(stream)));
 }
 
+size_t mxfp4_verify_gemm_w4a4_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (M < 1 || N < 1 || K < 32 || K % 32 != 0 || M > kMaxM || N > kMaxN || K > kMaxK) return 0;
+    // the in-place scale layout is assumed when K % 512 == 0
+    return mxs::gemm_w4a4_workspace_layout(M, N, K, true).bytes;
+}
+
+mxs_status mxfp4_verify_gemm_w4a4(const void* x, const uint8_t* nibbles, const uint8_t* scales, float* y,
+                                  int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, void* stream) {
+    if (!x || !nibbles || !scales || !y) return MXS_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return MXS_ERR_INVALID_ARG;
+    if (M > kMaxM || N > kMaxN || K > kMaxK) return MXS_ERR_UNSUPPORTED;
+    if (!aligned(x, 2) || !aligned(nibbles, 16) || !aligned(y, 4) || !aligned(dev_status, 4))
+        return MXS_ERR_MISALIGNED;
+    const bool sc_aligned = aligned(scales, 16);
+    if (K % 512 == 0 && !sc_aligned) return MXS_ERR_MISALIGNED;
+    const mxs::GemmWorkspace ws = mxs::gemm_w4a4_workspace_layout(M, N, K, sc_aligned);
+    if (!workspace || workspace_bytes < ws.bytes) return MXS_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return MXS_ERR_MISALIGNED;
+    return cuda_status(mxs::gemm_run_w4a4(static_cast<const uint16_t*>(x), nibbles, scales, y, M, N, K, workspace,
+                                          ws, dev_status, as_stream(stream)));
+}
+
 size_t nvfp4_verify_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (M < 1 || N < 1 || K < 32 || K % 32 != 0 || M > kMaxM || N > kMaxN || K > kMaxK) return 0;
     // the in-place scale layout is assumed when K % 256 == 0

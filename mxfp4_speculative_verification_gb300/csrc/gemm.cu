@@ -271,7 +271,8 @@ struct HostGemm {
 
 // Fill the launch's problem table for tiles of BN rows.
 // bs: the block-scaled kernel (256-k stages, scales read in place), 1 for
-// its mxf8f6f4 kind (padded E2M1 boxes), 2 for its mxf4 kind (packed boxes).
+// its mxf8f6f4 kind (padded E2M1 boxes), 2, 3 and 4 for its mxf4, mxf4nvf4
+// and W4A4 kinds (packed boxes).
 template <int G>
 static cudaError_t build_problems(ProblemSet<G>& S, const HostGemm* gs, int count, int M,
                                   int32_t* status, int BN, int64_t resident, int* sched,
@@ -495,13 +496,14 @@ static cudaError_t launch_bs_kind(int kind, const HostGemm* gs, int count, int M
                                   cudaStream_t stream) {
     if constexpr (G == 1) {
         if (kind == 2) return launch_bs<1, 2>(gs, count, M, status, stream);  // NVFP4: single calls only
+        if (kind == 3) return launch_bs<1, 3>(gs, count, M, status, stream);  // W4A4: single calls only
     }
     return kind ? launch_bs<G, 1>(gs, count, M, status, stream) : launch_bs<G, 0>(gs, count, M, status, stream);
 }
 
 // Every pass size the block-scaled kernel takes fits its shared and tensor memory.
 static constexpr bool bs_shapes_fit() {
-    for (int kind = 0; kind < 3; ++kind)
+    for (int kind = 0; kind < 4; ++kind)
         for (int m = 1; m <= bs_max_rows(kind); ++m) {
             const int npad = bs_npad(kind, m);
             const int rc = bs_ring(kind, npad);
@@ -926,6 +928,93 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
                        : launch_main_nt<kGroupMax>(NT, hs.data() + b, e - b, mc, dev_status, claim, stream);
             if (err != cudaSuccess) return err;
         }
+    }
+    return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
+// W4A4 ("Module 11 ...", §12: MX-FP4 weights and activations): X quantised
+// by the pack rule, block by block, then the block-scaled kind::mxf4 kernel
+// with one term, so that N = the pass's rows and W is streamed once for up
+// to 256 rows.  Its own workspace: the quantised X of a pass of up to 256
+// rows, per-row factors, split-K counters and partial tiles, realigned scales.
+// ---------------------------------------------------------------------------
+GemmWorkspace gemm_w4a4_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales_aligned) {
+    GemmWorkspace w{};
+    const int64_t nblk = K / 32;
+    const int64_t mc = std::min<int64_t>(M, kBsW4MaxRows);
+    const int npad = bs_npad(3, int(mc));
+    w.repack_scales = !(K % 512 == 0 && scales_aligned);
+    w.sc_pitch = w.repack_scales ? int(align_up(size_t(nblk), 16)) : int(nblk);
+    size_t off = 0;
+    w.xf_off = off;
+    off = align_up(off + size_t((K + 255) / 256) * size_t(bs_bstage_bytes(3, npad)), 256);
+    w.xun_off = off;
+    off = align_up(off + size_t(kBsW4MaxRows) * sizeof(float), 256);
+    const int64_t cap = bs_split_items_cap(N, K);
+    w.cnt_off = off;
+    w.n_counters = cap > 0 ? int(4 * ((N + kBsRows - 1) / kBsRows)) : 0;
+    off = align_up(off + size_t(w.n_counters) * sizeof(int), 256);
+    w.part_off = off;
+    off = align_up(off + size_t(cap > 0 ? cap * mc * kBsRows : 0) * sizeof(float), 256);
+    w.sc_off = off;
+    if (w.repack_scales) off = align_up(off + size_t(N) * size_t(w.sc_pitch), 256);
+    w.bytes = off;
+    return w;
+}
+
+cudaError_t gemm_run_w4a4(const uint16_t* x, const uint8_t* nibbles, const uint8_t* scales, float* y, int64_t M,
+                          int64_t N, int64_t K, void* workspace, const GemmWorkspace& ws, int32_t* dev_status,
+                          cudaStream_t stream) {
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    uint16_t* xf = reinterpret_cast<uint16_t*>(wsb + ws.xf_off);
+    float* xun = reinterpret_cast<float*>(wsb + ws.xun_off);
+    int* counters = reinterpret_cast<int*>(wsb + ws.cnt_off);
+    float* part = reinterpret_cast<float*>(wsb + ws.part_off);
+    uint8_t* sc_aligned = ws.repack_scales ? wsb + ws.sc_off : nullptr;
+    bool scales_realigned = false;
+    for (int64_t m0 = 0, mc = 0; m0 < M; m0 += mc) {
+        mc = bs_pass_rows(3, M - m0);
+        const bool repack = ws.repack_scales && !scales_realigned;
+        scales_realigned = true;
+        PrepSet Q{};
+        Q.job[0].x = x + m0 * K;
+        Q.job[0].xf = xf;
+        Q.job[0].xun = xun;
+        Q.job[0].K = int(K);
+        Q.njobs = 1;
+        Q.M = int(mc);
+        Q.NT = 1;
+        Q.bs_npad = bs_npad(3, int(mc));
+        Q.bs_kind = 3;
+        Q.counters = counters;
+        Q.ncounters = ws.n_counters;
+        if (repack) {
+            Q.sc_in = scales;
+            Q.N = N;
+            Q.nblk = int(K / 32);
+            Q.sc_pitch = ws.sc_pitch;
+            Q.sc_out = sc_aligned;
+            Q.repack_ctas = int(std::min<int64_t>((N * ws.sc_pitch + kPrepThreadsBs - 1) / kPrepThreadsBs, 1024));
+        }
+        cudaError_t err = launch_prep(Q, stream);
+        if (err != cudaSuccess) return err;
+        HostGemm h{};
+        h.nib = nibbles;
+        h.sc = ws.repack_scales ? sc_aligned : scales;
+        h.sc_pitch = ws.sc_pitch;
+        h.sc_from_prep = ws.repack_scales;
+        h.xf = xf;
+        h.xun = xun;
+        h.y = y + m0 * N;
+        h.part = part;
+        h.counters = counters;
+        h.N = N;
+        h.K = K;
+        const int64_t cap = bs_split_items_cap(N, K);
+        h.items_cap = (cap > 0 && ws.n_counters >= 4 * ((N + kBsRows - 1) / kBsRows)) ? cap : 0;
+        err = launch_bs_kind<1>(3, &h, 1, int(mc), dev_status, stream);
+        if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
 }

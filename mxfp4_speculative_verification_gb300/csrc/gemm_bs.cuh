@@ -28,6 +28,12 @@
 //     Y in the epilogue.  Four terms carry a bf16 row to ~1e-5 of its
 //     maximum (rows are first scaled by a power of two into [2^10, 2^11),
 //     inside the UE4M3 range).
+//   * kind::mxf4 in W4A4 form (KIND 3, passes of up to 256 rows): X itself
+//     quantised to MX-FP4 by the pack rule (one E2M1 term per element, one
+//     UE8M0 factor per 32-k block; rows below 1 scaled up by a power of
+//     two first, which the rule commutes with), so the product is that of
+//     the quantised X ("Module 11 ...", §12, W4A4); N = the pass's rows,
+//     so W is streamed once for up to 256 rows.
 //   The terms are stacked as B rows (row t * Npad + m = term t of X row m),
 //   so one MMA of N = T * Npad reads A from shared memory once, and
 //   Y[m] = sum over t of D[t * Npad + m].  Shared memory per stage is what
@@ -79,19 +85,27 @@ constexpr int kBsMaxRing = 8;
 constexpr int kBsScBytes = kBsRows * 16;     // TMA box of weight scales: 16 blocks x 128 rows
 constexpr int kBsCopyBytes = 512;            // one group x 128 columns of X's factor cells
 constexpr int kBsF4MaxRows = 32;             // the mxf4 kind takes passes of at most this many rows
+constexpr int kBsW4MaxRows = 256;            // W4A4 (X as one E2M1 term): MMA N up to 256
 
 // X rows a pass pads to (multiples of 16 keep every term row group's swizzle
 // and tensor-memory columns aligned).
 __host__ __device__ constexpr int bs_npad(int kind, int m) {
-    return kind == 2 ? (m <= 16 ? 16 : (m <= 32 ? 32 : 64)) : (kind ? (m <= 16 ? 16 : 32) : (m <= 32 ? 32 : 64));
+    return kind == 3   ? (m + 15) / 16 * 16
+           : kind == 2 ? (m <= 16 ? 16 : (m <= 32 ? 32 : 64))
+                       : (kind ? (m <= 16 ? 16 : 32) : (m <= 32 ? 32 : 64));
 }
 // X rows a pass of this kind takes at most
-__host__ __device__ constexpr int bs_max_rows(int kind) { return kind == 1 ? 32 : 64; }
+__host__ __device__ constexpr int bs_max_rows(int kind) { return kind == 3 ? kBsW4MaxRows : (kind == 1 ? 32 : 64); }
 // One D buffer in tensor memory instead of two (the next tile's MMAs wait for
 // the epilogue): NVFP4 passes of 33..64 rows, whose N = 4 x 64 = 256 columns
-// leave no room for a second buffer beside the factor slots.
-__host__ __device__ constexpr bool bs_single_d(int kind, int npad) { return kind == 2 && npad == 64; }
-__host__ __device__ constexpr int bs_terms(int kind) { return kind == 2 ? kBsNvTerms : (kind ? kBsF4Terms : 2); }
+// leave no room for a second buffer beside the factor slots, and W4A4
+// passes of more than 192 rows.
+__host__ __device__ constexpr bool bs_single_d(int kind, int npad) {
+    return (kind == 2 && npad == 64) || (kind == 3 && npad > 192);
+}
+__host__ __device__ constexpr int bs_terms(int kind) {
+    return kind == 3 ? 1 : (kind == 2 ? kBsNvTerms : (kind ? kBsF4Terms : 2));
+}
 // factor groups per 256-k stage: one per MMA of 64 k (NVFP4), else per 4 blocks of 32 k
 __host__ __device__ constexpr int bs_groups(int kind) { return kind == 2 ? 4 : 2; }
 // MMA N: the term rows of B

@@ -39,6 +39,16 @@ __device__ __forceinline__ uint32_t scale_bf16x2_to_f16x2(uint32_t w, float f1, 
 // residual still lies in the E4M3 range of its block (within 2^16 of the
 // block maximum); smaller elements keep about 16 bits.
 //
+// kind 3 (W4A4, mxf4): X quantised by the pack rule, block by block (the
+// exponent e with amax <= 6 2^e at its smallest, 0 for an all-zero block;
+// each element the nearest E2M1 value of x 2^-e, ties to the even code):
+// one term, the MX-FP4 image of X itself.  A row whose largest |x| is
+// below 1 is first scaled up by 2^sh as for kind 1 (never down), which
+// keeps the tensor core's block products clear of fp32's subnormal range;
+// the rule commutes with that exactly once the rule's clamp of e at -127
+// is applied as e >= sh - 127 in the scaled row: the same codes, every
+// block exponent shifted by sh.
+//
 // kind 1 (mxf4): each row is first multiplied by 2^sh, which puts its
 // largest |x| in [1, 2) (xun = 2^-sh undoes it), so that the term scales
 // below stay inside UE8M0's range for any row; then per 32-k block six E2M1
@@ -151,7 +161,8 @@ __device__ void prep_bs_row(const uint16_t* __restrict__ x, uint8_t* __restrict_
     const uint16_t* row = x + int64_t(m) * K;
     const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
     const int nchunks = K / 8;
-    float rsc = 1.f, run = 1.f;  // row scale 2^sh and its inverse (mxf4, mxf4nvf4)
+    float rsc = 1.f, run = 1.f;  // row scale 2^sh and its inverse (mxf4, mxf4nvf4, W4A4)
+    int shr = 0;                 // sh itself
     if (KIND >= 1 && m < M) {
         uint32_t mx = 0;  // largest |x| of the row, as bf16 bits (NaN and Inf above every finite)
         for (int k = threadIdx.x; k < K; k += blockDim.x) mx = max(mx, uint32_t(row[k] & 0x7FFFu));
@@ -163,13 +174,15 @@ __device__ void prep_bs_row(const uint16_t* __restrict__ x, uint8_t* __restrict_
         // the first term's UE4M3 factor, max / 6, stays below 448 and the
         // fourth's well above its smallest value)
         if (ef >= 1 && ef <= 254) {
-            const int sh = min(KIND == 2 ? 137 - ef : 127 - ef, 127);
+            const int sh = KIND == 3 ? max(127 - ef, 0) : min(KIND == 2 ? 137 - ef : 127 - ef, 127);
             rsc = pow2f_exact(sh);
             run = pow2f_exact(-sh);
+            shr = sh;
         } else if (ef == 0 && s_max != 0) {  // a row of subnormals (below 2^-126): into the normal range
             const int sh = KIND == 2 ? 127 : 64;
             rsc = pow2f_exact(sh);
             run = pow2f_exact(-sh);
+            shr = sh;
         }
     }
     const int nst = (K + 255) / 256;
@@ -262,17 +275,22 @@ __device__ void prep_bs_row(const uint16_t* __restrict__ x, uint8_t* __restrict_
                 if (lead16) sfb[bs_sfb_offset(n, blk >> 2, blk & 3, copies)] = act ? uint8_t(sbyte) : uint8_t(0x38);
             }
         } else {
-            // 8 codes = 4 bytes of the stage's 128-byte row segment
+            // 8 codes = 4 bytes of the stage's 128-byte row segment (W4A4:
+            // one term, the pack rule itself: e >= -127 before the row
+            // scale, an all-zero block gets e = 0)
             const int b = (k0 & 255) >> 1;
             const int unit = (((b >> 4) ^ (m & 7)) << 4) + (b & 15);
+            constexpr int kTerms = KIND == 3 ? 1 : kBsF4Terms;
 #pragma unroll 1
-            for (int t = 0; t < kBsF4Terms; ++t) {
+            for (int t = 0; t < kTerms; ++t) {
                 float amax = 0.f;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                const int e = e2m1_block_exp(amax);
+                const int e = KIND != 3     ? e2m1_block_exp(amax)
+                              : amax > 0.f ? max(e2m1_block_exp(amax), shr - 127)
+                                           : 0;
                 const uint32_t codes = act ? e2m1x8(f, pow2f_exact(-e)) : 0u;
                 float d[8];
                 e2m1x8_decode(codes, d);
@@ -308,7 +326,8 @@ struct PrepSet {
     int umma_npad;        // 0: mma.sync fragments; else swizzled tcgen05 tiles of this many rows
     int bs_npad;          // > 0: X terms + block scales for the block-scaled kernel, this many rows
     int bs_kind;          // its kind: 0 = two E4M3 terms (mxf8f6f4), 1 = six E2M1 terms (mxf4),
-                          // 2 = four E2M1 terms with UE4M3 factors per 16 k (mxf4nvf4)
+                          // 2 = four E2M1 terms with UE4M3 factors per 16 k (mxf4nvf4),
+                          // 3 = X quantised by the pack rule, one E2M1 term (W4A4, mxf4)
     int* counters;        // split-K counters to zero (may be null)
     int ncounters;
     const uint8_t* sc_in;  // scale realignment (single GEMM only; null otherwise)
@@ -330,6 +349,8 @@ __global__ void __launch_bounds__(kPrepThreads) mxfp4_gemm_prep_kernel(const __g
         const PrepJob& J = Q.job[blockIdx.x / mpad];
         if (Q.bs_kind == 2)
             prep_bs_row<2>(J.x, reinterpret_cast<uint8_t*>(J.xf), J.xun, J.K, blockIdx.x % mpad, M, Q.bs_npad);
+        else if (Q.bs_kind == 3)
+            prep_bs_row<3>(J.x, reinterpret_cast<uint8_t*>(J.xf), J.xun, J.K, blockIdx.x % mpad, M, Q.bs_npad);
         else if (Q.bs_kind)
             prep_bs_row<1>(J.x, reinterpret_cast<uint8_t*>(J.xf), J.xun, J.K, blockIdx.x % mpad, M, Q.bs_npad);
         else

@@ -32,6 +32,11 @@ cudaError_t gemm_run(const uint16_t* x, const uint8_t* nibbles, const uint8_t* s
                      const GemmWorkspace& ws, int32_t* dev_status, cudaStream_t stream);
 
 // The same GEMM on NVFP4 weights: scales [N, K/16] E4M3, one FP32 tensor scale.
+// W4A4: X quantised by the pack rule, passes of up to 256 rows (block-scaled kind::mxf4, one term)
+GemmWorkspace gemm_w4a4_workspace_layout(int64_t M, int64_t N, int64_t K, bool scales_aligned);
+cudaError_t gemm_run_w4a4(const uint16_t* x, const uint8_t* nibbles, const uint8_t* scales, float* y, int64_t M,
+                          int64_t N, int64_t K, void* workspace, const GemmWorkspace& ws, int32_t* dev_status,
+                          cudaStream_t stream);
 cudaError_t gemm_run_nv(const uint16_t* x, const uint8_t* nibbles, const uint8_t* scales, float global_scale,
                         float* y, int64_t M, int64_t N, int64_t K, void* workspace, const GemmWorkspace& ws,
                         int32_t* dev_status, cudaStream_t stream);

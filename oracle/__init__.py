@@ -17,6 +17,9 @@ What each entry point follows (page title, section):
 * ``gemm`` -- the definition Y[m,n] = sum_k x[m,k] * w[n,k], summed in double.
 * ``pack`` -- Module 11 §12-§13 (one power-of-two scale per block, nearest grid
   value, zero block gets scale 1).
+* ``gemm_w4a4`` -- Module 11 §12 (W4A4: activations in MX-FP4 as well):
+  X quantised by ``pack``'s rule, then the plain definition on the quantised
+  values.
 * ``spec_accept`` -- Module 11 §4 (left-to-right acceptance, residual
   norm((p-q)+), bonus token) and §5 (strict "draw < acceptance", acceptance 0
   where q = 0).
@@ -181,6 +184,32 @@ def pack(w: np.ndarray, *, dtype: str = "f32") -> tuple[np.ndarray, np.ndarray, 
     if rc not in (0, 4):
         raise ValueError(f"oracle pack failed ({rc})")
     return nib, sc, rc == 0
+
+
+def gemm_w4a4(x_bf16_bits: np.ndarray, nibbles: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Y[M, N] (float64) = dequant(pack(X)) . dequant(W)^T: both operands MX-FP4.
+
+    X (bf16 bit patterns [M, K]) is quantised block by block by the same rule
+    as ``pack``; a row holding a non-finite value, and a weight row with a NaN
+    scale (E8M0 byte 255), give NaN outputs.
+    """
+    x = _c(x_bf16_bits, np.uint16)
+    nib = _c(nibbles, np.uint8)
+    sc = _c(scales, np.uint8)
+    M, K = x.shape
+    N = nib.shape[0]
+    assert nib.shape == (N, K // 2) and sc.shape == (N, K // 32)
+    xn, xs, _ = pack(x, dtype="bf16")
+    xq = dequant(xn, xs)
+    w = dequant(nib, sc)
+    bad_x = np.any(xs == 255, axis=1)
+    bad_w = np.any(sc == 255, axis=1)
+    xq[bad_x] = 0.0
+    w[bad_w] = 0.0
+    y = xq @ w.T
+    y[bad_x, :] = np.nan
+    y[:, bad_w] = np.nan
+    return y
 
 
 def spec_accept(p: np.ndarray, q: np.ndarray, draft: np.ndarray, u: np.ndarray,

@@ -57,6 +57,32 @@ def test_gemm_rejects_bad_arguments_on_host(L):
     assert f(FAKE, FAKE, FAKE, FAKE, 5, 64, 512, FAKE, 16, None, None) == 5
 
 
+def test_w4a4_gemm_rules_on_host(L):
+    assert L.mxfp4_verify_gemm_w4a4_workspace_size(5, 4096, 4096) > 0
+    assert L.mxfp4_verify_gemm_w4a4_workspace_size(0, 4096, 4096) == 0
+    assert L.mxfp4_verify_gemm_w4a4_workspace_size(5, 4096, 4100) == 0  # K % 32
+    # passes of up to 256 rows: the quantised X of one pass, whatever M
+    assert (L.mxfp4_verify_gemm_w4a4_workspace_size(256, 4096, 4096)
+            == L.mxfp4_verify_gemm_w4a4_workspace_size(1000, 4096, 4096))
+    assert (L.mxfp4_verify_gemm_w4a4_workspace_size(16, 4096, 4096)
+            < L.mxfp4_verify_gemm_w4a4_workspace_size(256, 4096, 4096))
+    a = L.mxfp4_verify_gemm_w4a4_workspace_size(80, 1000, 544)
+    b = L.mxfp4_verify_gemm_w4a4_workspace_size(80, 1000, 512)
+    assert a >= b + 1000 * 32  # realigned scale rows
+    ws = 1 << 30
+    f = L.mxfp4_verify_gemm_w4a4
+    assert f(None, FAKE, FAKE, FAKE, 5, 64, 512, FAKE, ws, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, 0, 64, 512, FAKE, ws, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, 5, 64, 500, FAKE, ws, None, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, 1 << 20, 64, 512, FAKE, ws, None, None) == 3
+    assert f(FAKE + 1, FAKE, FAKE, FAKE, 5, 64, 512, FAKE, ws, None, None) == 2   # x 2B
+    assert f(FAKE, FAKE + 8, FAKE, FAKE, 5, 64, 512, FAKE, ws, None, None) == 2   # nibbles 16B
+    assert f(FAKE, FAKE, FAKE + 1, FAKE, 5, 64, 512, FAKE, ws, None, None) == 2   # scales, K%512==0
+    assert f(FAKE, FAKE, FAKE, FAKE, 5, 64, 512, None, ws, None, None) == 5
+    assert f(FAKE, FAKE, FAKE, FAKE, 5, 64, 512, FAKE, 16, None, None) == 5
+    assert f(FAKE, FAKE, FAKE, FAKE, 5, 64, 512, FAKE + 8, ws, None, None) == 2   # workspace 16B
+
+
 def test_nvfp4_gemm_rules_on_host(L):
     assert L.nvfp4_verify_gemm_workspace_size(5, 4096, 4096) > 0
     assert L.nvfp4_verify_gemm_workspace_size(5, 4096, 4100) == 0  # K % 32
