@@ -55,19 +55,19 @@ GEMM_TRAFFIC = {
     # (a single lm_head call at M=5 measured 1.0064)
     "mma": {"ratio": 1.0000, "sha": "bf0b691ec7beb45b"},
     # mxfp4_gemm_bs_kernel, kind::mxf8f6f4 (passes of 33..64 rows): lm_head at M=64
-    "bs8": {"ratio": 0.9171, "sha": "4dfbefb90e4d63a5"},
+    "bs8": {"ratio": 0.9171, "sha": "f9e1d7d859d66455"},
     # mxfp4_gemm_bs_kernel, kind::mxf4 (passes of 9..32 rows): lm_head at M=20
-    "bs4": {"ratio": 0.9849, "sha": "4dfbefb90e4d63a5"},
+    "bs4": {"ratio": 0.9850, "sha": "f9e1d7d859d66455"},
     # mxfp4_gemm_bs_kernel, W4A4 (X quantised in the call, passes of <= 256 rows): lm_head at M=256
-    "w4a4": {"ratio": 0.8917, "sha": "4dfbefb90e4d63a5"},
+    "w4a4": {"ratio": 0.8905, "sha": "f9e1d7d859d66455"},
 }
 # sm__pipe_tensor_cycles_active (% of peak, elapsed) of each kernel, from the
 # same captures as GEMM_TRAFFIC (keyed alike: None once the kernel changed)
 GEMM_TENSOR_PCT = {
     "mma": 27.89,   # grouped instance, 8 layers at M=5
-    "bs8": 34.34,   # lm_head at M=64
+    "bs8": 35.18,   # lm_head at M=64
     "bs4": 34.47,   # lm_head at M=20
-    "w4a4": 13.67,  # lm_head at M=256
+    "w4a4": 15.19,  # lm_head at M=256
 }
 
 

@@ -256,6 +256,17 @@ __device__ __forceinline__ uint32_t bs_sfid(uint32_t j) { return (j << 29) | (j 
 
 __device__ __forceinline__ bool has_byte_ff(uint32_t w) { return __vcmpeq4(w, 0xFFFFFFFFu) != 0; }
 
+// Wait for this thread's tensor-memory loads, naming the registers the last
+// one writes: the compiler then keeps every read of them after the wait.
+__device__ __forceinline__ void tmem_wait_ld_into(uint32_t (&v)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                   "+r"(v[15])
+                 :
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
                  "r"(c), "r"(d)
@@ -561,32 +572,60 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             const bool nan = nanflags[db * kBsRows + r] != 0;
             const float* xun = pb.xun;
             const int64_t Ny = pb.N;
+            const int nsplit = pb.nsplit;
+            const float gs = pb.gscale;
+            float* const ycol = pb.y + n0 + r;  // this lane's column of Y
             float* mine = pb.part + int64_t(wl) * M * kBsRows;
             const uint32_t dcol = tbase + lane_addr + (db ? d1col : 0u);
-#pragma unroll 1
-            for (int c0 = 0; c0 < npad; c0 += 16) {
-                // Y rows c0 .. c0 + 15: the sum of their T term columns, in term order
-                float acc[16];
-#pragma unroll 1
-                for (int t = 0; t < T; ++t) {
-                    uint32_t d[16];
-                    tmem_ld16(dcol + uint32_t(t * npad + c0), d);
-                    tmem_wait_ld();
+            // Y rows c0 .. c0 + 15 from their accumulators: the 16 rows' unscale
+            // factors are loaded together first (read-only here: written by the
+            // preparation kernel), so that no store waits on a load behind it
+            auto put16 = [&](int c0, const float (&acc)[16]) {
+                float xs[16];
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) acc[c] = t == 0 ? __uint_as_float(d[c]) : acc[c] + __uint_as_float(d[c]);
-                }
+                for (int c = 0; c < 16; ++c) xs[c] = c0 + c < M ? __ldg(xun + c0 + c) : 0.f;
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const int m = c0 + c;
                     if (m < M) {
                         const float v = nan ? __int_as_float(0x7FC00000) : acc[c];
-                        if (pb.nsplit == 1) {
-                            if (r < rows)
-                                pb.y[int64_t(m) * Ny + n0 + r] = KIND == 2 ? (v * xun[m]) * pb.gscale : v * xun[m];
+                        if (nsplit == 1) {
+                            if (r < rows) ycol[int64_t(m) * Ny] = KIND == 2 ? (v * xs[c]) * gs : v * xs[c];
                         } else {
                             __stcg(mine + int64_t(m) * kBsRows + r, v);
                         }
                     }
+                }
+            };
+            if constexpr (KIND == 3) {
+                // one term: the next 16 columns' tensor-memory load is in flight
+                // while this chunk is stored
+                uint32_t d[16];
+                tmem_ld16(dcol, d);
+#pragma unroll 1
+                for (int c0 = 0; c0 < npad; c0 += 16) {
+                    tmem_wait_ld_into(d);
+                    float acc[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) acc[c] = __uint_as_float(d[c]);
+                    if (c0 + 16 < npad) tmem_ld16(dcol + uint32_t(c0 + 16), d);
+                    put16(c0, acc);
+                }
+            } else {
+#pragma unroll 1
+                for (int c0 = 0; c0 < npad; c0 += 16) {
+                    // the sum of the rows' T term columns, in term order
+                    float acc[16];
+#pragma unroll 1
+                    for (int t = 0; t < T; ++t) {
+                        uint32_t d[16];
+                        tmem_ld16(dcol + uint32_t(t * npad + c0), d);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            acc[c] = t == 0 ? __uint_as_float(d[c]) : acc[c] + __uint_as_float(d[c]);
+                    }
+                    put16(c0, acc);
                 }
             }
             tc_fence_before();
@@ -602,19 +641,35 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
                     __threadfence();
-                    if (r < rows)
-                        for (int m = 0; m < M; ++m) {
-                            float s = 0.f;
-                            if constexpr (G == 1) {
-                                s = sum_partials(pb.part + int64_t(RI.tile) * M * kBsRows + int64_t(m) * kBsRows + r,
-                                                 int64_t(pb.ntiles) * M * kBsRows, pb.nsplit);
-                            } else {
-                                for (int sp = 0; sp < pb.nsplit; ++sp)
-                                    s += __ldcg(pb.part + (int64_t(sp) * pb.ntiles + RI.tile) * M * kBsRows +
-                                                int64_t(m) * kBsRows + r);
+                    if (r < rows) {
+                        // 8 rows at a time, so that their loads are in flight
+                        // together; each row summed in split order
+                        const float* pt = pb.part + int64_t(RI.tile) * M * kBsRows + r;
+                        const int64_t sstride = int64_t(pb.ntiles) * M * kBsRows;
+#pragma unroll 1
+                        for (int m0 = 0; m0 < M; m0 += 8) {
+                            float s[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) s[j] = 0.f;
+#pragma unroll 4
+                            for (int sp = 0; sp < nsplit; ++sp) {
+                                float v[8];
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    v[j] = m0 + j < M ? __ldcg(pt + sp * sstride + int64_t(m0 + j) * kBsRows) : 0.f;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) s[j] += v[j];
                             }
-                            pb.y[int64_t(m) * Ny + n0 + r] = KIND == 2 ? (s * xun[m]) * pb.gscale : s * xun[m];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int m = m0 + j;
+                                if (m < M) {
+                                    const float xm = __ldg(xun + m);
+                                    ycol[int64_t(m) * Ny] = KIND == 2 ? (s[j] * xm) * gs : s[j] * xm;
+                                }
+                            }
                         }
+                    }
                     if (lane == 0) pb.counters[4 * RI.tile + q] = 0;  // ready for the next call
                 }
             }
