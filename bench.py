@@ -53,21 +53,21 @@ GEMM_TRAFFIC = {
     # mxfp4_gemm_kernel, passes of <= 8 rows, as the step launches it: the grouped
     # instance over the 8B stack's first 8 layers (32 GEMMs, 936 MB) at M=5
     # (a single lm_head call at M=5 measured 1.0064)
-    "mma": {"ratio": 1.0000, "sha": "bf0b691ec7beb45b"},
+    "mma": {"ratio": 1.0001, "sha": "d39faf7c557d3a85"},
     # mxfp4_gemm_bs_kernel, kind::mxf8f6f4 (passes of 33..64 rows): lm_head at M=64
-    "bs8": {"ratio": 0.9171, "sha": "f9e1d7d859d66455"},
+    "bs8": {"ratio": 0.9171, "sha": "f1ace49f13d1d758"},
     # mxfp4_gemm_bs_kernel, kind::mxf4 (passes of 9..32 rows): lm_head at M=20
-    "bs4": {"ratio": 0.9850, "sha": "f9e1d7d859d66455"},
+    "bs4": {"ratio": 0.9851, "sha": "f1ace49f13d1d758"},
     # mxfp4_gemm_bs_kernel, W4A4 (X quantised in the call, passes of <= 256 rows): lm_head at M=256
-    "w4a4": {"ratio": 0.8905, "sha": "f9e1d7d859d66455"},
+    "w4a4": {"ratio": 0.8927, "sha": "f1ace49f13d1d758"},
 }
 # sm__pipe_tensor_cycles_active (% of peak, elapsed) of each kernel, from the
 # same captures as GEMM_TRAFFIC (keyed alike: None once the kernel changed)
 GEMM_TENSOR_PCT = {
-    "mma": 27.89,   # grouped instance, 8 layers at M=5
-    "bs8": 35.18,   # lm_head at M=64
-    "bs4": 34.47,   # lm_head at M=20
-    "w4a4": 15.19,  # lm_head at M=256
+    "mma": 28.21,   # grouped instance, 8 layers at M=5
+    "bs8": 37.94,   # lm_head at M=64
+    "bs4": 34.30,   # lm_head at M=20
+    "w4a4": 25.52,  # lm_head at M=256
 }
 
 

@@ -464,12 +464,12 @@ static cudaError_t launch_umma_np(int npad, const HostGemm* gs, int count, int M
 
 // Stage slots of the block-scaled kernel for a pass of npad rows;
 // MXS_GEMM_BS_RINGS=c overrides it when c slots fit shared and tensor memory.
-static int bs_ring_for(int kind, int npad) {
+static int bs_ring_for(int kind, int npad, int ybytes) {
     const int c = env_int("MXS_GEMM_BS_RINGS", 0);
-    if (c >= 2 && c <= kBsMaxRing && bs_smem_bytes(kind, npad, c) <= kBsSmemAttr &&
+    if (c >= 2 && c <= kBsMaxRing && bs_smem_bytes(kind, npad, c, ybytes) <= kBsSmemAttr &&
         bs_tmem_need(kind, npad, c) <= int(kBsTmemCols))
         return c;
-    return bs_ring(kind, npad);
+    return bs_ring(kind, npad, ybytes);
 }
 
 // Block-scaled kernel: one CTA per SM, 128-row tiles, K split only for a
@@ -486,9 +486,22 @@ static cudaError_t launch_bs(const HostGemm* gs, int count, int M, int32_t* stat
     err = build_problems(*S_buf, gs, count, M, status, kBsRows, int64_t(sms), nullptr, KIND == 0 ? 1 : KIND + 1);
     if (err != cudaSuccess) return err;
     const int npad = bs_npad(KIND, M);
-    S_buf->ring = bs_ring_for(KIND, npad);
+    // single-GEMM launches keep room for the output staging where it costs
+    // no stage slot, or where passes have 64 rows or more (their thread
+    // stores of Y cost more than the slot); then, without a K split and with
+    // 16-byte aligned rows of Y, Y goes out by tensor stores
+    const int ybytes =
+        G == 1 && (npad >= 64 || bs_ring(KIND, npad, kBsYStageBytes) == bs_ring(KIND, npad, 0)) ? kBsYStageBytes : 0;
+    S_buf->y_tma = 0;
+    if constexpr (G == 1) {
+        const HostGemm& h = gs[0];
+        if (ybytes && count == 1 && S_buf->p[0].nsplit == 1 && h.N % 4 == 0 &&
+            (reinterpret_cast<uintptr_t>(h.y) & 15) == 0 && make_map(&S_buf->tm_y, h.y, M, h.N * 4, h.N * 4, 128, 16, false))
+            S_buf->y_tma = 1;
+    }
+    S_buf->ring = bs_ring_for(KIND, npad, ybytes);
     const int64_t grid = std::min<int64_t>(S_buf->items, int64_t(sms));
-    return launch_persistent(kern, *S_buf, kBsThreads, bs_smem_bytes(KIND, npad, S_buf->ring), grid, stream);
+    return launch_persistent(kern, *S_buf, kBsThreads, bs_smem_bytes(KIND, npad, S_buf->ring, ybytes), grid, stream);
 }
 
 template <int G>
@@ -506,10 +519,12 @@ static constexpr bool bs_shapes_fit() {
     for (int kind = 0; kind < 4; ++kind)
         for (int m = 1; m <= bs_max_rows(kind); ++m) {
             const int npad = bs_npad(kind, m);
-            const int rc = bs_ring(kind, npad);
-            if (bs_smem_bytes(kind, npad, rc) > kBsSmemAttr || bs_tmem_need(kind, npad, rc) > int(kBsTmemCols) ||
-                rc > kBsMaxRing || rc < 3 || bs_slot_bytes(kind, npad) % 1024 != 0)
-                return false;
+            for (int yb = 0; yb <= kBsYStageBytes; yb += kBsYStageBytes) {
+                const int rc = bs_ring(kind, npad, yb);
+                if (bs_smem_bytes(kind, npad, rc, yb) > kBsSmemAttr || bs_tmem_need(kind, npad, rc) > int(kBsTmemCols) ||
+                    rc > kBsMaxRing || rc < 3 || bs_slot_bytes(kind, npad) % 1024 != 0)
+                    return false;
+            }
         }
     return true;
 }

@@ -147,14 +147,23 @@ __host__ __device__ constexpr int bs_tmem_need(int kind, int npad, int ring) {
 }
 // shared memory beyond the ring: barriers, NaN flags, TMEM base, abort flag
 constexpr int kBsMiscBytes = 8 * 64 + 2 * kBsRows + 64;
-__host__ __device__ constexpr int bs_smem_bytes(int kind, int npad, int ring) {
-    return ring * bs_slot_bytes(kind, npad) + kBsMiscBytes + 1024;
+// Output staging of single-GEMM launches (Y written by TMA tensor stores):
+// per epilogue warp two buffers of 16 rows x 32 fp32 columns.
+constexpr int kBsYStageBytes = 4 * 2 * 16 * 32 * 4;
+// Offset of the output staging (1024-aligned, after the barriers and flags).
+__host__ __device__ constexpr int bs_ystage_off(int kind, int npad, int ring) {
+    return (ring * bs_slot_bytes(kind, npad) + kBsMiscBytes + 1023) / 1024 * 1024;
+}
+__host__ __device__ constexpr int bs_smem_bytes(int kind, int npad, int ring, int ybytes = 0) {
+    return ybytes ? bs_ystage_off(kind, npad, ring) + ybytes + 1024 : ring * bs_slot_bytes(kind, npad) + kBsMiscBytes + 1024;
 }
 constexpr int kBsSmemAttr = 232448;  // dynamic shared memory the kernel may ask for
 // Stage slots: as many as shared and tensor memory hold (at most kBsMaxRing).
-__host__ __device__ constexpr int bs_ring(int kind, int npad) {
+__host__ __device__ constexpr int bs_ring(int kind, int npad, int ybytes = 0) {
     int r = kBsMaxRing;
-    while (r > 2 && (bs_smem_bytes(kind, npad, r) > kBsSmemAttr || bs_tmem_need(kind, npad, r) > int(kBsTmemCols))) --r;
+    while (r > 2 &&
+           (bs_smem_bytes(kind, npad, r, ybytes) > kBsSmemAttr || bs_tmem_need(kind, npad, r) > int(kBsTmemCols)))
+        --r;
     return r;
 }
 
@@ -256,6 +265,20 @@ __device__ __forceinline__ uint32_t bs_sfid(uint32_t j) { return (j << 29) | (j 
 
 __device__ __forceinline__ bool has_byte_ff(uint32_t w) { return __vcmpeq4(w, 0xFFFFFFFFu) != 0; }
 
+// TMA tensor store of a shared-memory box to global memory (bulk-group
+// completion), and the group operations of the issuing thread.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// all but the newest group have finished reading their shared memory
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// every group has completed (its writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Wait for this thread's tensor-memory loads, naming the registers the last
 // one writes: the compiler then keeps every read of them after the wait.
 __device__ __forceinline__ void tmem_wait_ld_into(uint32_t (&v)[16]) {
@@ -307,6 +330,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     const uint32_t fin_b = bars + 8u * (kB2 + 6);
     static_assert(kB2 + 7 <= 64, "barrier area");
     uint8_t* nanflags = smem + misc + 8 * 64;                       // [2][128]
+    constexpr int kYB = G == 1 ? kBsYStageBytes : 0;  // output staging (single-GEMM launches)
+    float* ystage = reinterpret_cast<float*>(smem + bs_ystage_off(KIND, npad, R));
     uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(smem + misc + 8 * 64 + 2 * kBsRows);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + misc + 8 * 64 + 2 * kBsRows + 4);
 
@@ -555,6 +580,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         const uint32_t lane_addr = uint32_t(32 * q) << 16;
         bool waited_pdl = false;
         int tc = 0;
+        int ychunk = 0;  // output chunks staged so far (buffer parity)
         for (int w = int(blockIdx.x); w < S.items; w += int(gridDim.x), ++tc) {
             const Problem& pb = S.p[find_problem(S, w)];
             const int wl = w - pb.item_begin;
@@ -584,6 +610,29 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 float xs[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) xs[c] = c0 + c < M ? __ldg(xun + c0 + c) : 0.f;
+                if (kYB && S.y_tma && nsplit == 1) {
+                    // single GEMM, no split: the 16 x 32 box of this warp through
+                    // shared memory and one tensor store (rows of Y lie N floats
+                    // apart: one thread store per row and lane group stalls on each)
+                    if (lane == 0) bulk_wait_read_1();  // the buffer's store two chunks ago has read it
+                    __syncwarp();
+                    float* buf = ystage + (q * 2 + (ychunk & 1)) * (16 * 32);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float v = nan ? __int_as_float(0x7FC00000) : acc[c];
+                        buf[c * 32 + lane] = KIND == 2 ? (v * xs[c]) * gs : v * xs[c];
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        // boxes reaching past N or M are clipped by the copy; one
+                        // group per chunk, so that the waits above count chunks
+                        if (n0 + 32 * q < Ny && c0 < M) tma_store_2d(&S.tm_y, smem_u32(buf), int(n0 + 32 * q) * 4, c0);
+                        bulk_commit();
+                    }
+                    ++ychunk;
+                    return;
+                }
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const int m = c0 + c;
@@ -674,6 +723,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 }
             }
         }
+        if (kYB && S.y_tma && lane == 0) bulk_wait_all();  // the staged stores have landed
     }
     tc_fence_before();
     __syncthreads();

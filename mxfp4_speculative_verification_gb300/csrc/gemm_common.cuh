@@ -43,6 +43,10 @@ struct ProblemSet {
     // and a stage that CTA 0's producer leaves out entirely (-1: none)
     unsigned long long wait_ns;
     int skip_stage;
+    // block-scaled kernel, single GEMM without a K split: Y [M, N] as bytes
+    // (rows N * 4 apart), written by tensor stores of 16 x 32 boxes when set
+    int y_tma;
+    CUtensorMap tm_y;
 };
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
