@@ -1024,7 +1024,8 @@ def w4a4_rows(mxs, torch, dev, peak, reps=20):
     entry point on the same MXFP4 weights: the 8B lm_head (K = 4096,
     N = 128256, 279 MB, beyond L2) at M = 80 / 160 / 256 / 320, back-to-back
     calls; and the whole 8B stack (32 layers x 4 GEMMs + lm_head, 4.3 GB) at
-    M = 80 and 256, one call per GEMM, in a CUDA graph.  Algorithmic bytes as
+    M = 80 / 256 / 320 as grouped plans, and at M = 80 one call per GEMM, in
+    CUDA graphs.  Algorithmic bytes as
     for the verify GEMM: nibbles + scales + bf16 X + fp32 Y."""
     N, K = workloads.VOCAB_LLAMA, 4096
     lo, hi = workloads.LLAMA_EXP_RANGE
@@ -1064,29 +1065,39 @@ def w4a4_rows(mxs, torch, dev, peak, reps=20):
     shapes = workloads.stack_shapes("llama8b")
     weights = [workloads.device_mxfp4_weights(N_, K_, lo, hi, seed=900 + i, device=dev)
                for i, (_, K_, N_) in enumerate(shapes)]
-    for M in (80, 256):
+    for M in (80, 256, 320):
         xs = {K_: workloads.device_bf16_normal(M, K_, seed=K_ + M, device=dev) for K_ in sorted({k for _, k, _ in shapes})}
         ys = [torch.empty((M, N_), dtype=torch.float32, device=dev) for _, _, N_ in shapes]
         nb = sum(gemm_bytes(M, N_, K_) for _, K_, N_ in shapes)
-        for mode in ("w4a4", "w4a16"):
-            size = mxs.mxfp4_verify_gemm_w4a4_workspace_size if mode == "w4a4" else mxs.mxfp4_verify_gemm_workspace_size
-            fn = mxs.mxfp4_verify_gemm_w4a4 if mode == "w4a4" else mxs.mxfp4_verify_gemm
-            ws = torch.empty(max(size(M, N_, K_) for _, K_, N_ in shapes), dtype=torch.uint8, device=dev)
+        probs = [(xs[K_], wn, wsc, y_) for (_, K_, _), (wn, wsc), y_ in zip(shapes, weights, ys)]
+        forms = [("w4a4", "grouped"), ("w4a16", "grouped")] + ([("w4a4", "per_call"), ("w4a16", "per_call")]
+                                                               if M == 80 else [])
+        for mode, form in forms:
+            if form == "grouped":
+                plan = mxs.GroupedGemm(probs, w4a4=mode == "w4a4")
+                us = graph_us(torch, dev, plan, reps=5)
+                del plan
+            else:
+                size = (mxs.mxfp4_verify_gemm_w4a4_workspace_size if mode == "w4a4"
+                        else mxs.mxfp4_verify_gemm_workspace_size)
+                fn = mxs.mxfp4_verify_gemm_w4a4 if mode == "w4a4" else mxs.mxfp4_verify_gemm
+                ws = torch.empty(max(size(M, N_, K_) for _, K_, N_ in shapes), dtype=torch.uint8, device=dev)
 
-            def stack_call():
-                for (_, K_, N_), (wn, wsc), y_ in zip(shapes, weights, ys):
-                    fn(xs[K_], wn, wsc, out=y_, workspace=ws)
+                def stack_call():
+                    for (_, K_, N_), (wn, wsc), y_ in zip(shapes, weights, ys):
+                        fn(xs[K_], wn, wsc, out=y_, workspace=ws)
 
-            us = graph_us(torch, dev, stack_call, reps=5)
-            stack.append({"mode": mode, "M": M, "gemms": len(shapes), "us_per_stack": us, "bytes": nb,
+                us = graph_us(torch, dev, stack_call, reps=5)
+                del ws
+            stack.append({"mode": mode, "form": form, "M": M, "gemms": len(shapes), "us_per_stack": us, "bytes": nb,
                           "hbm_gbs": nb / (us * 1e-6) / 1e9, "pct_of_peak": nb / (us * 1e-6) / 1e9 / peak})
-            del ws
-        del xs, ys
+        del xs, ys, probs
     del weights
     torch.cuda.empty_cache()
     return {"metric": "W4A4 verify GEMM (X quantised to MX-FP4 in the call) vs W4A16, us per call",
-            "timing": "lm_head: back-to-back calls, weights 279 MB beyond L2; stack: one call per GEMM "
-                      "(quantisation + product each) in a CUDA graph, 4.3 GB of weights",
+            "timing": "lm_head: back-to-back calls, weights 279 MB beyond L2; stack (4.3 GB of weights, CUDA "
+                      "graphs): grouped plans (each distinct X prepared once a pass, every W streamed once a "
+                      "pass) and, at M = 80, one call per GEMM",
             "lm_head": rows, "stack_llama8b": stack}
 
 

@@ -311,6 +311,21 @@ mxs_status mxfp4_verify_gemm_grouped(const mxs_gemm_problem* problems,
                                      size_t workspace_bytes,
                                      int32_t* dev_status, void* stream);
 
+/* mxfp4_verify_gemm_grouped_w4a4 -- the grouped form of mxfp4_verify_gemm_w4a4
+ * (W4A4, "Module 11 ...", §12): each distinct x is quantised to MX-FP4 by the
+ * pack rule once per pass, and every weight matrix is streamed once per pass
+ * of up to 256 rows.  Same problems, limits, errors and workspace rules as
+ * mxfp4_verify_gemm_grouped (with its own workspace size); K is never split,
+ * so each problem's result is bit-identical to mxfp4_verify_gemm_w4a4 on it
+ * whenever that single call does not split K either. */
+size_t mxfp4_verify_gemm_grouped_w4a4_workspace_size(const mxs_gemm_problem* problems,
+                                                     int32_t count, int64_t M);
+
+mxs_status mxfp4_verify_gemm_grouped_w4a4(const mxs_gemm_problem* problems,
+                                          int32_t count, int64_t M, void* workspace,
+                                          size_t workspace_bytes,
+                                          int32_t* dev_status, void* stream);
+
 /* ------------------------------------------------------------------------
  * mxfp4_verify_gemm_noalloc -- the same GEMM for callers that cannot
  * allocate device memory.  (The pages have no counterpart: this is an

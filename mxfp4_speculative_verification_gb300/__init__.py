@@ -95,6 +95,10 @@ def lib():
     L.mxfp4_verify_gemm_grouped_workspace_size.restype = sz
     L.mxfp4_verify_gemm_grouped.argtypes = [vp, i32, i64, vp, sz, vp, vp]
     L.mxfp4_verify_gemm_grouped.restype = i32
+    L.mxfp4_verify_gemm_grouped_w4a4_workspace_size.argtypes = [vp, i32, i64]
+    L.mxfp4_verify_gemm_grouped_w4a4_workspace_size.restype = sz
+    L.mxfp4_verify_gemm_grouped_w4a4.argtypes = [vp, i32, i64, vp, sz, vp, vp]
+    L.mxfp4_verify_gemm_grouped_w4a4.restype = i32
     L.spec_accept.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, vp, vp, vp]
     L.spec_accept.restype = i32
     L.spec_sampling_law.argtypes = [vp, i64, i64, vp, vp, vp, vp]
@@ -359,9 +363,19 @@ def _problem_array(problems):
     return arr, M
 
 
-def mxfp4_verify_gemm_grouped_workspace_size(problems) -> int:
+def _grouped_fns(w4a4: bool):
+    L = lib()
+    if w4a4:
+        return L.mxfp4_verify_gemm_grouped_w4a4_workspace_size, L.mxfp4_verify_gemm_grouped_w4a4
+    return L.mxfp4_verify_gemm_grouped_workspace_size, L.mxfp4_verify_gemm_grouped
+
+
+_GROUPED_LIMITS = "unsupported grouped GEMM (need 1 <= M <= 65536, K % 512 == 0, aligned W)"
+
+
+def mxfp4_verify_gemm_grouped_workspace_size(problems, *, w4a4: bool = False) -> int:
     arr, M = _problem_array(problems)
-    return int(lib().mxfp4_verify_gemm_grouped_workspace_size(arr, len(problems), M))
+    return int(_grouped_fns(w4a4)[0](arr, len(problems), M))
 
 
 class GroupedGemm:
@@ -370,18 +384,20 @@ class GroupedGemm:
     stream.  For a stack called every step (checking 129 problems in Python
     takes about 0.4 ms of host time).  The plan keeps its tensors alive; it
     reads whatever they hold at each call (in-place updates of x are the way to
-    feed new inputs).  Without a workspace it owns one of its own."""
+    feed new inputs).  Without a workspace it owns one of its own.  With
+    w4a4=True it binds mxfp4_verify_gemm_grouped_w4a4 (X quantised to MX-FP4)."""
 
-    def __init__(self, problems, *, workspace: torch.Tensor | None = None):
+    def __init__(self, problems, *, workspace: torch.Tensor | None = None, w4a4: bool = False):
         if not problems:
             raise MxsError("a grouped GEMM needs at least one problem")
         self._arr, self._M = _problem_array(problems)
         self._n = len(problems)
         self._tensors = [t for p in problems for t in p]
         self._dev = _need_cuda(*self._tensors, workspace)
-        need = int(lib().mxfp4_verify_gemm_grouped_workspace_size(self._arr, self._n, self._M))
+        size_fn, self._fn = _grouped_fns(w4a4)
+        need = int(size_fn(self._arr, self._n, self._M))
         if need == 0:
-            raise MxsError("unsupported grouped GEMM (need 1 <= M <= 64, K % 512 == 0, aligned W)")
+            raise MxsError(_GROUPED_LIMITS)
         if workspace is None:
             workspace = torch.empty(need, dtype=torch.uint8, device=self._dev)
         elif workspace.dtype != torch.uint8 or workspace.numel() < need:
@@ -392,26 +408,27 @@ class GroupedGemm:
         _check_status(dev_status)
         if dev_status is not None:
             _need_cuda(self._ws, dev_status)
-        _check(lib().mxfp4_verify_gemm_grouped(self._arr, self._n, self._M, _ptr(self._ws), self._ws.numel(),
-                                               _ptr(dev_status), _stream(self._dev)))
+        _check(self._fn(self._arr, self._n, self._M, _ptr(self._ws), self._ws.numel(), _ptr(dev_status),
+                        _stream(self._dev)))
 
 
 def mxfp4_verify_gemm_grouped(problems, *, workspace: torch.Tensor | None = None,
-                              dev_status: torch.Tensor | None = None) -> None:
+                              dev_status: torch.Tensor | None = None, w4a4: bool = False) -> None:
     """Independent GEMMs sharing M: problems is a list of (x, nibbles, scales, y)
-    device tensors; each y [M, N] is written with X . dequant(W)^T."""
+    device tensors; each y [M, N] is written with X . dequant(W)^T (w4a4=True:
+    with X quantised to MX-FP4 by the pack rule, mxfp4_verify_gemm_grouped_w4a4)."""
     if not problems:
         return
     arr, M = _problem_array(problems)
     dev = _need_cuda(*[t for p in problems for t in p], workspace, dev_status)
-    need = int(lib().mxfp4_verify_gemm_grouped_workspace_size(arr, len(problems), M))
+    size_fn, fn = _grouped_fns(w4a4)
+    need = int(size_fn(arr, len(problems), M))
     if need == 0:
-        raise MxsError("unsupported grouped GEMM (need 1 <= M <= 64, K % 512 == 0, aligned W)")
+        raise MxsError(_GROUPED_LIMITS)
     if workspace is None:
         workspace = _workspace(dev, need)
-    _check(lib().mxfp4_verify_gemm_grouped(arr, len(problems), M, _ptr(workspace),
-                                           workspace.numel() * workspace.element_size(),
-                                           _ptr(dev_status), _stream(dev)))
+    _check(fn(arr, len(problems), M, _ptr(workspace), workspace.numel() * workspace.element_size(),
+              _ptr(dev_status), _stream(dev)))
 
 
 # ---------------------------------------------------------- acceptance

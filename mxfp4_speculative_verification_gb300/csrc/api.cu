@@ -186,6 +186,27 @@ mxs_status mxfp4_verify_gemm_grouped(const mxs_gemm_problem* problems, int32_t c
                                              as_stream(stream)));
 }
 
+size_t mxfp4_verify_gemm_grouped_w4a4_workspace_size(const mxs_gemm_problem* problems, int32_t count,
+                                                     int64_t M) {
+    std::vector<mxs::GroupedGemm> gs;
+    mxs_status st;
+    if (!grouped_valid(problems, count, M, gs, st)) return 0;
+    return mxs::gemm_grouped_workspace(gs.data(), count, M, true);
+}
+
+mxs_status mxfp4_verify_gemm_grouped_w4a4(const mxs_gemm_problem* problems, int32_t count, int64_t M,
+                                          void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                          void* stream) {
+    std::vector<mxs::GroupedGemm> gs;
+    mxs_status st;
+    if (!grouped_valid(problems, count, M, gs, st)) return st;
+    if (!aligned(dev_status, 4)) return MXS_ERR_MISALIGNED;
+    const size_t need = mxs::gemm_grouped_workspace(gs.data(), count, M, true);
+    if (!workspace || workspace_bytes < need) return MXS_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return MXS_ERR_MISALIGNED;
+    return cuda_status(mxs::gemm_grouped_run(gs.data(), count, M, workspace, dev_status, as_stream(stream), true));
+}
+
 mxs_status spec_accept(const float* p, const float* q, const int32_t* draft, const float* u,
                        int64_t B, int64_t K, int64_t V, int32_t* out_tokens, int32_t* n_emitted,
                        int32_t* row_flags, int32_t* dev_status, void* stream) {

@@ -509,8 +509,8 @@ static cudaError_t launch_bs_kind(int kind, const HostGemm* gs, int count, int M
                                   cudaStream_t stream) {
     if constexpr (G == 1) {
         if (kind == 2) return launch_bs<1, 2>(gs, count, M, status, stream);  // NVFP4: single calls only
-        if (kind == 3) return launch_bs<1, 3>(gs, count, M, status, stream);  // W4A4: single calls only
     }
+    if (kind == 3) return launch_bs<G, 3>(gs, count, M, status, stream);  // W4A4
     return kind ? launch_bs<G, 1>(gs, count, M, status, stream) : launch_bs<G, 0>(gs, count, M, status, stream);
 }
 
@@ -842,21 +842,27 @@ static size_t xf_bytes(int64_t M, int64_t K) {
                     bs_may_run(M, K) ? bs_x_bytes(std::min<int64_t>(M, kBsMaxNpad), K) : size_t(0));
 }
 
-size_t gemm_grouped_workspace(const GroupedGemm* gs, int count, int64_t M) {
+// X of one W4A4 pass (the quantised rows of up to 256 rows) and its row factors
+static size_t xf_w4a4_bytes(int64_t M, int64_t K) {
+    const int m = int(std::min<int64_t>(M, kBsW4MaxRows));
+    return size_t((K + 255) / 256) * size_t(bs_bstage_bytes(3, bs_npad(3, m)));
+}
+
+size_t gemm_grouped_workspace(const GroupedGemm* gs, int count, int64_t M, bool w4a4) {
     size_t off = 0;
     for (int i = 0; i < count; ++i) {
         bool seen = false;
         for (int j = 0; j < i && !seen; ++j) seen = gs[j].x == gs[i].x && gs[j].K == gs[i].K;
         if (seen) continue;
-        off = align_up(off + xf_bytes(M, gs[i].K), 256);
-        off = align_up(off + kBsMaxNpad * sizeof(float), 256);
+        off = align_up(off + (w4a4 ? xf_w4a4_bytes(M, gs[i].K) : xf_bytes(M, gs[i].K)), 256);
+        off = align_up(off + size_t(w4a4 ? kBsW4MaxRows : kBsMaxNpad) * sizeof(float), 256);
     }
     // one item claim counter per launch of a pass
     return align_up(off + size_t((count + kGroupMax - 1) / kGroupMax) * sizeof(int), 256);
 }
 
 cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* workspace,
-                             int32_t* dev_status, cudaStream_t stream) {
+                             int32_t* dev_status, cudaStream_t stream, bool w4a4) {
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
     // distinct activations, in first-use order; X space sized for the largest pass
     std::vector<int> xid(count);
@@ -871,9 +877,9 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
             J.x = gs[i].x;
             J.K = int(gs[i].K);
             J.xf = reinterpret_cast<uint16_t*>(wsb + off);
-            off = align_up(off + xf_bytes(M, gs[i].K), 256);
+            off = align_up(off + (w4a4 ? xf_w4a4_bytes(M, gs[i].K) : xf_bytes(M, gs[i].K)), 256);
             J.xun = reinterpret_cast<float*>(wsb + off);
-            off = align_up(off + kBsMaxNpad * sizeof(float), 256);
+            off = align_up(off + size_t(w4a4 ? kBsW4MaxRows : kBsMaxNpad) * sizeof(float), 256);
             found = int(jobs.size());
             jobs.push_back(J);
         }
@@ -887,8 +893,9 @@ cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* 
     // matrix once
     for (int64_t m0 = 0, mcl = 0; m0 < M; m0 += mcl) {
         // one kind for every GEMM of the pass, or none if they would differ
-        int kind = count > 0 ? bs_kind_for(M - m0, gs[0].K, gs[0].nibbles) : -1;
-        for (int i = 1; i < count && kind >= 0; ++i)
+        // (W4A4: the quantised-X kind for every pass)
+        int kind = w4a4 ? 3 : (count > 0 ? bs_kind_for(M - m0, gs[0].K, gs[0].nibbles) : -1);
+        for (int i = 1; i < count && kind >= 0 && !w4a4; ++i)
             if (bs_kind_for(M - m0, gs[i].K, gs[i].nibbles) != kind) kind = -1;
         const bool bs = kind >= 0;
         mcl = bs ? bs_pass_rows(kind, M - m0) : std::min<int64_t>(kGemmMaxRowsPerPass, M - m0);

@@ -57,10 +57,12 @@ struct GroupedGemm {
     int64_t N, K;
 };
 
-size_t gemm_grouped_workspace(const GroupedGemm* gs, int count, int64_t M);
+// w4a4: every pass quantises X to MX-FP4 (the pack rule) and runs the
+// block-scaled kind::mxf4 kernel with one term, up to 256 rows a pass
+size_t gemm_grouped_workspace(const GroupedGemm* gs, int count, int64_t M, bool w4a4 = false);
 
 cudaError_t gemm_grouped_run(const GroupedGemm* gs, int count, int64_t M, void* workspace,
-                             int32_t* dev_status, cudaStream_t stream);
+                             int32_t* dev_status, cudaStream_t stream, bool w4a4 = false);
 
 // ---------------------------------------------------------- acceptance
 constexpr int kAcceptMaxK = 32;

@@ -189,3 +189,45 @@ def test_w4a4_llama8b_shapes_sampled(env, idx, name, K, N, M):
     rng = np.random.default_rng(idx)
     cols = np.unique(np.concatenate([rng.choice(N, size=min(N, 384), replace=False), [N - 1]]))
     _check(env, x, nib, sc, cols=cols)
+
+
+@pytest.mark.parametrize("M", [80, 300])
+def test_w4a4_grouped_equals_single_without_split(env, monkeypatch, M):
+    # the grouped form never splits K; with splitting off, each problem's
+    # single call runs the same kernel on the same quantised X: the same bits
+    torch, mxs = env
+    dev = torch.device("cuda:0")
+    monkeypatch.setenv("MXS_GEMM_SPLITS", "1")
+    probs = []
+    xs = {K: bf16_tensor_from_bits(torch, workloads.bf16_normal(M, K, seed=K, tensor_id=M), dev) for K in (4096, 14336)}
+    for i, (K, N) in enumerate([(4096, 6144), (14336, 4096), (4096, 1000), (4096, 6144)]):
+        nib, sc = workloads.mxfp4_weights(N, K, 118, 132, seed=i, tensor_id=400 + i)
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
+        probs.append((xs[K], torch.from_numpy(nib).to(dev), torch.from_numpy(sc).to(dev), y))
+    mxs.mxfp4_verify_gemm_grouped(probs, w4a4=True)
+    for x, nib, sc, y in probs:
+        single = mxs.mxfp4_verify_gemm_w4a4(x, nib, sc)
+        torch.cuda.synchronize()
+        assert torch.equal(single.view(torch.int32), y.view(torch.int32))
+
+
+def test_w4a4_grouped_plan_against_oracle(env):
+    torch, mxs = env
+    dev = torch.device("cuda:0")
+    M = 130
+    xb = {K: workloads.bf16_normal(M, K, seed=3, tensor_id=K) for K in (512, 1024)}
+    xd = {K: bf16_tensor_from_bits(torch, v, dev) for K, v in xb.items()}
+    host, probs = [], []
+    for i, (K, N) in enumerate([(1024, 300), (512, 129), (1024, 77)]):
+        nib, sc = workloads.mxfp4_weights(N, K, 118, 132, seed=i, tensor_id=500 + i)
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
+        host.append((K, nib, sc))
+        probs.append((xd[K], torch.from_numpy(nib).to(dev), torch.from_numpy(sc).to(dev), y))
+    plan = mxs.GroupedGemm(probs, w4a4=True)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    plan(dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for (K, nib, sc), (_, _, _, y) in zip(host, probs):
+        err = gemm_row_rel_err(y.cpu().numpy(), oracle.gemm_w4a4(xb[K], nib, sc))
+        assert np.all(err <= W4A4_REL_TOL)

@@ -154,6 +154,25 @@ def test_grouped_rejects_bad_arguments_on_host(L):
     assert f(arr, 2, 5, FAKE, 1 << 30, None, None) == 2
 
 
+def test_grouped_w4a4_rules_on_host(L):
+    P = mxs.GemmProblem
+    arr = (P * 2)(P(FAKE, FAKE, FAKE, FAKE, 4096, 4096), P(FAKE, FAKE, FAKE, FAKE, 1000, 4096))
+    a = L.mxfp4_verify_gemm_grouped_w4a4_workspace_size(arr, 2, 80)
+    assert a > 0
+    # one quantised X (both problems share x) of a pass of up to 256 rows
+    assert a < L.mxfp4_verify_gemm_grouped_w4a4_workspace_size(arr, 2, 256)
+    assert (L.mxfp4_verify_gemm_grouped_w4a4_workspace_size(arr, 2, 256)
+            == L.mxfp4_verify_gemm_grouped_w4a4_workspace_size(arr, 2, 1000))
+    f = L.mxfp4_verify_gemm_grouped_w4a4
+    assert f(arr, 2, 80, None, 1 << 30, None, None) == 5
+    assert f(arr, 2, 80, FAKE, 16, None, None) == 5
+    assert f(arr, 0, 80, FAKE, 1 << 30, None, None) == 1
+    bad = (P * 1)(P(FAKE, FAKE, FAKE, FAKE, 1000, 4000))
+    assert f(bad, 1, 80, FAKE, 1 << 30, None, None) == 3  # grouped: K % 512
+    bad = (P * 1)(P(FAKE, FAKE, FAKE, FAKE, 1000, 4001))
+    assert f(bad, 1, 80, FAKE, 1 << 30, None, None) == 1  # K % 32
+
+
 def test_grouped_workspace_layout(L):
     # problems sharing one X: the X space is counted once (16 rows of fp16 for a
     # 5-row pass, the wider of the two kernels' layouts, plus 64 unscale
