@@ -799,9 +799,11 @@ def profile_target(args):
         for i, (_, K, N) in enumerate(shapes):
             nib, sc = workloads.device_mxfp4_weights(N, K, lo, hi, seed=i, device=dev)
             problems.append((xs[K], nib, sc, torch.empty((M, N), dtype=torch.float32, device=dev)))
-        ws = torch.empty(mxs.mxfp4_verify_gemm_grouped_workspace_size(problems), dtype=torch.uint8, device=dev)
+        w4 = bool(args.profile_w4a4)
+        ws = torch.empty(mxs.mxfp4_verify_gemm_grouped_workspace_size(problems, w4a4=w4), dtype=torch.uint8,
+                         device=dev)
         for _ in range(4):
-            mxs.mxfp4_verify_gemm_grouped(problems, workspace=ws)
+            mxs.mxfp4_verify_gemm_grouped(problems, workspace=ws, w4a4=w4)
     elif args.profile_gemm:
         K, N = (int(v) for v in args.profile_gemm.split(","))
         x = workloads.device_bf16_normal(M, K, seed=1, device=dev)
@@ -1180,7 +1182,7 @@ def main():
     ap.add_argument("--profile-nvfp4", action="store_true",
                     help="with --profile-gemm: NVFP4 weights (nvfp4_verify_gemm) instead of MXFP4")
     ap.add_argument("--profile-w4a4", action="store_true",
-                    help="with --profile-gemm: the W4A4 entry point (mxfp4_verify_gemm_w4a4)")
+                    help="with --profile-gemm / --profile-grouped: the W4A4 entry points")
     ap.add_argument("--profile-law", action="store_true",
                     help="only run spec_sampling_law on the workload's target rows 4 times and exit (ncu target)")
     ap.add_argument("--profile-accept", action="store_true",
