@@ -595,6 +595,8 @@ def run_mxs(args, world, rank, local):
                 wcache[m2] = [workloads.device_mxfp4_weights(N, K, lo, hi, seed=i, device=dev)
                               for i, (_, K, N) in enumerate(workloads.stack_shapes(m2))]
             sweep.append(sweep_point(mxs, torch, dev, stream, wl, wcache[m2], args, peak_for_sweep()))
+            if wl in W4A4_SWEEP:
+                sweep.append(sweep_point(mxs, torch, dev, stream, wl, wcache[m2], args, peak_for_sweep(), w4a4=True))
         clk2 = clocks2.stop()
         for rec in sweep:
             rec["clocks"] = clk2
@@ -672,15 +674,18 @@ def run_mxs(args, world, rank, local):
 # The configurations reported beside the headline (each a sub-record of the
 # same JSON line): the 8B batch sweep and the 70B stack at three batch sizes.
 SWEEP_WORKLOADS = ("llama8b_b4", "llama8b_b16", "llama8b_b64", "llama70b_b1", "llama70b_b4", "llama70b")
+# of which these are also run in the grouped W4A4 form (beside the W4A16 step)
+W4A4_SWEEP = ("llama8b_b16", "llama8b_b64", "llama70b")
 
 
 def peak_for_sweep() -> float:
     return load_peaks()[0]
 
 
-def sweep_point(mxs, torch, dev, stream, wl, weights, args, peak):
+def sweep_point(mxs, torch, dev, stream, wl, weights, args, peak, w4a4=False):
     """One configuration: its grouped GEMM step and its acceptance call, each
-    captured in a CUDA graph and timed with CUDA events after warm-up."""
+    captured in a CUDA graph and timed with CUDA events after warm-up (w4a4:
+    the grouped W4A4 form, X quantised to MX-FP4, passes of up to 256 rows)."""
     model, B, K_spec = WORKLOADS[wl]
     M = B * (K_spec + 1)
     V = workloads.VOCAB_LLAMA
@@ -689,20 +694,21 @@ def sweep_point(mxs, torch, dev, stream, wl, weights, args, peak):
     x_dev = {K: workloads.device_bf16_normal(M, K, seed=K, device=dev) for K in ks}
     ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _, _, N in shapes]
     problems = [(x_dev[K], nib, sc, y) for (_, K, _), (nib, sc), y in zip(shapes, weights, ys)]
-    gws = torch.empty(mxs.mxfp4_verify_gemm_grouped_workspace_size(problems), dtype=torch.uint8, device=dev)
+    gws = torch.empty(mxs.mxfp4_verify_gemm_grouped_workspace_size(problems, w4a4=w4a4), dtype=torch.uint8,
+                      device=dev)
     p, q, d, u = workloads.spec_inputs(B, K_spec, V, seed=1, logit_std=ACCEPT_LOGIT_STD, draft_noise=draft_sigma())
     acc = [torch.from_numpy(a).to(dev) for a in (p, q, d, u)]
     out_tok = torch.empty((B, K_spec + 1), dtype=torch.int32, device=dev)
     n_emit = torch.empty((B,), dtype=torch.int32, device=dev)
     reps = 10
     with torch.cuda.stream(stream):
-        mxs.mxfp4_verify_gemm_grouped(problems, workspace=gws)
+        mxs.mxfp4_verify_gemm_grouped(problems, workspace=gws, w4a4=w4a4)
         mxs.spec_accept(*acc, out_tokens=out_tok, n_emitted=n_emit)
         torch.cuda.synchronize(dev)
         n_emitted = n_emit.cpu().numpy()
         g_gemm, g_acc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_gemm, stream=stream):
-            mxs.mxfp4_verify_gemm_grouped(problems, workspace=gws)
+            mxs.mxfp4_verify_gemm_grouped(problems, workspace=gws, w4a4=w4a4)
         with torch.cuda.graph(g_acc, stream=stream):
             for _ in range(reps):
                 mxs.spec_accept(*acc, out_tokens=out_tok, n_emitted=n_emit)
@@ -726,7 +732,7 @@ def sweep_point(mxs, torch, dev, stream, wl, weights, args, peak):
     ms_acc = timed(g_acc, steps) / reps
     gemm_b = sum(gemm_bytes(M, N, K) for _, K, N in shapes)
     acc_b = accept_bytes(B, K_spec, V, n_emitted)
-    passes = gemm_passes(M)
+    passes = [(min(256, M - m0), "w4a4") for m0 in range(0, M, 256)] if w4a4 else gemm_passes(M)
     n_main = len(passes) * ((len(shapes) + GROUP_MAX - 1) // GROUP_MAX)
     gbs = gemm_b / (ms_gemm * 1e-3) / 1e9
     flops = sum(2 * M * N * K for _, K, N in shapes)
@@ -735,7 +741,9 @@ def sweep_point(mxs, torch, dev, stream, wl, weights, args, peak):
     traffic = pass_traffic(shapes, passes, n_main)
     del x_dev, ys, problems, gws, acc
     return {
-        "workload": config_block(wl, model, B, K_spec)["workload"], "M": M,
+        "workload": config_block(wl, model, B, K_spec)["workload"]
+                    + (" (W4A4: X quantised to MX-FP4 by the pack rule)" if w4a4 else ""),
+        "mode": "w4a4" if w4a4 else "w4a16", "M": M,
         "ms_per_step": ms_gemm + ms_acc, "value": (gemm_b + acc_b) / ((ms_gemm + ms_acc) * 1e-3) / 1e12,
         "unit": "TB/s", "steps": steps,
         "passes": [f"{r} rows: {k}" for r, k in passes],
