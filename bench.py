@@ -298,6 +298,18 @@ def pass_traffic(shapes, passes, n_main):
     return total / n_main
 
 
+def w4a4_passes(M: int):
+    """Row passes of the W4A4 GEMM as the library plans them: as few as 256
+    rows allow, of equal size rounded up to 16 (320 rows: 2 x 160)."""
+    out, left = [], M
+    while left > 0:
+        n = -(-left // 256)
+        rows = min(left, -(-(-(-left // n)) // 16) * 16)
+        out.append((rows, "w4a4"))
+        left -= rows
+    return out
+
+
 def gemm_passes(M: int):
     """Row passes of the grouped GEMM and the kernel of each, as the library
     plans them for K % 128 == 0: fewer than BS_MIN_ROWS rows left go to
@@ -732,7 +744,7 @@ def sweep_point(mxs, torch, dev, stream, wl, weights, args, peak, w4a4=False):
     ms_acc = timed(g_acc, steps) / reps
     gemm_b = sum(gemm_bytes(M, N, K) for _, K, N in shapes)
     acc_b = accept_bytes(B, K_spec, V, n_emitted)
-    passes = [(min(256, M - m0), "w4a4") for m0 in range(0, M, 256)] if w4a4 else gemm_passes(M)
+    passes = w4a4_passes(M) if w4a4 else gemm_passes(M)
     n_main = len(passes) * ((len(shapes) + GROUP_MAX - 1) // GROUP_MAX)
     gbs = gemm_b / (ms_gemm * 1e-3) / 1e9
     flops = sum(2 * M * N * K for _, K, N in shapes)
@@ -1048,7 +1060,7 @@ def w4a4_rows(mxs, torch, dev, peak, reps=20):
             if mode == "w4a4":
                 ws = torch.empty(mxs.mxfp4_verify_gemm_w4a4_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
                 call = lambda: mxs.mxfp4_verify_gemm_w4a4(x, nib, sc, out=y, workspace=ws)
-                w_passes = (M + 255) // 256
+                w_passes = len(w4a4_passes(M))
             else:
                 ws = torch.empty(mxs.mxfp4_verify_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
                 call = lambda: mxs.mxfp4_verify_gemm(x, nib, sc, out=y, workspace=ws)

@@ -553,6 +553,13 @@ static int bs_kind_for(int64_t rows_left, int64_t K, const void* nib) {
 }
 // Rows of a block-scaled pass of the given kind.
 static int64_t bs_pass_rows(int kind, int64_t rows_left) {
+    if (kind == 3) {
+        // W4A4: as few passes as 256 rows allow, of equal size (rounded up to
+        // 16): 320 rows as 2 x 160 keep two D buffers in tensor memory, where
+        // 256 + 64 would run the first pass on one
+        const int64_t passes = (rows_left + kBsW4MaxRows - 1) / kBsW4MaxRows;
+        return std::min<int64_t>(rows_left, ((rows_left + passes - 1) / passes + 15) / 16 * 16);
+    }
     return std::min<int64_t>(bs_max_rows(kind), rows_left);
 }
 

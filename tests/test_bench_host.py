@@ -63,3 +63,13 @@ def test_tensor_pipe_table_covers_every_kernel():
     for M in (5, 20, 64, 80, 320):
         pct = bench.tensor_pct(bench.gemm_passes(M))
         assert all(v is None or 0.0 < v < 100.0 for v in pct.values())
+
+
+def test_w4a4_pass_plan():
+    # as few passes as 256 rows allow, of equal size (to 16), covering M exactly
+    for M in list(range(1, 1100, 7)) + [256, 257, 320, 512, 513]:
+        passes = bench.w4a4_passes(M)
+        assert sum(r for r, _ in passes) == M
+        assert len(passes) == -(-M // 256)
+        assert all(0 < r <= 256 for r, _ in passes)
+    assert [r for r, _ in bench.w4a4_passes(320)] == [160, 160]
