@@ -160,7 +160,8 @@ mxs_status mxfp4_verify_gemm(const void* x, const uint8_t* nibbles,
  *   Y[m, n] = sum_k q(X)[m, k] * dequant(W)[n, k]     (fp32 accumulation).
  * This is a different product from mxfp4_verify_gemm's (X is rounded to 4
  * bits); the block-scaled tensor core takes both operands as stored, and a
- * pass covers up to 256 rows of X, so W is read once for M <= 256.
+ * pass covers up to 256 rows of X, so W is read once for M <= 256 (more
+ * rows: as few passes as that allows, of equal size).
  *
  *   x, nibbles, scales, y, M, N, K: as for mxfp4_verify_gemm
  *   workspace  device, >= mxfp4_verify_gemm_w4a4_workspace_size(M, N, K)
