@@ -687,7 +687,7 @@ def run_mxs(args, world, rank, local):
 # same JSON line): the 8B batch sweep and the 70B stack at three batch sizes.
 SWEEP_WORKLOADS = ("llama8b_b4", "llama8b_b16", "llama8b_b64", "llama70b_b1", "llama70b_b4", "llama70b")
 # of which these are also run in the grouped W4A4 form (beside the W4A16 step)
-W4A4_SWEEP = ("llama8b_b16", "llama8b_b64", "llama70b")
+W4A4_SWEEP = SWEEP_WORKLOADS
 
 
 def peak_for_sweep() -> float:
